@@ -1,0 +1,244 @@
+"""Seeded synthetic inputs for the paged KV-cache store, the V4.1 inserts and
+the gather read path.
+
+This module holds none of the quantization arithmetic. It draws random
+numbers (numpy PCG64), rounds the drawn fp32 values to bf16 (input
+preparation), builds slot maps, positions, the rotary cos/sin table and
+poison fills, and says how big each buffer is. Both the CUDA path and the CPU
+oracle are fed from these arrays, so they see identical bytes.
+
+Large arrays are drawn in fixed-size row chunks, each from its own child of
+``SeedSequence(seed)``, so the bytes do not depend on how many threads drew
+them.
+
+Workloads (sizes of the published configurations; ``scaled`` variants keep
+the recipe and shrink the counts for fast tests):
+  store_small   64 tokens, contiguous 128-slot cache, injected edge groups
+  store_paged   16,384 tokens, 2048 blocks x 64 slots, block stride 192 rows
+  store_large   4,300,000 tokens, source row stride 576, 8,388,608 slots
+  rope_insert   65,536 tokens (or 4,194,304 for the large variant), R = 4
+  gather        1,048,576-slot packed cache, 128 queries x 2048 indices
+"""
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+LATENT = 512
+ROW_BYTES_MXFP4 = 272          # 512/2 code bytes + 512/32 scale bytes
+RECORD_BYTES_MXFP8 = 528       # 512 value bytes + 16 scale bytes
+RECORD_BYTES_NVFP4 = 288       # 256 code bytes + 32 scale bytes
+POISON = 0xAA                  # fill of this layer's cache rows before a store
+OTHER_LAYER_POISON = 0x5A      # fill of interleaved pages of other layers
+BF16_MAX_BITS = 0x7F7F         # fill of source columns past the latent
+BF16_QNAN_BITS = 0x7FC0
+CHUNK_ROWS = 16384
+
+
+def _threads() -> int:
+    return max(1, min(32, len(os.sched_getaffinity(0))))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 to bf16 (nearest even) and return the uint16 bit patterns.
+    Inputs here are finite draws; NaN is injected later as explicit bits."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32)
+    t = u >> 16
+    t &= 1
+    t += 0x7FFF
+    t += u
+    t >>= 16
+    return t.astype(np.uint16)
+
+
+def _draw_rows(seed: int, num_rows: int, width: int, fill, out: np.ndarray,
+               col0: int = 0, tag: int = 0) -> None:
+    """Fill out[:, col0:col0+width] (uint16) chunk by chunk; ``fill(rng, n)``
+    returns n fp32 values. Chunks draw from independent child seeds."""
+    n_chunks = max(1, math.ceil(num_rows / CHUNK_ROWS))
+    children = np.random.SeedSequence([seed, tag]).spawn(n_chunks)
+
+    def one(c):
+        lo = c * CHUNK_ROWS
+        hi = min(num_rows, lo + CHUNK_ROWS)
+        rng = np.random.default_rng(children[c])
+        vals = fill(rng, (hi - lo) * width).reshape(hi - lo, width)
+        out[lo:hi, col0:col0 + width] = f32_to_bf16_bits(vals)
+
+    if n_chunks == 1:
+        one(0)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(one, range(n_chunks)))
+
+
+def _normal(rng, n):
+    return rng.standard_normal(n, dtype=np.float32)
+
+
+def _student_t_outliers(rng, n):
+    """Student-t(nu=4) x 0.5, with 0.1% of the elements multiplied by 64."""
+    x = (rng.standard_t(4, n) * 0.5).astype(np.float32)
+    k = max(1, n // 1000)
+    x[rng.choice(n, k, replace=False)] *= 64.0
+    return x
+
+
+def _slots_with_pads(rng, num_slots: int, num_tokens: int, pad_count: int) -> np.ndarray:
+    slots = rng.choice(num_slots, num_tokens, replace=False).astype(np.int64)
+    if pad_count:
+        slots[rng.choice(num_tokens, pad_count, replace=False)] = -1
+    return slots
+
+
+# ------------------------------------------------------------ store_small ---
+
+E2M1_MIDPOINTS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def store_small(seed: int = 0) -> dict:
+    """64 tokens of N(0,1) x 2**U(-4,4) (per token), with injected groups:
+    one all-zero group, groups whose amax is exactly 6 * 2**k, and groups whose
+    members sit exactly on E2M1 midpoints times 2**k. Contiguous cache of 128
+    slots pre-filled with 0xAA; 64 distinct random slots, 8 of them -1."""
+    rng = np.random.default_rng(seed)
+    T = 64
+    x = rng.standard_normal((T, LATENT))
+    x *= np.exp2(rng.uniform(-4.0, 4.0, size=T))[:, None]
+    g = 32
+    # all-zero group (+0.0)
+    x[0, 3 * g:4 * g] = 0.0
+    # groups with amax exactly +-6 * 2**k, others strictly inside
+    for i, (t, grp) in enumerate([(1, 0), (2, 5), (3, 15), (4, 7), (5, 9), (6, 11)]):
+        k = int(rng.integers(-8, 9))
+        vals = rng.uniform(-0.99, 0.99, size=g) * 6.0 * 2.0 ** k
+        vals[int(rng.integers(0, g))] = (-1.0 if i % 2 else 1.0) * 6.0 * 2.0 ** k
+        x[t, grp * g:(grp + 1) * g] = vals
+    # groups on exact midpoints: amax 6 * 2**k pins the scale at 2**k
+    mids = np.array(E2M1_MIDPOINTS + (0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0))
+    for t, grp in [(7, 1), (8, 2), (9, 4), (10, 6), (11, 8), (12, 14)]:
+        k = int(rng.integers(-6, 7))
+        vals = np.concatenate([mids, -mids, [0.25, -0.25, 0.125, -0.125]])[:g] * 2.0 ** k
+        vals[0] = 6.0 * 2.0 ** k
+        x[t, grp * g:(grp + 1) * g] = rng.permutation(vals)
+    latent = f32_to_bf16_bits(x.astype(np.float32))
+    slots = _slots_with_pads(rng, 128, T, 8)
+    cache = np.full(128 * ROW_BYTES_MXFP4, POISON, dtype=np.uint8)
+    return dict(latent=latent, slot_mapping=slots, cache=cache, num_blocks=1, block_size=128,
+                block_stride_rows=128, cache_offset=0)
+
+
+# ------------------------------------------------------------ store_paged ---
+
+def store_paged(seed: int = 0, num_tokens: int = 16384, num_blocks: int = 2048,
+                block_size: int = 64, block_stride_rows: int = 192, layer_row_offset: int = 64,
+                pad_fraction: float = 0.05) -> dict:
+    """Student-t(4) x 0.5 latent with 0.1% outliers x 64. The buffer holds
+    num_blocks groups of block_stride_rows rows; this layer's block b is rows
+    [b*stride + offset, b*stride + offset + block_size), the rows around it
+    belong to other layers and carry a different poison."""
+    rng = np.random.default_rng(seed)
+    latent = np.empty((num_tokens, LATENT), dtype=np.uint16)
+    _draw_rows(seed, num_tokens, LATENT, _student_t_outliers, latent, tag=2)
+    num_slots = num_blocks * block_size
+    slots = _slots_with_pads(rng, num_slots, num_tokens, int(round(pad_fraction * num_tokens)))
+    rows = num_blocks * block_stride_rows
+    cache = np.full((rows, ROW_BYTES_MXFP4), OTHER_LAYER_POISON, dtype=np.uint8)
+    mine = (np.arange(num_blocks)[:, None] * block_stride_rows + layer_row_offset
+            + np.arange(block_size)[None, :]).reshape(-1)
+    cache[mine] = POISON
+    return dict(latent=latent, slot_mapping=slots, cache=cache.reshape(-1), num_blocks=num_blocks,
+                block_size=block_size, block_stride_rows=block_stride_rows,
+                cache_offset=layer_row_offset * ROW_BYTES_MXFP4)
+
+
+# ------------------------------------------------------------ store_large ---
+
+def store_large_slots(seed: int = 0, num_tokens: int = 4_300_000, num_slots: int = 8_388_608,
+                      pad_fraction: float = 0.01) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return _slots_with_pads(rng, num_slots, num_tokens, int(round(pad_fraction * num_tokens)))
+
+
+def store_large_latent(seed: int = 0, num_tokens: int = 4_300_000, row_stride: int = 576,
+                       out: np.ndarray = None) -> np.ndarray:
+    """[num_tokens, row_stride] uint16: N(0,1) bf16 in the first 512 columns,
+    bf16 max in the rest (to show any read past the latent)."""
+    if out is None:
+        out = np.empty((num_tokens, row_stride), dtype=np.uint16)
+    if row_stride > LATENT:
+        out[:, LATENT:] = BF16_MAX_BITS
+    _draw_rows(seed, num_tokens, LATENT, _normal, out, tag=3)
+    return out
+
+
+def store_large(seed: int = 0, num_tokens: int = 4_300_000, row_stride: int = 576,
+                num_slots: int = 8_388_608, pad_fraction: float = 0.01,
+                with_cache: bool = True) -> dict:
+    latent = store_large_latent(seed, num_tokens, row_stride)
+    slots = store_large_slots(seed, num_tokens, num_slots, pad_fraction)
+    d = dict(latent=latent[:, :LATENT], latent_full=latent, slot_mapping=slots,
+             num_blocks=1, block_size=num_slots, block_stride_rows=num_slots, cache_offset=0,
+             num_slots=num_slots)
+    if with_cache:
+        d["cache"] = np.full(num_slots * ROW_BYTES_MXFP4, POISON, dtype=np.uint8)
+    return d
+
+
+# ------------------------------------------------------------ rope_insert ---
+
+def rope_cos_sin_table(rows: int = 131072, rotary_dim: int = 64, base: float = 10000.0):
+    """fp32 [rows, rotary_dim]: cos(p * base**(-2i/rotary_dim)) for i < rotary_dim/2,
+    then the matching sines, evaluated in fp64 and rounded to fp32."""
+    half = rotary_dim // 2
+    inv_freq = base ** (-np.arange(half, dtype=np.float64) * 2.0 / rotary_dim)
+    ang = np.arange(rows, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def rope_insert(seed: int = 0, num_tokens: int = 65536, num_pages: int = 1024,
+                cache_block: int = 64, nan_fraction: float = 0.0005, table_rows: int = 131072,
+                compress_ratio: int = 4, record: str = "mxfp8", pad_count: int = 0) -> dict:
+    """N(0,1) bf16 latent with ``nan_fraction`` of the elements set to NaN
+    (0x7FC0); positions uniform in [0, table_rows); slots a random injection
+    into num_pages * cache_block slots (a permutation when the counts match);
+    optionally ``pad_count`` slots set to -1. Cache pre-filled with 0xAA."""
+    rng = np.random.default_rng(seed)
+    latent = np.empty((num_tokens, LATENT), dtype=np.uint16)
+    _draw_rows(seed, num_tokens, LATENT, _normal, latent, tag=4)
+    n_nan = int(round(nan_fraction * num_tokens * LATENT))
+    if n_nan:
+        flat = latent.reshape(-1)
+        flat[rng.choice(flat.size, n_nan, replace=False)] = BF16_QNAN_BITS
+    positions = rng.integers(0, table_rows, size=num_tokens, dtype=np.int64)
+    num_slots = num_pages * cache_block
+    slots = _slots_with_pads(rng, num_slots, num_tokens, pad_count)
+    record_bytes = {"mxfp8": RECORD_BYTES_MXFP8, "nvfp4": RECORD_BYTES_NVFP4}[record]
+    page_stride = cache_block * record_bytes
+    cache = np.full(num_pages * page_stride, POISON, dtype=np.uint8)
+    return dict(latent=latent, positions=positions, cos_sin=rope_cos_sin_table(table_rows),
+                cache=cache, cache_slots=slots, num_pages=num_pages, cache_block=cache_block,
+                page_stride_bytes=page_stride, compress_ratio=compress_ratio, record=record)
+
+
+# ----------------------------------------------------------------- gather ---
+
+def gather(seed: int = 0, num_slots: int = 1_048_576, num_queries: int = 128, topk: int = 2048,
+           max_pad: int = 64) -> dict:
+    """Rows to fill every slot of a packed cache (Student-t(4) x 0.5 with 0.1%
+    outliers x 64, slot i <- row i), and per query ``topk`` distinct random slot
+    indices whose last U{0..max_pad} entries are -1 pads."""
+    rng = np.random.default_rng(seed)
+    fill_latent = np.empty((num_slots, LATENT), dtype=np.uint16)
+    _draw_rows(seed, num_slots, LATENT, _student_t_outliers, fill_latent, tag=5)
+    fill_slots = np.arange(num_slots, dtype=np.int64)
+    idx = np.empty((num_queries, topk), dtype=np.int64)
+    for q in range(num_queries):
+        idx[q] = rng.choice(num_slots, topk, replace=False)
+        p = int(rng.integers(0, max_pad + 1))
+        if p:
+            idx[q, topk - p:] = -1
+    return dict(fill_latent=fill_latent, fill_slots=fill_slots, indices=idx, num_blocks=1,
+                block_size=num_slots, block_stride_rows=num_slots, num_slots=num_slots)
