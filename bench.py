@@ -1,0 +1,437 @@
+"""Benchmark of the paged KV-cache quantize-and-store hot path on GB300.
+
+Headline (one JSON line on stdout): mxfp4_mla_store on the large workload —
+4,300,000 tokens x 512 bf16 ~ N(0,1) read through a 576-element row stride
+(past 2**31 source elements), scattered into an 8,388,608-slot contiguous cache
+of 272-byte rows, 1% pad slots. One step = one store of the whole batch.
+
+  value      tokens/s of the whole job (all ranks), inputs resident in HBM
+  roofline   algorithmic bytes (8 B slot per token + 1024 B read and 272 B
+             written per valid token) / mean kernel time, against the measured
+             HBM copy bandwidth; traffic from the committed ncu summary
+  e2e        the same metric through the public API from pinned host buffers:
+             each step copies the latent and slots in and the cache back out
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  paths      the other hot-path rows measured in the same run: the V4.1
+             RoPE inserts (MXFP8, NVFP4) on 4,194,304 tokens and the gather of
+             128 x 2048 rows from a 1,048,576-slot cache
+
+--impl reference times the CPU oracle instead (the only reference this
+project has), on the same workload, metric and unit.
+Under torchrun (--gpus N > 1) every rank runs an independent replica on its
+own GPU (weak scaling); the slowest rank's time is reported.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MXFP4 KV-store tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+ROW = 272
+N_TOKENS = 4_300_000
+ROW_STRIDE = 576
+N_SLOTS = 8_388_608
+PROFILE = os.path.join(ROOT, "profiles", "mxfp4_mla_store_4300000tok.md")
+STORE_SOURCES = ["csrc/mxfp4_store.cu", "csrc/kvq_device.cuh", "csrc/kvq_host.h"]
+
+
+# ------------------------------------------------------------------ setup ---
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, x):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback (6.8 TB/s)"
+
+
+def store_bytes(num_tokens, valid):
+    read = 8 * num_tokens + 1024 * valid
+    write = ROW * valid
+    return read, write
+
+
+def source_sha256():
+    h = hashlib.sha256()
+    for rel in STORE_SOURCES:
+        with open(os.path.join(ROOT, "fp8_quantized_paged_store_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """(bytes per launch, note) from the committed ncu summary, or (None, why)
+    when there is none or the kernel source changed since it was taken."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None, "no committed ncu summary"
+    for line in text.splitlines():
+        if line.startswith("<!-- bench:"):
+            rec = json.loads(line[len("<!-- bench:"):line.rindex("-->")])
+            if rec.get("source_sha256") != source_sha256():
+                return None, "kernel changed since the ncu capture"
+            return float(rec["traffic_bytes_per_launch"]), rec.get("note", "")
+    return None, "ncu summary has no bench record"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) with host timestamps."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.samples = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if bus_id:
+            cmd.insert(1, f"--id={bus_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        win = [p for t, p in self.samples if t0 - 0.1 <= t <= t1 + 0.1]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(p[0]) for p in win if p[0].replace(".", "").isdigit()]
+        mx = [float(p[1]) for p in win if p[1].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win)}
+
+
+# ------------------------------------------------------------- reference ---
+
+def run_reference(args):
+    """The CPU oracle, single-threaded, as it stands: each step stores a
+    bounded sample of the large workload's tokens."""
+    import oracle
+    oracle.lib()
+    per_step = int(min(262_144, max(2_048, 6_000_000 // (args.steps + args.warmup))))
+    lat = workloads.store_large_latent(seed=0, num_tokens=per_step, row_stride=ROW_STRIDE)
+    slots = workloads.store_large_slots(seed=0)[:per_step].copy()
+    valid = int(np.sum(slots >= 0))
+    cache = np.full(N_SLOTS * ROW, 0xAA, dtype=np.uint8)
+    for _ in range(args.warmup):
+        oracle.mxfp4_mla_store(lat[:, :512], slots, cache, 1, N_SLOTS, N_SLOTS)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mxfp4_mla_store(lat[:, :512], slots, cache, 1, N_SLOTS, N_SLOTS)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    cores = 1
+    sample = (f"{per_step} tokens of the 4.3M-token workload per step (same generator, "
+              f"same slots, {valid} valid), single thread")
+    rd, wr = store_bytes(per_step, valid)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "mxfp4_mla_store_large", "num_tokens": N_TOKENS,
+                       "row_stride": ROW_STRIDE, "num_slots": N_SLOTS, "latent": 512,
+                       "group": 32, "sample_tokens_per_step": per_step},
+            "gbs": (rd + wr) * args.steps / dt / 1e9,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- ours ---
+
+def cpu_baseline_sample(lat_host, slots_host, seconds=10.0):
+    """Oracle (single thread, as it stands) on consecutive 50,000-token chunks
+    of the same host inputs until ~`seconds` of CPU work."""
+    import oracle
+    oracle.lib()
+    chunk = 50_000
+    cache = np.full(N_SLOTS * ROW, 0xAA, dtype=np.uint8)
+    done, t0 = 0, time.perf_counter()
+    while done < lat_host.shape[0] and time.perf_counter() - t0 < seconds:
+        n = min(chunk, lat_host.shape[0] - done)
+        oracle.mxfp4_mla_store(lat_host[done:done + n, :512], slots_host[done:done + n], cache,
+                               1, N_SLOTS, N_SLOTS)
+        done += n
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {done} tokens of the same 4.3M-token workload ({dt:.1f} s, "
+                      f"single thread)"}
+
+
+def time_events(torch, fn, reps, stream, flush=None):
+    """Mean and per-rep kernel times (ms) with CUDA events on `stream`."""
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.mean(times), times
+
+
+def secondary_paths(torch, kvq, dev, peak):
+    """RoPE inserts on 4,194,304 tokens and the 128 x 2048 gather: mean of
+    CUDA-event times over 20 reps each (L2 flushed before each gather rep)."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    for record, width in (("mxfp8", 528), ("nvfp4", 288)):
+        w = workloads.rope_insert(seed=0, num_tokens=4_194_304, num_pages=65_536, record=record)
+        lat = torch.from_numpy(w["latent"].view(np.int16)).to(dev).view(torch.bfloat16)
+        pos = torch.from_numpy(w["positions"]).to(dev)
+        tab = torch.from_numpy(w["cos_sin"]).to(dev)
+        slots = torch.from_numpy(w["cache_slots"]).to(dev)
+        cache = torch.from_numpy(w["cache"]).to(dev).view(w["num_pages"], 64, width)
+        fn = getattr(kvq, f"rope_quant_insert_{record}")
+        pos_np, slot_np = w["positions"], w["cache_slots"]
+        writers = int(np.sum((slot_np >= 0) & ((pos_np + 1) % 4 == 0)))
+        n = pos_np.size
+        algo = 16 * n + writers * (1024 + 256 + width)
+        call = lambda: fn(lat, pos, tab, cache, slots, 4)  # noqa: E731
+        for _ in range(3):
+            call()
+        ms, _ = time_events(torch, call, 20, stream)
+        out[f"rope_quant_insert_{record}"] = {
+            "workload": "4,194,304 tokens, R=4, 65,536 pages x 64, 0.05% NaN",
+            "tokens_per_s": n / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
+            "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
+            "writers": writers}
+        del lat, pos, tab, slots, cache
+    g = workloads.gather(seed=0)
+    lat = torch.from_numpy(g["fill_latent"].view(np.int16)).to(dev).view(torch.bfloat16)
+    slots = torch.from_numpy(g["fill_slots"]).to(dev)
+    cache = torch.empty(g["num_slots"] * ROW, dtype=torch.uint8, device=dev)
+    kvq.mxfp4_mla_store(lat, slots, cache)  # fill the packed cache (not timed)
+    del lat
+    idx = torch.from_numpy(g["indices"]).to(dev)
+    outb = torch.empty((idx.numel(), 512), dtype=torch.bfloat16, device=dev)
+    valid = int(np.sum(g["indices"] >= 0))
+    algo = 8 * idx.numel() + ROW * valid + 1024 * idx.numel()
+    call = lambda: kvq.mxfp4_mla_gather_dequant(cache, idx, out=outb)  # noqa: E731
+    for _ in range(3):
+        call()
+    ms, _ = time_events(torch, call, 20, stream, flush=flush)
+    out["mxfp4_mla_gather_dequant"] = {
+        "workload": "128 queries x 2048 indices (trailing pads) from 1,048,576 slots",
+        "rows_per_s": idx.numel() / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
+        "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
+        "l2": "flushed before each rep"}
+    return out
+
+
+def run_ours(args):
+    import torch
+
+    import __graft_entry__
+    world, rank, local = dist_env()
+    dist = init_dist(world)
+    __graft_entry__.build() if rank == 0 else None
+    barrier(dist)
+    import fp8_quantized_paged_store_gb300 as kvq
+    kvq.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, peak_src = peaks()
+
+    # host inputs (pinned), identical on every rank (independent replicas)
+    lat_np = workloads.store_large_latent(seed=0, num_tokens=N_TOKENS, row_stride=ROW_STRIDE)
+    slots_np = workloads.store_large_slots(seed=0)
+    valid = int(np.sum(slots_np >= 0))
+    lat_h = torch.from_numpy(lat_np.view(np.int16)).pin_memory()
+    slots_h = torch.from_numpy(slots_np).pin_memory()
+    cache_h = torch.empty(N_SLOTS * ROW, dtype=torch.uint8).pin_memory()
+
+    lat_d = lat_h.to(dev).view(torch.bfloat16)[:, :512]
+    slots_d = slots_h.to(dev)
+    cache_d = torch.full((N_SLOTS * ROW,), 0xAA, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    step = lambda: kvq.mxfp4_mla_store(lat_d, slots_d, cache_d)  # noqa: E731
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except AttributeError:
+        pass
+    sampler = ClockSampler(bus) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+
+    # timed region: K steps, one launch each; per-launch events on the stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t_wall1 = time.time()
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(dist, total_ms)
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+        clocks = sampler.summary(t_wall0, t_wall1)
+    gpu_launches = args.steps
+
+    # end to end: pinned host in, cache back to pinned host, every step
+    e2e_steps = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    barrier(dist)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    lat_full_d = torch.empty_like(lat_h, device=dev)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        lat_full_d.copy_(lat_h, non_blocking=True)
+        slots_d.copy_(slots_h, non_blocking=True)
+        kvq.mxfp4_mla_store(lat_full_d.view(torch.bfloat16)[:, :512], slots_d, cache_d)
+        cache_h.copy_(cache_d, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, a.elapsed_time(b))
+    h2d = lat_h.numel() * 2 + slots_h.numel() * 8
+    d2h = cache_h.numel()
+    del lat_full_d
+
+    paths = secondary_paths(torch, kvq, dev, peak) if (rank == 0 and not args.no_paths) else None
+    cpu = cpu_baseline_sample(lat_np, slots_np, args.cpu_seconds) if rank == 0 else None
+    if rank != 0:
+        return
+
+    rd, wr = store_bytes(N_TOKENS, valid)
+    mean_launch_ms = statistics.mean(per_launch)
+    achieved = (rd + wr) / (mean_launch_ms * 1e-3) / 1e9
+    traffic, traffic_note = profiled_traffic()
+    value = world * N_TOKENS * args.steps / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64, N(0,1) bf16)",
+        "config": {"workload": "mxfp4_mla_store_large", "num_tokens": N_TOKENS,
+                   "valid_tokens": valid, "row_stride": ROW_STRIDE, "num_slots": N_SLOTS,
+                   "latent": 512, "group": 32, "row_bytes": ROW,
+                   "l2": "inputs larger than L2 (4.95 GB source, 2.28 GB cache)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": rd + wr,
+                     "peak_source": peak_src, "traffic_note": traffic_note},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * N_TOKENS * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "paths": paths,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-paths", action="store_true",
+                    help="skip the secondary RoPE-insert and gather measurements")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        world, rank, _ = dist_env()
+        if rank != 0:
+            return
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+"""GB300 (sm_103a) quantize-and-scatter library for a paged MLA KV cache.
+
+Python binding of the C ABI in include/kvq.h. Every function here only
+marshals torch tensors into pointers, sizes and the current CUDA stream and
+calls the same-named entry point of libkvq.so; all work runs in the CUDA
+kernels. There is no fallback: if the library is not built, importing the
+functions works but every call raises.
+
+  mxfp4_mla_store            quantize bf16 latent rows to 272-byte MXFP4 rows
+  rope_quant_insert_mxfp8    GPT-J RoPE then the 528-byte MXFP8 record
+  rope_quant_insert_nvfp4    GPT-J RoPE then the 288-byte NVFP4 record
+  mxfp4_mla_gather_dequant   gather packed rows back to bf16
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = ["mxfp4_mla_store", "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
+           "mxfp4_mla_gather_dequant", "row_bytes", "cache_view", "KvqError", "lib",
+           "LIBRARY_PATH"]
+
+LIBRARY_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
+KVQ_OK, KVQ_EINVAL, KVQ_ECUDA = 0, -1, -2
+
+_i64, _i32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+_LIB = None
+
+
+class KvqError(RuntimeError):
+    def __init__(self, name, status):
+        self.status = status
+        super().__init__(f"{name} failed: {lib().kvq_strerror(status).decode()} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkvq.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIBRARY_PATH):
+            raise RuntimeError(
+                f"{LIBRARY_PATH} is not built; run `python -m fp8_quantized_paged_store_gb300.build`"
+                " or __graft_entry__.build() first")
+        L = ctypes.CDLL(LIBRARY_PATH)
+        L.kvq_strerror.restype = ctypes.c_char_p
+        L.kvq_strerror.argtypes = [ctypes.c_int]
+        L.kvq_row_bytes.restype = _i64
+        L.kvq_row_bytes.argtypes = [_i64, _i64]
+        L.mxfp4_mla_store.restype = ctypes.c_int
+        L.mxfp4_mla_store.argtypes = [_p, _i64, _i64, _i64, _p, _p, _i64, _i64, _i64, _i32, _p]
+        for name in ("rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _p, _p, _i64, _i64, _i64, _i32, _i32,
+                          _p]
+        L.mxfp4_mla_gather_dequant.restype = ctypes.c_int
+        L.mxfp4_mla_gather_dequant.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _p, _i64, _p]
+        _LIB = L
+    return _LIB
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _check(name, status):
+    if status != KVQ_OK:
+        raise KvqError(name, status)
+
+
+def _need(t: torch.Tensor, dtype, what):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA {dtype} tensor")
+
+
+def row_bytes(latent_dim: int = 512, group: int = 32) -> int:
+    return int(lib().kvq_row_bytes(latent_dim, group))
+
+
+def cache_view(cache: torch.Tensor, pitch: int):
+    """(num_blocks, block_size, block_stride_rows) of a uint8 cache: either a
+    paged [num_blocks, block_size, pitch] view whose rows are contiguous and
+    whose block stride is a whole number of rows, or any contiguous tensor
+    read as [numel // pitch, pitch] (one block)."""
+    _need(cache, torch.uint8, "cache")
+    if cache.dim() == 3:
+        nb, bs, width = cache.shape
+        if width != pitch or cache.stride(2) != 1 or cache.stride(1) != pitch or \
+                cache.stride(0) % pitch:
+            raise ValueError(f"paged cache {tuple(cache.shape)} with strides {cache.stride()} is "
+                             f"not a whole number of {pitch}-byte rows per block")
+        return nb, bs, cache.stride(0) // pitch
+    if not cache.is_contiguous() or cache.numel() % pitch:
+        raise ValueError(f"cache of {cache.numel()} bytes is not a contiguous multiple of {pitch}")
+    n = cache.numel() // pitch
+    return 1, n, n
+
+
+def mxfp4_mla_store(latent: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
+                    group: int = 32, stream=None) -> None:
+    """latent: bf16 [T, 512] (any row stride), slot_mapping: int64 [T],
+    cache: uint8 paged view (see cache_view) of 272-byte rows."""
+    _need(latent, torch.bfloat16, "latent")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    if latent.dim() != 2 or latent.stride(1) != 1:
+        raise ValueError("latent must be [tokens, latent_dim] with unit column stride")
+    if slot_mapping.dim() != 1 or slot_mapping.numel() < latent.shape[0] or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous [tokens] tensor")
+    nb, bs, bsr = cache_view(cache, row_bytes(latent.shape[1], group))
+    _check("mxfp4_mla_store", lib().mxfp4_mla_store(
+        latent.data_ptr(), latent.shape[0], latent.shape[1], latent.stride(0),
+        slot_mapping.data_ptr(), cache.data_ptr(), nb, bs, bsr, group, _stream(stream)))
+
+
+def _rope(name, record, latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
+          sanitize_nans, stream):
+    _need(latent, torch.bfloat16, "latent")
+    _need(positions, torch.int64, "positions")
+    _need(cos_sin, torch.float32, "cos_sin")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(kv_cache, torch.uint8, "kv_cache")
+    if latent.dim() != 2 or latent.shape[1] != 512 or latent.stride(1) != 1:
+        raise ValueError("latent must be [tokens, 512] with unit column stride")
+    if cos_sin.dim() != 2 or cos_sin.stride(1) != 1:
+        raise ValueError("cos_sin must be [rows, >= 64] with unit column stride")
+    if kv_cache.dim() != 3 or kv_cache.shape[-1] != record or not kv_cache[0].is_contiguous():
+        raise ValueError(f"kv_cache must be [pages, cache_block, {record}] with contiguous pages")
+    n = slot_mapping.numel()
+    if n > min(latent.shape[0], positions.numel()) or not slot_mapping.is_contiguous() or \
+            not positions.is_contiguous():
+        raise ValueError("slot_mapping / positions must be contiguous and cover the tokens")
+    _check(name, getattr(lib(), name)(
+        latent.data_ptr(), n, latent.stride(0), positions.data_ptr(), cos_sin.data_ptr(),
+        cos_sin.stride(0), cos_sin.shape[0], kv_cache.data_ptr(), slot_mapping.data_ptr(),
+        kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), int(compress_ratio),
+        1 if sanitize_nans else 0, _stream(stream)))
+
+
+def rope_quant_insert_mxfp8(latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
+                            sanitize_nans=False, stream=None) -> None:
+    """kv_cache: uint8 [pages, cache_block, 528]; a page holds cache_block x 512
+    value bytes then cache_block x 16 scale bytes."""
+    _rope("rope_quant_insert_mxfp8", 528, latent, positions, cos_sin, kv_cache, slot_mapping,
+          compress_ratio, sanitize_nans, stream)
+
+
+def rope_quant_insert_nvfp4(latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
+                            sanitize_nans=False, stream=None) -> None:
+    """kv_cache: uint8 [pages, cache_block, 288]; a page holds cache_block x 256
+    code bytes then cache_block x 32 scale bytes."""
+    _rope("rope_quant_insert_nvfp4", 288, latent, positions, cos_sin, kv_cache, slot_mapping,
+          compress_ratio, sanitize_nans, stream)
+
+
+def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor = None,
+                             latent_dim: int = 512, stream=None) -> torch.Tensor:
+    """indices: int64 (any shape, contiguous); returns bf16 [*indices.shape,
+    latent_dim] (or fills ``out``, whose last dim has unit stride)."""
+    _need(indices, torch.int64, "indices")
+    if not indices.is_contiguous():
+        raise ValueError("indices must be contiguous")
+    nb, bs, bsr = cache_view(cache, row_bytes(latent_dim, 32))
+    if out is None:
+        out = torch.empty((*indices.shape, latent_dim), dtype=torch.bfloat16,
+                          device=indices.device)
+    _need(out, torch.bfloat16, "out")
+    flat = out.view(-1, latent_dim) if out.is_contiguous() else out.reshape(-1, latent_dim)
+    if flat.data_ptr() != out.data_ptr() or flat.stride(1) != 1:
+        raise ValueError("out must be viewable as [num_indices, latent_dim] without a copy")
+    _check("mxfp4_mla_gather_dequant", lib().mxfp4_mla_gather_dequant(
+        cache.data_ptr(), nb, bs, bsr, latent_dim, indices.data_ptr(), indices.numel(),
+        out.data_ptr(), flat.stride(0), _stream(stream)))
+    return out

@@ -1,0 +1,226 @@
+// mxfp4_gather.cu — mxfp4_mla_gather_dequant: gather packed 272-byte MXFP4
+// rows by slot index and write them out as bf16.
+//
+// Follows PR 60321 "Add an mxfp4_mla KV cache for rope-free sparse MLA"
+// (Details, read path: gathered rows are unpacked to bf16 before use; Claims:
+// attention over the packed cache equals attention over those bf16 values).
+//
+// Every decoded value E2M1(code) * 2**(byte-127) has at most two significant
+// bits, so it is exact in bf16 and can be assembled from bits: the bf16
+// pattern of magnitude index i (1..7) is 0x3F00 + 64*i (0x3F00 for i = 1),
+// and the scale adds (byte-127) << 7 to it while the result stays a normal
+// bf16, i.e. for 2 <= byte <= 252. Per group the eight scaled patterns are
+// packed into byte tables, and the codes themselves (masked to three bits)
+// select from them with byte permutes: four values per pair of prmt. The
+// code's sign bit is bit 3 of a nibble; prmt's sign-replicate mode copies a
+// byte's top bit, so the signs of odd codes come straight from the code
+// bytes and those of even codes from the code word shifted left by 4.
+// Scale bytes 0, 1, 253, 254 (subnormal or overflowing results) and 255 (the
+// E8M0 NaN) take an arithmetic path.
+//
+// Work decomposition: one warp per output row, 32 indices per chunk (lane i
+// loads index i and turns it into a source offset once), two rows in flight.
+// Lane l reads code bytes 4l..4l+3 and 128+4l..128+4l+3 (two coalesced
+// 128-byte warp loads) and the scale bytes of groups l/4 and 8+l/4, and
+// writes 16 bytes at elements 8l and 256+8l (two coalesced 512-byte stores).
+// Pads and out-of-range indices write zeros.
+#include <cstdint>
+
+#include "kvq.h"
+#include "kvq_device.cuh"
+#include "kvq_host.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kGatherWarps = 8;
+constexpr int kGatherThreads = 32 * kGatherWarps;
+
+struct GatherParams {
+  const uint8_t* cache;
+  int64_t num_slots;
+  int64_t block_size;
+  int64_t block_stride_rows;
+  const int64_t* indices;
+  int64_t num_indices;
+  uint8_t* out;        // row k starts at out + k * out_pitch
+  int64_t out_pitch;   // bytes
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+struct ByteTables {
+  uint32_t lo_a, lo_b, hi_a, hi_b;  // low / high bytes of scaled patterns 0..3, 4..7
+};
+
+// Scaled bf16 magnitude patterns for a scale byte in [2, 252].
+__device__ __forceinline__ ByteTables make_tables(uint32_t scale_byte) {
+  const uint32_t off = (uint32_t)(((int)scale_byte - 127) << 7);
+  const uint32_t off2 = off * 0x00010001u;  // the same offset in both halves
+  const uint32_t p01 = (0x3F00u + off) << 16;  // index 0 stays +0
+  const uint32_t p23 = 0x3FC03F80u + off2;
+  const uint32_t p45 = 0x40404000u + off2;
+  const uint32_t p67 = 0x40C04080u + off2;
+  ByteTables t;
+  t.lo_a = prmt(p01, p23, 0x6420);
+  t.hi_a = prmt(p01, p23, 0x7531);
+  t.lo_b = prmt(p45, p67, 0x6420);
+  t.hi_b = prmt(p45, p67, 0x7531);
+  return t;
+}
+
+// Four codes (bits 16k..16k+15 of `c`) -> two bf16x2 words.
+template <int k>
+__device__ __forceinline__ void decode4(uint32_t c, uint32_t c_shl4, const ByteTables& t,
+                                        uint32_t& w0, uint32_t& w1) {
+  const uint32_t sel = (c >> (16 * k)) & 0x7777u;
+  const uint32_t lo4 = prmt(t.lo_a, t.lo_b, sel);
+  const uint32_t hi4 = prmt(t.hi_a, t.hi_b, sel);
+  w0 = prmt(lo4, hi4, 0x5140);
+  w1 = prmt(lo4, hi4, 0x7362);
+  // byte 2k of c holds codes 4k (low nibble) and 4k+1; byte 2k+1 codes 4k+2, 4k+3.
+  constexpr uint32_t s0 = ((8u | (2 * k)) << 12) | ((8u | (4 + 2 * k)) << 4);
+  constexpr uint32_t s1 = ((8u | (2 * k + 1)) << 12) | ((8u | (4 + 2 * k + 1)) << 4);
+  w0 |= prmt(c, c_shl4, s0) & 0x80008000u;
+  w1 |= prmt(c, c_shl4, s1) & 0x80008000u;
+}
+
+// Arithmetic decode of one code for any scale byte.
+__device__ __forceinline__ uint32_t decode_one_slow(uint32_t code, uint32_t scale_byte) {
+  if (scale_byte == 255u) return 0x7FC0u;
+  const uint32_t i = code & 7u;
+  const uint64_t pats = 0x40C0408040404000ull;  // patterns of indices 7..4
+  const uint64_t pats_lo = 0x3FC03F803F000000ull;  // indices 3..0
+  const uint32_t mag_bits =
+      (uint32_t)(((i < 4 ? pats_lo : pats) >> (16 * (i & 3))) & 0xFFFFu);
+  const int k = (int)scale_byte - 127;  // -127..127
+  const float pow2 = k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23)
+                               : __uint_as_float(0x00400000u);
+  const float v = __fmul_rn(__uint_as_float(mag_bits << 16), pow2);  // exact or +inf
+  return (__float_as_uint(v) >> 16) | ((code & 8u) << 12);
+}
+
+__device__ __noinline__ uint4 decode8_slow(uint32_t c, uint32_t scale_byte) {
+  uint32_t h[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) h[j] = decode_one_slow((c >> (4 * j)) & 0xFu, scale_byte);
+  return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                    h[6] | (h[7] << 16));
+}
+
+// Eight codes of one group -> 16 bytes of bf16.
+__device__ __forceinline__ uint4 decode8(uint32_t c, uint32_t scale_byte) {
+  if (scale_byte - 2u > 250u) return decode8_slow(c, scale_byte);
+  const ByteTables t = make_tables(scale_byte);
+  const uint32_t c4 = c << 4;
+  uint4 r;
+  decode4<0>(c, c4, t, r.x, r.y);
+  decode4<1>(c, c4, t, r.z, r.w);
+  return r;
+}
+
+template <bool kFlat>
+__global__ void __launch_bounds__(kGatherThreads) mxfp4_gather_kernel(GatherParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kGatherThreads + threadIdx.x) >> 5;
+  const int64_t num_warps = ((int64_t)gridDim.x * kGatherThreads) >> 5;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+
+  for (int64_t base = warp * 32; base < p.num_indices; base += num_warps * 32) {
+    int64_t src_off = -1;
+    if (base + lane < p.num_indices) {
+      const int64_t s = ld_once_i64(p.indices + base + lane);
+      if (s >= 0 && s < p.num_slots) {
+        if (kFlat) {
+          src_off = s * kMxfp4RowBytes;
+        } else {
+          int64_t blk, in_blk;
+          divmod_pos(s, p.block_size, blk, in_blk);
+          src_off = (blk * p.block_stride_rows + in_blk) * kMxfp4RowBytes;
+        }
+      }
+    }
+    const int n = (int)min((int64_t)32, p.num_indices - base);
+    for (int i = 0; i < n; i += 2) {
+      const int64_t s0 = __shfl_sync(0xFFFFFFFFu, src_off, i);
+      const int64_t s1 = __shfl_sync(0xFFFFFFFFu, src_off, (i + 1) & 31);
+      const bool has1 = i + 1 < n;
+      uint8_t* o0 = p.out + (base + i) * p.out_pitch;
+      uint8_t* o1 = o0 + p.out_pitch;
+      uint32_t c00 = 0, c01 = 0, b00 = 0, b01 = 0, c10 = 0, c11 = 0, b10 = 0, b11 = 0;
+      if (s0 >= 0) {
+        const uint8_t* r = p.cache + s0;
+        c00 = ld_u32(r + 4 * lane);
+        c01 = ld_u32(r + 128 + 4 * lane);
+        b00 = ld_u8(r + 256 + (lane >> 2));
+        b01 = ld_u8(r + 264 + (lane >> 2));
+      }
+      if (has1 && s1 >= 0) {
+        const uint8_t* r = p.cache + s1;
+        c10 = ld_u32(r + 4 * lane);
+        c11 = ld_u32(r + 128 + 4 * lane);
+        b10 = ld_u8(r + 256 + (lane >> 2));
+        b11 = ld_u8(r + 264 + (lane >> 2));
+      }
+      st_v4(o0 + 16 * lane, s0 >= 0 ? decode8(c00, b00) : zero);
+      st_v4(o0 + 512 + 16 * lane, s0 >= 0 ? decode8(c01, b01) : zero);
+      if (has1) {
+        st_v4(o1 + 16 * lane, s1 >= 0 ? decode8(c10, b10) : zero);
+        st_v4(o1 + 512 + 16 * lane, s1 >= 0 ? decode8(c11, b11) : zero);
+      }
+    }
+  }
+}
+
+int g_gather_occupancy[2][64];
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks,
+                                        int64_t block_size, int64_t block_stride_rows,
+                                        int64_t latent_dim, const int64_t* indices,
+                                        int64_t num_indices, void* out_bf16,
+                                        int64_t out_row_stride_elems, cudaStream_t stream) {
+  using namespace kvq;
+  if (latent_dim != kLatent) return KVQ_EINVAL;
+  if (num_indices < 0 || num_blocks < 1 || block_size < 1 || block_stride_rows < block_size)
+    return KVQ_EINVAL;
+  if (out_row_stride_elems < latent_dim || out_row_stride_elems % 8 != 0) return KVQ_EINVAL;
+  if (num_blocks > INT64_MAX / block_stride_rows / kMxfp4RowBytes) return KVQ_EINVAL;
+  if (num_blocks > INT64_MAX / block_size) return KVQ_EINVAL;
+  if (num_indices > INT64_MAX / 2 / out_row_stride_elems) return KVQ_EINVAL;
+  if (num_indices == 0) return KVQ_OK;
+  if (!cache || !indices || !out_bf16) return KVQ_EINVAL;
+  if (!aligned(cache, 16) || !aligned(out_bf16, 16) || !aligned(indices, 8)) return KVQ_EINVAL;
+
+  GatherParams p;
+  p.cache = cache;
+  p.num_slots = num_blocks * block_size;
+  p.block_size = block_size;
+  p.block_stride_rows = block_stride_rows;
+  p.indices = indices;
+  p.num_indices = num_indices;
+  p.out = static_cast<uint8_t*>(out_bf16);
+  p.out_pitch = out_row_stride_elems * 2;
+
+  const bool flat = (num_blocks == 1) || (block_stride_rows == block_size);
+  const int64_t chunks = (num_indices + 31) / 32;
+  const int64_t work_blocks = (chunks + kGatherWarps - 1) / kGatherWarps;
+  if (flat) {
+    auto k = mxfp4_gather_kernel<true>;
+    const unsigned grid =
+        grid_for(work_blocks, resident_blocks_per_sm(k, kGatherThreads, g_gather_occupancy[1]));
+    k<<<grid, kGatherThreads, 0, stream>>>(p);
+  } else {
+    auto k = mxfp4_gather_kernel<false>;
+    const unsigned grid =
+        grid_for(work_blocks, resident_blocks_per_sm(k, kGatherThreads, g_gather_occupancy[0]));
+    k<<<grid, kGatherThreads, 0, stream>>>(p);
+  }
+  return launch_status();
+}

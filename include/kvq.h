@@ -1,0 +1,184 @@
+/*
+ * kvq.h — C ABI of the GB300 (sm_103a) quantize-and-scatter library for a
+ * paged MLA KV cache: MXFP4 store, V4.1 RoPE-then-quantize inserts (MXFP8 and
+ * NVFP4 records), and the MXFP4 gather-and-dequantize read.
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [store] "vllm.v1.attention.ops.mxfp4_mla.store" (vLLM API docs):
+ *           module docstring, _ceil_pow2_exponent, _quantize_e2m1,
+ *           store_mxfp4_mla.
+ *   [v41]   "vllm.models.deepseek_v41.common.ops.fused_compress_quant_cache"
+ *           (vLLM API docs): _rope_quant_insert_mxfp8_kernel,
+ *           _rope_quant_insert_nvfp4_kernel, rope_quant_insert.
+ *   [pr]    "[ROCm][Attention] Add an mxfp4_mla KV cache for rope-free sparse
+ *           MLA (read/write path)", vLLM pull request 60321: Overview, Claims,
+ *           Details (format and write path; read path).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers owned by the caller (cudaMalloc'd, or
+ *     any memory the GPU can address). The library allocates nothing, keeps
+ *     no pointer past the call, and never synchronises: work is enqueued on
+ *     `stream` (0 = the legacy default stream) and the call returns.
+ *   - bf16 data is passed as raw 16-bit patterns (`const void*`).
+ *   - Status: 0 (KVQ_OK) on success; KVQ_EINVAL (-1) when an argument is
+ *     rejected before anything is launched (nothing is written); KVQ_ECUDA
+ *     (-2) when the launch itself failed (cudaGetLastError after the launch).
+ *     kvq_strerror() names every status.
+ *   - num_tokens / num_indices == 0 returns KVQ_OK without a launch, after
+ *     the shape arguments have been checked ([store] store_mxfp4_mla returns
+ *     early for an empty batch).
+ *   - Device-side conditions that the host cannot see (a slot or index
+ *     outside the cache, a position outside the table) never fault: the
+ *     affected token is skipped, or for the gather its row is written as
+ *     zeros. Two tokens that name the same slot race (last writer unknown),
+ *     as in any scatter.
+ *   - Alignment: bf16 row bases and row pitches must be multiples of 16
+ *     bytes (row strides multiples of 8 elements); cache and output bases
+ *     must be 16-byte aligned; int64 arrays 8-byte aligned; the cos/sin table
+ *     base 16-byte aligned with a row stride that is a multiple of 4 floats.
+ *     Misalignment is KVQ_EINVAL.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_OK 0
+#define KVQ_EINVAL (-1)
+#define KVQ_ECUDA (-2)
+
+/* Short English description of a status code (static storage). */
+const char* kvq_strerror(int status);
+
+/* Bytes of one packed MXFP4 row: latent_dim/2 code bytes + latent_dim/group
+ * scale bytes ([store] module docstring: row_bytes(d) = d//2 + d//32).
+ * kvq_row_bytes(512, 32) == 272. Returns -1 unless latent_dim > 0,
+ * group > 0, group even and latent_dim a multiple of group. */
+int64_t kvq_row_bytes(int64_t latent_dim, int64_t group);
+
+/*
+ * mxfp4_mla_store — quantize MLA latent rows to MXFP4 and scatter them into a
+ * paged cache. [store] store_mxfp4_mla, _ceil_pow2_exponent, _quantize_e2m1;
+ * [pr] Details (format and write path).
+ *
+ * For each token t in [0, num_tokens) with s = slot_mapping[t]:
+ *   - s < 0 (padding) or s >= num_blocks*block_size: skipped, nothing read.
+ *   - otherwise row t (latent_dim bf16 values starting at
+ *     latent_bf16 + t*row_stride_elems) is split into groups of `group`;
+ *     each group gets the E8M0 exponent e = ceil(log2(amax/6)) taken from the
+ *     binary32 bits of RN(amax/6) (0 for an all-zero group; NaN is ignored by
+ *     amax), and every value becomes the E2M1 code of x * 2**-e, rounded to
+ *     nearest with ties to the even code, sign bit set when x * 2**-e < 0.
+ *     The 272-byte row [256 code bytes, low nibble = lower index | 16 scale
+ *     bytes e+127] is written at byte offset
+ *       ((s / block_size) * block_stride_rows + s % block_size) * 272
+ *     of `cache`. Nothing else in the cache is touched.
+ *
+ * latent_bf16        bf16 [num_tokens, row_stride_elems], first latent_dim used
+ * num_tokens         >= 0
+ * latent_dim         must be 512
+ * row_stride_elems   >= latent_dim, multiple of 8
+ * slot_mapping       int64 [num_tokens]
+ * cache              uint8, this layer's view: block b starts at row
+ *                    b*block_stride_rows (rows of 272 bytes)
+ * num_blocks         >= 1
+ * block_size         >= 1 slots per block
+ * block_stride_rows  >= block_size (larger when other layers' pages sit
+ *                    between this layer's blocks); a flat cache of N rows is
+ *                    num_blocks = 1, block_size = block_stride_rows = N
+ * group              must be 32 (the OCP MX block size)
+ */
+int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int64_t latent_dim,
+                    int64_t row_stride_elems, const int64_t* slot_mapping, uint8_t* cache,
+                    int64_t num_blocks, int64_t block_size, int64_t block_stride_rows,
+                    int32_t group, cudaStream_t stream);
+
+/*
+ * rope_quant_insert_mxfp8 — V4.1 528-byte record: GPT-J RoPE, then MXFP8.
+ * [v41] _rope_quant_insert_mxfp8_kernel, rope_quant_insert.
+ *
+ * For each token t with slot s = cache_slots[t] and position p = positions[t]:
+ *   - skipped if s < 0, s >= num_pages*cache_block, p < 0,
+ *     (p + 1) % compress_ratio != 0, or the table row
+ *     r = (p / compress_ratio) * compress_ratio is >= cos_sin_rows.
+ *   - otherwise the 512 bf16 values are widened to binary32 and pair i
+ *     (elements 2i, 2i+1) is rotated to (e*c - o*s, o*c + e*s), each product
+ *     and sum rounded separately (no fused multiply-add), with
+ *     c = cos_sin[r*cos_stride + i-224], s = cos_sin[r*cos_stride + 32 + i-224]
+ *     for i >= 224 and c = 1, s = 0 for i < 224. If sanitize_nans, NaN
+ *     results become +0.0.
+ *   - per group of 32: amax = max(largest |x| ignoring NaN, 1e-4f),
+ *     e = ceil(log2(amax * (1/448.f))) exactly, values E4M3(x * 2**-e)
+ *     clamped to +-448 and rounded to nearest even (NaN -> 0x7F), scale byte
+ *     clamp(e + 127, 0, sanitize_nans ? 254 : 255).
+ *   - page P = s / cache_block starts at cache + P*page_stride_bytes; the 512
+ *     value bytes go to page + (s % cache_block)*512 and the 16 scale bytes to
+ *     page + cache_block*512 + (s % cache_block)*16.
+ *
+ * latent_bf16       bf16 [num_tokens, row_stride_elems], 512 used
+ * positions         int64 [num_tokens]
+ * cos_sin           float32 [cos_sin_rows, cos_stride], 32 cos then 32 sin
+ * cos_stride        >= 64, multiple of 4
+ * cache             uint8, num_pages pages of page_stride_bytes
+ * cache_slots       int64 [num_tokens]
+ * cache_block       >= 1 slots per page
+ * page_stride_bytes >= cache_block*528, multiple of 16
+ * compress_ratio    >= 1
+ * sanitize_nans     0 or 1
+ */
+int rope_quant_insert_mxfp8(const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
+                            const int64_t* positions, const float* cos_sin, int64_t cos_stride,
+                            int64_t cos_sin_rows, uint8_t* cache, const int64_t* cache_slots,
+                            int64_t num_pages, int64_t cache_block, int64_t page_stride_bytes,
+                            int32_t compress_ratio, int32_t sanitize_nans, cudaStream_t stream);
+
+/*
+ * rope_quant_insert_nvfp4 — V4.1 288-byte NVFP4 record: GPT-J RoPE, then E2M1
+ * with one E4M3 scale per 16 values. [v41] _rope_quant_insert_nvfp4_kernel.
+ *
+ * Gates, rotation and sanitising as rope_quant_insert_mxfp8. Per tile of 16:
+ * amax = largest |x| ignoring NaN; sc = E4M3(clamp(amax * (1/6.f), 2**-9,
+ * 448)) rounded to nearest even; each value becomes the E2M1 code (same rule
+ * as mxfp4_mla_store) of the correctly rounded binary32 quotient x / sc. Codes
+ * pack two per byte, even element in the low nibble: 256 code bytes at
+ * page + (s % cache_block)*256, then the 32 E4M3 scale bytes at
+ * page + cache_block*256 + (s % cache_block)*32.
+ * page_stride_bytes must be >= cache_block*288 and a multiple of 16.
+ */
+int rope_quant_insert_nvfp4(const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
+                            const int64_t* positions, const float* cos_sin, int64_t cos_stride,
+                            int64_t cos_sin_rows, uint8_t* cache, const int64_t* cache_slots,
+                            int64_t num_pages, int64_t cache_block, int64_t page_stride_bytes,
+                            int32_t compress_ratio, int32_t sanitize_nans, cudaStream_t stream);
+
+/*
+ * mxfp4_mla_gather_dequant — read packed MXFP4 rows back to bf16.
+ * [pr] Details (read path: gathered rows are unpacked to bf16 before use);
+ * [pr] Claims (attention over the packed cache equals attention over these
+ * dequantized values stored as bf16).
+ *
+ * For each k in [0, num_indices) with s = indices[k]: if 0 <= s <
+ * num_blocks*block_size, the 272-byte row of slot s (addressed as in
+ * mxfp4_mla_store) becomes 512 bf16 values
+ *   out[k*out_row_stride_elems + j] = E2M1(code_j) * 2**(scale_byte - 127),
+ * exact in bf16 (byte 254 with magnitude >= 2 gives +-inf; byte 255, the
+ * E8M0 NaN, gives 0x7FC0 for the whole group). Otherwise (a -1 pad, or an
+ * index outside the cache) the output row is 512 x +0.0.
+ *
+ * latent_dim must be 512; out_row_stride_elems >= 512, multiple of 8.
+ */
+int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks, int64_t block_size,
+                             int64_t block_stride_rows, int64_t latent_dim, const int64_t* indices,
+                             int64_t num_indices, void* out_bf16, int64_t out_row_stride_elems,
+                             cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

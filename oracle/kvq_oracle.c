@@ -315,6 +315,10 @@ static int64_t rope_gate(int64_t slot, int64_t position, int64_t num_pages, int6
                          int32_t compress_ratio, int64_t cos_sin_rows) {
     if (slot < 0 || slot >= num_pages * cache_block) return -1;
     if (position < 0) return -1;
+    /* A table row is at least position - (R - 1), so position - R >= rows can
+     * only give a row past the table; testing it first keeps position + 1
+     * from overflowing and changes no result. */
+    if (position - compress_ratio >= cos_sin_rows) return -1;
     if ((position + 1) % compress_ratio != 0) return -1;
     int64_t table_row = (position / compress_ratio) * compress_ratio;
     if (table_row >= cos_sin_rows) return -1;

@@ -1,0 +1,100 @@
+"""CPU-only checks of the C ABI: the CUDA library builds for sm_103a, loads,
+exports every function include/kvq.h declares, and rejects bad arguments on
+the host before any CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import fp8_quantized_paged_store_gb300 as kvq
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    return kvq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert set(names) == {"kvq_strerror", "kvq_row_bytes", "mxfp4_mla_store",
+                          "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
+                          "mxfp4_mla_gather_dequant"}
+    for n in names:
+        assert hasattr(L, n), n
+    # exported with C linkage from the shared object itself
+    lib = ctypes.CDLL(kvq.LIBRARY_PATH)
+    for n in names:
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_row_bytes_and_strerror(L):
+    assert kvq.row_bytes(512, 32) == 272
+    assert L.kvq_row_bytes(1024, 32) == 544
+    assert L.kvq_row_bytes(512, 0) == -1 and L.kvq_row_bytes(500, 32) == -1
+    assert L.kvq_row_bytes(512, 3) == -1
+    assert b"success" in L.kvq_strerror(0)
+    assert b"invalid" in L.kvq_strerror(-1) and b"launch" in L.kvq_strerror(-2)
+    assert b"unknown" in L.kvq_strerror(7)
+
+
+# Fake device addresses: never dereferenced, because every case below is
+# rejected (or returns for an empty batch) before anything is launched.
+A16, A8 = 0x7F0000000000, 0x7F0000001000
+
+
+def test_store_validation_on_host(L):
+    f = L.mxfp4_mla_store
+    ok = [A16, 4, 512, 512, A8, A16, 1, 8, 8, 32, None]
+    assert f(*[A16, 0, 512, 512, None, None, 1, 8, 8, 32, None]) == 0   # empty batch
+    cases = {2: 256, 3: 500, 9: 16}                                      # dim, stride, group
+    for i, v in cases.items():
+        a = list(ok); a[i] = v
+        assert f(*a) == -1, (i, v)
+    for i, v in {1: -1, 6: 0, 7: 0, 8: 7, 0: A16 + 2, 4: A8 + 4, 5: A16 + 8, 3: 516}.items():
+        a = list(ok); a[i] = v
+        assert f(*a) == -1, (i, v)
+    a = list(ok); a[0] = None
+    assert f(*a) == -1
+    a = list(ok); a[6] = 2 ** 62
+    assert f(*a) == -1                                                   # view overflows int64
+
+
+def test_insert_validation_on_host(L):
+    for f, rec in ((L.rope_quant_insert_mxfp8, 528), (L.rope_quant_insert_nvfp4, 288)):
+        ok = [A16, 4, 512, A8, A16, 64, 10, A16, A8, 2, 64, 64 * rec, 4, 0, None]
+        empty = list(ok); empty[1] = 0; empty[0] = None
+        assert f(*empty) == 0
+        bad = {1: -3, 2: 500, 5: 62, 5.1: 66, 6: 0, 9: 0, 10: 0, 11: 64 * rec - 16,
+               11.1: 64 * rec + 8, 12: 0, 13: 2, 0: A16 + 8, 4: A16 + 4, 7: A16 + 1, 3: A8 + 1}
+        for k, v in bad.items():
+            a = list(ok); a[int(k)] = v
+            assert f(*a) == -1, (rec, k, v)
+
+
+def test_gather_validation_on_host(L):
+    f = L.mxfp4_mla_gather_dequant
+    ok = [A16, 1, 8, 8, 512, A8, 4, A16, 512, None]
+    empty = list(ok); empty[6] = 0; empty[5] = None
+    assert f(*empty) == 0
+    for k, v in {4: 256, 8: 500, 8.1: 516, 1: 0, 3: 7, 6: -1, 0: A16 + 4, 7: A16 + 2,
+                 5: A8 + 2}.items():
+        a = list(ok); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
+
+
+def test_binding_has_the_abi_names():
+    for n in ("mxfp4_mla_store", "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
+              "mxfp4_mla_gather_dequant"):
+        assert callable(getattr(kvq, n))
