@@ -412,6 +412,58 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """One kernel on a reduced case, for Nsight Compute: inputs still larger
+    than L2, a few hundred MB on the device. Prints per-launch times."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import fp8_quantized_paged_store_gb300 as kvq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = args.profile_tokens
+    if args.profile == "store":
+        lat = workloads.store_large_latent(seed=0, num_tokens=n, row_stride=ROW_STRIDE)
+        slots = workloads.store_large_slots(seed=0, num_tokens=n, num_slots=2 * n)
+        lat_d = torch.from_numpy(lat.view(np.int16)).to(dev).view(torch.bfloat16)[:, :512]
+        slots_d = torch.from_numpy(slots).to(dev)
+        cache = torch.full((2 * n * ROW,), 0xAA, dtype=torch.uint8, device=dev)
+        call = lambda: kvq.mxfp4_mla_store(lat_d, slots_d, cache)  # noqa: E731
+        valid = int(np.sum(slots >= 0))
+        algo = sum(store_bytes(n, valid))
+    elif args.profile in ("rope_mxfp8", "rope_nvfp4"):
+        record = args.profile[5:]
+        width = 528 if record == "mxfp8" else 288
+        w = workloads.rope_insert(seed=0, num_tokens=n, num_pages=n // 64, record=record)
+        lat_d = torch.from_numpy(w["latent"].view(np.int16)).to(dev).view(torch.bfloat16)
+        pos = torch.from_numpy(w["positions"]).to(dev)
+        tab = torch.from_numpy(w["cos_sin"]).to(dev)
+        sl = torch.from_numpy(w["cache_slots"]).to(dev)
+        cache = torch.from_numpy(w["cache"]).to(dev).view(n // 64, 64, width)
+        fn = getattr(kvq, f"rope_quant_insert_{record}")
+        call = lambda: fn(lat_d, pos, tab, cache, sl, 4)  # noqa: E731
+        writers = int(np.sum((w["cache_slots"] >= 0) & ((w["positions"] + 1) % 4 == 0)))
+        algo = 16 * n + writers * (1024 + 256 + width)
+    else:
+        g = workloads.gather(seed=0)
+        lat_d = torch.from_numpy(g["fill_latent"].view(np.int16)).to(dev).view(torch.bfloat16)
+        cache = torch.empty(g["num_slots"] * ROW, dtype=torch.uint8, device=dev)
+        kvq.mxfp4_mla_store(lat_d, torch.from_numpy(g["fill_slots"]).to(dev), cache)
+        idx = torch.from_numpy(g["indices"]).to(dev)
+        out = torch.empty((idx.numel(), 512), dtype=torch.bfloat16, device=dev)
+        call = lambda: kvq.mxfp4_mla_gather_dequant(cache, idx, out=out)  # noqa: E731
+        valid = int(np.sum(g["indices"] >= 0))
+        algo = 8 * idx.numel() + ROW * valid + 1024 * idx.numel()
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ms, times = time_events(torch, call, args.steps, torch.cuda.current_stream())
+    print(json.dumps({"profile": args.profile, "units": n, "algorithmic_bytes": algo,
+                      "mean_ms": ms, "gbs": algo / (ms * 1e-3) / 1e9, "times_ms": times}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,9 +473,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the secondary RoPE-insert and gather measurements")
+    ap.add_argument("--profile", choices=["store", "rope_mxfp8", "rope_nvfp4", "gather"],
+                    help="run one kernel on a reduced case (for Nsight Compute) and exit")
+    ap.add_argument("--profile-tokens", type=int, default=400_000)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         world, rank, _ = dist_env()
         if rank != 0:

@@ -79,6 +79,50 @@ __device__ __forceinline__ void st_u8(void* p, uint32_t v) {
   asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// ------------------------------------------------------------- cp.async ---
+
+// 16-byte asynchronous global -> shared copy, L2 only. Completion is tracked
+// per thread with commit groups, so a thread that later reads back only the
+// bytes it copied needs no barrier besides cp.async.wait_group.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most n of this thread's most recent commit groups are pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(const uint4* p) {
+  uint4 r;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(a)
+               : "memory");
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(const void* p) {
+  uint32_t r;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a) : "memory");
+  return r;
+}
+
+__device__ __forceinline__ uint32_t lds_u8(const void* p) {
+  uint32_t r;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(r) : "r"(a) : "memory");
+  return r;
+}
+
 // ------------------------------------------------------------ bf16 words ---
 
 // Low / high bf16 of a bf16x2 word widened to binary32 (exact).
@@ -90,6 +134,13 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// As bf16x2_maxabs, but NaN-propagating: a half is NaN if either input is.
+__device__ __forceinline__ uint32_t bf16x2_maxabs_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 

@@ -30,12 +30,12 @@ inline int sm_count() {
 // Blocks of a kernel that fit on one SM at once (queried once per kernel and
 // device through the occupancy calculator).
 template <typename Kernel>
-inline int resident_blocks_per_sm(Kernel kernel, int threads, int* cache64) {
+inline int resident_blocks_per_sm(Kernel kernel, int threads, size_t dynamic_smem, int* cache64) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (cache64[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, dynamic_smem) != cudaSuccess ||
         n <= 0)
       n = 1;
     cache64[dev] = n;

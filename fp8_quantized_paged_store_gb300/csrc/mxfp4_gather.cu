@@ -18,12 +18,13 @@
 // Scale bytes 0, 1, 253, 254 (subnormal or overflowing results) and 255 (the
 // E8M0 NaN) take an arithmetic path.
 //
-// Work decomposition: one warp per output row, 32 indices per chunk (lane i
-// loads index i and turns it into a source offset once), two rows in flight.
-// Lane l reads code bytes 4l..4l+3 and 128+4l..128+4l+3 (two coalesced
-// 128-byte warp loads) and the scale bytes of groups l/4 and 8+l/4, and
-// writes 16 bytes at elements 8l and 256+8l (two coalesced 512-byte stores).
-// Pads and out-of-range indices write zeros.
+// Work decomposition: one wave of 256-thread blocks, each warp a contiguous
+// range of output rows; indices 32 at a time (lane i loads index i and turns
+// it into a source row once); packed rows staged through a per-warp
+// cp.async ring seven rows ahead. Lane l decodes code bytes 4l..4l+3 and
+// 128+4l..128+4l+3 with the scale bytes of groups l/4 and 8+l/4, and writes
+// 16 bytes at elements 8l and 256+8l (two coalesced 512-byte stores). Pads
+// and out-of-range indices write zeros.
 #include <cstdint>
 
 #include "kvq.h"
@@ -112,10 +113,16 @@ __device__ __noinline__ uint4 decode8_slow(uint32_t c, uint32_t scale_byte) {
                     h[6] | (h[7] << 16));
 }
 
-// Eight codes of one group -> 16 bytes of bf16.
-__device__ __forceinline__ uint4 decode8(uint32_t c, uint32_t scale_byte) {
+// Eight codes of one group -> 16 bytes of bf16. `lut` holds make_tables(b)
+// for every scale byte b in [2, 252] (built once per block).
+__device__ __forceinline__ uint4 decode8(uint32_t c, uint32_t scale_byte, const uint4* lut) {
   if (scale_byte - 2u > 250u) return decode8_slow(c, scale_byte);
-  const ByteTables t = make_tables(scale_byte);
+  const uint4 v = lds_v4(lut + scale_byte);
+  ByteTables t;
+  t.lo_a = v.x;
+  t.hi_a = v.y;
+  t.lo_b = v.z;
+  t.hi_b = v.w;
   const uint32_t c4 = c << 4;
   uint4 r;
   decode4<0>(c, c4, t, r.x, r.y);
@@ -123,57 +130,98 @@ __device__ __forceinline__ uint4 decode8(uint32_t c, uint32_t scale_byte) {
   return r;
 }
 
+constexpr int kGatherPrefetch = 7;  // rows per warp in flight
+constexpr int kGatherStages = 8;    // a power of two: stage = row & 7
+constexpr int kStagePitch = 288;    // 272-byte row, 16-byte multiple
+constexpr int kLutBytes = 256 * 16;
+constexpr size_t kGatherSmem =
+    (size_t)kLutBytes + (size_t)kGatherWarps * kGatherStages * kStagePitch;
+
+// Row index (272-byte rows from the view's base) of output row k, or
+// 0xFFFFFFFF for a zero row (pad, outside the cache, past the range). The
+// host guarantees that row indices fit in 32 bits.
+template <bool kFlat>
+__device__ __forceinline__ uint32_t src_row(const GatherParams& p, int64_t k, int64_t k_end) {
+  if (k >= k_end) return 0xFFFFFFFFu;
+  const int64_t s = ld_once_i64(p.indices + k);
+  if (s < 0 || s >= p.num_slots) return 0xFFFFFFFFu;
+  if (kFlat) return (uint32_t)s;
+  int64_t blk, in_blk;
+  divmod_pos(s, p.block_size, blk, in_blk);
+  return (uint32_t)(blk * p.block_stride_rows + in_blk);
+}
+
+// Each warp owns a contiguous range of output rows. Packed rows stream
+// through a per-warp shared-memory ring: lanes 0..16 copy the 272 bytes of
+// the row kGatherPrefetch ahead (17 x 16-byte cp.async); after its own copies
+// land, __syncwarp makes the other lanes' bytes visible, and a second
+// __syncwarp before each refill keeps a stage from being overwritten while a
+// lane still reads it. The block first fills the table of byte-permute
+// tables, one 16-byte entry per scale byte (the one block-wide barrier).
 template <bool kFlat>
 __global__ void __launch_bounds__(kGatherThreads) mxfp4_gather_kernel(GatherParams p) {
+  extern __shared__ uint4 smem[];
+  uint4* lut = smem;
+  if (threadIdx.x >= 2 && threadIdx.x <= 252) {
+    const ByteTables t = make_tables(threadIdx.x);
+    lut[threadIdx.x] = make_uint4(t.lo_a, t.hi_a, t.lo_b, t.hi_b);
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kGatherThreads + threadIdx.x) >> 5;
-  const int64_t num_warps = ((int64_t)gridDim.x * kGatherThreads) >> 5;
+  const int warp_in_block = threadIdx.x >> 5;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(smem) + kLutBytes +
+                  warp_in_block * (kGatherStages * kStagePitch);
+  const int64_t warp = (int64_t)blockIdx.x * kGatherWarps + warp_in_block;
+  const int64_t num_warps = (int64_t)gridDim.x * kGatherWarps;
+  const int64_t k_begin = p.num_indices * warp / num_warps;
+  const int64_t k_end = p.num_indices * (warp + 1) / num_warps;
+  const int n = (int)(k_end - k_begin);  // < 2**31, checked at launch
+  if (n <= 0) return;
   const uint4 zero = make_uint4(0, 0, 0, 0);
+  uint8_t* out_base = p.out + k_begin * p.out_pitch + 16 * lane;
+  const uint32_t pitch = (uint32_t)p.out_pitch;
+  const uint8_t* cache_lane = p.cache + 16 * lane;
 
-  for (int64_t base = warp * 32; base < p.num_indices; base += num_warps * 32) {
-    int64_t src_off = -1;
-    if (base + lane < p.num_indices) {
-      const int64_t s = ld_once_i64(p.indices + base + lane);
-      if (s >= 0 && s < p.num_slots) {
-        if (kFlat) {
-          src_off = s * kMxfp4RowBytes;
-        } else {
-          int64_t blk, in_blk;
-          divmod_pos(s, p.block_size, blk, in_blk);
-          src_off = (blk * p.block_stride_rows + in_blk) * kMxfp4RowBytes;
-        }
-      }
+  auto issue = [&](int i, uint32_t row) {
+    if (row != 0xFFFFFFFFu && lane < 17)
+      cp_async_16(ring + (i & (kGatherStages - 1)) * kStagePitch + 16 * lane,
+                  cache_lane + (size_t)row * kMxfp4RowBytes);
+    cp_async_commit();
+  };
+
+  uint32_t w0 = src_row<kFlat>(p, k_begin + lane, k_end);
+  uint32_t w1 = src_row<kFlat>(p, k_begin + 32 + lane, k_end);
+#pragma unroll
+  for (int d = 0; d < kGatherPrefetch; ++d) issue(d, __shfl_sync(0xFFFFFFFFu, w0, d));
+
+  for (int i = 0; i < n; ++i) {
+    const int k = i & 31;
+    if (k == 0 && i > 0) {
+      w0 = w1;
+      w1 = src_row<kFlat>(p, k_begin + i + 32 + lane, k_end);
     }
-    const int n = (int)min((int64_t)32, p.num_indices - base);
-    for (int i = 0; i < n; i += 2) {
-      const int64_t s0 = __shfl_sync(0xFFFFFFFFu, src_off, i);
-      const int64_t s1 = __shfl_sync(0xFFFFFFFFu, src_off, (i + 1) & 31);
-      const bool has1 = i + 1 < n;
-      uint8_t* o0 = p.out + (base + i) * p.out_pitch;
-      uint8_t* o1 = o0 + p.out_pitch;
-      uint32_t c00 = 0, c01 = 0, b00 = 0, b01 = 0, c10 = 0, c11 = 0, b10 = 0, b11 = 0;
-      if (s0 >= 0) {
-        const uint8_t* r = p.cache + s0;
-        c00 = ld_u32(r + 4 * lane);
-        c01 = ld_u32(r + 128 + 4 * lane);
-        b00 = ld_u8(r + 256 + (lane >> 2));
-        b01 = ld_u8(r + 264 + (lane >> 2));
-      }
-      if (has1 && s1 >= 0) {
-        const uint8_t* r = p.cache + s1;
-        c10 = ld_u32(r + 4 * lane);
-        c11 = ld_u32(r + 128 + 4 * lane);
-        b10 = ld_u8(r + 256 + (lane >> 2));
-        b11 = ld_u8(r + 264 + (lane >> 2));
-      }
-      st_v4(o0 + 16 * lane, s0 >= 0 ? decode8(c00, b00) : zero);
-      st_v4(o0 + 512 + 16 * lane, s0 >= 0 ? decode8(c01, b01) : zero);
-      if (has1) {
-        st_v4(o1 + 16 * lane, s1 >= 0 ? decode8(c10, b10) : zero);
-        st_v4(o1 + 512 + 16 * lane, s1 >= 0 ? decode8(c11, b11) : zero);
-      }
+    const int kp = k + kGatherPrefetch;
+    const uint32_t rp = __shfl_sync(0xFFFFFFFFu, kp < 32 ? w0 : w1, kp & 31);
+    __syncwarp();  // every lane is done with the stage about to be refilled
+    issue(i + kGatherPrefetch, i + kGatherPrefetch < n ? rp : 0xFFFFFFFFu);
+    cp_async_wait<kGatherPrefetch>();
+    __syncwarp();  // row i's bytes from all 17 copying lanes are visible
+    const uint32_t row = __shfl_sync(0xFFFFFFFFu, w0, k);
+    uint8_t* out = out_base + (size_t)i * pitch;
+    if (row != 0xFFFFFFFFu) {
+      const uint8_t* r = ring + (i & (kGatherStages - 1)) * kStagePitch;
+      const uint32_t c0 = lds_u32(r + 4 * lane);
+      const uint32_t c1 = lds_u32(r + 128 + 4 * lane);
+      const uint32_t b0 = lds_u8(r + 256 + (lane >> 2));
+      const uint32_t b1 = lds_u8(r + 264 + (lane >> 2));
+      st_v4(out, decode8(c0, b0, lut));
+      st_v4(out + 512, decode8(c1, b1, lut));
+    } else {
+      st_v4(out, zero);
+      st_v4(out + 512, zero);
     }
   }
+  cp_async_wait<0>();
 }
 
 int g_gather_occupancy[2][64];
@@ -194,6 +242,9 @@ extern "C" int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks
   if (num_blocks > INT64_MAX / block_stride_rows / kMxfp4RowBytes) return KVQ_EINVAL;
   if (num_blocks > INT64_MAX / block_size) return KVQ_EINVAL;
   if (num_indices > INT64_MAX / 2 / out_row_stride_elems) return KVQ_EINVAL;
+  // cache rows are addressed with 32-bit indices (2**32 rows would be 1.1 TB)
+  if ((num_blocks - 1) * block_stride_rows + block_size > (int64_t)0xFFFFFFFE) return KVQ_EINVAL;
+  if (out_row_stride_elems * 2 > (int64_t)0xFFFFFFFF) return KVQ_EINVAL;
   if (num_indices == 0) return KVQ_OK;
   if (!cache || !indices || !out_bf16) return KVQ_EINVAL;
   if (!aligned(cache, 16) || !aligned(out_bf16, 16) || !aligned(indices, 8)) return KVQ_EINVAL;
@@ -209,18 +260,12 @@ extern "C" int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks
   p.out_pitch = out_row_stride_elems * 2;
 
   const bool flat = (num_blocks == 1) || (block_stride_rows == block_size);
-  const int64_t chunks = (num_indices + 31) / 32;
-  const int64_t work_blocks = (chunks + kGatherWarps - 1) / kGatherWarps;
-  if (flat) {
-    auto k = mxfp4_gather_kernel<true>;
-    const unsigned grid =
-        grid_for(work_blocks, resident_blocks_per_sm(k, kGatherThreads, g_gather_occupancy[1]));
-    k<<<grid, kGatherThreads, 0, stream>>>(p);
-  } else {
-    auto k = mxfp4_gather_kernel<false>;
-    const unsigned grid =
-        grid_for(work_blocks, resident_blocks_per_sm(k, kGatherThreads, g_gather_occupancy[0]));
-    k<<<grid, kGatherThreads, 0, stream>>>(p);
-  }
+  const int64_t work_blocks = (num_indices + 32 * kGatherWarps - 1) / (32 * kGatherWarps);
+  auto k = flat ? mxfp4_gather_kernel<true> : mxfp4_gather_kernel<false>;
+  const unsigned grid = grid_for(
+      work_blocks, resident_blocks_per_sm(k, kGatherThreads, kGatherSmem, g_gather_occupancy[flat]));
+  // each warp's row count must fit the kernel's 32-bit loop counter
+  if (num_indices / ((int64_t)grid * kGatherWarps) >= (int64_t)0x7FFFFFFF) return KVQ_EINVAL;
+  k<<<grid, kGatherThreads, kGatherSmem, stream>>>(p);
   return launch_status();
 }

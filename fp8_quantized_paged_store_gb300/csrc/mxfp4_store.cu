@@ -6,13 +6,14 @@
 // for rope-free sparse MLA" (Details: format and write path).
 //
 // Work decomposition (GB300: 152 SMs, HBM-bound streaming codec):
-//   * one warp owns 32 consecutive tokens at a time (grid-stride over chunks);
-//     lane i loads slot_mapping of token i once and turns it into the row's
-//     byte offset (one division per lane per chunk, not per row);
-//   * a ballot lists the chunk's valid tokens, so pads cost no row traffic;
-//   * rows are processed two at a time, both rows' loads issued first; one
-//     row is 1 KiB read as two fully coalesced 512-byte warp loads: lane l
-//     holds elements 8l..8l+7 (half 0, groups 0..7) and 256+8l..256+8l+7
+//   * one wave of 256-thread blocks; each warp owns a contiguous token range;
+//   * lane i reads slot_mapping of token i of a 32-token window once and turns
+//     it into the row's byte offset (one division per lane per window);
+//   * rows stream through a per-warp shared-memory ring filled by cp.async
+//     four rows ahead of the row being quantized (pad tokens issue no copy),
+//     which keeps ~160 KiB of loads in flight per SM;
+//   * one row is 1 KiB read as two fully coalesced 512-byte warp copies: lane
+//     l holds elements 8l..8l+7 (half 0, groups 0..7) and 256+8l..256+8l+7
 //     (half 1, groups 8..15), so a 32-element group spans four lanes;
 //   * group amax: bf16x2 max-of-magnitudes (NaN ignored) within the lane, then
 //     two xor-shuffles across the four lanes, both halves packed in one word;
@@ -45,47 +46,79 @@ struct StoreParams {
 };
 
 // Eight bf16 (one 16-byte load) of a group with scale 2**e -> eight E2M1
-// codes. NaN and -0.0 are turned into +0.0 first: the conversion would give
-// them codes 7 and 8, the E2M1 rule gives both code 0. A product can only
-// underflow to -0.0 (which the rule also codes 0) when e >= 17, since the
-// smallest bf16 magnitude is 2**-133; kGuard adds +0.0 after the product for
-// that case, turning -0.0 into +0.0 and changing nothing else.
-template <bool kGuard>
+// codes, element k in bits 4k+3:4k.
+//
+// The conversion takes the sign from the sign bit (-0.0 -> code 8) and maps
+// NaN to code 7, where the E2M1 rule gives both code 0. Fast path (the row
+// holds no NaN or infinity and every group exponent is <= 16): the scaled
+// value is fma(x, 2**-e, +0.0), which equals RN(x * 2**-e) except that -0.0
+// becomes +0.0; a product of a non-zero bf16 (magnitude >= 2**-133) and
+// 2**-e >= 2**-16 never underflows to zero, so no other -0.0 can appear.
+// Special path: NaN and -0.0 inputs are cleared to +0.0 first, the product is
+// rounded on its own and then +0.0 is added, which turns an underflowed
+// -0.0 (possible when e >= 17) into +0.0 and changes nothing else.
+template <bool kSpecial>
 __device__ __forceinline__ uint32_t encode8(uint4 w, float inv_scale) {
-  w.x &= bf16x2_nonzero_number_mask(w.x);
-  w.y &= bf16x2_nonzero_number_mask(w.y);
-  w.z &= bf16x2_nonzero_number_mask(w.z);
-  w.w &= bf16x2_nonzero_number_mask(w.w);
+  if (kSpecial) {
+    w.x &= bf16x2_nonzero_number_mask(w.x);
+    w.y &= bf16x2_nonzero_number_mask(w.y);
+    w.z &= bf16x2_nonzero_number_mask(w.z);
+    w.w &= bf16x2_nonzero_number_mask(w.w);
+  }
   float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                 bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    f[k] = __fmul_rn(f[k], inv_scale);
-    if (kGuard) f[k] = __fadd_rn(f[k], 0.0f);
-  }
+  for (int k = 0; k < 8; ++k)
+    f[k] = kSpecial ? __fadd_rn(__fmul_rn(f[k], inv_scale), 0.0f)
+                    : __fmaf_rn(f[k], inv_scale, 0.0f);
   return cvt_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+}
+
+// Per-lane |amax| of a half row as bf16 bits, in the low (half 0) and high
+// (half 1) 16 bits, folded over the four lanes of each group.
+template <bool kNanPropagating>
+__device__ __forceinline__ uint32_t group_amax2(uint4 x0, uint4 x1) {
+  auto mx = [](uint32_t a, uint32_t b) {
+    return kNanPropagating ? bf16x2_maxabs_nan(a, b) : bf16x2_maxabs(a, b);
+  };
+  const uint32_t m0 = mx(mx(x0.x, x0.y), mx(x0.z, x0.w));
+  const uint32_t m1 = mx(mx(x1.x, x1.y), mx(x1.z, x1.w));
+  uint32_t g = mx(__byte_perm(m0, m1, 0x5410), __byte_perm(m0, m1, 0x7632));
+  g &= 0x7FFF7FFFu;
+  auto mg = [](uint32_t a, uint32_t b) {
+    return kNanPropagating ? bf16x2_maxabs_nan(a, b) : bf16x2_max(a, b);
+  };
+  g = mg(g, __shfl_xor_sync(0xFFFFFFFFu, g, 1));
+  g = mg(g, __shfl_xor_sync(0xFFFFFFFFu, g, 2));
+  return g & 0x7FFF7FFFu;
+}
+
+// Group exponent for a finite amax (bf16 bits a < 0x7F80): the closed form of
+// mxfp4_group_exponent without its NaN and infinity cases. (a + 0x3F) >> 7
+// adds 1 to the exponent field exactly when the 7-bit mantissa exceeds 0x40.
+__device__ __forceinline__ int finite_group_exponent(uint32_t a) {
+  const int e = (int)((a + 0x3Fu) >> 7) - 129;
+  return a == 0u ? 0 : (e < -126 ? -126 : e);
 }
 
 // Quantize one row held by the warp (x0: half 0, x1: half 1) and write its 272
 // bytes at dst.
 __device__ __forceinline__ void quantize_store_row(uint4 x0, uint4 x1, uint8_t* dst, int lane) {
-  uint32_t m0 = bf16x2_maxabs(bf16x2_maxabs(x0.x, x0.y), bf16x2_maxabs(x0.z, x0.w));
-  uint32_t m1 = bf16x2_maxabs(bf16x2_maxabs(x1.x, x1.y), bf16x2_maxabs(x1.z, x1.w));
-  // [half 0 | half 1] in the low / high 16 bits, then fold even and odd.
-  uint32_t g = bf16x2_maxabs(__byte_perm(m0, m1, 0x5410), __byte_perm(m0, m1, 0x7632));
-  g &= 0x7FFF7FFFu;
-  g = bf16x2_max(g, __shfl_xor_sync(0xFFFFFFFFu, g, 1));
-  g = bf16x2_max(g, __shfl_xor_sync(0xFFFFFFFFu, g, 2));
-  const int e0 = mxfp4_group_exponent(g & 0xFFFFu);  // group lane/4
-  const int e1 = mxfp4_group_exponent(g >> 16);      // group 8 + lane/4
-  const float s0 = exp2_neg(e0), s1 = exp2_neg(e1);
+  const uint32_t g = group_amax2<true>(x0, x1);
+  const uint32_t a0 = g & 0xFFFFu, a1 = g >> 16;
+  int e0 = finite_group_exponent(a0);  // group lane/4
+  int e1 = finite_group_exponent(a1);  // group 8 + lane/4
   uint32_t c0, c1;
-  if (__any_sync(0xFFFFFFFFu, (e0 > 16) | (e1 > 16))) {
-    c0 = encode8<true>(x0, s0);
-    c1 = encode8<true>(x1, s1);
+  const bool special = (a0 >= 0x7F80u) | (a1 >= 0x7F80u) | (e0 > 16) | (e1 > 16);
+  if (__any_sync(0xFFFFFFFFu, special)) {
+    const uint32_t gi = group_amax2<false>(x0, x1);  // NaN ignored
+    e0 = mxfp4_group_exponent(gi & 0xFFFFu);
+    e1 = mxfp4_group_exponent(gi >> 16);
+    c0 = encode8<true>(x0, exp2_neg(e0));
+    c1 = encode8<true>(x1, exp2_neg(e1));
   } else {
-    c0 = encode8<false>(x0, s0);
-    c1 = encode8<false>(x1, s1);
+    c0 = encode8<false>(x0, __uint_as_float((uint32_t)(127 - e0) << 23));
+    c1 = encode8<false>(x1, __uint_as_float((uint32_t)(127 - e1) << 23));
   }
   st_u32(dst + 4 * lane, c0);
   st_u32(dst + 128 + 4 * lane, c1);
@@ -95,51 +128,90 @@ __device__ __forceinline__ void quantize_store_row(uint4 x0, uint4 x1, uint8_t* 
   }
 }
 
+// Prefetch distance (rows per warp in flight) and ring stages: one more stage
+// than the distance, so the copy issued at the top of an iteration never
+// lands in the stage being read in that iteration.
+constexpr int kPrefetch = 4;
+constexpr int kStages = kPrefetch + 1;
+constexpr int kStageVecs = 64;  // one 1 KiB row = 64 x 16 bytes
+constexpr size_t kStoreSmem = (size_t)kStoreWarps * kStages * kStageVecs * sizeof(uint4);
+
+// Cache row index of token t (rows of 272 bytes from the view's base), or
+// 0xFFFFFFFF to skip it (pad, outside the cache, or past the warp's range).
+// The host guarantees that row indices fit in 32 bits.
+template <bool kFlat>
+__device__ __forceinline__ uint32_t row_index(const StoreParams& p, int64_t t, int64_t t_end) {
+  if (t >= t_end) return 0xFFFFFFFFu;
+  const int64_t s = ld_once_i64(p.slots + t);
+  if (s < 0 || s >= p.num_slots) return 0xFFFFFFFFu;
+  if (kFlat) return (uint32_t)s;
+  int64_t blk, in_blk;
+  divmod_pos(s, p.block_size, blk, in_blk);
+  return (uint32_t)(blk * p.block_stride_rows + in_blk);
+}
+
+// Each warp owns a contiguous token range and streams its rows through a
+// per-warp shared-memory ring with cp.async, kPrefetch rows ahead of the row
+// it quantizes. Lane l copies, and later reads back, only bytes 16l..16l+15
+// and 512+16l..512+16l+15 of each row, so the per-thread commit groups alone
+// order the ring: no barrier and no spin-wait. Row indices come 32 tokens at
+// a time (lane i holds token base+i); the window after the current one is
+// loaded early so that prefetches crossing into it find their indices ready.
+// The loop is unrolled over the ring's stages so that stage offsets are
+// constants.
 template <bool kFlat>
 __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams p) {
+  extern __shared__ uint4 smem[];
   const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kStoreThreads + threadIdx.x) >> 5;
-  const int64_t num_warps = ((int64_t)gridDim.x * kStoreThreads) >> 5;
+  const int warp_in_block = threadIdx.x >> 5;
+  uint4* ring = smem + warp_in_block * (kStages * kStageVecs) + lane;
+  const int64_t warp = (int64_t)blockIdx.x * kStoreWarps + warp_in_block;
+  const int64_t num_warps = (int64_t)gridDim.x * kStoreWarps;
+  const int64_t t_begin = p.num_tokens * warp / num_warps;
+  const int64_t t_end = p.num_tokens * (warp + 1) / num_warps;
+  const int n = (int)(t_end - t_begin);  // < 2**31, checked at launch
+  if (n <= 0) return;
+  const uint8_t* src = p.latent + t_begin * p.row_pitch + 16 * lane;
+  const uint32_t pitch = (uint32_t)p.row_pitch;
 
-  for (int64_t base = warp * 32; base < p.num_tokens; base += num_warps * 32) {
-    // Lane i: token base+i -> byte offset of its cache row, or -1 to skip.
-    int64_t dst_off = -1;
-    if (base + lane < p.num_tokens) {
-      const int64_t s = ld_once_i64(p.slots + base + lane);
-      if (s >= 0 && s < p.num_slots) {
-        if (kFlat) {
-          dst_off = s * kMxfp4RowBytes;
-        } else {
-          int64_t blk, in_blk;
-          divmod_pos(s, p.block_size, blk, in_blk);
-          dst_off = (blk * p.block_stride_rows + in_blk) * kMxfp4RowBytes;
-        }
-      }
+  uint32_t w0 = row_index<kFlat>(p, t_begin + lane, t_end);       // tokens [0, 32)
+  uint32_t w1 = row_index<kFlat>(p, t_begin + 32 + lane, t_end);  // tokens [32, 64)
+
+  auto issue = [&](int i, int stage, uint32_t row) {
+    if (row != 0xFFFFFFFFu) {
+      const uint8_t* s = src + (size_t)i * pitch;
+      cp_async_16(ring + stage * kStageVecs, s);
+      cp_async_16(ring + stage * kStageVecs + 32, s + 512);
     }
-    uint32_t todo = __ballot_sync(0xFFFFFFFFu, dst_off >= 0);
-    while (todo) {
-      const int i0 = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const int i1 = todo ? __ffs(todo) - 1 : -1;
-      if (todo) todo &= todo - 1;
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int d = 0; d < kPrefetch; ++d) issue(d, d, __shfl_sync(0xFFFFFFFFu, w0, d));
 
-      const uint8_t* r0 = p.latent + (base + i0) * p.row_pitch;
-      const uint4 x00 = ld_once_v4(r0 + 16 * lane);
-      const uint4 x01 = ld_once_v4(r0 + 512 + 16 * lane);
-      uint4 x10 = make_uint4(0, 0, 0, 0), x11 = make_uint4(0, 0, 0, 0);
-      if (i1 >= 0) {
-        const uint8_t* r1 = p.latent + (base + i1) * p.row_pitch;
-        x10 = ld_once_v4(r1 + 16 * lane);
-        x11 = ld_once_v4(r1 + 512 + 16 * lane);
-      }
-      const int64_t d0 = __shfl_sync(0xFFFFFFFFu, dst_off, i0);
-      quantize_store_row(x00, x01, p.cache + d0, lane);
-      if (i1 >= 0) {
-        const int64_t d1 = __shfl_sync(0xFFFFFFFFu, dst_off, i1);
-        quantize_store_row(x10, x11, p.cache + d1, lane);
+  for (int i0 = 0; i0 < n; i0 += kStages) {
+#pragma unroll
+    for (int u = 0; u < kStages; ++u) {
+      const int i = i0 + u;
+      if (i < n) {
+        const int k = i & 31;
+        if (k == 0 && i > 0) {  // next window of 32 tokens
+          w0 = w1;
+          w1 = row_index<kFlat>(p, t_begin + i + 32 + lane, t_end);
+        }
+        // prefetch row i + kPrefetch into the stage read kPrefetch rows later
+        const int kp = k + kPrefetch;
+        const uint32_t rp = __shfl_sync(0xFFFFFFFFu, kp < 32 ? w0 : w1, kp & 31);
+        issue(i + kPrefetch, (u + kPrefetch) % kStages,
+              i + kPrefetch < n ? rp : 0xFFFFFFFFu);
+        cp_async_wait<kPrefetch>();  // row i has landed
+        const uint32_t row = __shfl_sync(0xFFFFFFFFu, w0, k);
+        if (row != 0xFFFFFFFFu)
+          quantize_store_row(lds_v4(ring + u * kStageVecs), lds_v4(ring + u * kStageVecs + 32),
+                             p.cache + (size_t)row * kMxfp4RowBytes, lane);
       }
     }
   }
+  cp_async_wait<0>();
 }
 
 int g_store_occupancy[2][64];
@@ -160,6 +232,9 @@ extern "C" int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int6
   if (num_blocks > INT64_MAX / block_stride_rows / kMxfp4RowBytes) return KVQ_EINVAL;
   if (num_blocks > INT64_MAX / block_size) return KVQ_EINVAL;
   if (num_tokens > INT64_MAX / 2 / row_stride_elems) return KVQ_EINVAL;
+  // cache rows are addressed with 32-bit indices (2**32 rows would be 1.1 TB)
+  if ((num_blocks - 1) * block_stride_rows + block_size > (int64_t)0xFFFFFFFE) return KVQ_EINVAL;
+  if (row_stride_elems * 2 > (int64_t)0xFFFFFFFF) return KVQ_EINVAL;
   if (num_tokens == 0) return KVQ_OK;
   if (!latent_bf16 || !slot_mapping || !cache) return KVQ_EINVAL;
   if (!aligned(latent_bf16, 16) || !aligned(cache, 16) || !aligned(slot_mapping, 8))
@@ -176,18 +251,13 @@ extern "C" int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int6
   p.block_stride_rows = block_stride_rows;
 
   const bool flat = (num_blocks == 1) || (block_stride_rows == block_size);
-  const int64_t chunks = (num_tokens + 31) / 32;
-  const int64_t work_blocks = (chunks + kStoreWarps - 1) / kStoreWarps;
-  if (flat) {
-    auto k = mxfp4_store_kernel<true>;
-    const unsigned grid =
-        grid_for(work_blocks, resident_blocks_per_sm(k, kStoreThreads, g_store_occupancy[1]));
-    k<<<grid, kStoreThreads, 0, stream>>>(p);
-  } else {
-    auto k = mxfp4_store_kernel<false>;
-    const unsigned grid =
-        grid_for(work_blocks, resident_blocks_per_sm(k, kStoreThreads, g_store_occupancy[0]));
-    k<<<grid, kStoreThreads, 0, stream>>>(p);
-  }
+  // at least 32 tokens per warp on average, at most one wave of blocks
+  const int64_t work_blocks = (num_tokens + 32 * kStoreWarps - 1) / (32 * kStoreWarps);
+  auto k = flat ? mxfp4_store_kernel<true> : mxfp4_store_kernel<false>;
+  const unsigned grid = grid_for(
+      work_blocks, resident_blocks_per_sm(k, kStoreThreads, kStoreSmem, g_store_occupancy[flat]));
+  // each warp's token count must fit the kernel's 32-bit loop counter
+  if (num_tokens / ((int64_t)grid * kStoreWarps) >= (int64_t)0x7FFFFFFF) return KVQ_EINVAL;
+  k<<<grid, kStoreThreads, kStoreSmem, stream>>>(p);
   return launch_status();
 }

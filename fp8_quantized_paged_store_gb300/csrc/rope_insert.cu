@@ -33,7 +33,7 @@
 namespace kvq {
 namespace {
 
-constexpr int kRopeWarps = 8;
+constexpr int kRopeWarps = 4;
 constexpr int kRopeThreads = 32 * kRopeWarps;
 
 struct RopeParams {
@@ -146,6 +146,23 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
             : __uint_as_float(0x3B000000u) * (float)man;  // man * 2**-9, exact
 }
 
+// Correctly rounded binary32 x / s for a tile's E4M3 scale s, given
+// y = RN(1/s): the product q0 = RN(x * y) is corrected once,
+// q1 = RN(q0 + (x - q0 * s) * y) with both steps fused (Markstein's
+// correction). A GB300 check over every E4M3 significand and every binary32
+// significand of x, both signs, found q1 == RN(x / s) in all 2**29 cases.
+// Scaling x or s by powers of two scales every step exactly while all
+// intermediates stay normal, which |q0| in [2**-60, 2**61) ensures for
+// s in [2**-9, 448] (the remainder is then >= 2**-115); outside that range
+// (and for zero, infinite or NaN q0) the IEEE division is used.
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const uint32_t ex = (__float_as_uint(q0) >> 23) & 0xFFu;
+  if (ex - 67u > 120u) return __fdiv_rn(x, s);
+  const float r = __fmaf_rn(-q0, s, x);
+  return __fmaf_rn(r, y, q0);
+}
+
 // NaN in an NVFP4 record always ends as code 0 (the code rule gives NaN code
 // 0, and amax ignores NaN), so sanitising changes nothing here: callers pass
 // values with NaN already turned into +0.0. The +0.0 added to the quotient
@@ -159,81 +176,182 @@ __device__ __forceinline__ void nvfp4_half(const float f[8], uint8_t* codes, uin
   target = fminf(fmaxf(target, 0.001953125f), 448.0f);
   const uint32_t sbyte = cvt_e4m3x2(target, 0.0f) & 0xFFu;
   const float s = e4m3_value(sbyte);
+  const float y = __frcp_rn(s);
   float q[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) q[k] = __fadd_rn(__fdiv_rn(f[k], s), 0.0f);
+  for (int k = 0; k < 8; ++k) q[k] = __fadd_rn(div_by_scale(f[k], s, y), 0.0f);
   st_u32(codes + 4 * lane, cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]));
   if ((lane & 1) == 0) st_u8(scales + (lane >> 1), sbyte);
 }
 
 // ------------------------------------------------------------------ kernel ---
 
-template <bool kNvfp4, bool kSanitize>
-__global__ void __launch_bounds__(kRopeThreads) rope_insert_kernel(RopeParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 5;
-  const int64_t num_warps = ((int64_t)gridDim.x * kRopeThreads) >> 5;
-  const int64_t value_bytes = kNvfp4 ? 256 : 512;
-  const int64_t scale_bytes = kNvfp4 ? 32 : 16;
+// Ring stage of one writer: latent row (1024 B), its table row's 32 cos and
+// 32 sin (256 B), then the destination (page byte offset, slot in page).
+constexpr int kRopePrefetch = 4;  // writers per warp in flight
+constexpr int kRopeStages = kRopePrefetch + 1;
+constexpr int kStageTable = 1024;
+constexpr int kStageMeta = 1280;
+constexpr int kRopeStageBytes = 1296;
+constexpr size_t kRopeSmem = (size_t)kRopeWarps * kRopeStages * kRopeStageBytes;
 
-  for (int64_t base = warp * 32; base < p.num_tokens; base += num_warps * 32) {
-    // Lane i: gates and addresses of token base+i.
-    int64_t page_off = -1, table_off = 0;
-    int64_t in_page = 0;
-    if (base + lane < p.num_tokens) {
-      const int64_t s = ld_once_i64(p.slots + base + lane);
-      if (s >= 0 && s < p.num_slots) {
-        const int64_t pos = ld_once_i64(p.positions + base + lane);
-        // pos - R >= cos_rows puts the table row past the table whatever the
-        // remainder; testing it first also keeps pos + 1 from overflowing.
-        if (pos >= 0 && pos - p.ratio < p.cos_rows) {
-          int64_t q, r;
-          divmod_pos(pos + 1, p.ratio, q, r);
-          // (pos+1) % R == 0 makes (pos // R) * R equal to pos + 1 - R.
-          const int64_t row = pos + 1 - p.ratio;
-          if (r == 0 && row < p.cos_rows) {
-            int64_t page;
-            divmod_pos(s, p.cache_block, page, in_page);
-            page_off = page * p.page_stride;
-            table_off = row * p.cos_stride;
-          }
-        }
-      }
-    }
-    uint32_t todo = __ballot_sync(0xFFFFFFFFu, page_off >= 0);
-    while (todo) {
-      const int i = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const uint8_t* src = p.latent + (base + i) * p.row_pitch;
-      const uint4 x0 = ld_once_v4(src + 16 * lane);
-      const uint4 x1 = ld_once_v4(src + 512 + 16 * lane);
-      const int64_t pg = __shfl_sync(0xFFFFFFFFu, page_off, i);
-      const int64_t slot_in_page = __shfl_sync(0xFFFFFFFFu, in_page, i);
-      const int64_t tab = __shfl_sync(0xFFFFFFFFu, table_off, i);
-      float4 c = make_float4(1.f, 1.f, 1.f, 1.f), sn = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (lane >= 24) {
-        const float* cs = p.cos_sin + tab + 4 * (lane - 24);
-        c = ld_f4(cs);
-        sn = ld_f4(cs + 32);
-      }
-      float f0[8], f1[8];
-      rotate_row(x0, x1, c, sn, lane, f0, f1);
-      if (kSanitize || kNvfp4) {
-        nan_to_zero(f0);
-        nan_to_zero(f1);
-      }
-      uint8_t* page = p.cache + pg;
-      uint8_t* values = page + slot_in_page * value_bytes;
-      uint8_t* scales = page + p.cache_block * value_bytes + slot_in_page * scale_bytes;
-      if (kNvfp4) {
-        nvfp4_half(f0, values, scales, lane);
-        nvfp4_half(f1, values + 128, scales + 16, lane);
-      } else {
-        mxfp8_half<kSanitize>(f0, values, scales, lane);
-        mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
-      }
+__device__ __forceinline__ float4 lds_f4(const void* p) {
+  const uint4 v = lds_v4(static_cast<const uint4*>(p));
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                     __uint_as_float(v.w));
+}
+
+__device__ __forceinline__ int64_t lds_i64(const void* p) {
+  int64_t r;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ld.shared.s64 %0, [%1];" : "=l"(r) : "r"(a) : "memory");
+  return r;
+}
+
+__device__ __forceinline__ void sts_i64x2(void* p, int64_t a, int64_t b) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("st.shared.v2.s64 [%0], {%1, %2};" ::"r"(d), "l"(a), "l"(b) : "memory");
+}
+
+// The writers of a warp's token range, found 32 tokens at a time. Lane i
+// evaluates token base+i (slot range, (pos+1) % R == 0, table row in range)
+// and keeps its destination and table offsets; `mask` lists the writers not
+// yet issued. The raw slot and position of the following window are loaded
+// one window early to hide their latency.
+struct WriterCursor {
+  int64_t base, end;
+  uint32_t mask;
+  int64_t page_off, in_page, table_off;
+  int64_t next_slot, next_pos;
+
+  __device__ __forceinline__ void fetch_raw(const RopeParams& p, int64_t b, int lane) {
+    next_slot = -1;
+    next_pos = -1;
+    if (b + lane < end) {
+      next_slot = ld_once_i64(p.slots + b + lane);
+      next_pos = ld_once_i64(p.positions + b + lane);
     }
   }
+
+  __device__ __forceinline__ void open(const RopeParams& p, int lane) {
+    const int64_t s = next_slot, pos = next_pos;
+    page_off = -1;
+    in_page = 0;
+    table_off = 0;
+    // pos - R >= cos_rows puts the table row past the table whatever the
+    // remainder; testing it first also keeps pos + 1 from overflowing.
+    if (s >= 0 && s < p.num_slots && pos >= 0 && pos - p.ratio < p.cos_rows) {
+      int64_t q, r;
+      divmod_pos(pos + 1, p.ratio, q, r);
+      const int64_t row = pos + 1 - p.ratio;  // (pos // R) * R when R divides pos + 1
+      if (r == 0 && row < p.cos_rows) {
+        int64_t page;
+        divmod_pos(s, p.cache_block, page, in_page);
+        page_off = page * p.page_stride;
+        table_off = row * p.cos_stride;
+      }
+    }
+    mask = __ballot_sync(0xFFFFFFFFu, page_off >= 0);
+    fetch_raw(p, base + 32, lane);
+  }
+
+  // Issue the next writer's copies into `stage`; false when the range is done.
+  __device__ __forceinline__ bool issue_next(const RopeParams& p, uint8_t* stage, int lane) {
+    while (mask == 0) {
+      base += 32;
+      if (base >= end) return false;
+      open(p, lane);
+    }
+    const int src = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const int64_t pg = __shfl_sync(0xFFFFFFFFu, page_off, src);
+    const int64_t sp = __shfl_sync(0xFFFFFFFFu, in_page, src);
+    const int64_t tab = __shfl_sync(0xFFFFFFFFu, table_off, src);
+    const uint8_t* row = p.latent + (base + src) * p.row_pitch + 16 * lane;
+    cp_async_16(stage + 16 * lane, row);
+    cp_async_16(stage + 512 + 16 * lane, row + 512);
+    if (lane >= 24) {
+      const float* cs = p.cos_sin + tab + 4 * (lane - 24);
+      cp_async_16(stage + kStageTable + 16 * (lane - 24), cs);
+      cp_async_16(stage + kStageTable + 128 + 16 * (lane - 24), cs + 32);
+    }
+    if (lane == 0) sts_i64x2(stage + kStageMeta, pg, sp);
+    return true;
+  }
+};
+
+// Each warp owns a contiguous token range. The cursor issues writers into a
+// per-warp shared-memory ring kRopePrefetch writers ahead of the one being
+// quantized (non-writers cost no row traffic and no pipeline slot). Every
+// iteration commits exactly one cp.async group, so writer c is in group c.
+// __syncwarp before a refill (the stage was read by all lanes last
+// iteration) and after the wait (other lanes' copies and lane 0's metadata
+// become visible).
+template <bool kNvfp4, bool kSanitize>
+__global__ void __launch_bounds__(kRopeThreads) rope_insert_kernel(RopeParams p) {
+  extern __shared__ uint4 smem[];
+  const int lane = threadIdx.x & 31;
+  const int warp_in_block = threadIdx.x >> 5;
+  uint8_t* ring =
+      reinterpret_cast<uint8_t*>(smem) + warp_in_block * (kRopeStages * kRopeStageBytes);
+  const int64_t warp = (int64_t)blockIdx.x * kRopeWarps + warp_in_block;
+  const int64_t num_warps = (int64_t)gridDim.x * kRopeWarps;
+  WriterCursor cur;
+  cur.base = p.num_tokens * warp / num_warps;
+  cur.end = p.num_tokens * (warp + 1) / num_warps;
+  if (cur.base >= cur.end) return;
+  cur.fetch_raw(p, cur.base, lane);
+  cur.open(p, lane);
+
+  const int64_t value_bytes = kNvfp4 ? 256 : 512;
+  const int64_t scale_bytes = kNvfp4 ? 32 : 16;
+  int64_t issued = 0;
+  bool more = true;
+#pragma unroll
+  for (int d = 0; d < kRopePrefetch; ++d) {
+    if (more) {
+      more = cur.issue_next(p, ring + (int)(issued % kRopeStages) * kRopeStageBytes, lane);
+      issued += more ? 1 : 0;
+    }
+    cp_async_commit();
+  }
+  for (int64_t c = 0; c < issued; ++c) {
+    __syncwarp();
+    if (more) {
+      more = cur.issue_next(p, ring + (int)(issued % kRopeStages) * kRopeStageBytes, lane);
+      issued += more ? 1 : 0;
+    }
+    cp_async_commit();
+    cp_async_wait<kRopePrefetch>();
+    __syncwarp();
+    const uint8_t* st = ring + (int)(c % kRopeStages) * kRopeStageBytes;
+    const uint4 x0 = lds_v4(reinterpret_cast<const uint4*>(st + 16 * lane));
+    const uint4 x1 = lds_v4(reinterpret_cast<const uint4*>(st + 512 + 16 * lane));
+    float4 cs = make_float4(1.f, 1.f, 1.f, 1.f), sn = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane >= 24) {
+      cs = lds_f4(st + kStageTable + 16 * (lane - 24));
+      sn = lds_f4(st + kStageTable + 128 + 16 * (lane - 24));
+    }
+    const int64_t pg = lds_i64(st + kStageMeta);
+    const int64_t slot_in_page = lds_i64(st + kStageMeta + 8);
+    float f0[8], f1[8];
+    rotate_row(x0, x1, cs, sn, lane, f0, f1);
+    if (kSanitize || kNvfp4) {
+      nan_to_zero(f0);
+      nan_to_zero(f1);
+    }
+    uint8_t* page = p.cache + pg;
+    uint8_t* values = page + slot_in_page * value_bytes;
+    uint8_t* scales = page + p.cache_block * value_bytes + slot_in_page * scale_bytes;
+    if (kNvfp4) {
+      nvfp4_half(f0, values, scales, lane);
+      nvfp4_half(f1, values + 128, scales + 16, lane);
+    } else {
+      mxfp8_half<kSanitize>(f0, values, scales, lane);
+      mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
+    }
+  }
+  cp_async_wait<0>();
 }
 
 int g_rope_occupancy[4][64];
@@ -241,11 +359,11 @@ int g_rope_occupancy[4][64];
 template <bool kNvfp4, bool kSanitize>
 int launch(const RopeParams& p, cudaStream_t stream) {
   auto k = rope_insert_kernel<kNvfp4, kSanitize>;
-  const int64_t chunks = (p.num_tokens + 31) / 32;
-  const int64_t work_blocks = (chunks + kRopeWarps - 1) / kRopeWarps;
+  const int64_t work_blocks = (p.num_tokens + 32 * kRopeWarps - 1) / (32 * kRopeWarps);
   const unsigned grid = grid_for(
-      work_blocks, resident_blocks_per_sm(k, kRopeThreads, g_rope_occupancy[2 * kNvfp4 + kSanitize]));
-  k<<<grid, kRopeThreads, 0, stream>>>(p);
+      work_blocks,
+      resident_blocks_per_sm(k, kRopeThreads, kRopeSmem, g_rope_occupancy[2 * kNvfp4 + kSanitize]));
+  k<<<grid, kRopeThreads, kRopeSmem, stream>>>(p);
   return launch_status();
 }
 

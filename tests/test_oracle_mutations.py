@@ -1,0 +1,85 @@
+"""The pins must catch plausible mistakes in the oracle (CPU only).
+
+Each case plants one mistake in a temporary copy of oracle/kvq_oracle.c,
+rebuilds that copy, and runs the pin test expected to catch it against the
+copy in a subprocess: that test must fail. The real oracle is not touched.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, original text, planted mistake, pin test that must fail)
+MUTANTS = [
+    ("ties_all_strict", "int passed = upper_is_even ? (a >= midpoint) : (a > midpoint);",
+     "int passed = (a > midpoint);", "test_oracle_pins_formats.py::test_e2m1_midpoints_golden"),
+    ("ties_flipped", "int upper_is_even = ((k + 1) % 2) == 0;",
+     "int upper_is_even = ((k + 1) % 2) == 1;",
+     "test_oracle_pins_formats.py::test_e2m1_midpoints_golden"),
+    ("sign_from_signbit", "uint8_t sign = (normalized < 0.0f) ? 8u : 0u;",
+     "uint8_t sign = signbit(normalized) ? 8u : 0u;",
+     "test_oracle_pins_formats.py::test_e2m1_special_inputs"),
+    ("nibbles_swapped", "row[(g0 + j) / 2] = (uint8_t)(lo | (uint8_t)(hi << 4));",
+     "row[(g0 + j) / 2] = (uint8_t)(hi | (uint8_t)(lo << 4));",
+     "test_oracle_pins_store.py::test_store_low_nibble_holds_lower_index"),
+    ("ceil_off_by_one", "if (fraction != 0u) e += 1;", "if (fraction != 0u) e += 0;",
+     "test_oracle_pins_formats.py::test_ceil_pow2_exponent_is_exact_ceil_log2"),
+    ("zero_group_byte_0", "if (amax == 0.0f) return 0;", "if (amax == 0.0f) return -127;",
+     "test_oracle_pins_formats.py::test_mxfp4_zero_group_scale_is_127"),
+    ("scale_divisor_4", "float v = amax / 6.0f;", "float v = amax / 4.0f;",
+     "test_oracle_pins_formats.py::test_mxfp4_scale_power_of_two_times_six_lands_on_six"),
+    ("rope_sign", "float r_even = ec - os;", "float r_even = ec + os;",
+     "test_oracle_pins_rope.py::test_quarter_and_half_turns"),
+    ("rope_sin_column", "s = cs[32 + (i - 224)];", "s = cs[31 + (i - 224)];",
+     "test_oracle_pins_rope.py::test_quarter_and_half_turns"),
+    ("table_row_unrounded", "int64_t table_row = (position / compress_ratio) * compress_ratio;",
+     "int64_t table_row = position;",
+     "test_oracle_pins_rope.py::test_slot_and_ratio_gates_and_table_row"),
+    ("ratio_gate", "if ((position + 1) % compress_ratio != 0) return -1;",
+     "if (position % compress_ratio != 0) return -1;",
+     "test_oracle_pins_rope.py::test_slot_and_ratio_gates_and_table_row"),
+    ("mxfp8_cap_ignores_sanitize", "int32_t cap = sanitize ? 254 : 255;", "int32_t cap = 255;",
+     "test_oracle_pins_rope.py::test_mxfp8_scale_cap_depends_on_sanitising"),
+    ("mxfp8_amax_floor", "const float kMinAmax = 1e-4f;", "const float kMinAmax = 1e-5f;",
+     "test_oracle_pins_rope.py::test_worked_records"),
+    ("nvfp4_reciprocal", "uint8_t lo = oracle_e2m1_code(x[j] / s);",
+     "uint8_t lo = oracle_e2m1_code(x[j] * (1.0f / s));",
+     "test_oracle_pins_rope.py::test_nvfp4_division_ties"),
+    ("nvfp4_scale_floor", "const float kMinScale = 0.001953125f; /* 2**-9 */",
+     "const float kMinScale = 0.015625f;", "test_oracle_pins_rope.py::test_worked_records"),
+    ("e4m3_ties_up", "    return (fmodf(lower, 2.0f) == 0.0f) ? lower : lower + 1.0f;",
+     "    return lower + 1.0f;", "test_oracle_pins_formats.py::test_e4m3_named_values"),
+    ("gather_scale_byte", "uint8_t scale_byte = row[latent_dim / 2 + j / group];",
+     "uint8_t scale_byte = row[latent_dim / 2 + j / group] + 1;",
+     "test_oracle_pins_store.py::test_gather_equals_independent_decode"),
+    ("slot_upper_bound", "if (slot < 0 || slot >= num_slots) continue;",
+     "if (slot < 0) continue;",
+     "test_oracle_pins_store.py::test_store_skips_pads_and_out_of_range_and_keeps_poison"),
+    ("block_stride_ignored", "return (block * block_stride_rows + row_in_block) * row_bytes;",
+     "return (block * block_size + row_in_block) * row_bytes;",
+     "test_oracle_pins_store.py::test_store_paged_addressing_with_block_stride"),
+    ("amax_keeps_nan", "if (a > amax) amax = a;", "if (a > amax || a != a) amax = a;",
+     "test_oracle_pins_store.py::test_store_worked_row"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mutated,pin", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pin_catches_planted_mistake(tmp_path, name, orig, mutated, pin):
+    src = open(os.path.join(ROOT, "oracle", "kvq_oracle.c")).read()
+    assert src.count(orig) == 1, f"{name}: the text to mutate is not unique in the oracle"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__", "*.tmp*"))
+    (tmp_path / "oracle" / "kvq_oracle.c").write_text(src.replace(orig, mutated))
+    shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests",
+                    ignore=shutil.ignore_patterns("__pycache__", "test_*.py"))
+    shutil.copy(os.path.join(ROOT, "tests", pin.split("::")[0]), tmp_path / "tests")
+    shutil.copy(os.path.join(ROOT, "workloads.py"), tmp_path)
+    env = dict(os.environ, PYTHONPATH=str(tmp_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        f"tests/{pin}"], cwd=tmp_path, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 1, f"{name} was not caught by {pin}:\n{r.stdout[-2000:]}"
