@@ -158,6 +158,14 @@ __device__ __forceinline__ uint32_t bf16x2_nonzero_number_mask(uint32_t w) {
   return m;
 }
 
+// Per half: 0xFFFF where the value is not NaN. AND-ing a word with it turns
+// NaN into +0.0 and leaves every other value (including -0.0).
+__device__ __forceinline__ uint32_t bf16x2_number_mask(uint32_t w) {
+  uint32_t m;
+  asm("set.num.u32.bf16x2 %0, %1, %1;" : "=r"(m) : "r"(w));
+  return m;
+}
+
 // ----------------------------------------------------------- conversions ---
 
 // Two binary32 -> one byte of two E2M1 codes, `lo` in bits 3:0.

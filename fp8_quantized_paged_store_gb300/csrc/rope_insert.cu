@@ -7,13 +7,19 @@
 // (_rope_quant_insert_mxfp8_kernel, _rope_quant_insert_nvfp4_kernel,
 // rope_quant_insert).
 //
-// Work decomposition mirrors the MXFP4 store: a warp owns 32 tokens at a
-// time, lane i evaluates token i's gates (slot range, (pos+1) % R == 0,
-// table row in range) and addresses once, a ballot lists the writers, and
-// each writer row is held as lane l: elements 8l..8l+7 (half 0) and
-// 256+8l..256+8l+7 (half 1). Rotary pairs 224..255 are elements 448..511,
-// i.e. half 1 of lanes 24..31, which alone read the table row (lane l reads
-// cos and sin 4(l-24)..4(l-24)+3 as two 16-byte loads).
+// Work decomposition: a warp owns 32 tokens at a time (grid-stride over
+// chunks); lane i evaluates token i's gates (slot range, (pos+1) % R == 0,
+// table row in range) and addresses once, and a ballot lists the writers, so
+// non-writers cost no row traffic. Writers are taken two at a time with both
+// rows' loads (and their table rows) issued before either is quantized. A
+// writer row is held as lane l: elements 8l..8l+7 (half 0) and
+// 256+8l..256+8l+7 (half 1), each 16-byte load of the warp covering 512
+// contiguous bytes. Rotary pairs 224..255 are elements 448..511, i.e. half 1
+// of lanes 24..31, which alone read the table row (lane l reads cos and sin
+// 4(l-24)..4(l-24)+3 as two 16-byte loads). With at most two writers per
+// warp in flight and 32 warps per SM, loads stay in flight while other warps
+// compute; a shared-memory cp.async ring measured slower here, the gate and
+// ballot work per window then sitting on the critical path.
 //
 // The pages evaluate the rotation formula on all 256 pairs, with cos 1 and
 // sin 0 outside the rotary range. There it is the identity except for NaN,
@@ -33,7 +39,7 @@
 namespace kvq {
 namespace {
 
-constexpr int kRopeWarps = 4;
+constexpr int kRopeWarps = 8;
 constexpr int kRopeThreads = 32 * kRopeWarps;
 
 struct RopeParams {
@@ -73,19 +79,27 @@ __device__ __forceinline__ void widen8(uint4 w, float f[8]) {
   f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
 }
 
-// Rotated (or identity) binary32 values of the lane's two halves.
+// Rotated (or identity) binary32 values of the lane's two halves. With
+// kZeroNan, NaN results become +0.0 (the sanitising step): on NoPE words by a
+// bf16x2 mask (the NoPE formula's result is already exact in bf16), on the
+// rotary values by a binary32 select.
+template <bool kZeroNan>
 __device__ __forceinline__ void rotate_row(uint4 x0, uint4 x1, float4 c, float4 s, int lane,
                                            float f0[8], float f1[8]) {
-  x0.x = nope_pair(x0.x);
-  x0.y = nope_pair(x0.y);
-  x0.z = nope_pair(x0.z);
-  x0.w = nope_pair(x0.w);
+  auto nope = [](uint32_t w) {
+    const uint32_t r = nope_pair(w);
+    return kZeroNan ? (r & bf16x2_number_mask(r)) : r;
+  };
+  x0.x = nope(x0.x);
+  x0.y = nope(x0.y);
+  x0.z = nope(x0.z);
+  x0.w = nope(x0.w);
   widen8(x0, f0);
   if (lane < 24) {
-    x1.x = nope_pair(x1.x);
-    x1.y = nope_pair(x1.y);
-    x1.z = nope_pair(x1.z);
-    x1.w = nope_pair(x1.w);
+    x1.x = nope(x1.x);
+    x1.y = nope(x1.y);
+    x1.z = nope(x1.z);
+    x1.w = nope(x1.w);
     widen8(x1, f1);
   } else {
     float v[8];
@@ -95,15 +109,16 @@ __device__ __forceinline__ void rotate_row(uint4 x0, uint4 x1, float4 c, float4 
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float e = v[2 * k], o = v[2 * k + 1];
-      f1[2 * k] = __fsub_rn(__fmul_rn(e, cc[k]), __fmul_rn(o, ss[k]));
-      f1[2 * k + 1] = __fadd_rn(__fmul_rn(o, cc[k]), __fmul_rn(e, ss[k]));
+      float re = __fsub_rn(__fmul_rn(e, cc[k]), __fmul_rn(o, ss[k]));
+      float ro = __fadd_rn(__fmul_rn(o, cc[k]), __fmul_rn(e, ss[k]));
+      if (kZeroNan) {
+        re = (re == re) ? re : 0.0f;
+        ro = (ro == ro) ? ro : 0.0f;
+      }
+      f1[2 * k] = re;
+      f1[2 * k + 1] = ro;
     }
   }
-}
-
-__device__ __forceinline__ void nan_to_zero(float f[8]) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k) f[k] = (f[k] == f[k]) ? f[k] : 0.0f;
 }
 
 __device__ __forceinline__ float abs_max8(const float f[8]) {
@@ -148,26 +163,21 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
 
 // Correctly rounded binary32 x / s for a tile's E4M3 scale s, given
 // y = RN(1/s): the product q0 = RN(x * y) is corrected once,
-// q1 = RN(q0 + (x - q0 * s) * y) with both steps fused (Markstein's
-// correction). A GB300 check over every E4M3 significand and every binary32
-// significand of x, both signs, found q1 == RN(x / s) in all 2**29 cases.
-// Scaling x or s by powers of two scales every step exactly while all
-// intermediates stay normal, which |q0| in [2**-60, 2**61) ensures for
-// s in [2**-9, 448] (the remainder is then >= 2**-115); outside that range
-// (and for zero, infinite or NaN q0) the IEEE division is used.
-__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
-  const float q0 = __fmul_rn(x, y);
-  const uint32_t ex = (__float_as_uint(q0) >> 23) & 0xFFu;
-  if (ex - 67u > 120u) return __fdiv_rn(x, s);
-  const float r = __fmaf_rn(-q0, s, x);
-  return __fmaf_rn(r, y, q0);
-}
-
+// q1 = RN(q0 + (x - q0 * s) * y), both steps fused (Markstein's correction).
+// A GB300 check over every E4M3 significand and every binary32 significand
+// of x, both signs, found q1 == RN(x / s) in all 2**29 cases. Scaling x or s
+// by powers of two scales every step exactly while all intermediates stay
+// normal, which |q0| in [2**-60, 2**61) ensures for s in [2**-9, 448] (the
+// remainder is then >= 2**-115). The upper bound is checked once per tile
+// (amax * y < 2**61, which also excludes infinite or NaN amax); the lower
+// one per value. Elsewhere (tiny, zero or infinite values) the IEEE division
+// is used, followed by +0.0 to turn a -0.0 quotient into +0.0.
+//
 // NaN in an NVFP4 record always ends as code 0 (the code rule gives NaN code
 // 0, and amax ignores NaN), so sanitising changes nothing here: callers pass
-// values with NaN already turned into +0.0. The +0.0 added to the quotient
-// turns -0.0 (x = -0.0, or a tiny negative quotient that underflows) into
-// +0.0, which the code rule also codes 0.
+// values with NaN already turned into +0.0. The corrected quotient is never
+// -0.0 (x = +-0 takes the IEEE branch), and -0.0 would be code 8 where the
+// rule gives 0.
 __device__ __forceinline__ void nvfp4_half(const float f[8], uint8_t* codes, uint8_t* scales,
                                            int lane) {
   float amax = abs_max8(f);
@@ -177,181 +187,106 @@ __device__ __forceinline__ void nvfp4_half(const float f[8], uint8_t* codes, uin
   const uint32_t sbyte = cvt_e4m3x2(target, 0.0f) & 0xFFu;
   const float s = e4m3_value(sbyte);
   const float y = __frcp_rn(s);
+  const bool tile_ok = __fmul_rn(amax, y) < 0x1p61f;
   float q[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) q[k] = __fadd_rn(div_by_scale(f[k], s, y), 0.0f);
+  for (int k = 0; k < 8; ++k) {
+    const float q0 = __fmul_rn(f[k], y);
+    if (tile_ok && fabsf(q0) >= 0x1p-60f) {
+      q[k] = __fmaf_rn(__fmaf_rn(-q0, s, f[k]), y, q0);
+    } else {
+      q[k] = __fadd_rn(__fdiv_rn(f[k], s), 0.0f);
+    }
+  }
   st_u32(codes + 4 * lane, cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]));
   if ((lane & 1) == 0) st_u8(scales + (lane >> 1), sbyte);
 }
 
 // ------------------------------------------------------------------ kernel ---
 
-// Ring stage of one writer: latent row (1024 B), its table row's 32 cos and
-// 32 sin (256 B), then the destination (page byte offset, slot in page).
-constexpr int kRopePrefetch = 4;  // writers per warp in flight
-constexpr int kRopeStages = kRopePrefetch + 1;
-constexpr int kStageTable = 1024;
-constexpr int kStageMeta = 1280;
-constexpr int kRopeStageBytes = 1296;
-constexpr size_t kRopeSmem = (size_t)kRopeWarps * kRopeStages * kRopeStageBytes;
-
-__device__ __forceinline__ float4 lds_f4(const void* p) {
-  const uint4 v = lds_v4(static_cast<const uint4*>(p));
-  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                     __uint_as_float(v.w));
-}
-
-__device__ __forceinline__ int64_t lds_i64(const void* p) {
-  int64_t r;
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-  asm volatile("ld.shared.s64 %0, [%1];" : "=l"(r) : "r"(a) : "memory");
-  return r;
-}
-
-__device__ __forceinline__ void sts_i64x2(void* p, int64_t a, int64_t b) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(p);
-  asm volatile("st.shared.v2.s64 [%0], {%1, %2};" ::"r"(d), "l"(a), "l"(b) : "memory");
-}
-
-// The writers of a warp's token range, found 32 tokens at a time. Lane i
-// evaluates token base+i (slot range, (pos+1) % R == 0, table row in range)
-// and keeps its destination and table offsets; `mask` lists the writers not
-// yet issued. The raw slot and position of the following window are loaded
-// one window early to hide their latency.
-struct WriterCursor {
-  int64_t base, end;
-  uint32_t mask;
-  int64_t page_off, in_page, table_off;
-  int64_t next_slot, next_pos;
-
-  __device__ __forceinline__ void fetch_raw(const RopeParams& p, int64_t b, int lane) {
-    next_slot = -1;
-    next_pos = -1;
-    if (b + lane < end) {
-      next_slot = ld_once_i64(p.slots + b + lane);
-      next_pos = ld_once_i64(p.positions + b + lane);
-    }
-  }
-
-  __device__ __forceinline__ void open(const RopeParams& p, int lane) {
-    const int64_t s = next_slot, pos = next_pos;
-    page_off = -1;
-    in_page = 0;
-    table_off = 0;
-    // pos - R >= cos_rows puts the table row past the table whatever the
-    // remainder; testing it first also keeps pos + 1 from overflowing.
-    if (s >= 0 && s < p.num_slots && pos >= 0 && pos - p.ratio < p.cos_rows) {
-      int64_t q, r;
-      divmod_pos(pos + 1, p.ratio, q, r);
-      const int64_t row = pos + 1 - p.ratio;  // (pos // R) * R when R divides pos + 1
-      if (r == 0 && row < p.cos_rows) {
-        int64_t page;
-        divmod_pos(s, p.cache_block, page, in_page);
-        page_off = page * p.page_stride;
-        table_off = row * p.cos_stride;
-      }
-    }
-    mask = __ballot_sync(0xFFFFFFFFu, page_off >= 0);
-    fetch_raw(p, base + 32, lane);
-  }
-
-  // Issue the next writer's copies into `stage`; false when the range is done.
-  __device__ __forceinline__ bool issue_next(const RopeParams& p, uint8_t* stage, int lane) {
-    while (mask == 0) {
-      base += 32;
-      if (base >= end) return false;
-      open(p, lane);
-    }
-    const int src = __ffs(mask) - 1;
-    mask &= mask - 1;
-    const int64_t pg = __shfl_sync(0xFFFFFFFFu, page_off, src);
-    const int64_t sp = __shfl_sync(0xFFFFFFFFu, in_page, src);
-    const int64_t tab = __shfl_sync(0xFFFFFFFFu, table_off, src);
-    const uint8_t* row = p.latent + (base + src) * p.row_pitch + 16 * lane;
-    cp_async_16(stage + 16 * lane, row);
-    cp_async_16(stage + 512 + 16 * lane, row + 512);
-    if (lane >= 24) {
-      const float* cs = p.cos_sin + tab + 4 * (lane - 24);
-      cp_async_16(stage + kStageTable + 16 * (lane - 24), cs);
-      cp_async_16(stage + kStageTable + 128 + 16 * (lane - 24), cs + 32);
-    }
-    if (lane == 0) sts_i64x2(stage + kStageMeta, pg, sp);
-    return true;
-  }
-};
-
-// Each warp owns a contiguous token range. The cursor issues writers into a
-// per-warp shared-memory ring kRopePrefetch writers ahead of the one being
-// quantized (non-writers cost no row traffic and no pipeline slot). Every
-// iteration commits exactly one cp.async group, so writer c is in group c.
-// __syncwarp before a refill (the stage was read by all lanes last
-// iteration) and after the wait (other lanes' copies and lane 0's metadata
-// become visible).
 template <bool kNvfp4, bool kSanitize>
 __global__ void __launch_bounds__(kRopeThreads) rope_insert_kernel(RopeParams p) {
-  extern __shared__ uint4 smem[];
   const int lane = threadIdx.x & 31;
-  const int warp_in_block = threadIdx.x >> 5;
-  uint8_t* ring =
-      reinterpret_cast<uint8_t*>(smem) + warp_in_block * (kRopeStages * kRopeStageBytes);
-  const int64_t warp = (int64_t)blockIdx.x * kRopeWarps + warp_in_block;
-  const int64_t num_warps = (int64_t)gridDim.x * kRopeWarps;
-  WriterCursor cur;
-  cur.base = p.num_tokens * warp / num_warps;
-  cur.end = p.num_tokens * (warp + 1) / num_warps;
-  if (cur.base >= cur.end) return;
-  cur.fetch_raw(p, cur.base, lane);
-  cur.open(p, lane);
-
+  const int64_t warp = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 5;
+  const int64_t num_warps = ((int64_t)gridDim.x * kRopeThreads) >> 5;
   const int64_t value_bytes = kNvfp4 ? 256 : 512;
   const int64_t scale_bytes = kNvfp4 ? 32 : 16;
-  int64_t issued = 0;
-  bool more = true;
+
+  for (int64_t base = warp * 32; base < p.num_tokens; base += num_warps * 32) {
+    // Lane i: gates and addresses of token base+i.
+    int64_t page_off = -1, table_off = 0;
+    int64_t in_page = 0;
+    if (base + lane < p.num_tokens) {
+      const int64_t s = ld_once_i64(p.slots + base + lane);
+      if (s >= 0 && s < p.num_slots) {
+        const int64_t pos = ld_once_i64(p.positions + base + lane);
+        // pos - R >= cos_rows puts the table row past the table whatever the
+        // remainder; testing it first also keeps pos + 1 from overflowing.
+        if (pos >= 0 && pos - p.ratio < p.cos_rows) {
+          int64_t q, r;
+          divmod_pos(pos + 1, p.ratio, q, r);
+          // (pos+1) % R == 0 makes (pos // R) * R equal to pos + 1 - R.
+          const int64_t row = pos + 1 - p.ratio;
+          if (r == 0 && row < p.cos_rows) {
+            int64_t page;
+            divmod_pos(s, p.cache_block, page, in_page);
+            page_off = page * p.page_stride;
+            table_off = row * p.cos_stride;
+          }
+        }
+      }
+    }
+    uint32_t todo = __ballot_sync(0xFFFFFFFFu, page_off >= 0);
+    while (todo) {
+      const int ia = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int ib = todo ? __ffs(todo) - 1 : -1;
+      if (todo) todo &= todo - 1;
+      const uint8_t* sa = p.latent + (base + ia) * p.row_pitch;
+      const uint4 xa0 = ld_once_v4(sa + 16 * lane);
+      const uint4 xa1 = ld_once_v4(sa + 512 + 16 * lane);
+      uint4 xb0 = make_uint4(0, 0, 0, 0), xb1 = xb0;
+      if (ib >= 0) {
+        const uint8_t* sb = p.latent + (base + ib) * p.row_pitch;
+        xb0 = ld_once_v4(sb + 16 * lane);
+        xb1 = ld_once_v4(sb + 512 + 16 * lane);
+      }
+      const int64_t ta = __shfl_sync(0xFFFFFFFFu, table_off, ia);
+      const int64_t tb = __shfl_sync(0xFFFFFFFFu, table_off, ib < 0 ? ia : ib);
+      float4 ca = make_float4(1.f, 1.f, 1.f, 1.f), sna = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 cb = ca, snb = sna;
+      if (lane >= 24) {
+        const float* csa = p.cos_sin + ta + 4 * (lane - 24);
+        ca = ld_f4(csa);
+        sna = ld_f4(csa + 32);
+        if (ib >= 0) {
+          const float* csb = p.cos_sin + tb + 4 * (lane - 24);
+          cb = ld_f4(csb);
+          snb = ld_f4(csb + 32);
+        }
+      }
 #pragma unroll
-  for (int d = 0; d < kRopePrefetch; ++d) {
-    if (more) {
-      more = cur.issue_next(p, ring + (int)(issued % kRopeStages) * kRopeStageBytes, lane);
-      issued += more ? 1 : 0;
-    }
-    cp_async_commit();
-  }
-  for (int64_t c = 0; c < issued; ++c) {
-    __syncwarp();
-    if (more) {
-      more = cur.issue_next(p, ring + (int)(issued % kRopeStages) * kRopeStageBytes, lane);
-      issued += more ? 1 : 0;
-    }
-    cp_async_commit();
-    cp_async_wait<kRopePrefetch>();
-    __syncwarp();
-    const uint8_t* st = ring + (int)(c % kRopeStages) * kRopeStageBytes;
-    const uint4 x0 = lds_v4(reinterpret_cast<const uint4*>(st + 16 * lane));
-    const uint4 x1 = lds_v4(reinterpret_cast<const uint4*>(st + 512 + 16 * lane));
-    float4 cs = make_float4(1.f, 1.f, 1.f, 1.f), sn = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane >= 24) {
-      cs = lds_f4(st + kStageTable + 16 * (lane - 24));
-      sn = lds_f4(st + kStageTable + 128 + 16 * (lane - 24));
-    }
-    const int64_t pg = lds_i64(st + kStageMeta);
-    const int64_t slot_in_page = lds_i64(st + kStageMeta + 8);
-    float f0[8], f1[8];
-    rotate_row(x0, x1, cs, sn, lane, f0, f1);
-    if (kSanitize || kNvfp4) {
-      nan_to_zero(f0);
-      nan_to_zero(f1);
-    }
-    uint8_t* page = p.cache + pg;
-    uint8_t* values = page + slot_in_page * value_bytes;
-    uint8_t* scales = page + p.cache_block * value_bytes + slot_in_page * scale_bytes;
-    if (kNvfp4) {
-      nvfp4_half(f0, values, scales, lane);
-      nvfp4_half(f1, values + 128, scales + 16, lane);
-    } else {
-      mxfp8_half<kSanitize>(f0, values, scales, lane);
-      mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
+      for (int w = 0; w < 2; ++w) {
+        const int i = w ? ib : ia;
+        if (i < 0) break;
+        const int64_t pg = __shfl_sync(0xFFFFFFFFu, page_off, i);
+        const int64_t slot_in_page = __shfl_sync(0xFFFFFFFFu, in_page, i);
+        float f0[8], f1[8];
+        rotate_row<kSanitize || kNvfp4>(w ? xb0 : xa0, w ? xb1 : xa1, w ? cb : ca, w ? snb : sna,
+                                         lane, f0, f1);
+        uint8_t* page = p.cache + pg;
+        uint8_t* values = page + slot_in_page * value_bytes;
+        uint8_t* scales = page + p.cache_block * value_bytes + slot_in_page * scale_bytes;
+        if (kNvfp4) {
+          nvfp4_half(f0, values, scales, lane);
+          nvfp4_half(f1, values + 128, scales + 16, lane);
+        } else {
+          mxfp8_half<kSanitize>(f0, values, scales, lane);
+          mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
+        }
+      }
     }
   }
-  cp_async_wait<0>();
 }
 
 int g_rope_occupancy[4][64];
@@ -359,11 +294,11 @@ int g_rope_occupancy[4][64];
 template <bool kNvfp4, bool kSanitize>
 int launch(const RopeParams& p, cudaStream_t stream) {
   auto k = rope_insert_kernel<kNvfp4, kSanitize>;
-  const int64_t work_blocks = (p.num_tokens + 32 * kRopeWarps - 1) / (32 * kRopeWarps);
+  const int64_t chunks = (p.num_tokens + 31) / 32;
+  const int64_t work_blocks = (chunks + kRopeWarps - 1) / kRopeWarps;
   const unsigned grid = grid_for(
-      work_blocks,
-      resident_blocks_per_sm(k, kRopeThreads, kRopeSmem, g_rope_occupancy[2 * kNvfp4 + kSanitize]));
-  k<<<grid, kRopeThreads, kRopeSmem, stream>>>(p);
+      work_blocks, resident_blocks_per_sm(k, kRopeThreads, 0, g_rope_occupancy[2 * kNvfp4 + kSanitize]));
+  k<<<grid, kRopeThreads, 0, stream>>>(p);
   return launch_status();
 }
 
