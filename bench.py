@@ -425,10 +425,11 @@ def run_profile(args):
     n = args.profile_tokens
     if args.profile == "store":
         lat = workloads.store_large_latent(seed=0, num_tokens=n, row_stride=ROW_STRIDE)
-        slots = workloads.store_large_slots(seed=0, num_tokens=n, num_slots=2 * n)
+        nslots = args.profile_slots or 2 * n
+        slots = workloads.store_large_slots(seed=0, num_tokens=n, num_slots=nslots)
         lat_d = torch.from_numpy(lat.view(np.int16)).to(dev).view(torch.bfloat16)[:, :512]
         slots_d = torch.from_numpy(slots).to(dev)
-        cache = torch.full((2 * n * ROW,), 0xAA, dtype=torch.uint8, device=dev)
+        cache = torch.full((nslots * ROW,), 0xAA, dtype=torch.uint8, device=dev)
         call = lambda: kvq.mxfp4_mla_store(lat_d, slots_d, cache)  # noqa: E731
         valid = int(np.sum(slots >= 0))
         algo = sum(store_bytes(n, valid))
@@ -476,6 +477,8 @@ def main():
     ap.add_argument("--profile", choices=["store", "rope_mxfp8", "rope_nvfp4", "gather"],
                     help="run one kernel on a reduced case (for Nsight Compute) and exit")
     ap.add_argument("--profile-tokens", type=int, default=400_000)
+    ap.add_argument("--profile-slots", type=int, default=0,
+                    help="cache slots for --profile store (default: twice the tokens)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -178,15 +178,22 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
 // values with NaN already turned into +0.0. The corrected quotient is never
 // -0.0 (x = +-0 takes the IEEE branch), and -0.0 would be code 8 where the
 // rule gives 0.
+// The rare branch of the quotient, kept out of line so that the eight values
+// of a tile share one copy of the division code.
+__device__ __noinline__ float nvfp4_quotient_ieee(float x, float s) {
+  return __fadd_rn(__fdiv_rn(x, s), 0.0f);
+}
+
+// `sy` holds (s, RN(1/s)) for every positive E4M3 code (built once per block).
 __device__ __forceinline__ void nvfp4_half(const float f[8], uint8_t* codes, uint8_t* scales,
-                                           int lane) {
+                                           int lane, const float2* sy) {
   float amax = abs_max8(f);
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   float target = __fmul_rn(amax, 1.0f / 6.0f);
   target = fminf(fmaxf(target, 0.001953125f), 448.0f);
-  const uint32_t sbyte = cvt_e4m3x2(target, 0.0f) & 0xFFu;
-  const float s = e4m3_value(sbyte);
-  const float y = __frcp_rn(s);
+  const uint32_t sbyte = cvt_e4m3x2(target, 0.0f) & 0xFFu;  // 0x01..0x7E
+  const float2 t = sy[sbyte];
+  const float s = t.x, y = t.y;
   const bool tile_ok = __fmul_rn(amax, y) < 0x1p61f;
   float q[8];
 #pragma unroll
@@ -195,7 +202,7 @@ __device__ __forceinline__ void nvfp4_half(const float f[8], uint8_t* codes, uin
     if (tile_ok && fabsf(q0) >= 0x1p-60f) {
       q[k] = __fmaf_rn(__fmaf_rn(-q0, s, f[k]), y, q0);
     } else {
-      q[k] = __fadd_rn(__fdiv_rn(f[k], s), 0.0f);
+      q[k] = nvfp4_quotient_ieee(f[k], s);
     }
   }
   st_u32(codes + 4 * lane, cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]));
@@ -206,6 +213,14 @@ __device__ __forceinline__ void nvfp4_half(const float f[8], uint8_t* codes, uin
 
 template <bool kNvfp4, bool kSanitize>
 __global__ void __launch_bounds__(kRopeThreads) rope_insert_kernel(RopeParams p) {
+  __shared__ float2 scale_table[kNvfp4 ? 128 : 1];
+  if (kNvfp4) {
+    if (threadIdx.x < 128) {
+      const float sv = e4m3_value(threadIdx.x);
+      scale_table[threadIdx.x] = make_float2(sv, __frcp_rn(sv));
+    }
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 5;
   const int64_t num_warps = ((int64_t)gridDim.x * kRopeThreads) >> 5;
@@ -278,8 +293,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_insert_kernel(RopeParams p)
         uint8_t* values = page + slot_in_page * value_bytes;
         uint8_t* scales = page + p.cache_block * value_bytes + slot_in_page * scale_bytes;
         if (kNvfp4) {
-          nvfp4_half(f0, values, scales, lane);
-          nvfp4_half(f1, values + 128, scales + 16, lane);
+          nvfp4_half(f0, values, scales, lane, scale_table);
+          nvfp4_half(f1, values + 128, scales + 16, lane, scale_table);
         } else {
           mxfp8_half<kSanitize>(f0, values, scales, lane);
           mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
