@@ -54,6 +54,11 @@ def lib() -> ctypes.CDLL:
         L.oracle_mxfp4_mla_gather_dequant.restype = None
         L.oracle_mxfp4_mla_gather_dequant.argtypes = [_ptr, _i64, _i64, _i64, _i64, _i32, _ptr,
                                                       _i64, _ptr, _i64]
+        L.oracle_rmsnorm_rows.restype = None
+        L.oracle_rmsnorm_rows.argtypes = [_ptr, _i64, _i64, _ptr, ctypes.c_float, _ptr]
+        L.oracle_mxfp4_mla_rmsnorm_store.restype = None
+        L.oracle_mxfp4_mla_rmsnorm_store.argtypes = [_ptr, _i64, _i64, _ptr, ctypes.c_float, _ptr,
+                                                     _ptr, _i64, _i64, _i64]
         for name in ("oracle_rope_quant_insert_mxfp8", "oracle_rope_quant_insert_nvfp4"):
             getattr(L, name).restype = None
             getattr(L, name).argtypes = [_ptr, _i64, _i64, _ptr, _ptr, _i64, _i64, _ptr, _ptr,
@@ -155,6 +160,36 @@ def mxfp4_mla_store(latent: np.ndarray, slot_mapping: np.ndarray, cache: np.ndar
         L.oracle_mxfp4_mla_store(base + lo * stride * 2, hi - lo, d, stride,
                                  _addr(slots, lo * 8), _addr(cache, cache_offset),
                                  num_blocks, block_size, block_stride_rows, group)
+    _run_split(T, threads, body)
+
+
+def rmsnorm_rows(latent: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """bf16 bits [T, 512] of the normalised rows (the reading in kvq_oracle.c)."""
+    base, stride, T, d = _latent_args(latent)
+    assert d == 512
+    w = _contig(weight, np.uint16)
+    assert w.shape == (512,)
+    out = np.empty((T, 512), dtype=np.uint16)
+    lib().oracle_rmsnorm_rows(base, T, stride, _addr(w), eps, _addr(out))
+    return out
+
+
+def mxfp4_mla_rmsnorm_store(latent: np.ndarray, weight: np.ndarray, eps: float,
+                            slot_mapping: np.ndarray, cache: np.ndarray, num_blocks: int,
+                            block_size: int, block_stride_rows: int, cache_offset: int = 0,
+                            threads: int = 1) -> None:
+    """RMSNorm of each row (bf16 weight [512], fp32 eps), then the MXFP4 store."""
+    base, stride, T, d = _latent_args(latent)
+    assert d == 512
+    w = _contig(weight, np.uint16)
+    slots = _contig(slot_mapping, np.int64)
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    L = lib()
+
+    def body(lo, hi):
+        L.oracle_mxfp4_mla_rmsnorm_store(base + lo * stride * 2, hi - lo, stride, _addr(w), eps,
+                                         _addr(slots, lo * 8), _addr(cache, cache_offset),
+                                         num_blocks, block_size, block_stride_rows)
     _run_split(T, threads, body)
 
 

@@ -461,6 +461,75 @@ void oracle_rope_quant_insert_nvfp4(const uint16_t* latent, int64_t num_tokens, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm ahead of the MXFP4 store                                           */
+/* ------------------------------------------------------------------------ */
+
+/* [store] store_mxfp4_mla takes "the post-RMSNorm latent"; the V4.1 page's
+ * fused_save_compress_norm normalises with a bf16 [512] weight and an fp32
+ * epsilon into a bf16 latent. The pages fix neither the summation order nor
+ * how the reciprocal square root is formed, so this reading fixes both in a
+ * form that can be reproduced exactly:
+ *   partial[l] = x[8l]^2 + ... + x[8l+7]^2 + x[256+8l]^2 + ... + x[256+8l+7]^2
+ *                (l = 0..31, accumulated left to right, each square and sum
+ *                rounded to binary32),
+ *   S = pairwise tree over l: partial[l] + partial[l ^ 1], then the pairs of
+ *       those (l ^ 2), then l ^ 4, l ^ 8, l ^ 16,
+ *   r = RN(1 / RN(sqrt(RN(S / 512 + eps)))),      (S / 512 is exact scaling)
+ *   y = bf16(RN(x * r)),   z = bf16(y * w)        (y * w is exact in binary32).
+ * The row is normalised when latent_dim is 512; z is then quantized exactly
+ * as by oracle_mxfp4_mla_store. */
+static void rmsnorm_row_512(const uint16_t* x, const uint16_t* w, float eps, uint16_t* z) {
+    float partial[32];
+    for (int l = 0; l < 32; ++l) {
+        float acc = 0.0f;
+        for (int h = 0; h < 2; ++h) {
+            for (int k = 0; k < 8; ++k) {
+                float v = bf16_to_f32(x[256 * h + 8 * l + k]);
+                float sq = v * v;
+                acc = acc + sq;
+            }
+        }
+        partial[l] = acc;
+    }
+    for (int stride = 1; stride < 32; stride *= 2) {
+        float next[32];
+        for (int l = 0; l < 32; ++l) next[l] = partial[l] + partial[l ^ stride];
+        memcpy(partial, next, sizeof next);
+    }
+    float mean = partial[0] / 512.0f;
+    float var = mean + eps;
+    float root = sqrtf(var);
+    float r = 1.0f / root;
+    for (int j = 0; j < 512; ++j) {
+        float xr = bf16_to_f32(x[j]) * r;
+        uint16_t y = f32_to_bf16_rne(xr);
+        float yw = bf16_to_f32(y) * bf16_to_f32(w[j]);
+        z[j] = f32_to_bf16_rne(yw);
+    }
+}
+
+void oracle_rmsnorm_rows(const uint16_t* x, int64_t num_rows, int64_t row_stride,
+                         const uint16_t* weight, float eps, uint16_t* out) {
+    for (int64_t t = 0; t < num_rows; ++t) rmsnorm_row_512(x + t * row_stride, weight, eps, out + t * 512);
+}
+
+/* RMSNorm, then the MXFP4 store of the normalised row (latent_dim 512). */
+void oracle_mxfp4_mla_rmsnorm_store(const uint16_t* latent, int64_t num_tokens, int64_t row_stride,
+                                    const uint16_t* weight, float eps,
+                                    const int64_t* slot_mapping, uint8_t* cache,
+                                    int64_t num_blocks, int64_t block_size,
+                                    int64_t block_stride_rows) {
+    /* By definition: normalise the token's row, then store it as a one-token
+     * batch (the store applies the slot rules). */
+    uint16_t z[512];
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        rmsnorm_row_512(latent + t * row_stride, weight, eps, z);
+        oracle_mxfp4_mla_store(z, 1, 512, 512, slot_mapping + t, cache, num_blocks, block_size,
+                               block_stride_rows, 32);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Element-wise entry points used by the pin tests                            */
 /* ------------------------------------------------------------------------ */
 

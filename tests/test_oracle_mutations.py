@@ -53,6 +53,16 @@ MUTANTS = [
      "const float kMinScale = 0.015625f;", "test_oracle_pins_rope.py::test_worked_records"),
     ("e4m3_ties_up", "    return (fmodf(lower, 2.0f) == 0.0f) ? lower : lower + 1.0f;",
      "    return lower + 1.0f;", "test_oracle_pins_formats.py::test_e4m3_named_values"),
+    ("rmsnorm_eps_dropped", "float var = mean + eps;", "float var = mean;",
+     "test_oracle_pins_rmsnorm.py::test_rmsnorm_eps_sits_inside_the_root"),
+    ("rmsnorm_mean_511", "float mean = partial[0] / 512.0f;", "float mean = partial[0] / 511.0f;",
+     "test_oracle_pins_rmsnorm.py::test_rmsnorm_matches_float64_within_one_ulp"),
+    ("rmsnorm_weight_dropped", "float yw = bf16_to_f32(y) * bf16_to_f32(w[j]);",
+     "float yw = bf16_to_f32(y);",
+     "test_oracle_pins_rmsnorm.py::test_rmsnorm_weight_power_of_two_scales_exactly"),
+    ("rmsnorm_y_unrounded", "float yw = bf16_to_f32(y) * bf16_to_f32(w[j]);",
+     "float yw = xr * bf16_to_f32(w[j]); (void)y;",
+     "test_oracle_pins_rmsnorm.py::test_rmsnorm_matches_float64_within_one_ulp"),
     ("gather_scale_byte", "uint8_t scale_byte = row[latent_dim / 2 + j / group];",
      "uint8_t scale_byte = row[latent_dim / 2 + j / group] + 1;",
      "test_oracle_pins_store.py::test_gather_equals_independent_decode"),
