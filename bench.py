@@ -12,9 +12,10 @@ of 272-byte rows, 1% pad slots. One step = one store of the whole batch.
   e2e        the same metric through the public API from pinned host buffers:
              each step copies the latent and slots in and the cache back out
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
-  paths      the other hot-path rows measured in the same run: the V4.1
-             RoPE inserts (MXFP8, NVFP4) on 4,194,304 tokens and the gather of
-             128 x 2048 rows from a 1,048,576-slot cache
+  paths      the other hot-path rows measured in the same run: the
+             RMSNorm-fused store on the same batch, the V4.1 RoPE inserts
+             (MXFP8, NVFP4) on 4,194,304 tokens and the gather of 128 x 2048
+             rows from a 1,048,576-slot cache
 
 --impl reference times the CPU oracle instead (the only reference this
 project has), on the same workload, metric and unit.
@@ -242,15 +243,30 @@ def time_events(torch, fn, reps, stream, flush=None):
     return statistics.mean(times), times
 
 
-def secondary_paths(torch, kvq, dev, peak):
-    """RoPE inserts on 4,194,304 tokens and the 128 x 2048 gather: mean of
-    CUDA-event times over 20 reps each (L2 flushed before each gather rep)."""
+def secondary_paths(torch, kvq, dev, peak, store_inputs):
+    """The RMSNorm-fused store on the headline workload, the RoPE inserts on
+    4,194,304 tokens and the 128 x 2048 gather: mean of CUDA-event times over
+    20 reps each (L2 flushed before each gather rep)."""
     out = {}
     stream = torch.cuda.current_stream()
     flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
 
     def flush():
         flush_buf.fill_(1)
+
+    lat_d, slots_d, cache_d, valid = store_inputs
+    g = torch.Generator().manual_seed(0)
+    weight = (0.5 + torch.rand(512, generator=g)).to(torch.bfloat16).to(dev)
+    call = lambda: kvq.mxfp4_mla_rmsnorm_store(lat_d, weight, 1e-6, slots_d, cache_d)  # noqa: E731
+    for _ in range(3):
+        call()
+    ms, _ = time_events(torch, call, 20, stream)
+    rd, wr = store_bytes(N_TOKENS, valid)
+    algo = rd + wr + 1024
+    out["mxfp4_mla_rmsnorm_store"] = {
+        "workload": "4,300,000 tokens, stride 576, 8,388,608 slots, bf16 weight, eps 1e-6",
+        "tokens_per_s": N_TOKENS / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
+        "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak}
 
     for record, width in (("mxfp8", 528), ("nvfp4", 288)):
         w = workloads.rope_insert(seed=0, num_tokens=4_194_304, num_pages=65_536, record=record)
@@ -377,7 +393,8 @@ def run_ours(args):
     d2h = cache_h.numel()
     del lat_full_d
 
-    paths = secondary_paths(torch, kvq, dev, peak) if (rank == 0 and not args.no_paths) else None
+    paths = secondary_paths(torch, kvq, dev, peak, (lat_d, slots_d, cache_d, valid)) \
+        if (rank == 0 and not args.no_paths) else None
     cpu = cpu_baseline_sample(lat_np, slots_np, args.cpu_seconds) if rank == 0 else None
     if rank != 0:
         return
@@ -423,16 +440,23 @@ def run_profile(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     n = args.profile_tokens
-    if args.profile == "store":
+    if args.profile in ("store", "rmsnorm_store"):
         lat = workloads.store_large_latent(seed=0, num_tokens=n, row_stride=ROW_STRIDE)
         nslots = args.profile_slots or 2 * n
         slots = workloads.store_large_slots(seed=0, num_tokens=n, num_slots=nslots)
         lat_d = torch.from_numpy(lat.view(np.int16)).to(dev).view(torch.bfloat16)[:, :512]
         slots_d = torch.from_numpy(slots).to(dev)
         cache = torch.full((nslots * ROW,), 0xAA, dtype=torch.uint8, device=dev)
-        call = lambda: kvq.mxfp4_mla_store(lat_d, slots_d, cache)  # noqa: E731
         valid = int(np.sum(slots >= 0))
         algo = sum(store_bytes(n, valid))
+        if args.profile == "store":
+            call = lambda: kvq.mxfp4_mla_store(lat_d, slots_d, cache)  # noqa: E731
+        else:
+            g = torch.Generator().manual_seed(0)
+            weight = (0.5 + torch.rand(512, generator=g)).to(torch.bfloat16).to(dev)
+            call = lambda: kvq.mxfp4_mla_rmsnorm_store(  # noqa: E731
+                lat_d, weight, 1e-6, slots_d, cache)
+            algo += 1024
     elif args.profile in ("rope_mxfp8", "rope_nvfp4"):
         record = args.profile[5:]
         width = 528 if record == "mxfp8" else 288
@@ -474,7 +498,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the secondary RoPE-insert and gather measurements")
-    ap.add_argument("--profile", choices=["store", "rope_mxfp8", "rope_nvfp4", "gather"],
+    ap.add_argument("--profile", choices=["store", "rmsnorm_store", "rope_mxfp8", "rope_nvfp4",
+                                         "gather"],
                     help="run one kernel on a reduced case (for Nsight Compute) and exit")
     ap.add_argument("--profile-tokens", type=int, default=400_000)
     ap.add_argument("--profile-slots", type=int, default=0,

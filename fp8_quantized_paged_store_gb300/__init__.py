@@ -7,6 +7,7 @@ kernels. There is no fallback: if the library is not built, importing the
 functions works but every call raises.
 
   mxfp4_mla_store            quantize bf16 latent rows to 272-byte MXFP4 rows
+  mxfp4_mla_rmsnorm_store    RMSNorm (bf16 weight, eps) then the MXFP4 store, one pass
   rope_quant_insert_mxfp8    GPT-J RoPE then the 528-byte MXFP8 record
   rope_quant_insert_nvfp4    GPT-J RoPE then the 288-byte NVFP4 record
   mxfp4_mla_gather_dequant   gather packed rows back to bf16
@@ -16,7 +17,8 @@ import os
 
 import torch
 
-__all__ = ["mxfp4_mla_store", "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
+__all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
+           "rope_quant_insert_nvfp4",
            "mxfp4_mla_gather_dequant", "row_bytes", "cache_view", "KvqError", "lib",
            "LIBRARY_PATH"]
 
@@ -48,6 +50,9 @@ def lib() -> ctypes.CDLL:
         L.kvq_row_bytes.argtypes = [_i64, _i64]
         L.mxfp4_mla_store.restype = ctypes.c_int
         L.mxfp4_mla_store.argtypes = [_p, _i64, _i64, _i64, _p, _p, _i64, _i64, _i64, _i32, _p]
+        L.mxfp4_mla_rmsnorm_store.restype = ctypes.c_int
+        L.mxfp4_mla_rmsnorm_store.argtypes = [_p, _i64, _i64, _i64, _p, ctypes.c_float, _p, _p,
+                                              _i64, _i64, _i64, _i32, _p]
         for name in ("rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -113,6 +118,28 @@ def mxfp4_mla_store(latent: torch.Tensor, slot_mapping: torch.Tensor, cache: tor
     _check("mxfp4_mla_store", lib().mxfp4_mla_store(
         latent.data_ptr(), latent.shape[0], latent.shape[1], latent.stride(0),
         slot_mapping.data_ptr(), cache.data_ptr(), nb, bs, bsr, group, _stream(stream)))
+
+
+def mxfp4_mla_rmsnorm_store(latent: torch.Tensor, weight: torch.Tensor, eps: float,
+                            slot_mapping: torch.Tensor, cache: torch.Tensor, group: int = 32,
+                            stream=None) -> None:
+    """RMSNorm of each latent row (bf16 weight [512], fp32 eps), then the
+    MXFP4 store, in one pass; arguments otherwise as mxfp4_mla_store."""
+    _need(latent, torch.bfloat16, "latent")
+    _need(weight, torch.bfloat16, "weight")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    if latent.dim() != 2 or latent.stride(1) != 1:
+        raise ValueError("latent must be [tokens, latent_dim] with unit column stride")
+    if weight.shape != (latent.shape[1],) or not weight.is_contiguous():
+        raise ValueError("weight must be a contiguous [latent_dim] tensor")
+    if slot_mapping.dim() != 1 or slot_mapping.numel() < latent.shape[0] or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous [tokens] tensor")
+    nb, bs, bsr = cache_view(cache, row_bytes(latent.shape[1], group))
+    _check("mxfp4_mla_rmsnorm_store", lib().mxfp4_mla_rmsnorm_store(
+        latent.data_ptr(), latent.shape[0], latent.shape[1], latent.stride(0), weight.data_ptr(),
+        float(eps), slot_mapping.data_ptr(), cache.data_ptr(), nb, bs, bsr, group,
+        _stream(stream)))
 
 
 def _rope(name, record, latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,

@@ -10,8 +10,10 @@
 //   * lane i reads slot_mapping of token i of a 32-token window once and turns
 //     it into the row's byte offset (one division per lane per window);
 //   * rows stream through a per-warp shared-memory ring filled by cp.async
-//     four rows ahead of the row being quantized (pad tokens issue no copy),
-//     which keeps ~160 KiB of loads in flight per SM;
+//     three rows ahead of the row being quantized (pad tokens issue no copy);
+//     with 32 KiB of ring per block, six blocks (48 warps, ~144 KiB of loads
+//     in flight) fit an SM, which measured faster than four rows ahead with
+//     five blocks, or two rows ahead;
 //   * one row is 1 KiB read as two fully coalesced 512-byte warp copies: lane
 //     l holds elements 8l..8l+7 (half 0, groups 0..7) and 256+8l..256+8l+7
 //     (half 1, groups 8..15), so a 32-element group spans four lanes;
@@ -22,6 +24,7 @@
 //     by cvt.rn.satfinite.e2m1x2.f32 (NaN and -0.0 are cleared first);
 //   * each lane stores two 4-byte code words (two coalesced 128-byte warp
 //     stores) and four lanes store the two scale bytes of their groups.
+#include <cmath>
 #include <cstdint>
 
 #include "kvq.h"
@@ -43,6 +46,8 @@ struct StoreParams {
   int64_t num_slots;        // num_blocks * block_size
   int64_t block_size;
   int64_t block_stride_rows;
+  const uint8_t* weight;  // RMSNorm weight, bf16 [512] (fused variant only)
+  float eps;
 };
 
 // Eight bf16 (one 16-byte load) of a group with scale 2**e -> eight E2M1
@@ -128,10 +133,56 @@ __device__ __forceinline__ void quantize_store_row(uint4 x0, uint4 x1, uint8_t* 
   }
 }
 
+// RMSNorm of one row held by the warp (fused variant), in the order this
+// library fixes so that the result is reproducible bit for bit: lane l sums
+// the squares of its 16 values (half 0 then half 1, left to right, each
+// square and sum rounded to binary32), an xor-butterfly over strides 1, 2, 4,
+// 8, 16 adds the lane sums (every lane ends with the same bits, since each
+// step adds the same two operands), then r = RN(1 / RN(sqrt(S / 512 + eps)))
+// with correctly rounded square root and reciprocal, y = bf16(x * r) and
+// z = bf16(y * w). A bf16 product is exact in binary32, so mul.rn.bf16x2
+// rounds it once.
+__device__ __forceinline__ uint32_t bf16x2_from_f32(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void rmsnorm_row(uint4& x0, uint4& x1, const uint4& w0, const uint4& w1,
+                                            float eps) {
+  const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[2 * k] = bf16_lo(xw[k]);
+    v[2 * k + 1] = bf16_hi(xw[k]);
+  }
+  float acc = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc = __fadd_rn(acc, __fmul_rn(v[k], v[k]));
+#pragma unroll
+  for (int stride = 1; stride < 32; stride *= 2)
+    acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, stride));
+  const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(acc, 0x1p-9f), eps)));
+  const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  uint32_t z[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    z[k] = bf16x2_mul(bf16x2_from_f32(__fmul_rn(v[2 * k], r), __fmul_rn(v[2 * k + 1], r)), ww[k]);
+  x0 = make_uint4(z[0], z[1], z[2], z[3]);
+  x1 = make_uint4(z[4], z[5], z[6], z[7]);
+}
+
 // Prefetch distance (rows per warp in flight) and ring stages: one more stage
 // than the distance, so the copy issued at the top of an iteration never
 // lands in the stage being read in that iteration.
-constexpr int kPrefetch = 4;
+constexpr int kPrefetch = 3;
 constexpr int kStages = kPrefetch + 1;
 constexpr int kStageVecs = 64;  // one 1 KiB row = 64 x 16 bytes
 constexpr size_t kStoreSmem = (size_t)kStoreWarps * kStages * kStageVecs * sizeof(uint4);
@@ -159,7 +210,7 @@ __device__ __forceinline__ uint32_t row_index(const StoreParams& p, int64_t t, i
 // loaded early so that prefetches crossing into it find their indices ready.
 // The loop is unrolled over the ring's stages so that stage offsets are
 // constants.
-template <bool kFlat>
+template <bool kFlat, bool kNorm>
 __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams p) {
   extern __shared__ uint4 smem[];
   const int lane = threadIdx.x & 31;
@@ -173,6 +224,11 @@ __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams 
   if (n <= 0) return;
   const uint8_t* src = p.latent + t_begin * p.row_pitch + 16 * lane;
   const uint32_t pitch = (uint32_t)p.row_pitch;
+  uint4 wt0 = make_uint4(0, 0, 0, 0), wt1 = wt0;  // the lane's RMSNorm weights
+  if (kNorm) {
+    wt0 = ld_once_v4(p.weight + 16 * lane);
+    wt1 = ld_once_v4(p.weight + 512 + 16 * lane);
+  }
 
   uint32_t w0 = row_index<kFlat>(p, t_begin + lane, t_end);       // tokens [0, 32)
   uint32_t w1 = row_index<kFlat>(p, t_begin + 32 + lane, t_end);  // tokens [32, 64)
@@ -205,25 +261,29 @@ __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams 
               i + kPrefetch < n ? rp : 0xFFFFFFFFu);
         cp_async_wait<kPrefetch>();  // row i has landed
         const uint32_t row = __shfl_sync(0xFFFFFFFFu, w0, k);
-        if (row != 0xFFFFFFFFu)
-          quantize_store_row(lds_v4(ring + u * kStageVecs), lds_v4(ring + u * kStageVecs + 32),
-                             p.cache + (size_t)row * kMxfp4RowBytes, lane);
+        if (row != 0xFFFFFFFFu) {
+          uint4 x0 = lds_v4(ring + u * kStageVecs), x1 = lds_v4(ring + u * kStageVecs + 32);
+          if (kNorm) rmsnorm_row(x0, x1, wt0, wt1, p.eps);
+          quantize_store_row(x0, x1, p.cache + (size_t)row * kMxfp4RowBytes, lane);
+        }
       }
     }
   }
   cp_async_wait<0>();
 }
 
-int g_store_occupancy[2][64];
+int g_store_occupancy[4][64];
 
 }  // namespace
 }  // namespace kvq
 
-extern "C" int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int64_t latent_dim,
-                               int64_t row_stride_elems, const int64_t* slot_mapping,
-                               uint8_t* cache, int64_t num_blocks, int64_t block_size,
-                               int64_t block_stride_rows, int32_t group, cudaStream_t stream) {
-  using namespace kvq;
+namespace kvq {
+namespace {
+
+int store_entry(const void* latent_bf16, int64_t num_tokens, int64_t latent_dim,
+                int64_t row_stride_elems, const void* weight_bf16, float eps, bool norm,
+                const int64_t* slot_mapping, uint8_t* cache, int64_t num_blocks, int64_t block_size,
+                int64_t block_stride_rows, int32_t group, cudaStream_t stream) {
   if (latent_dim != kLatent || group != 32) return KVQ_EINVAL;
   if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || block_stride_rows < block_size)
     return KVQ_EINVAL;
@@ -235,10 +295,12 @@ extern "C" int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int6
   // cache rows are addressed with 32-bit indices (2**32 rows would be 1.1 TB)
   if ((num_blocks - 1) * block_stride_rows + block_size > (int64_t)0xFFFFFFFE) return KVQ_EINVAL;
   if (row_stride_elems * 2 > (int64_t)0xFFFFFFFF) return KVQ_EINVAL;
+  if (norm && !(eps >= 0.0f && eps < INFINITY)) return KVQ_EINVAL;
   if (num_tokens == 0) return KVQ_OK;
-  if (!latent_bf16 || !slot_mapping || !cache) return KVQ_EINVAL;
+  if (!latent_bf16 || !slot_mapping || !cache || (norm && !weight_bf16)) return KVQ_EINVAL;
   if (!aligned(latent_bf16, 16) || !aligned(cache, 16) || !aligned(slot_mapping, 8))
     return KVQ_EINVAL;
+  if (norm && !aligned(weight_bf16, 16)) return KVQ_EINVAL;
 
   StoreParams p;
   p.latent = static_cast<const uint8_t*>(latent_bf16);
@@ -249,15 +311,43 @@ extern "C" int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int6
   p.num_slots = num_blocks * block_size;
   p.block_size = block_size;
   p.block_stride_rows = block_stride_rows;
+  p.weight = static_cast<const uint8_t*>(weight_bf16);
+  p.eps = eps;
 
   const bool flat = (num_blocks == 1) || (block_stride_rows == block_size);
   // at least 32 tokens per warp on average, at most one wave of blocks
   const int64_t work_blocks = (num_tokens + 32 * kStoreWarps - 1) / (32 * kStoreWarps);
-  auto k = flat ? mxfp4_store_kernel<true> : mxfp4_store_kernel<false>;
-  const unsigned grid = grid_for(
-      work_blocks, resident_blocks_per_sm(k, kStoreThreads, kStoreSmem, g_store_occupancy[flat]));
+  auto k = norm ? (flat ? mxfp4_store_kernel<true, true> : mxfp4_store_kernel<false, true>)
+                : (flat ? mxfp4_store_kernel<true, false> : mxfp4_store_kernel<false, false>);
+  const unsigned grid =
+      grid_for(work_blocks, resident_blocks_per_sm(k, kStoreThreads, kStoreSmem,
+                                                   g_store_occupancy[2 * norm + flat]));
   // each warp's token count must fit the kernel's 32-bit loop counter
   if (num_tokens / ((int64_t)grid * kStoreWarps) >= (int64_t)0x7FFFFFFF) return KVQ_EINVAL;
   k<<<grid, kStoreThreads, kStoreSmem, stream>>>(p);
   return launch_status();
+}
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int64_t latent_dim,
+                               int64_t row_stride_elems, const int64_t* slot_mapping,
+                               uint8_t* cache, int64_t num_blocks, int64_t block_size,
+                               int64_t block_stride_rows, int32_t group, cudaStream_t stream) {
+  return kvq::store_entry(latent_bf16, num_tokens, latent_dim, row_stride_elems, nullptr, 0.0f,
+                          false, slot_mapping, cache, num_blocks, block_size, block_stride_rows,
+                          group, stream);
+}
+
+extern "C" int mxfp4_mla_rmsnorm_store(const void* latent_bf16, int64_t num_tokens,
+                                       int64_t latent_dim, int64_t row_stride_elems,
+                                       const void* weight_bf16, float eps,
+                                       const int64_t* slot_mapping, uint8_t* cache,
+                                       int64_t num_blocks, int64_t block_size,
+                                       int64_t block_stride_rows, int32_t group,
+                                       cudaStream_t stream) {
+  return kvq::store_entry(latent_bf16, num_tokens, latent_dim, row_stride_elems, weight_bf16, eps,
+                          true, slot_mapping, cache, num_blocks, block_size, block_stride_rows,
+                          group, stream);
 }

@@ -99,6 +99,34 @@ int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int64_t latent_
                     int32_t group, cudaStream_t stream);
 
 /*
+ * mxfp4_mla_rmsnorm_store — RMSNorm of the pre-norm latent, then the MXFP4
+ * store, in one pass (the latent is never written back as bf16).
+ * "vllm.v1.attention.ops.mxfp4_mla.store" (store_mxfp4_mla stores the
+ * post-RMSNorm latent) and
+ * "vllm.models.deepseek_v41.common.ops.fused_compress_quant_cache"
+ * (fused_save_compress_norm: bf16 [512] weight, fp32 epsilon, bf16 latent).
+ *
+ * Per token with a valid slot: the RMSNorm below, then exactly what
+ * mxfp4_mla_store does with the normalised bf16 row. The pages fix neither
+ * the summation order nor the reciprocal square root; this library fixes
+ * both so the result is reproducible bit for bit:
+ *   lane sums  p_l = sum of x^2 over elements 8l..8l+7 then 256+8l..256+8l+7
+ *              (l = 0..31, left to right, every square and sum in binary32),
+ *   S          = xor-butterfly over l with strides 1, 2, 4, 8, 16,
+ *   r          = RN(1 / RN(sqrt(RN(RN(S / 512) + eps)))),
+ *   y          = bf16(RN(x * r)),   z = bf16(y * w).
+ *
+ * weight_bf16  bf16 [512], 16-byte aligned
+ * eps          >= 0 and finite
+ * Other arguments, layout, ownership and errors as mxfp4_mla_store.
+ */
+int mxfp4_mla_rmsnorm_store(const void* latent_bf16, int64_t num_tokens, int64_t latent_dim,
+                            int64_t row_stride_elems, const void* weight_bf16, float eps,
+                            const int64_t* slot_mapping, uint8_t* cache, int64_t num_blocks,
+                            int64_t block_size, int64_t block_stride_rows, int32_t group,
+                            cudaStream_t stream);
+
+/*
  * rope_quant_insert_mxfp8 — V4.1 528-byte record: GPT-J RoPE, then MXFP8.
  * [v41] _rope_quant_insert_mxfp8_kernel, rope_quant_insert.
  *

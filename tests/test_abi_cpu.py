@@ -29,6 +29,7 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(L):
     names = declared_functions()
     assert set(names) == {"kvq_strerror", "kvq_row_bytes", "mxfp4_mla_store",
+                          "mxfp4_mla_rmsnorm_store",
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
                           "mxfp4_mla_gather_dequant"}
     for n in names:
@@ -69,6 +70,20 @@ def test_store_validation_on_host(L):
     assert f(*a) == -1
     a = list(ok); a[6] = 2 ** 62
     assert f(*a) == -1                                                   # view overflows int64
+
+
+def test_rmsnorm_store_validation_on_host(L):
+    f = L.mxfp4_mla_rmsnorm_store
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]
+    ok = [A16, 4, 512, 512, A16, 1e-6, A8, A16, 1, 8, 8, 32, None]
+    empty = list(ok); empty[1] = 0; empty[0] = None
+    assert f(*empty) == 0
+    for k, v in {4: None, 4.1: A16 + 2, 5: -1.0, 5.1: float("nan"), 5.2: float("inf"),
+                 2: 256, 9: 16}.items():
+        a = list(ok); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
 
 
 def test_insert_validation_on_host(L):
