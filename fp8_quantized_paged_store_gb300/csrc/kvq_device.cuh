@@ -41,6 +41,18 @@ __device__ __forceinline__ int64_t ld_once_i64(const int64_t* p) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t ld_once_u32(const void* p) {
+  uint32_t r;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float ld_f32(const float* p) {
+  float r;
+  asm("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t ld_u32(const void* p) {
   uint32_t r;
   asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));

@@ -153,6 +153,39 @@ def test_nvfp4_division_ties_on_gpu():
     assert G.first_diff(got, want) is None, G.first_diff(got, want)
 
 
+def _every_scale_tiles():
+    """[N, 16] bf16 tiles: for every positive E4M3 scale s, the tile amax 6*s
+    followed by every bf16 value of magnitude up to 6*s, both signs."""
+    tiles = []
+    for sb in range(1, 127):
+        s = float(oracle.e4m3_decode(np.array([sb], np.uint8))[0])
+        a = int(workloads.f32_to_bf16_bits(np.array([6.0 * s], np.float32))[0])
+        mags = np.arange(0, a + 1, dtype=np.uint16)
+        vals = np.concatenate([mags, mags | np.uint16(0x8000)])
+        vals = np.concatenate([vals, np.zeros((-vals.size) % 15, np.uint16)]).reshape(-1, 15)
+        tiles.append(np.concatenate([np.full((vals.shape[0], 1), a, np.uint16), vals], axis=1))
+    return np.concatenate(tiles)
+
+
+def test_nvfp4_every_scale_and_bf16_value():
+    """Every positive E4M3 tile scale with every finite bf16 value up to the
+    tile amax, in NoPE tiles (the kernel's code rule for bf16 numbers) and in
+    rotary tiles under an identity table (its corrected quotient): codes and
+    scales against the oracle's division, over about four million values."""
+    tiles = _every_scale_tiles()
+    tiles = np.concatenate([tiles, np.zeros(((-tiles.shape[0]) % 32, 16), np.uint16)])
+    lat = tiles.reshape(-1, 512)
+    T = lat.shape[0]
+    pages = -(-T // 64)
+    table = np.zeros((1, 64), np.float32)
+    table[0, :32] = 1.0
+    slots = np.random.default_rng(11).permutation(pages * 64)[:T].astype(np.int64)
+    cache = np.full(pages * 64 * 288, 0xAA, dtype=np.uint8)
+    got, want = _insert_both("nvfp4", lat, np.zeros(T, np.int64), table, cache, slots, pages, 64,
+                             1, False, threads=oracle.default_threads())
+    assert G.first_diff(got, want) is None, G.first_diff(got, want)
+
+
 def test_insert_rejects_bad_arguments():
     L = kvq.lib()
     lat = G.bf16_dev(np.zeros((4, 512), np.uint16))
