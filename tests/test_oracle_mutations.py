@@ -1,6 +1,7 @@
 """The pins must catch plausible mistakes in the oracle (CPU only).
 
-Each case plants one mistake in a temporary copy of oracle/kvq_oracle.c,
+Each case plants one mistake in a temporary copy of oracle/kvq_oracle.c (or
+oracle/attention.py),
 rebuilds that copy, and runs the pin test expected to catch it against the
 copy in a subprocess: that test must fail. The real oracle is not touched.
 """
@@ -74,16 +75,33 @@ MUTANTS = [
      "test_oracle_pins_store.py::test_store_paged_addressing_with_block_stride"),
     ("amax_keeps_nan", "if (a > amax) amax = a;", "if (a > amax || a != a) amax = a;",
      "test_oracle_pins_store.py::test_store_worked_row"),
+    # sparse attention (oracle/attention.py)
+    ("attn_scale_dropped", "s = float(sm_scale) * (_bf16_to_f64(q[n]) @ k.T)",
+     "s = (_bf16_to_f64(q[n]) @ k.T)",
+     "test_oracle_pins_attention.py::test_two_keys_give_the_logistic_weights", "attention.py"),
+    ("attn_pads_as_zero_rows", "valid = idx[n][(idx[n] >= 0) & (idx[n] < num_slots)]",
+     "valid = np.where((idx[n] >= 0) & (idx[n] < num_slots), idx[n], -1)",
+     "test_oracle_pins_attention.py::test_pads_are_dropped_and_order_does_not_matter",
+     "attention.py"),
+    ("attn_max_over_keys_axis", "m = s.max(axis=1, keepdims=True)",
+     "m = s.max(axis=0, keepdims=True)",
+     "test_oracle_pins_attention.py::test_brute_force_loops_on_a_tiny_case", "attention.py"),
+    ("attn_lse_without_max", "lse[n] = m[:, 0] + np.log(l[:, 0])", "lse[n] = np.log(l[:, 0])",
+     "test_oracle_pins_attention.py::test_single_valid_key_returns_its_row", "attention.py"),
+    ("attn_abs_values", "out[n] = (p @ k) / l", "out[n] = (p @ np.abs(k)) / l",
+     "test_oracle_pins_attention.py::test_single_valid_key_returns_its_row", "attention.py"),
 ]
 
 
-@pytest.mark.parametrize("name,orig,mutated,pin", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pin_catches_planted_mistake(tmp_path, name, orig, mutated, pin):
-    src = open(os.path.join(ROOT, "oracle", "kvq_oracle.c")).read()
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pin_catches_planted_mistake(tmp_path, mutant):
+    name, orig, mutated, pin = mutant[:4]
+    target = mutant[4] if len(mutant) > 4 else "kvq_oracle.c"
+    src = open(os.path.join(ROOT, "oracle", target)).read()
     assert src.count(orig) == 1, f"{name}: the text to mutate is not unique in the oracle"
     shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
                     ignore=shutil.ignore_patterns("*.so", "__pycache__", "*.tmp*"))
-    (tmp_path / "oracle" / "kvq_oracle.c").write_text(src.replace(orig, mutated))
+    (tmp_path / "oracle" / target).write_text(src.replace(orig, mutated))
     shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests",
                     ignore=shutil.ignore_patterns("__pycache__", "test_*.py"))
     shutil.copy(os.path.join(ROOT, "tests", pin.split("::")[0]), tmp_path / "tests")

@@ -18,6 +18,7 @@ the recipe and shrink the counts for fast tests):
   store_large   4,300,000 tokens, source row stride 576, 8,388,608 slots
   rope_insert   65,536 tokens (or 4,194,304 for the large variant), R = 4
   gather        1,048,576-slot packed cache, 128 queries x 2048 indices
+  sparse_attention  the gather's cache and indices + 128 heads of bf16 queries
 """
 import math
 import os
@@ -242,3 +243,18 @@ def gather(seed: int = 0, num_slots: int = 1_048_576, num_queries: int = 128, to
             idx[q, topk - p:] = -1
     return dict(fill_latent=fill_latent, fill_slots=fill_slots, indices=idx, num_blocks=1,
                 block_size=num_slots, block_stride_rows=num_slots, num_slots=num_slots)
+
+
+# ------------------------------------------------------- sparse attention ---
+
+def sparse_attention(seed: int = 0, num_queries: int = 128, num_heads: int = 128,
+                     topk: int = 2048, num_slots: int = 1_048_576, max_pad: int = 64) -> dict:
+    """The gather workload's cache fill and top-k indices, plus decode queries
+    q: bf16 N(0, 1) [num_queries, num_heads, 512] (absorbed NoPE queries in the
+    latent space), and sm_scale = 1/sqrt(512)."""
+    d = gather(seed, num_slots, num_queries, topk, max_pad)
+    q = np.empty((num_queries * num_heads, LATENT), dtype=np.uint16)
+    _draw_rows(seed, num_queries * num_heads, LATENT, _normal, q, tag=7)
+    d["q"] = q.reshape(num_queries, num_heads, LATENT)
+    d["sm_scale"] = 1.0 / math.sqrt(LATENT)
+    return d
