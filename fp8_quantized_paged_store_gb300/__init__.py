@@ -11,6 +11,7 @@ functions works but every call raises.
   rope_quant_insert_mxfp8    GPT-J RoPE then the 528-byte MXFP8 record
   rope_quant_insert_nvfp4    GPT-J RoPE then the 288-byte NVFP4 record
   mxfp4_mla_gather_dequant   gather packed rows back to bf16
+  mxfp4_mla_sparse_attention sparse MLA decode attention on the packed cache
 """
 import ctypes
 import os
@@ -19,7 +20,8 @@ import torch
 
 __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
            "rope_quant_insert_nvfp4",
-           "mxfp4_mla_gather_dequant", "row_bytes", "cache_view", "KvqError", "lib",
+           "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "row_bytes",
+           "cache_view", "KvqError", "lib",
            "LIBRARY_PATH"]
 
 LIBRARY_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
@@ -60,6 +62,10 @@ def lib() -> ctypes.CDLL:
                           _p]
         L.mxfp4_mla_gather_dequant.restype = ctypes.c_int
         L.mxfp4_mla_gather_dequant.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _p, _i64, _p]
+        L.mxfp4_mla_sparse_attention.restype = ctypes.c_int
+        L.mxfp4_mla_sparse_attention.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64, _i64,
+                                                 _p, _i64, ctypes.c_float, _p, _i64, _i64, _p, _p,
+                                                 _p]
         _LIB = L
     return _LIB
 
@@ -201,3 +207,38 @@ def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: to
         cache.data_ptr(), nb, bs, bsr, latent_dim, indices.data_ptr(), indices.numel(),
         out.data_ptr(), flat.stride(0), _stream(stream)))
     return out
+
+
+def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tensor,
+                               sm_scale: float, out: torch.Tensor = None, lse: torch.Tensor = None,
+                               status: torch.Tensor = None, stream=None):
+    """q: bf16 [num_queries, num_heads <= 128, 512] (unit last stride, strides
+    multiples of 8); cache: uint8 paged view (see cache_view) of 272-byte rows;
+    indices: int64 [num_queries, topk] (contiguous; -1 pads). Returns (out bf16
+    [num_queries, num_heads, 512], lse fp32 [num_queries, num_heads] or None).
+    ``status`` (int32, one element) is set nonzero if a kernel wait timed out."""
+    _need(q, torch.bfloat16, "q")
+    _need(indices, torch.int64, "indices")
+    if q.dim() != 3 or q.shape[2] != 512 or q.stride(2) != 1:
+        raise ValueError("q must be [num_queries, num_heads, 512] with unit last stride")
+    nq, nh, _ = q.shape
+    if indices.dim() != 2 or indices.shape[0] != nq or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous [num_queries, topk] tensor")
+    nb, bs, bsr = cache_view(cache, row_bytes(512, 32))
+    if out is None:
+        out = torch.empty((nq, nh, 512), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    if out.dim() != 3 or tuple(out.shape) != (nq, nh, 512) or out.stride(2) != 1:
+        raise ValueError("out must be [num_queries, num_heads, 512] with unit last stride")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+        if tuple(lse.shape) != (nq, nh) or not lse.is_contiguous():
+            raise ValueError("lse must be a contiguous [num_queries, num_heads] tensor")
+    if status is not None:
+        _need(status, torch.int32, "status")
+    _check("mxfp4_mla_sparse_attention", lib().mxfp4_mla_sparse_attention(
+        q.data_ptr(), nq, nh, q.stride(0), q.stride(1), cache.data_ptr(), nb, bs, bsr,
+        indices.data_ptr(), indices.shape[1], float(sm_scale), out.data_ptr(), out.stride(0),
+        out.stride(1), lse.data_ptr() if lse is not None else None,
+        status.data_ptr() if status is not None else None, _stream(stream)))
+    return out, lse

@@ -205,6 +205,50 @@ int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks, int64_t b
                              int64_t num_indices, void* out_bf16, int64_t out_row_stride_elems,
                              cudaStream_t stream);
 
+/*
+ * mxfp4_mla_sparse_attention — sparse MLA decode attention computed directly
+ * on the packed MXFP4 cache. [pr] Details (read path: the top-k rows of each
+ * query are gathered, unpacked to bf16 and feed both dots, q.k and p.v);
+ * [pr] Claims (attention over the packed cache equals attention over the
+ * dequantized bf16 values). For the rope-free latent a token's key and value
+ * are the same 512-wide row.
+ *
+ * For query n and head h (h < num_heads), over the valid indices j of row n
+ * of `indices` (0 <= s < num_blocks*block_size; pads and out-of-range
+ * entries are dropped, repeats count as separate entries):
+ *   s_j   = sm_scale * sum_d q[n,h,d] * k_j[d],   k_j = the dequantized row
+ *   out[n,h,:] = sum_j softmax(s)_j * k_j          (bf16)
+ *   lse[n,h]   = log(sum_j exp(s_j))               (natural log, fp32)
+ * A query with no valid index gets out = 0 and lse = -inf.
+ * Arithmetic: bf16 inputs, fp32 accumulation on the tensor cores, fp32
+ * softmax with exp2, probabilities rounded to bf16 for the p.v product, the
+ * output rounded to bf16 once: |out - exact| is within about 2**-8 of
+ * sum_j softmax(s)_j |k_j[d]| plus the final bf16 rounding.
+ *
+ * q_bf16           bf16; head h of query n at element
+ *                  n*q_query_stride + h*q_head_stride (both multiples of 8,
+ *                  q_head_stride >= 512), 16-byte aligned base
+ * num_queries      >= 0; num_heads in [1, 128]
+ * cache            as mxfp4_mla_store (272-byte rows, block stride in rows)
+ * indices          int64 [num_queries, topk], row-major; topk >= 0
+ * sm_scale         finite, >= 0
+ * out_bf16         bf16; head h of query n at element
+ *                  n*out_query_stride + h*out_head_stride (multiples of 8,
+ *                  out_head_stride >= 512), 16-byte aligned base
+ * lse              fp32 [num_queries, num_heads] or NULL
+ * status           device int32 or NULL: set to a nonzero value if an
+ *                  internal wait of the kernel timed out (the output is then
+ *                  undefined); never written otherwise
+ * The library allocates nothing and keeps no pointer after the call.
+ */
+int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries, int64_t num_heads,
+                               int64_t q_query_stride, int64_t q_head_stride,
+                               const uint8_t* cache, int64_t num_blocks, int64_t block_size,
+                               int64_t block_stride_rows, const int64_t* indices, int64_t topk,
+                               float sm_scale, void* out_bf16, int64_t out_query_stride,
+                               int64_t out_head_stride, float* lse, int32_t* status,
+                               cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) == {"kvq_strerror", "kvq_row_bytes", "mxfp4_mla_store",
                           "mxfp4_mla_rmsnorm_store",
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
-                          "mxfp4_mla_gather_dequant"}
+                          "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention"}
     for n in names:
         assert hasattr(L, n), n
     # exported with C linkage from the shared object itself
@@ -109,7 +109,24 @@ def test_gather_validation_on_host(L):
         assert f(*a) == -1, (k, v)
 
 
+def test_attention_validation_on_host(L):
+    f = L.mxfp4_mla_sparse_attention
+    ok = [A16, 2, 128, 128 * 512, 512, A16, 1, 8, 8, A8, 16, 0.05, A16, 128 * 512, 512, None,
+          None, None]
+    empty = list(ok); empty[1] = 0; empty[0] = None
+    assert f(*empty) == 0
+    bad = {1: -1, 2: 0, 2.1: 129, 4: 256, 4.1: 516, 3: 12, 6: 0, 7: 0, 8: 7, 10: -1,
+           11: -0.5, 11.1: float("nan"), 11.2: float("inf"), 13: 4, 14: 500, 0: A16 + 2,
+           5: A16 + 8, 9: A8 + 4, 12: A16 + 8, 15: A16 + 2, 16: A16 + 1}
+    for k, v in bad.items():
+        a = list(ok); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
+    a = list(ok); a[0] = None
+    assert f(*a) == -1
+
+
 def test_binding_has_the_abi_names():
-    for n in ("mxfp4_mla_store", "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
-              "mxfp4_mla_gather_dequant"):
+    for n in ("mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
+              "rope_quant_insert_nvfp4", "mxfp4_mla_gather_dequant",
+              "mxfp4_mla_sparse_attention"):
         assert callable(getattr(kvq, n))

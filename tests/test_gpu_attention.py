@@ -1,0 +1,165 @@
+"""GPU parity of mxfp4_mla_sparse_attention against the float64 oracle.
+
+The kernel rounds the probabilities to bf16 for the p.v product and the
+output to bf16, and accumulates in fp32 on the tensor cores, so outputs are
+compared with a bound derived from that arithmetic rather than bit for bit:
+  |out - exact| <= 2**-7 * (sum_j softmax_j |k_j[d]| + |exact|) + 2**-100
+per element (the bf16 rounding of P contributes at most 2**-9 of the first
+term, the final rounding 2**-9 of the second, fp32 score and exp2 errors well
+under 2**-12; 2**-7 leaves a margin of about four). The absolute 2**-100
+covers the fp32 floor: exp2 flushes probabilities below 2**-126 of the
+running maximum to zero, and at most 2**11 keys with |k| < 2**14 can lose
+less than 2**-101 that way (an exact output of 6e-50 comes out as 0).
+lse: |lse - exact| <= 2e-3.
+The packed cache is written by the oracle's store, never by the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import fp8_quantized_paged_store_gb300 as kvq
+import oracle
+import workloads
+from oracle.attention import mxfp4_mla_sparse_attention as attn_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    __graft_entry__.build()
+
+
+def _fill_cache(num_slots, seed, num_blocks=1, block_size=None, block_stride_rows=None):
+    block_size = block_size or num_slots
+    block_stride_rows = block_stride_rows or block_size
+    rng = np.random.default_rng(seed)
+    lat = workloads.f32_to_bf16_bits(
+        (rng.standard_t(4, (num_slots, 512)) * 0.5).astype(np.float32))
+    rows = (num_blocks - 1) * block_stride_rows + block_size
+    cache = np.full(rows * 272, 0x5A, np.uint8)
+    oracle.mxfp4_mla_store(lat, np.arange(num_slots, dtype=np.int64), cache, num_blocks,
+                           block_size, block_stride_rows, threads=oracle.default_threads())
+    return cache
+
+
+def _run(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full=None):
+    """Kernel on the GPU; q_full (optional) is a wider buffer q is a view of."""
+    dev = torch.device("cuda", 0)
+    src = q if q_full is None else q_full
+    qd = torch.from_numpy(np.ascontiguousarray(src).view(np.int16)).to(dev).view(torch.bfloat16)
+    if q_full is not None:
+        qd = qd[:, :q.shape[1], :512]
+    cd = torch.from_numpy(cache).to(dev)
+    if num_blocks > 1:
+        cd = cd.as_strided((num_blocks, block_size, 272), (block_stride_rows * 272, 272, 1))
+    else:
+        cd = cd[:num_blocks * block_size * 272]
+    idd = torch.from_numpy(np.ascontiguousarray(idx)).to(dev)
+    lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, _ = kvq.mxfp4_mla_sparse_attention(qd, cd, idd, sm_scale, lse=lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "a kernel wait timed out"
+    o = out.float().cpu().numpy().astype(np.float64)
+    return o, lse.cpu().numpy().astype(np.float64)
+
+
+def _check(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full=None):
+    out, lse = _run(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full)
+    want, want_lse, mass = attn_oracle(q, cache, num_blocks, block_size, block_stride_rows, idx,
+                                       sm_scale)
+    err = np.abs(out - want)
+    bound = 2.0 ** -7 * (mass + np.abs(want)) + 2.0 ** -100
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, (bad[:5], out[tuple(bad[0])], want[tuple(bad[0])],
+                           mass[tuple(bad[0])])
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.all(np.isneginf(lse[~fin]))
+    np.testing.assert_allclose(lse[fin], want_lse[fin], rtol=0, atol=2e-3)
+    assert np.all(out[~fin] == 0)
+    return out, want
+
+
+def _queries(seed, nq, nh, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return workloads.f32_to_bf16_bits((rng.standard_normal((nq, nh, 512)) * scale)
+                                      .astype(np.float32))
+
+
+def test_small_two_tiles_with_pads():
+    cache = _fill_cache(4096, seed=1)
+    q = _queries(2, 3, 128)
+    rng = np.random.default_rng(3)
+    idx = np.stack([rng.permutation(4096)[:64] for _ in range(3)]).astype(np.int64)
+    idx[0, 60:] = -1
+    idx[1, 5] = 4096                         # outside the cache: dropped
+    idx[2, ::7] = -1
+    _check(q, cache, idx, 1 / np.sqrt(512), 1, 4096, 4096)
+
+
+@pytest.mark.parametrize("heads", [1, 64, 127, 128])
+@pytest.mark.parametrize("topk", [1, 31, 33, 100])
+def test_ragged_heads_and_topk(heads, topk):
+    cache = _fill_cache(2048, seed=4)
+    q = _queries(5 + heads, 2, heads)
+    rng = np.random.default_rng(topk)
+    idx = np.stack([rng.integers(-1, 2048, topk) for _ in range(2)]).astype(np.int64)
+    idx[:, 0] = rng.integers(0, 2048, 2)     # at least one valid key per query
+    _check(q, cache, idx, 0.05, 1, 2048, 2048)
+
+
+def test_paged_cache_with_block_stride_and_strided_query():
+    nb, bs, bsr = 40, 64, 96
+    cache = _fill_cache(nb * bs, seed=6, num_blocks=nb, block_size=bs, block_stride_rows=bsr)
+    rng = np.random.default_rng(7)
+    q_full = workloads.f32_to_bf16_bits(rng.standard_normal((4, 130, 576)).astype(np.float32))
+    q = np.ascontiguousarray(q_full[:, :128, :512])
+    idx = np.stack([rng.permutation(nb * bs)[:256] for _ in range(4)]).astype(np.int64)
+    _check(q, cache, idx, 0.04, nb, bs, bsr, q_full=q_full)
+
+
+def test_queries_without_valid_keys_and_empty_topk():
+    cache = _fill_cache(256, seed=8)
+    q = _queries(9, 3, 128)
+    idx = np.array([[-1] * 40, [300] * 40, list(range(40))], np.int64)
+    out, _ = _check(q, cache, idx, 0.05, 1, 256, 256)
+    assert np.all(out[:2] == 0)
+    out0, lse0 = _run(q, cache, np.zeros((3, 0), np.int64), 0.05, 1, 256, 256)
+    assert np.all(out0 == 0) and np.all(np.isneginf(lse0))
+
+
+def test_growing_scores_exercise_the_output_rescale():
+    """Keys ordered by increasing score with a large scale: the running max
+    grows by more than 2**8 (log2 units) from tile to tile several times."""
+    cache = _fill_cache(1024, seed=10)
+    q = _queries(11, 1, 128)
+    rows = oracle.mxfp4_mla_gather_dequant(cache, 1, 1024, 1024, np.arange(1024, dtype=np.int64))
+    k = (rows.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    qd = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    order = np.argsort(k @ qd[0, 0])           # ascending for head 0
+    idx = order[None, -512:].astype(np.int64)
+    _check(q, cache, idx, 2.0, 1, 1024, 1024)
+
+
+def test_full_workload_128_queries_2048_keys():
+    """The benchmark workload: 1,048,576-slot cache, 128 queries x 128 heads x
+    2048 top-k indices with trailing pads; every output compared."""
+    w = workloads.sparse_attention(seed=0)
+    cache = np.zeros(w["num_slots"] * 272, np.uint8)
+    oracle.mxfp4_mla_store(w["fill_latent"], w["fill_slots"], cache, 1, w["num_slots"],
+                           w["num_slots"], threads=oracle.default_threads())
+    _check(w["q"], cache, w["indices"], w["sm_scale"], 1, w["num_slots"], w["num_slots"])
+
+
+def test_rejects_bad_arguments_on_gpu():
+    dev = torch.device("cuda", 0)
+    q = torch.zeros((2, 129, 512), dtype=torch.bfloat16, device=dev)
+    cache = torch.zeros(64 * 272, dtype=torch.uint8, device=dev)
+    idx = torch.zeros((2, 4), dtype=torch.int64, device=dev)
+    with pytest.raises(kvq.KvqError):
+        kvq.mxfp4_mla_sparse_attention(q, cache, idx, 0.1)    # 129 heads
+    with pytest.raises(kvq.KvqError):
+        kvq.mxfp4_mla_sparse_attention(q[:, :4], cache, idx, float("nan"))

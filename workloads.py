@@ -247,14 +247,19 @@ def gather(seed: int = 0, num_slots: int = 1_048_576, num_queries: int = 128, to
 
 # ------------------------------------------------------- sparse attention ---
 
-def sparse_attention(seed: int = 0, num_queries: int = 128, num_heads: int = 128,
-                     topk: int = 2048, num_slots: int = 1_048_576, max_pad: int = 64) -> dict:
-    """The gather workload's cache fill and top-k indices, plus decode queries
-    q: bf16 N(0, 1) [num_queries, num_heads, 512] (absorbed NoPE queries in the
-    latent space), and sm_scale = 1/sqrt(512)."""
-    d = gather(seed, num_slots, num_queries, topk, max_pad)
+def attention_queries(seed: int = 0, num_queries: int = 128, num_heads: int = 128) -> np.ndarray:
+    """Decode queries: bf16 N(0, 1) [num_queries, num_heads, 512] (absorbed
+    NoPE queries in the latent space)."""
     q = np.empty((num_queries * num_heads, LATENT), dtype=np.uint16)
     _draw_rows(seed, num_queries * num_heads, LATENT, _normal, q, tag=7)
-    d["q"] = q.reshape(num_queries, num_heads, LATENT)
+    return q.reshape(num_queries, num_heads, LATENT)
+
+
+def sparse_attention(seed: int = 0, num_queries: int = 128, num_heads: int = 128,
+                     topk: int = 2048, num_slots: int = 1_048_576, max_pad: int = 64) -> dict:
+    """The gather workload's cache fill and top-k indices, plus the decode
+    queries of attention_queries, and sm_scale = 1/sqrt(512)."""
+    d = gather(seed, num_slots, num_queries, topk, max_pad)
+    d["q"] = attention_queries(seed, num_queries, num_heads)
     d["sm_scale"] = 1.0 / math.sqrt(LATENT)
     return d
