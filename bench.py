@@ -14,8 +14,9 @@ of 272-byte rows, 1% pad slots. One step = one store of the whole batch.
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
   paths      the other hot-path rows measured in the same run: the
              RMSNorm-fused store on the same batch, the V4.1 RoPE inserts
-             (MXFP8, NVFP4) on 4,194,304 tokens and the gather of 128 x 2048
-             rows from a 1,048,576-slot cache
+             (MXFP8, NVFP4) on 4,194,304 tokens, the gather of 128 x 2048
+             rows from a 1,048,576-slot cache, and sparse attention of 128
+             queries x 128 heads over the same rows (TFLOP/s)
 
 --impl reference times the CPU oracle instead (the only reference this
 project has), on the same workload, metric and unit.
@@ -87,6 +88,31 @@ def peaks():
         return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback (6.8 TB/s)"
+
+
+def bf16_peak():
+    """(TFLOP/s, source) of a dense bf16 contraction timed alone."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback (1.9 PFLOP/s)"
+
+
+def attention_case(torch, kvq, dev, cache, idx, valid):
+    """(call, flops, hbm bytes, status tensor) of sparse attention over the
+    gather workload's cache and indices: 128 queries x 128 heads."""
+    q = torch.from_numpy(workloads.attention_queries(0, 128, 128).view(np.int16)).to(dev)
+    q = q.view(torch.bfloat16)
+    idx2 = idx.view(128, -1)
+    outa = torch.empty((128, 128, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((128, 128), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    call = lambda: kvq.mxfp4_mla_sparse_attention(  # noqa: E731
+        q, cache, idx2, 1.0 / 512 ** 0.5, out=outa, lse=lse, status=status)
+    flops = 4.0 * 128 * valid * 512            # q.k and p.v over the valid keys, 128 heads
+    hbm = ROW * valid + 8 * idx.numel() + 2 * 128 * 128 * 1024 + 4 * 128 * 128
+    return call, flops, hbm, status
 
 
 def store_bytes(num_tokens, valid):
@@ -309,6 +335,19 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
         "rows_per_s": idx.numel() / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
         "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
         "l2": "flushed before each rep"}
+
+    # sparse MLA decode attention on the same packed cache and indices
+    call, flops, hbm, status = attention_case(torch, kvq, dev, cache, idx, valid)
+    for _ in range(3):
+        call()
+    ms, _ = time_events(torch, call, 20, stream, flush=flush)
+    tpeak, tpeak_src = bf16_peak()
+    out["mxfp4_mla_sparse_attention"] = {
+        "workload": "128 queries x 128 heads x 2048 top-k (trailing pads), 1,048,576 slots",
+        "ms": ms, "algorithmic_flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
+        "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tpeak, "bf16_peak_tflops": tpeak,
+        "bf16_peak_source": tpeak_src, "hbm_bytes": hbm, "gbs": hbm / (ms * 1e-3) / 1e9,
+        "wait_status": int(status.item()), "l2": "flushed before each rep"}
     return out
 
 
@@ -470,16 +509,19 @@ def run_profile(args):
         call = lambda: fn(lat_d, pos, tab, cache, sl, 4)  # noqa: E731
         writers = int(np.sum((w["cache_slots"] >= 0) & ((w["positions"] + 1) % 4 == 0)))
         algo = 16 * n + writers * (1024 + 256 + width)
-    else:
+    else:  # gather, attention
         g = workloads.gather(seed=0)
         lat_d = torch.from_numpy(g["fill_latent"].view(np.int16)).to(dev).view(torch.bfloat16)
         cache = torch.empty(g["num_slots"] * ROW, dtype=torch.uint8, device=dev)
         kvq.mxfp4_mla_store(lat_d, torch.from_numpy(g["fill_slots"]).to(dev), cache)
         idx = torch.from_numpy(g["indices"]).to(dev)
-        out = torch.empty((idx.numel(), 512), dtype=torch.bfloat16, device=dev)
-        call = lambda: kvq.mxfp4_mla_gather_dequant(cache, idx, out=out)  # noqa: E731
         valid = int(np.sum(g["indices"] >= 0))
-        algo = 8 * idx.numel() + ROW * valid + 1024 * idx.numel()
+        if args.profile == "gather":
+            out = torch.empty((idx.numel(), 512), dtype=torch.bfloat16, device=dev)
+            call = lambda: kvq.mxfp4_mla_gather_dequant(cache, idx, out=out)  # noqa: E731
+            algo = 8 * idx.numel() + ROW * valid + 1024 * idx.numel()
+        else:
+            call, _, algo, _ = attention_case(torch, kvq, dev, cache, idx, valid)
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
@@ -499,7 +541,7 @@ def main():
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the secondary RoPE-insert and gather measurements")
     ap.add_argument("--profile", choices=["store", "rmsnorm_store", "rope_mxfp8", "rope_nvfp4",
-                                         "gather"],
+                                         "gather", "attention"],
                     help="run one kernel on a reduced case (for Nsight Compute) and exit")
     ap.add_argument("--profile-tokens", type=int, default=400_000)
     ap.add_argument("--profile-slots", type=int, default=0,

@@ -7,26 +7,32 @@
 // attention over the dequantized bf16 values). For the rope-free latent the
 // key and the value of a token are the same 512-wide row.
 //
-// Work decomposition. One CTA (128 threads, one TMEM lane and one head per
-// thread) per (query, half of the 512 value columns): the two CTAs of a query
-// both form the full scores q.k (512-deep) and each accumulates 256 output
-// columns, so the output accumulator (128 heads x 256 fp32 = 256 TMEM
-// columns) and two 32-key score buffers fit the 512 TMEM columns. Keys go in
-// tiles of 32:
-//   - warp 0 stages the packed rows of tile t+2 with cp.async (17 x 16 bytes
-//     per key; pads and out-of-range indices copy nothing and get a -inf
-//     score bias);
-//   - all threads dequantize tile t+1 into bf16 (byte-permute decode) in the
-//     128-byte-swizzled K-major layout the tensor core reads, zero rows for
-//     pads; thread 0 then issues S(t+1) = Q K^T (M 128, N 32, K 512) into
-//     the free score buffer;
-//   - meanwhile all threads take the scores of tile t from TMEM, run the
-//     online softmax in fp32 (exp2, running max with a rescale of the output
-//     only when the max grows by more than 2**8), and write P (bf16) to
-//     shared memory; thread 0 issues O += P V (M 128, N 256, K 32), reading
-//     the same dequantized key tile as an MN-major operand.
-// MMA completion is tracked with tcgen05.commit on mbarriers; every wait is
-// bounded and a timeout ends the CTA with a status code instead of hanging.
+// Work decomposition. One CTA per (query, half of the 512 value columns): the
+// two CTAs of a query both form the full scores q.k (512-deep) and each
+// accumulates 256 output columns. Tensor memory (512 columns x 128 lanes,
+// lane = head) holds the output accumulator (256 columns), two 64-key score
+// buffers (128) and the first 256 dims of Q as bf16 pairs (128): the q.k
+// products over those dims take Q from tensor memory and read only the key
+// tile from shared memory, which halves their shared-memory traffic (a
+// 128 x 64 x 16 product that reads both operands from shared memory is bound
+// by it). The other 256 dims of Q stay in shared memory. Keys go in tiles of
+// 64, and three groups of warps run as a pipeline through mbarriers:
+//   - producers (warps 4-11, lane = key, two warps per quarter of the row):
+//     load the packed rows two tiles ahead into registers (pads and
+//     out-of-range indices load nothing and decode to zero rows),
+//     dequantize them with byte permutes into a 128-byte-swizzled K-major
+//     bf16 key tile (two buffers), and arrive on its "full" barrier;
+//   - the issuer (warp 12, one thread): S(t) = Q K^T (M 128, N 64, K 512)
+//     into one of two score buffers once the tile and the buffer are free,
+//     then O += P(t-1) V(t-1) (M 128, N 256, K 64; V is the same key tile read
+//     MN-major) once softmax has written P; tcgen05.commit on mbarriers
+//     tracks completion;
+//   - softmax (warps 0-3, one head per thread): read S(t), release its
+//     buffer, run the online softmax in fp32 (exp2, running max with a
+//     rescale of the output only when the max grows by more than 2**8), and
+//     write P (bf16, two buffers) to shared memory.
+// Every wait is bounded; a timeout sets a CTA-wide abort flag that ends the
+// other roles' waits, and the CTA reports through an optional status word.
 //
 // Numerics: scores and the output accumulate in fp32 on the tensor core from
 // exact bf16 inputs (the dequantized rows are exact); the probabilities are
@@ -44,28 +50,33 @@ namespace {
 
 constexpr int kHeads = 128;     // MMA M: rows = heads of one query
 constexpr int kDim = 512;       // latent width (score depth)
-constexpr int kTileKeys = 32;   // MMA N of q.k, K of p.v
+constexpr int kTileKeys = 64;   // MMA N of q.k, K of p.v
 constexpr int kHalf = 256;      // output columns per CTA
-constexpr int kThreads = 128;
+constexpr int kThreads = 416;   // softmax warps 0-3, producers 4-11, issuer 12
+constexpr int kIssuerWarp = 12;
 constexpr int kRow = 272;       // packed row bytes
+constexpr int kDepth = 2;       // tiles a producer has in flight
 
-constexpr uint32_t kQBytes = kHeads * kDim * 2;          // 8 K-blocks x 128 rows x 128 B
-constexpr uint32_t kKBytes = kTileKeys * kDim * 2;       // 8 K-blocks x 32 rows x 128 B
-constexpr uint32_t kPBytes = kHeads * kTileKeys * 2;     // 16 row groups x 4 core matrices
-constexpr uint32_t kStageBytes = kTileKeys * kRow;
+constexpr uint32_t kQhiBytes = kHeads * 256 * 2;         // dims 256..511: 4 K-blocks x 128 rows
+constexpr uint32_t kKBytes = kTileKeys * kDim * 2;       // 8 K-blocks x 64 rows x 128 B
+constexpr uint32_t kKBlock = kTileKeys * 128;            // bytes of one K-block of a key tile
+constexpr uint32_t kPBytes = kHeads * kTileKeys * 2;     // 16 row groups x 8 core matrices
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;              // two buffers
+constexpr uint32_t kOffK = kOffQ + kQhiBytes;            // two buffers
 constexpr uint32_t kOffP = kOffK + 2 * kKBytes;          // two buffers
-constexpr uint32_t kOffStage = kOffP + 2 * kPBytes;      // two buffers
-constexpr uint32_t kOffBias = kOffStage + 2 * kStageBytes;  // four tiles x 32 floats
-constexpr uint32_t kOffBar = kOffBias + 4 * kTileKeys * 4;  // three mbarriers
-constexpr uint32_t kOffTmemSlot = kOffBar + 32;
-constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;        // ten mbarriers
+constexpr uint32_t kOffTmemSlot = kOffBar + 128;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 16;
+constexpr uint32_t kSmemUsed = kOffAbort + 16;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
+
+// mbarriers, two of each (buffer t & 1)
+constexpr uint32_t kBarKFull = 0, kBarSFull = 16, kBarSEmpty = 32, kBarPFull = 48, kBarPvDone = 64;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
-constexpr uint32_t kColS = 256;   // two buffers of 32 columns
+constexpr uint32_t kColS = 256;   // two buffers of 64 columns
+constexpr uint32_t kColQ = 384;   // Q dims 0..255 as 128 columns of bf16 pairs
 
 constexpr uint32_t kWaitPolls = 1u << 22;
 
@@ -96,21 +107,6 @@ __device__ __forceinline__ void sts_v4(uint32_t a, uint4 v) {
                : "memory");
 }
 
-__device__ __forceinline__ uint4 lds_v4a(uint32_t a) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "r"(a)
-               : "memory");
-  return r;
-}
-
-__device__ __forceinline__ uint32_t lds_u32a(uint32_t a) {
-  uint32_t r;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a) : "memory");
-  return r;
-}
-
 __device__ __forceinline__ void cp_async_16a(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -135,11 +131,26 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Bounded wait for the completion of the phase with the given parity.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for the completion of the phase with the given parity. Gives
+// up when another role of the CTA has raised the abort flag, or after
+// kWaitPolls polls (then raises it itself).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (mbar_test(bar, parity)) return true;
+    if ((i & 31u) == 31u && *abort) return false;
+  }
+  *abort = 1;
   return false;
+}
+
+// mbar_wait with one outcome for the whole warp (the softmax warps follow it
+// with warp-collective TMEM loads).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort));
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -170,6 +181,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// As mma_bf16 with A (M x 16, lane = row, 8 columns of bf16 pairs) in TMEM.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -243,93 +265,99 @@ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major) {
 constexpr uint32_t kIdescQK = instr_desc(kHeads, kTileKeys, false);
 constexpr uint32_t kIdescPV = instr_desc(kHeads, kHalf, true);
 
-// ---------------------------------------------------------------- stages ---
+// --------------------------------------------------------------- producer ---
 
-// Warp 0: cp.async the packed rows of tile t into staging buffer t & 1 and
-// write the tile's score bias (0 valid, -inf pad or out of range) to bias
-// buffer t & 3. Always commits one group (empty past the last tile).
-__device__ __forceinline__ void stage_tile(const AttnParams& p, const int64_t* idx_row, int64_t t,
-                                           int64_t num_tiles, uint32_t stage_base, float* bias,
-                                           int lane) {
-  if (t < num_tiles) {
-    const int64_t k = t * kTileKeys + lane;
-    int64_t s = -1;
-    if (k < p.topk) s = ld_once_i64(idx_row + k);
-    const bool valid = s >= 0 && s < p.num_slots;
-    bias[(t & 3) * kTileKeys + lane] = valid ? 0.0f : -__int_as_float(0x7F800000);
-    if (valid) {
-      int64_t blk, in_blk;
-      divmod_pos(s, p.block_size, blk, in_blk);
-      const uint8_t* src = p.cache + (blk * p.block_stride_rows + in_blk) * kRow;
-      const uint32_t dst = stage_base + (uint32_t)(t & 1) * kStageBytes + (uint32_t)lane * kRow;
-#pragma unroll
-      for (int c = 0; c < kRow / 16; ++c) cp_async_16a(dst + 16 * c, src + 16 * c);
-    }
-  }
-  cp_async_commit();
+// One producer thread's share of a key row: the 64 code bytes of dims
+// [128q, 128q + 128) and the four scale bytes of those groups. A pad or an
+// out-of-range index loads nothing: zero codes decode to +0.0 under any
+// scale byte in [2, 252].
+struct Packed {
+  uint4 c[4];
+  uint32_t s;
+};
+
+__device__ __forceinline__ int64_t key_index(const AttnParams& p, const int64_t* idx_row,
+                                             int64_t k) {
+  return k < p.topk ? ld_once_i64(idx_row + k) : -1;
 }
 
-// All threads: dequantize tile t (staging buffer t & 1) into key buffer t & 1
-// in the 128-byte-swizzled K-major layout: element (key j, dim d) at
-// kb*4096 + j*128 + ((c ^ (j & 7)) << 4) + 2*(d & 7), kb = d / 64,
-// c = (d % 64) / 8. Thread (j, q) = (tid / 4, tid % 4) does dims
-// [128q, 128q + 128) of key j; pad keys become zero rows.
-__device__ __forceinline__ void dequant_tile(int64_t t, uint32_t stage_base, uint32_t k_base,
-                                             const float* bias, int tid) {
-  const int j = tid >> 2, q = tid & 3;
-  const uint32_t kdst = k_base + (uint32_t)(t & 1) * kKBytes + (uint32_t)j * 128;
-  const uint32_t swz = (uint32_t)(j & 7);
-  if (bias[(t & 3) * kTileKeys + j] != 0.0f) {
-    const uint4 z = make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, int q) {
+  Packed r;
+  if (s >= 0 && s < p.num_slots) {
+    int64_t blk, in_blk;
+    divmod_pos(s, p.block_size, blk, in_blk);
+    const uint8_t* row = p.cache + (blk * p.block_stride_rows + in_blk) * kRow;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      sts_v4(kdst + (uint32_t)(2 * q + (i >> 3)) * 4096 + ((((uint32_t)i & 7) ^ swz) << 4), z);
-    return;
+    for (int g = 0; g < 4; ++g) r.c[g] = ld_once_v4(row + 64 * q + 16 * g);
+    r.s = ld_once_u32(row + 256 + 4 * q);
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) r.c[g] = make_uint4(0, 0, 0, 0);
+    r.s = 0x7F7F7F7Fu;
   }
-  const uint32_t src = stage_base + (uint32_t)(t & 1) * kStageBytes + (uint32_t)j * kRow;
-  const uint32_t sw = lds_u32a(src + 256 + 4 * q);
+  return r;
+}
+
+// Dims [128q, 128q + 128) of key j into key buffer `kbuf`, 128-byte-swizzled
+// K-major: element (key j, dim d) at kb*kKBlock + j*128 + ((c ^ (j & 7)) << 4)
+// + 2*(d & 7), kb = d / 64, c = (d % 64) / 8. With lane = key, each 8-lane
+// phase of a 16-byte store covers eight keys and all eight bank groups.
+__device__ __forceinline__ void dequant_share(const Packed& x, uint32_t kbuf, int j, int q) {
+  const uint32_t kdst = kbuf + (uint32_t)j * 128;
+  const uint32_t swz = (uint32_t)(j & 7);
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const uint4 c = lds_v4a(src + 64 * q + 16 * g);  // codes of dims 128q + 32g .. +31
-    const uint32_t sb = (sw >> (8 * g)) & 0xFFu;
+    const uint32_t sb = (x.s >> (8 * g)) & 0xFFu;
     const ByteTables tb = make_tables(sb);
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    const uint32_t words[4] = {x.c[g].x, x.c[g].y, x.c[g].z, x.c[g].w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = 4 * g + u;  // chunk of 8 dims within the thread's 128
       const uint4 v = decode8_direct(words[u], sb, tb);
-      sts_v4(kdst + (uint32_t)(2 * q + (i >> 3)) * 4096 + ((((uint32_t)i & 7) ^ swz) << 4), v);
+      sts_v4(kdst + (uint32_t)(2 * q + (i >> 3)) * kKBlock + ((((uint32_t)i & 7) ^ swz) << 4),
+             v);
     }
   }
 }
 
-// Thread 0: S(t) = Q K(t)^T into score buffer t & 1.
+// --------------------------------------------------------------- issuer ---
+
+// S(t) = Q K(t)^T into score buffer t & 1: dims 0..255 with Q from TMEM
+// (16 steps of 8 columns), dims 256..511 with Q from shared memory.
 __device__ __forceinline__ void issue_qk(int64_t t, uint32_t q_base, uint32_t k_base,
                                          uint32_t tmem) {
   const uint32_t kb_base = k_base + (uint32_t)(t & 1) * kKBytes;
   const uint32_t d = tmem + kColS + (uint32_t)(t & 1) * kTileKeys;
 #pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
+  for (int kb = 0; kb < 4; ++kb) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t a = smem_desc(q_base + kb * (kHeads * 128) + ks * 32, 16, 1024, 2);
-      const uint64_t b = smem_desc(kb_base + kb * (kTileKeys * 128) + ks * 32, 16, 1024, 2);
-      mma_bf16(d, a, b, kIdescQK, (kb | ks) != 0);
+      const uint64_t b = smem_desc(kb_base + kb * kKBlock + ks * 32, 16, 1024, 2);
+      mma_bf16_ta(d, tmem + kColQ + (uint32_t)(8 * (4 * kb + ks)), b, kIdescQK, (kb | ks) != 0);
+    }
+  }
+#pragma unroll
+  for (int kb = 4; kb < 8; ++kb) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t a = smem_desc(q_base + (kb - 4) * (kHeads * 128) + ks * 32, 16, 1024, 2);
+      const uint64_t b = smem_desc(kb_base + kb * kKBlock + ks * 32, 16, 1024, 2);
+      mma_bf16(d, a, b, kIdescQK, 1);
     }
   }
 }
 
-// Thread 0: O (+)= P(t) V(t), V = key buffer t & 1 read MN-major from column
-// block 4v (LBO: next 64 columns, SBO: next 8 keys), P K-major without swizzle
+// O (+)= P(t) V(t), V = key buffer t & 1 read MN-major from column block 4v
+// (LBO: next 64 columns, SBO: next 8 keys), P K-major without swizzle
 // (8x16-byte core matrices; LBO: next 8 keys, SBO: next 8 heads).
 __device__ __forceinline__ void issue_pv(int64_t t, int v, uint32_t p_base, uint32_t k_base,
                                          uint32_t tmem) {
   const uint32_t pb = p_base + (uint32_t)(t & 1) * kPBytes;
-  const uint32_t vb = k_base + (uint32_t)(t & 1) * kKBytes + (uint32_t)v * 4 * (kTileKeys * 128);
+  const uint32_t vb = k_base + (uint32_t)(t & 1) * kKBytes + (uint32_t)v * 4 * kKBlock;
 #pragma unroll
   for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-    const uint64_t a = smem_desc(pb + ks * 256, 128, 512, 0);
-    const uint64_t b = smem_desc(vb + ks * 2048, kTileKeys * 128, 1024, 2);
+    const uint64_t a = smem_desc(pb + ks * 256, 128, 1024, 0);
+    const uint64_t b = smem_desc(vb + ks * 2048, kKBlock, 1024, 2);
     mma_bf16(tmem + kColO, a, b, kIdescPV, (t | ks) != 0);
   }
 }
@@ -345,180 +373,257 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   const int64_t n = blockIdx.x >> 1;
   const int v = blockIdx.x & 1;
   const uint32_t q_base = base + kOffQ, k_base = base + kOffK, p_base = base + kOffP;
-  const uint32_t stage_base = base + kOffStage;
-  float* bias = reinterpret_cast<float*>(sm + kOffBias);
-  const uint32_t bar_s0 = base + kOffBar, bar_s1 = bar_s0 + 8, bar_o = bar_s0 + 16;
+  const uint32_t bars = base + kOffBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
   const int64_t num_tiles = (p.topk + kTileKeys - 1) / kTileKeys;
   const int64_t* idx_row = p.indices + n * p.topk;
 
-  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  if (warp == kIssuerWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   if (tid == 0) {
-    mbar_init(bar_s0, 1);
-    mbar_init(bar_s1, 1);
-    mbar_init(bar_o, 1);
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars + kBarKFull + 8 * b, 256);
+      mbar_init(bars + kBarSFull + 8 * b, 1);
+      mbar_init(bars + kBarSEmpty + 8 * b, 128);
+      mbar_init(bars + kBarPFull + 8 * b, 128);
+      mbar_init(bars + kBarPvDone + 8 * b, 1);
+    }
+    *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // Q: head r of this query into the swizzled K-major layout (zero rows past
+  // Q dims 256..511 of head r into the swizzled K-major layout (zero rows past
   // num_heads), 16 bytes per cp.async.
   const uint8_t* qn = p.q + n * p.q_qstride;
-  for (int i = 0; i < kHeads * kDim / 8 / kThreads; ++i) {
-    const int id = i * kThreads + tid;
-    const int r = id >> 6, c64 = id & 63;
-    const uint32_t dst = q_base + (uint32_t)(c64 >> 3) * (kHeads * 128) + (uint32_t)r * 128 +
-                         ((((uint32_t)c64 & 7) ^ ((uint32_t)r & 7)) << 4);
+  for (int id = tid; id < kHeads * 32; id += kThreads) {
+    const int r = id >> 5, c32 = id & 31;
+    const uint32_t dst = q_base + (uint32_t)(c32 >> 3) * (kHeads * 128) + (uint32_t)r * 128 +
+                         ((((uint32_t)c32 & 7) ^ ((uint32_t)r & 7)) << 4);
     if (r < p.num_heads)
-      cp_async_16a(dst, qn + r * p.q_hstride + c64 * 16);
+      cp_async_16a(dst, qn + r * p.q_hstride + 512 + c32 * 16);
     else
       sts_v4(dst, make_uint4(0, 0, 0, 0));
   }
   cp_async_commit();
-  if (warp == 0) {
-    stage_tile(p, idx_row, 0, num_tiles, stage_base, bias, lane);
-    stage_tile(p, idx_row, 1, num_tiles, stage_base, bias, lane);
-    cp_async_wait<1>();  // Q and tile 0 have landed
-  } else {
-    cp_async_wait<0>();
-  }
+  cp_async_wait<0>();
+  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-
-  bool ok = true;
-  if (num_tiles > 0) {
-    dequant_tile(0, stage_base, k_base, bias, tid);
-    fence_proxy_async();
-  }
-  __syncthreads();
-  if (tid == 0 && num_tiles > 0) {
-    tc_fence_after();
-    issue_qk(0, q_base, k_base, tmem);
-    mma_commit(bar_s0);
-  }
-
-  float m_ref = -__int_as_float(0x7F800000);  // reference max (log2 units)
-  float l = 0.0f;                              // sum of p against m_ref
-  for (int64_t t = 0; t < num_tiles; ++t) {
-    // A: stage t+2, dequantize t+1 into the key buffer PV(t-1) has released,
-    // and start S(t+1) on the tensor core.
-    if (warp == 0) stage_tile(p, idx_row, t + 2, num_tiles, stage_base, bias, lane);
-    bool good = t == 0 || mbar_wait(bar_o, (uint32_t)((t - 1) & 1));
-    if (warp == 0) cp_async_wait<1>();  // tile t+1 staged
-    if (__syncthreads_or(!good)) {
-      ok = false;
-      break;
-    }
-    if (t + 1 < num_tiles) {
-      dequant_tile(t + 1, stage_base, k_base, bias, tid);
-      fence_proxy_async();
-    }
-    __syncthreads();
-    if (tid == 0 && t + 1 < num_tiles) {
-      tc_fence_after();
-      issue_qk(t + 1, q_base, k_base, tmem);
-      mma_commit(((t + 1) & 1) ? bar_s1 : bar_s0);
-    }
-    // B: scores of tile t -> probabilities -> P(t); then O += P(t) V(t).
-    good = mbar_wait((t & 1) ? bar_s1 : bar_s0, (uint32_t)((t >> 1) & 1));
-    if (__syncthreads_or(!good)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    uint32_t sr[32];
-    tmem_ld32(lane_base + kColS + (uint32_t)(t & 1) * kTileKeys, sr);
-    const float* bt = bias + (t & 3) * kTileKeys;
-    float s[32];
-    float mt = -__int_as_float(0x7F800000);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      s[j] = __fmaf_rn(__uint_as_float(sr[j]), p.scale_log2, bt[j]);
-      mt = fmaxf(mt, s[j]);
-    }
-    const bool need = mt > m_ref + 8.0f;
-    if (__any_sync(0xFFFFFFFFu, need)) {
-      const float f = need ? ex2(m_ref - mt) : 1.0f;  // ex2(-inf) = 0
-      if (t > 0) {
+  if (warp < 4) {
+    // Q dims 0..255 of head `tid` into TMEM lane `tid`, columns kColQ.. as
+    // bf16 pairs (the A operand of the first 16 q.k steps).
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint8_t* qrow = qn + (int64_t)tid * p.q_hstride;
 #pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + kColO + 32 * c, o);
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-          tmem_st32(lane_base + kColO + 32 * c, o);
-        }
+      for (int k = 0; k < 8; ++k) {
+        const uint4 x = tid < p.num_heads ? ld_once_v4(qrow + 128 * c + 16 * k)
+                                          : make_uint4(0, 0, 0, 0);
+        w[4 * k] = x.x;
+        w[4 * k + 1] = x.y;
+        w[4 * k + 2] = x.z;
+        w[4 * k + 3] = x.w;
       }
-      l *= f;
-      if (need) m_ref = mt;
+      tmem_st32(lane_base + kColQ + 32 * c, w);
     }
-    const float mu = m_ref == -__int_as_float(0x7F800000) ? 0.0f : m_ref;
-    uint32_t pk[16];
-    float lsum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float p0 = ex2(s[2 * j] - mu), p1 = ex2(s[2 * j + 1] - mu);
-      lsum += p0;
-      lsum += p1;
-      pk[j] = pack_bf16x2(p0, p1);
-    }
-    l += lsum;
-    const uint32_t prow = p_base + (uint32_t)(t & 1) * kPBytes + (uint32_t)(tid >> 3) * 512 +
-                          (uint32_t)(tid & 7) * 16;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      sts_v4(prow + 128 * c, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      issue_pv(t, v, p_base, k_base, tmem);
-      mma_commit(bar_o);
-    }
-  }
-  if (ok && num_tiles > 0) {
-    const bool good = mbar_wait(bar_o, (uint32_t)((num_tiles - 1) & 1));
-    if (__syncthreads_or(!good)) ok = false;
-  }
-  if (!ok) {
-    if (tid == 0 && p.status) atomicExch(p.status, 1);
-  } else {
-    tc_fence_after();
-    const int h = tid;
-    const bool store = h < p.num_heads;
-    uint8_t* orow = p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-#pragma unroll 1
-    for (int c = 0; c < kHalf / 32; ++c) {
-      uint32_t o[32];
-      if (num_tiles > 0) {
-        tmem_ld32(lane_base + kColO + 32 * c, o);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = 0;
-      }
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        w[j] = l > 0.0f ? pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
-                                      __uint_as_float(o[2 * j + 1]) * inv)
-                        : 0u;
-      if (store) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_v4(orow + 64 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                                    w[4 * u + 3]));
-      }
-    }
-    if (v == 0 && store && p.lse)
-      p.lse[n * p.num_heads + h] =
-          l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -__int_as_float(0x7F800000);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  tc_fence_after();
+
+  if (warp >= 4 && warp < kIssuerWarp) {
+    // ------------------------------------------------------------ producers
+    const int j = lane + 32 * (warp & 1), q = (warp - 4) >> 1;
+    Packed buf[kDepth];
+#pragma unroll
+    for (int u = 0; u < kDepth; ++u)
+      buf[u] = load_packed(p, key_index(p, idx_row, (int64_t)u * kTileKeys + j), q);
+    int64_t s_next = key_index(p, idx_row, (int64_t)kDepth * kTileKeys + j);
+    bool live = true;
+    for (int64_t t0 = 0; t0 < num_tiles && live; t0 += kDepth) {
+#pragma unroll
+      for (int u = 0; u < kDepth; ++u) {
+        const int64_t t = t0 + u;
+        if (t < num_tiles && live) {
+          const Packed cur = buf[u];
+          buf[u] = load_packed(p, s_next, q);  // tile t + kDepth
+          s_next = key_index(p, idx_row, (t + kDepth + 1) * kTileKeys + j);
+          // key buffer t & 1 is free once PV(t-2) has completed
+          if (t >= 2 && !mbar_wait(bars + kBarPvDone + 8 * (t & 1), (uint32_t)(((t - 2) >> 1) & 1),
+                                   abort)) {
+            live = false;
+          } else {
+            dequant_share(cur, k_base + (uint32_t)(t & 1) * kKBytes, j, q);
+            fence_proxy_async();
+            mbar_arrive(bars + kBarKFull + 8 * (t & 1));
+          }
+        }
+      }
+    }
+  } else if (warp == kIssuerWarp) {
+    // --------------------------------------------------------------- issuer
+    if (lane == 0) {
+      for (int64_t t = 0; t <= num_tiles; ++t) {
+        if (t < num_tiles) {
+          if (!mbar_wait(bars + kBarKFull + 8 * (t & 1), (uint32_t)((t >> 1) & 1), abort)) break;
+          if (t >= 2 && !mbar_wait(bars + kBarSEmpty + 8 * (t & 1),
+                                   (uint32_t)(((t - 2) >> 1) & 1), abort))
+            break;
+          tc_fence_after();
+          issue_qk(t, q_base, k_base, tmem);
+          mma_commit(bars + kBarSFull + 8 * (t & 1));
+        }
+        if (t >= 1) {
+          const int64_t u = t - 1;
+          if (!mbar_wait(bars + kBarPFull + 8 * (u & 1), (uint32_t)((u >> 1) & 1), abort)) break;
+          tc_fence_after();
+          issue_pv(u, v, p_base, k_base, tmem);
+          mma_commit(bars + kBarPvDone + 8 * (u & 1));
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_ref = -__int_as_float(0x7F800000);  // reference max (log2 units)
+    float l = 0.0f;                              // sum of p against m_ref
+    bool live = true;
+    int64_t s_lo = key_index(p, idx_row, lane), s_hi = key_index(p, idx_row, 32 + lane);
+    for (int64_t t = 0; t < num_tiles && live; ++t) {
+      const uint32_t mask_lo = __ballot_sync(0xFFFFFFFFu, s_lo >= 0 && s_lo < p.num_slots);
+      const uint32_t mask_hi = __ballot_sync(0xFFFFFFFFu, s_hi >= 0 && s_hi < p.num_slots);
+      s_lo = key_index(p, idx_row, (t + 1) * kTileKeys + lane);
+      s_hi = key_index(p, idx_row, (t + 1) * kTileKeys + 32 + lane);
+      if (!warp_wait(bars + kBarSFull + 8 * (t & 1), (uint32_t)((t >> 1) & 1), abort)) {
+        live = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t scol = lane_base + kColS + (uint32_t)(t & 1) * kTileKeys;
+      // Pass 1: the tile max (scores in log2 units, -inf for dropped keys).
+      float mt = -__int_as_float(0x7F800000);
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[32];
+        tmem_ld32(scol + 32 * hf, sr);
+        const uint32_t m = hf ? mask_hi : mask_lo;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if ((m >> k) & 1u) mt = fmaxf(mt, __fmul_rn(__uint_as_float(sr[k]), p.scale_log2));
+      }
+      const bool need = mt > m_ref + 8.0f;
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        const float f = need ? ex2(m_ref - mt) : 1.0f;  // ex2(-inf) = 0
+        if (t > 0) {
+          // O may be touched only once PV(t-1) has completed
+          if (!warp_wait(bars + kBarPvDone + 8 * ((t - 1) & 1), (uint32_t)(((t - 1) >> 1) & 1),
+                         abort)) {
+            live = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < kHalf / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + kColO + 32 * c, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+            tmem_st32(lane_base + kColO + 32 * c, o);
+          }
+        }
+        l *= f;
+        if (need) m_ref = mt;
+      }
+      const float mu = m_ref == -__int_as_float(0x7F800000) ? 0.0f : m_ref;
+      // P buffer t & 1 is free once PV(t-2) has completed
+      if (t >= 2 && !warp_wait(bars + kBarPvDone + 8 * (t & 1), (uint32_t)(((t - 2) >> 1) & 1),
+                               abort)) {
+        live = false;
+        break;
+      }
+      // Pass 2: probabilities, their sum, and P (bf16) for this head's row.
+      const uint32_t prow = p_base + (uint32_t)(t & 1) * kPBytes + (uint32_t)(tid >> 3) * 1024 +
+                            (uint32_t)(tid & 7) * 16;
+      float lsum0 = 0.0f, lsum1 = 0.0f;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[32];
+        tmem_ld32(scol + 32 * hf, sr);
+        const uint32_t m = hf ? mask_hi : mask_lo;
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float x0 = ((m >> (2 * k)) & 1u)
+                               ? __fmul_rn(__uint_as_float(sr[2 * k]), p.scale_log2)
+                               : -__int_as_float(0x7F800000);
+          const float x1 = ((m >> (2 * k + 1)) & 1u)
+                               ? __fmul_rn(__uint_as_float(sr[2 * k + 1]), p.scale_log2)
+                               : -__int_as_float(0x7F800000);
+          const float p0 = ex2(x0 - mu), p1 = ex2(x1 - mu);
+          lsum0 += p0;
+          lsum1 += p1;
+          pk[k] = pack_bf16x2(p0, p1);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          sts_v4(prow + 128 * (4 * hf + c),
+                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+      }
+      l += lsum0 + lsum1;
+      tc_fence_before();
+      mbar_arrive(bars + kBarSEmpty + 8 * (t & 1));
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(bars + kBarPFull + 8 * (t & 1));
+    }
+    if (live && num_tiles > 0 &&
+        !warp_wait(bars + kBarPvDone + 8 * ((num_tiles - 1) & 1),
+                   (uint32_t)(((num_tiles - 1) >> 1) & 1), abort))
+      live = false;
+    live = __all_sync(0xFFFFFFFFu, live && !*abort);
+    if (live) {
+      tc_fence_after();
+      const int h = tid;
+      const bool store = h < p.num_heads;
+      uint8_t* orow =
+          p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t o[32];
+        if (num_tiles > 0) {
+          tmem_ld32(lane_base + kColO + 32 * c, o);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = 0;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = l > 0.0f ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv,
+                                        __uint_as_float(o[2 * k + 1]) * inv)
+                          : 0u;
+        if (store) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_v4(orow + 64 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                      w[4 * u + 3]));
+        }
+      }
+      if (v == 0 && store && p.lse)
+        p.lse[n * p.num_heads + h] = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f
+                                              : -__int_as_float(0x7F800000);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort && p.status) atomicExch(p.status, 1);
+  if (warp == kIssuerWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
