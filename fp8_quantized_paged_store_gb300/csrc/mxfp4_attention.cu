@@ -111,6 +111,22 @@ __device__ __forceinline__ void cp_async_16a(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Global loads issued where they stand (asm volatile): a producer's prefetch
+// of packed rows must not be moved down to its first use a tile later.
+__device__ __forceinline__ uint4 ld_issue_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_issue_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -288,8 +304,8 @@ __device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, in
     divmod_pos(s, p.block_size, blk, in_blk);
     const uint8_t* row = p.cache + (blk * p.block_stride_rows + in_blk) * kRow;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) r.c[g] = ld_once_v4(row + 64 * q + 16 * g);
-    r.s = ld_once_u32(row + 256 + 4 * q);
+    for (int g = 0; g < 4; ++g) r.c[g] = ld_issue_v4(row + 64 * q + 16 * g);
+    r.s = ld_issue_u32(row + 256 + 4 * q);
   } else {
 #pragma unroll
     for (int g = 0; g < 4; ++g) r.c[g] = make_uint4(0, 0, 0, 0);
