@@ -59,10 +59,17 @@ def lib() -> ctypes.CDLL:
         L.oracle_mxfp4_mla_rmsnorm_store.restype = None
         L.oracle_mxfp4_mla_rmsnorm_store.argtypes = [_ptr, _i64, _i64, _ptr, ctypes.c_float, _ptr,
                                                      _ptr, _i64, _i64, _i64]
-        for name in ("oracle_rope_quant_insert_mxfp8", "oracle_rope_quant_insert_nvfp4"):
+        for name in ("oracle_rope_quant_insert_mxfp8", "oracle_rope_quant_insert_nvfp4",
+                     "oracle_rope_quant_insert_v4"):
             getattr(L, name).restype = None
             getattr(L, name).argtypes = [_ptr, _i64, _i64, _ptr, _ptr, _i64, _i64, _ptr, _ptr,
                                          _i64, _i64, _i64, _i32, _i32]
+        L.oracle_rope_plain_insert.restype = None
+        L.oracle_rope_plain_insert.argtypes = [_ptr, _i64, _i64, _ptr, _ptr, _i64, _i64, _ptr,
+                                               _ptr, _i64, _i64, _i64, _i64, _i32, _i32,
+                                               ctypes.c_float]
+        L.oracle_save_ring_rows.restype = None
+        L.oracle_save_ring_rows.argtypes = [_ptr, _i64, _i64, _ptr, _ptr, _i64, _i64, _i64, _i64]
         _LIB = L
     return _LIB
 
@@ -247,6 +254,48 @@ def rope_quant_insert_nvfp4(latent, positions, cos_sin, cache, cache_slots, num_
                             threads: int = 1) -> None:
     _rope_insert("oracle_rope_quant_insert_nvfp4", latent, positions, cos_sin, cache, cache_slots,
                  num_pages, cache_block, page_stride_bytes, compress_ratio, sanitize, threads)
+
+
+def rope_quant_insert_v4(latent, positions, cos_sin, cache, cache_slots, num_pages,
+                         cache_block, page_stride_bytes, compress_ratio, sanitize,
+                         threads: int = 1) -> None:
+    """The 584-byte V4 record (reading in kvq_oracle.c)."""
+    _rope_insert("oracle_rope_quant_insert_v4", latent, positions, cos_sin, cache, cache_slots,
+                 num_pages, cache_block, page_stride_bytes, compress_ratio, sanitize, threads)
+
+
+def rope_plain_insert(latent, positions, cos_sin, cache, cache_slots, num_pages, cache_block,
+                      page_stride, slot_stride, compress_ratio, fp8: bool = False,
+                      fp8_scale: float = 1.0, threads: int = 1) -> None:
+    """Plain [448 NoPE | 64 RoPE] rows into a bf16 (uint8 buffer of 2-byte
+    elements) or fp8 cache; strides in elements."""
+    base, stride, T, d = _latent_args(latent)
+    assert d == 512
+    pos = _contig(positions, np.int64)
+    slots = _contig(cache_slots, np.int64)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and compress_ratio >= 1
+    L = lib()
+
+    def body(lo, hi):
+        L.oracle_rope_plain_insert(base + lo * stride * 2, hi - lo, stride, _addr(pos, lo * 8),
+                                   _addr(cs), cs.shape[1], cs.shape[0], _addr(cache),
+                                   _addr(slots, lo * 8), num_pages, cache_block, page_stride,
+                                   slot_stride, compress_ratio, 1 if fp8 else 0, fp8_scale)
+    _run_split(T, threads, body)
+
+
+def save_ring_rows(rows: np.ndarray, slot_mapping: np.ndarray, state: np.ndarray,
+                   num_blocks: int, state_block: int, state_stride: int,
+                   state_row_stride: int) -> None:
+    """rows: float32 [N, >= 1024] (unit column stride); state: flat float32
+    buffer modified in place; strides in floats."""
+    assert rows.dtype == np.float32 and rows.ndim == 2 and rows.strides[1] == 4
+    slots = _contig(slot_mapping, np.int64)
+    assert state.dtype == np.float32 and state.flags.c_contiguous
+    lib().oracle_save_ring_rows(rows.ctypes.data, rows.shape[0], rows.strides[0] // 4,
+                                _addr(slots), _addr(state), num_blocks, state_block,
+                                state_stride, state_row_stride)
 
 
 def default_threads() -> int:

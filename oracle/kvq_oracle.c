@@ -530,6 +530,129 @@ void oracle_mxfp4_mla_rmsnorm_store(const uint16_t* latent, int64_t num_tokens, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* The other rope_quant_insert layouts, and save_ring_rows                    */
+/* ------------------------------------------------------------------------ */
+
+/* [v41] rope_quant_insert, docstring: a bfloat16 or float8_e4m3fn cache holds
+ * the plain [448 NoPE | 64 RoPE] rows read by FlashInfer, the fp8 one scaled
+ * by the per-tensor fp8_scale; the cache is [pages, CACHE_BLOCK, 512] with its
+ * own page and row strides and unit element stride. The kernel
+ * (_rope_plain_insert_kernel) is not printed. Readings: the gates and table
+ * row of the paged records (rope_gate); elements 0..447 are the latent's own
+ * values (copied bit for bit into the bf16 cache), elements 448..511 the
+ * rotated pairs (binary32 as rope_rotate_row, no sanitising) rounded to bf16,
+ * nearest even. The fp8 cache stores E4M3(clamp(RN(x / fp8_scale), -448,
+ * 448)) of each element x (the latent's value, or the rotated binary32
+ * value): a quotient, as the scale is the dequantizing factor; NaN as 0x7F.
+ * Strides are in elements (2 bytes for bf16, 1 for fp8). */
+void oracle_rope_plain_insert(const uint16_t* latent, int64_t num_tokens, int64_t row_stride,
+                              const int64_t* positions, const float* cos_sin, int64_t cos_stride,
+                              int64_t cos_sin_rows, uint8_t* cache, const int64_t* cache_slots,
+                              int64_t num_pages, int64_t cache_block, int64_t page_stride,
+                              int64_t slot_stride, int32_t compress_ratio, int32_t fp8,
+                              float fp8_scale) {
+    float rotated[512];
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = cache_slots[t];
+        int64_t table_row = rope_gate(slot, positions[t], num_pages, cache_block, compress_ratio,
+                                      cos_sin_rows);
+        if (table_row < 0) continue;
+        const uint16_t* src = latent + t * row_stride;
+        rope_rotate_row(src, cos_sin + table_row * cos_stride, 0, rotated);
+        int64_t base = (slot / cache_block) * page_stride + (slot % cache_block) * slot_stride;
+        for (int j = 0; j < 512; ++j) {
+            if (!fp8) {
+                uint16_t h = j < 448 ? src[j] : f32_to_bf16_rne(rotated[j]);
+                uint8_t* dst = cache + 2 * (base + j);
+                dst[0] = (uint8_t)(h & 0xFF);
+                dst[1] = (uint8_t)(h >> 8);
+            } else {
+                float x = j < 448 ? bf16_to_f32(src[j]) : rotated[j];
+                float y = x / fp8_scale;
+                if (y > 448.0f) y = 448.0f;
+                if (y < -448.0f) y = -448.0f;
+                cache[base + j] = oracle_e4m3_encode(y);
+            }
+        }
+    }
+}
+
+/* [v41] rope_quant_insert, docstring: the 584-byte V4 record holds 576 value
+ * bytes and eight segregated UE8M0 scale bytes, one of them a zero padding
+ * scale. The kernel (_rope_quant_insert_kernel) is not printed. Reading (the
+ * split 584 = 448 + 2 * 64 + 8 implies): value bytes 0..447 are the 448 NoPE
+ * values as E4M3 in seven tiles of 64, each tile under the V4.1 MXFP8 rule
+ * (amax floor 1e-4, e = ceil(log2(amax * (1/448))), values
+ * E4M3(clamp(x * 2**-e, -448, 448)), scale byte clamp(e + 127, 0,
+ * sanitize ? 254 : 255)); value bytes 448..575 are the 64 rotated values as
+ * bf16 (nearest even, little-endian); scale bytes 0..6 belong to the tiles and
+ * byte 7 is 0. All 512 values go through rope_rotate_row (identity formula on
+ * the NoPE pairs, sanitising as asked), as in the V4.1 records of the same
+ * page. Page layout as those records: CACHE_BLOCK * 576 value bytes, then
+ * CACHE_BLOCK * 8 scale bytes. */
+void oracle_rope_quant_insert_v4(const uint16_t* latent, int64_t num_tokens, int64_t row_stride,
+                                 const int64_t* positions, const float* cos_sin,
+                                 int64_t cos_stride, int64_t cos_sin_rows, uint8_t* cache,
+                                 const int64_t* cache_slots, int64_t num_pages,
+                                 int64_t cache_block, int64_t page_stride_bytes,
+                                 int32_t compress_ratio, int32_t sanitize) {
+    const float kMinAmax = 1e-4f;
+    const float kInv448 = 1.0f / 448.0f;
+    float rotated[512];
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = cache_slots[t];
+        int64_t table_row = rope_gate(slot, positions[t], num_pages, cache_block, compress_ratio,
+                                      cos_sin_rows);
+        if (table_row < 0) continue;
+        rope_rotate_row(latent + t * row_stride, cos_sin + table_row * cos_stride, sanitize,
+                        rotated);
+        uint8_t* page = cache + (slot / cache_block) * page_stride_bytes;
+        uint8_t* values = page + (slot % cache_block) * 576;
+        uint8_t* scales = page + cache_block * 576 + (slot % cache_block) * 8;
+        for (int g = 0; g < 7; ++g) {
+            const float* x = rotated + 64 * g;
+            float amax = group_amax(x, 64);
+            if (!(amax >= kMinAmax)) amax = kMinAmax;
+            float v = amax * kInv448;
+            int32_t e = oracle_ceil_pow2_exponent(v);
+            float inv_scale = pow2f(-e);
+            for (int j = 0; j < 64; ++j) {
+                float y = x[j] * inv_scale;
+                if (y > 448.0f) y = 448.0f;
+                if (y < -448.0f) y = -448.0f;
+                values[64 * g + j] = oracle_e4m3_encode(y);
+            }
+            int32_t encoded = e + 127;
+            int32_t cap = sanitize ? 254 : 255;
+            if (encoded < 0) encoded = 0;
+            if (encoded > cap) encoded = cap;
+            scales[g] = (uint8_t)encoded;
+        }
+        scales[7] = 0;
+        for (int j = 0; j < 64; ++j) {
+            uint16_t h = f32_to_bf16_rne(rotated[448 + j]);
+            values[448 + 2 * j] = (uint8_t)(h & 0xFF);
+            values[448 + 2 * j + 1] = (uint8_t)(h >> 8);
+        }
+    }
+}
+
+/* [v41] save_ring_rows: store fp32 [kv, score] rows of 1024 values to their
+ * ring slots, skipping slot -1. Reading: slot s goes to row s % STATE_BLOCK of
+ * block s / STATE_BLOCK (strides in floats); a slot < 0 or >= num_blocks *
+ * STATE_BLOCK is skipped; the row is copied bit for bit. */
+void oracle_save_ring_rows(const float* rows, int64_t num_rows, int64_t row_stride,
+                           const int64_t* slot_mapping, float* state, int64_t num_blocks,
+                           int64_t state_block, int64_t state_stride, int64_t state_row_stride) {
+    for (int64_t t = 0; t < num_rows; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0 || slot >= num_blocks * state_block) continue;
+        float* dst = state + (slot / state_block) * state_stride + (slot % state_block) * state_row_stride;
+        memcpy(dst, rows + t * row_stride, 1024 * sizeof(float));
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Element-wise entry points used by the pin tests                            */
 /* ------------------------------------------------------------------------ */
 

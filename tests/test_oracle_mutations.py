@@ -75,6 +75,23 @@ MUTANTS = [
      "test_oracle_pins_store.py::test_store_paged_addressing_with_block_stride"),
     ("amax_keeps_nan", "if (a > amax) amax = a;", "if (a > amax || a != a) amax = a;",
      "test_oracle_pins_store.py::test_store_worked_row"),
+    # remaining insert layouts and save_ring_rows
+    ("plain_nope_through_formula",
+     "uint16_t h = j < 448 ? src[j] : f32_to_bf16_rne(rotated[j]);",
+     "uint16_t h = f32_to_bf16_rne(rotated[j]);",
+     "test_oracle_pins_inserts.py::test_plain_bf16_copies_nope_bits_and_rounds_rotary_values"),
+    ("plain_fp8_reciprocal", "float y = x / fp8_scale;", "float y = x * (1.0f / fp8_scale);",
+     "test_oracle_pins_inserts.py::test_plain_fp8_divides_by_the_scale"),
+    ("v4_pad_scale", "scales[7] = 0;", "scales[7] = 127;",
+     "test_oracle_pins_inserts.py::test_v4_record_layout_and_values"),
+    ("v4_tile_32", "float amax = group_amax(x, 64);", "float amax = group_amax(x, 32);",
+     "test_oracle_pins_inserts.py::test_v4_tiles_are_64_wide"),
+    ("v4_bf16_byte_order", "values[448 + 2 * j] = (uint8_t)(h & 0xFF);",
+     "values[448 + 2 * j] = (uint8_t)(h >> 8);",
+     "test_oracle_pins_inserts.py::test_v4_record_layout_and_values"),
+    ("ring_upper_bound", "if (slot < 0 || slot >= num_blocks * state_block) continue;",
+     "if (slot < 0) continue;",
+     "test_oracle_pins_inserts.py::test_ring_rows_copied_bit_for_bit_pads_skipped_slack_untouched"),
     # sparse attention (oracle/attention.py)
     ("attn_scale_dropped", "s = float(sm_scale) * (_bf16_to_f64(q[n]) @ k.T)",
      "s = (_bf16_to_f64(q[n]) @ k.T)",
