@@ -359,6 +359,30 @@ static void rope_rotate_row(const uint16_t* src, const float* cs, int32_t saniti
     }
 }
 
+/* One MXFP8 tile of n rotated values (the rule the comment below states):
+ * n E4M3 value bytes and the E8M0 scale byte. */
+static void mxfp8_tile(const float* x, int n, int32_t sanitize, uint8_t* values,
+                       uint8_t* scale_byte) {
+    const float kMinAmax = 1e-4f;
+    const float kInv448 = 1.0f / 448.0f;
+    float amax = group_amax(x, n);
+    if (!(amax >= kMinAmax)) amax = kMinAmax;
+    float v = amax * kInv448;
+    int32_t e = oracle_ceil_pow2_exponent(v);
+    float inv_scale = pow2f(-e);
+    for (int j = 0; j < n; ++j) {
+        float y = x[j] * inv_scale;
+        if (y > 448.0f) y = 448.0f;
+        if (y < -448.0f) y = -448.0f;
+        values[j] = oracle_e4m3_encode(y);
+    }
+    int32_t encoded = e + 127;
+    int32_t cap = sanitize ? 254 : 255;
+    if (encoded < 0) encoded = 0;
+    if (encoded > cap) encoded = cap;
+    *scale_byte = (uint8_t)encoded;
+}
+
 /* [v41] _rope_quant_insert_mxfp8_kernel: the 528-byte V4.1 record. Per group
  * of 32 rotated values:
  *   amax  = max(largest |value| (NaN ignored), fl32(1e-4))
@@ -377,8 +401,6 @@ void oracle_rope_quant_insert_mxfp8(const uint16_t* latent, int64_t num_tokens, 
                                     const int64_t* cache_slots, int64_t num_pages,
                                     int64_t cache_block, int64_t page_stride_bytes,
                                     int32_t compress_ratio, int32_t sanitize) {
-    const float kMinAmax = 1e-4f;
-    const float kInv448 = 1.0f / 448.0f;
     float rotated[512];
     for (int64_t t = 0; t < num_tokens; ++t) {
         int64_t slot = cache_slots[t];
@@ -390,25 +412,8 @@ void oracle_rope_quant_insert_mxfp8(const uint16_t* latent, int64_t num_tokens, 
         uint8_t* page = cache + (slot / cache_block) * page_stride_bytes;
         uint8_t* values = page + (slot % cache_block) * 512;
         uint8_t* scales = page + cache_block * 512 + (slot % cache_block) * 16;
-        for (int g = 0; g < 16; ++g) {
-            const float* x = rotated + 32 * g;
-            float amax = group_amax(x, 32);
-            if (!(amax >= kMinAmax)) amax = kMinAmax;
-            float v = amax * kInv448;
-            int32_t e = oracle_ceil_pow2_exponent(v);
-            float inv_scale = pow2f(-e);
-            for (int j = 0; j < 32; ++j) {
-                float y = x[j] * inv_scale;
-                if (y > 448.0f) y = 448.0f;
-                if (y < -448.0f) y = -448.0f;
-                values[32 * g + j] = oracle_e4m3_encode(y);
-            }
-            int32_t encoded = e + 127;
-            int32_t cap = sanitize ? 254 : 255;
-            if (encoded < 0) encoded = 0;
-            if (encoded > cap) encoded = cap;
-            scales[g] = (uint8_t)encoded;
-        }
+        for (int g = 0; g < 16; ++g) mxfp8_tile(rotated + 32 * g, 32, sanitize, values + 32 * g,
+                                                scales + g);
     }
 }
 
@@ -596,8 +601,7 @@ void oracle_rope_quant_insert_v4(const uint16_t* latent, int64_t num_tokens, int
                                  const int64_t* cache_slots, int64_t num_pages,
                                  int64_t cache_block, int64_t page_stride_bytes,
                                  int32_t compress_ratio, int32_t sanitize) {
-    const float kMinAmax = 1e-4f;
-    const float kInv448 = 1.0f / 448.0f;
+    const int kTile = 64;
     float rotated[512];
     for (int64_t t = 0; t < num_tokens; ++t) {
         int64_t slot = cache_slots[t];
@@ -609,25 +613,8 @@ void oracle_rope_quant_insert_v4(const uint16_t* latent, int64_t num_tokens, int
         uint8_t* page = cache + (slot / cache_block) * page_stride_bytes;
         uint8_t* values = page + (slot % cache_block) * 576;
         uint8_t* scales = page + cache_block * 576 + (slot % cache_block) * 8;
-        for (int g = 0; g < 7; ++g) {
-            const float* x = rotated + 64 * g;
-            float amax = group_amax(x, 64);
-            if (!(amax >= kMinAmax)) amax = kMinAmax;
-            float v = amax * kInv448;
-            int32_t e = oracle_ceil_pow2_exponent(v);
-            float inv_scale = pow2f(-e);
-            for (int j = 0; j < 64; ++j) {
-                float y = x[j] * inv_scale;
-                if (y > 448.0f) y = 448.0f;
-                if (y < -448.0f) y = -448.0f;
-                values[64 * g + j] = oracle_e4m3_encode(y);
-            }
-            int32_t encoded = e + 127;
-            int32_t cap = sanitize ? 254 : 255;
-            if (encoded < 0) encoded = 0;
-            if (encoded > cap) encoded = cap;
-            scales[g] = (uint8_t)encoded;
-        }
+        for (int g = 0; g < 7; ++g) mxfp8_tile(rotated + kTile * g, kTile, sanitize,
+                                               values + kTile * g, scales + g);
         scales[7] = 0;
         for (int j = 0; j < 64; ++j) {
             uint16_t h = f32_to_bf16_rne(rotated[448 + j]);

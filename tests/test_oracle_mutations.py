@@ -84,7 +84,7 @@ MUTANTS = [
      "test_oracle_pins_inserts.py::test_plain_fp8_divides_by_the_scale"),
     ("v4_pad_scale", "scales[7] = 0;", "scales[7] = 127;",
      "test_oracle_pins_inserts.py::test_v4_record_layout_and_values"),
-    ("v4_tile_32", "float amax = group_amax(x, 64);", "float amax = group_amax(x, 32);",
+    ("v4_tile_32", "const int kTile = 64;", "const int kTile = 32;",
      "test_oracle_pins_inserts.py::test_v4_tiles_are_64_wide"),
     ("v4_bf16_byte_order", "values[448 + 2 * j] = (uint8_t)(h & 0xFF);",
      "values[448 + 2 * j] = (uint8_t)(h >> 8);",
