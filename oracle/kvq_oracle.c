@@ -52,11 +52,14 @@ static float f32_from_bits(uint32_t u) {
 /* bfloat16 is the top half of a binary32, so widening is exact. */
 static float bf16_to_f32(uint16_t h) { return f32_from_bits((uint32_t)h << 16); }
 
-/* binary32 -> bfloat16, round to nearest even; NaN becomes the quiet NaN
- * 0x7FC0 with the input's sign. */
+/* binary32 -> bfloat16, round to nearest even; every NaN becomes the quiet
+ * NaN 0x7FC0. The sign and payload of a NaN that arithmetic produced are not
+ * the same on every processor (x86's default NaN is negative, Arm's and
+ * CUDA's positive), so a stored NaN carries neither; 0x7FC0 is also what
+ * PyTorch's float -> bfloat16 conversion gives for any NaN. */
 static uint16_t f32_to_bf16_rne(float f) {
     uint32_t u = f32_bits(f);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
     uint32_t lower = u & 0xFFFFu;
     uint32_t upper = u >> 16;
     if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;

@@ -200,3 +200,19 @@ def test_v4_sanitising_and_cap():
     rot1 = _v4_slot(c1, 0)[0][448:].view(np.uint16)
     # element 450 is the even half of rotary pair 225: both halves become NaN
     assert np.all((rot0[2:4] & 0x7FFF) > 0x7F80) and np.all(rot1[2:4] == 0)
+
+
+def test_rotated_nan_is_stored_as_the_canonical_bf16_nan():
+    """A NaN that the rotation produces is stored as 0x7FC0 whatever the
+    input NaN's sign or payload, and so is the NaN of inf * 0 (negative on
+    x86, positive on Arm and CUDA); finite neighbours are untouched."""
+    lat = np.zeros((1, 512), np.uint16)
+    lat[0, 448] = 0xFFC1            # negative NaN with a payload: pair 224 -> both NaN
+    lat[0, 450] = 0x7F80            # +inf with sin 0: inf * 0 in the odd half of pair 225
+    lat[0, 452:454] = _bf([1.5, -2.0])
+    cache = _plain(lat, [0], _table(), [0], 1)
+    rot = _plain_row(cache, 0)[448:]
+    assert list(rot[:4]) == [0x7FC0, 0x7FC0, 0x7F80, 0x7FC0]
+    assert list(rot[4:6]) == list(_bf([1.5, -2.0]))
+    v4 = _v4(lat, [0], _table(), [0], 1)
+    assert list(_v4_slot(v4, 0)[0][448:].view(np.uint16)[:4]) == [0x7FC0, 0x7FC0, 0x7F80, 0x7FC0]
