@@ -19,7 +19,8 @@ import os
 import torch
 
 __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
-           "rope_quant_insert_nvfp4",
+           "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
+           "save_ring_rows",
            "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "row_bytes",
            "cache_view", "KvqError", "lib",
            "LIBRARY_PATH"]
@@ -55,11 +56,17 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_mla_rmsnorm_store.restype = ctypes.c_int
         L.mxfp4_mla_rmsnorm_store.argtypes = [_p, _i64, _i64, _i64, _p, ctypes.c_float, _p, _p,
                                               _i64, _i64, _i64, _i32, _p]
-        for name in ("rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4"):
+        for name in ("rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
+                     "rope_quant_insert_v4"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _p, _p, _i64, _i64, _i64, _i32, _i32,
                           _p]
+        L.rope_plain_insert.restype = ctypes.c_int
+        L.rope_plain_insert.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _p, _p, _i64, _i64,
+                                        _i64, _i64, _i32, _i32, ctypes.c_float, _p]
+        L.save_ring_rows.restype = ctypes.c_int
+        L.save_ring_rows.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _i64, _i64, _p]
         L.mxfp4_mla_gather_dequant.restype = ctypes.c_int
         L.mxfp4_mla_gather_dequant.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _p, _i64, _p]
         L.mxfp4_mla_sparse_attention.restype = ctypes.c_int
@@ -148,23 +155,28 @@ def mxfp4_mla_rmsnorm_store(latent: torch.Tensor, weight: torch.Tensor, eps: flo
         _stream(stream)))
 
 
-def _rope(name, record, latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
-          sanitize_nans, stream):
+def _rope_inputs(latent, positions, cos_sin, slot_mapping):
     _need(latent, torch.bfloat16, "latent")
     _need(positions, torch.int64, "positions")
     _need(cos_sin, torch.float32, "cos_sin")
     _need(slot_mapping, torch.int64, "slot_mapping")
-    _need(kv_cache, torch.uint8, "kv_cache")
     if latent.dim() != 2 or latent.shape[1] != 512 or latent.stride(1) != 1:
         raise ValueError("latent must be [tokens, 512] with unit column stride")
     if cos_sin.dim() != 2 or cos_sin.stride(1) != 1:
         raise ValueError("cos_sin must be [rows, >= 64] with unit column stride")
-    if kv_cache.dim() != 3 or kv_cache.shape[-1] != record or not kv_cache[0].is_contiguous():
-        raise ValueError(f"kv_cache must be [pages, cache_block, {record}] with contiguous pages")
     n = slot_mapping.numel()
     if n > min(latent.shape[0], positions.numel()) or not slot_mapping.is_contiguous() or \
             not positions.is_contiguous():
         raise ValueError("slot_mapping / positions must be contiguous and cover the tokens")
+    return n
+
+
+def _rope(name, record, latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
+          sanitize_nans, stream):
+    n = _rope_inputs(latent, positions, cos_sin, slot_mapping)
+    _need(kv_cache, torch.uint8, "kv_cache")
+    if kv_cache.dim() != 3 or kv_cache.shape[-1] != record or not kv_cache[0].is_contiguous():
+        raise ValueError(f"kv_cache must be [pages, cache_block, {record}] with contiguous pages")
     _check(name, getattr(lib(), name)(
         latent.data_ptr(), n, latent.stride(0), positions.data_ptr(), cos_sin.data_ptr(),
         cos_sin.stride(0), cos_sin.shape[0], kv_cache.data_ptr(), slot_mapping.data_ptr(),
@@ -186,6 +198,58 @@ def rope_quant_insert_nvfp4(latent, positions, cos_sin, kv_cache, slot_mapping, 
     code bytes then cache_block x 32 scale bytes."""
     _rope("rope_quant_insert_nvfp4", 288, latent, positions, cos_sin, kv_cache, slot_mapping,
           compress_ratio, sanitize_nans, stream)
+
+
+def rope_quant_insert_v4(latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
+                         sanitize_nans=False, stream=None) -> None:
+    """kv_cache: uint8 [pages, cache_block, 584]; a page holds cache_block x 576
+    value bytes (448 E4M3 | 64 bf16) then cache_block x 8 scale bytes."""
+    _rope("rope_quant_insert_v4", 584, latent, positions, cos_sin, kv_cache, slot_mapping,
+          compress_ratio, sanitize_nans, stream)
+
+
+def rope_plain_insert(latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
+                      fp8_scale=None, stream=None) -> None:
+    """kv_cache: bf16 or float8_e4m3fn [pages, cache_block, 512] with unit last
+    stride (page and slot strides free, multiples of 8 elements). An fp8 cache
+    needs ``fp8_scale`` (the per-tensor dequantizing factor)."""
+    n = _rope_inputs(latent, positions, cos_sin, slot_mapping)
+    if kv_cache.dtype == torch.bfloat16:
+        fp8, scale = 0, 1.0
+    elif kv_cache.dtype == torch.float8_e4m3fn:
+        if fp8_scale is None:
+            raise ValueError("an fp8 kv_cache needs fp8_scale")
+        fp8, scale = 1, float(fp8_scale)
+    else:
+        raise TypeError(f"kv_cache must be bfloat16 or float8_e4m3fn, got {kv_cache.dtype}")
+    if not kv_cache.is_cuda:
+        raise ValueError("kv_cache must be a CUDA tensor")
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != 512 or kv_cache.stride(2) != 1:
+        raise ValueError("kv_cache must be [pages, cache_block, 512] with unit last stride")
+    _check("rope_plain_insert", lib().rope_plain_insert(
+        latent.data_ptr(), n, latent.stride(0), positions.data_ptr(), cos_sin.data_ptr(),
+        cos_sin.stride(0), cos_sin.shape[0], kv_cache.data_ptr(), slot_mapping.data_ptr(),
+        kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1),
+        int(compress_ratio), fp8, scale, _stream(stream)))
+
+
+def save_ring_rows(rows: torch.Tensor, slot_mapping: torch.Tensor, state: torch.Tensor,
+                   stream=None) -> None:
+    """rows: fp32 [N, >= 1024] (unit column stride; the first 1024 values are
+    saved); state: fp32 [blocks, state_block, >= 1024] with unit last stride."""
+    _need(rows, torch.float32, "rows")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(state, torch.float32, "state")
+    if rows.dim() != 2 or rows.shape[1] < 1024 or rows.stride(1) != 1:
+        raise ValueError("rows must be [N, >= 1024] with unit column stride")
+    if state.dim() != 3 or state.shape[2] < 1024 or state.stride(2) != 1:
+        raise ValueError("state must be [blocks, state_block, >= 1024] with unit last stride")
+    if slot_mapping.numel() > rows.shape[0] or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous and cover the rows")
+    _check("save_ring_rows", lib().save_ring_rows(
+        rows.data_ptr(), slot_mapping.numel(), rows.stride(0), slot_mapping.data_ptr(),
+        state.data_ptr(), state.shape[0], state.shape[1], state.stride(0), state.stride(1),
+        _stream(stream)))
 
 
 def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor = None,

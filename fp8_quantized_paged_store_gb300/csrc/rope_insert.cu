@@ -1,13 +1,18 @@
-// rope_insert.cu — rope_quant_insert_mxfp8 / rope_quant_insert_nvfp4: the
-// V4.1 compressed-cache inserts. GPT-J RoPE on the last 64 elements, then
-// MXFP8 (E4M3 values, E8M0 scale per 32) or NVFP4 (E2M1 codes, E4M3 scale per
-// 16) into a page layout with the scales segregated after the values.
+// rope_insert.cu — the V4.1 and V4 compressed-cache inserts:
+// rope_quant_insert_mxfp8 / _nvfp4 / _v4 and rope_plain_insert. GPT-J RoPE on
+// the last 64 elements, then one of five layouts: MXFP8 (E4M3 values, E8M0
+// scale per 32; 528-byte record), NVFP4 (E2M1 codes, E4M3 scale per 16;
+// 288-byte record), the V4 584-byte record (448 E4M3 values in tiles of 64
+// with E8M0 scales, 64 bf16 rotary values, 8 scale bytes of which the last
+// is 0), or a plain [448 | 64] row of bf16 or per-tensor-scaled E4M3. The
+// records keep their scales segregated after the values in each page.
 //
 // Follows "vllm.models.deepseek_v41.common.ops.fused_compress_quant_cache"
 // (_rope_quant_insert_mxfp8_kernel, _rope_quant_insert_nvfp4_kernel,
-// rope_quant_insert).
+// rope_quant_insert: its docstring describes the V4 record and the plain
+// rows, whose kernels the page does not print).
 //
-// Work decomposition (both kernels): a warp owns 32 tokens at a time
+// Work decomposition (all kernels): a warp owns 32 tokens at a time
 // (grid-stride over chunks); lane i evaluates token i's gates (slot range,
 // (pos+1) % R == 0, table row in range) and addresses once, and a ballot lists
 // the writers, so non-writers cost no row traffic. Writers are taken two at a
@@ -19,8 +24,10 @@
 // 256+8l..256+8l+7 (half 1), each 16-byte load of the warp covering 512
 // contiguous bytes. Rotary pairs 224..255 are elements 448..511.
 //
-// MXFP8: the rotary elements are half 1 of lanes 24..31, which alone read the
-// table row (lane l: cos and sin 4(l-24)..4(l-24)+3, two 16-byte loads).
+// MXFP8, V4 and plain rows: the rotary elements are half 1 of lanes 24..31,
+// which alone read the table row (lane l: cos and sin 4(l-24)..4(l-24)+3, two
+// 16-byte loads). A V4 tile of 64 is eight lanes' halves, so its amax takes
+// three xor-shuffles; lanes 24..31 write their rotated half 1 as bf16.
 //
 // NVFP4: lanes 0..23 load half 1 as above, and every lane j loads rotary pair
 // j (4 bytes) with its own cos and sin, so the rotation and the exact quotient
@@ -36,7 +43,8 @@
 // exact, and each sum is the element itself, a zero, or NaN, so no rounding
 // happens and the result equals the binary32 formula bit for bit. Rotary
 // pairs use the binary32 formula with every product and sum rounded
-// separately (no fused multiply-add).
+// separately (no fused multiply-add). Plain rows take the 448 NoPE values as
+// they are (bit for bit in bf16, divided by the scale in fp8).
 #include <cstdint>
 
 #include "kvq.h"
@@ -63,7 +71,14 @@ struct RopeParams {
   int64_t cache_block;
   int64_t page_stride;  // bytes
   int64_t ratio;
+  int64_t slot_pitch;   // plain rows: bytes between the rows of a page
+  float fp8_scale;      // plain fp8 rows: the per-tensor scale
 };
+
+// Layouts written by fp8_family_insert_kernel (the MXFP8 record and the ones
+// that share its structure).
+enum class Layout { kMxfp8, kV4, kPlainBf16, kPlainFp8 };
+constexpr int kV4Record = 584;   // 576 value bytes (448 E4M3 + 64 bf16) + 8 scale bytes
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -156,6 +171,123 @@ __device__ __forceinline__ void mxfp8_half(const float f[8], uint8_t* values, ui
     const int cap = kSanitize ? 254 : 255;
     const int enc = e + 127;  // >= 105
     st_u8(scales + (lane >> 2), (uint32_t)(enc < cap ? enc : cap));
+  }
+}
+
+// ------------------------------------------------------------ V4 and plain ---
+
+// V4 record, one NoPE half of the row held by this lane (8 values): tiles of
+// 64 values span eight lanes (tile = lane / 8, plus 4 for half 1), each under
+// the MXFP8 scale rule; lanes with `store` false (the rotary lanes of half 1)
+// take part in the shuffles only.
+template <bool kSanitize>
+__device__ __forceinline__ void v4_nope_half(const float f[8], uint8_t* values, uint8_t* scales,
+                                             int tile, int lane, bool store) {
+  float amax = abs_max8(f);
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+  amax = fmaxf(amax, 1e-4f);
+  const int e = ceil_pow2_exponent(__fmul_rn(amax, 1.0f / 448.0f));
+  const float inv = exp2_neg(e);
+  const uint32_t a = cvt_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
+                     (cvt_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
+  const uint32_t b = cvt_e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
+                     (cvt_e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
+  if (store) {
+    st_v2(values, a, b);
+    if ((lane & 7) == 0) {
+      const int cap = kSanitize ? 254 : 255;
+      const int enc = e + 127;
+      st_u8(scales + tile, (uint32_t)(enc < cap ? enc : cap));
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Two binary32 values rounded to bf16 (nearest even) with every NaN stored
+// as the quiet NaN 0x7FC0: the sign of a NaN that arithmetic produced is not
+// portable, so a stored one carries none.
+__device__ __forceinline__ uint32_t bf16x2_rn_nan(float lo, float hi) {
+  uint32_t d = bf16x2_rn(lo, hi);
+  if (lo != lo) d = (d & 0xFFFF0000u) | 0x7FC0u;
+  if (hi != hi) d = (d & 0x0000FFFFu) | 0x7FC00000u;
+  return d;
+}
+
+// Eight binary32 values as bf16 (bf16x2_rn_nan), 16 bytes.
+__device__ __forceinline__ uint4 bf16x8_rn(const float f[8]) {
+  return make_uint4(bf16x2_rn_nan(f[0], f[1]), bf16x2_rn_nan(f[2], f[3]),
+                    bf16x2_rn_nan(f[4], f[5]), bf16x2_rn_nan(f[6], f[7]));
+}
+
+// Eight values as E4M3 of RN(x / scale), clamped to +-448 (NaN -> 0x7F).
+__device__ __forceinline__ uint2 e4m3x8_div(const float f[8], float scale) {
+  uint32_t w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    w[h] = cvt_e4m3x2(__fdiv_rn(f[4 * h], scale), __fdiv_rn(f[4 * h + 1], scale)) |
+           (cvt_e4m3x2(__fdiv_rn(f[4 * h + 2], scale), __fdiv_rn(f[4 * h + 3], scale)) << 16);
+  return make_uint2(w[0], w[1]);
+}
+
+// The rotary values of the lane's half 1 (lanes 24..31), binary32 formula
+// without contraction and without sanitising.
+__device__ __forceinline__ void rotate_pairs(uint4 x1, float4 c, float4 s, float f[8]) {
+  float v[8];
+  widen8(x1, v);
+  const float cc[4] = {c.x, c.y, c.z, c.w};
+  const float ss[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float e = v[2 * k], o = v[2 * k + 1];
+    f[2 * k] = __fsub_rn(__fmul_rn(e, cc[k]), __fmul_rn(o, ss[k]));
+    f[2 * k + 1] = __fadd_rn(__fmul_rn(o, cc[k]), __fmul_rn(e, ss[k]));
+  }
+}
+
+// One writer row of a layout other than the MXFP8 record. `page` points at
+// the slot's page, `slot_in_page` is its row there.
+template <Layout kL, bool kSanitize>
+__device__ __forceinline__ void write_other(const RopeParams& p, uint4 x0, uint4 x1, float4 c,
+                                            float4 s, uint8_t* page, int64_t slot_in_page,
+                                            int lane) {
+  if constexpr (kL == Layout::kV4) {
+    float f0[8], f1[8];
+    rotate_row<kSanitize>(x0, x1, c, s, lane, f0, f1);
+    uint8_t* values = page + slot_in_page * 576;
+    uint8_t* scales = page + p.cache_block * 576 + slot_in_page * 8;
+    v4_nope_half<kSanitize>(f0, values + 8 * lane, scales, lane >> 3, lane, true);
+    v4_nope_half<kSanitize>(f1, values + 256 + 8 * lane, scales, 4 + (lane >> 3), lane, lane < 24);
+    if (lane >= 24) st_v4(values + 448 + 16 * (lane - 24), bf16x8_rn(f1));
+    if (lane == 24) st_u8(scales + 7, 0u);
+  } else if constexpr (kL == Layout::kPlainBf16) {
+    uint8_t* row = page + slot_in_page * p.slot_pitch;
+    st_v4(row + 16 * lane, x0);
+    if (lane < 24) {
+      st_v4(row + 512 + 16 * lane, x1);
+    } else {
+      float f1[8];
+      rotate_pairs(x1, c, s, f1);
+      st_v4(row + 512 + 16 * lane, bf16x8_rn(f1));
+    }
+  } else {  // kPlainFp8
+    uint8_t* row = page + slot_in_page * p.slot_pitch;
+    float f0[8], f1[8];
+    widen8(x0, f0);
+    if (lane < 24) {
+      widen8(x1, f1);
+    } else {
+      rotate_pairs(x1, c, s, f1);
+    }
+    const uint2 a = e4m3x8_div(f0, p.fp8_scale), b = e4m3x8_div(f1, p.fp8_scale);
+    st_v2(row + 8 * lane, a.x, a.y);
+    st_v2(row + 256 + 8 * lane, b.x, b.y);
   }
 }
 
@@ -329,12 +461,14 @@ __device__ __forceinline__ void token_gates(const RopeParams& p, int64_t t, int6
 
 // ---------------------------------------------------------------- kernels ---
 
-// Five resident blocks (40 warps) per SM: the 48-register cap costs a few
-// spilled words in the MXFP8 kernel, but the extra writers in flight lifted it
+// The MXFP8 record and the layouts that share its structure (V4 record, plain
+// bf16 and fp8 rows). Five resident blocks (40 warps) per SM: the 48-register
+// cap costs a few spilled words in the MXFP8 kernel, but the extra writers in
+// flight lifted it
 // by 7 % (4,194,304-token insert: 5292 -> 5680 GB/s; six blocks at 40
 // registers lose it again).
-template <bool kSanitize>
-__global__ void __launch_bounds__(kRopeThreads, 5) mxfp8_insert_kernel(RopeParams p) {
+template <Layout kL, bool kSanitize>
+__global__ void __launch_bounds__(kRopeThreads, 5) fp8_family_insert_kernel(RopeParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 5;
   const int64_t num_warps = ((int64_t)gridDim.x * kRopeThreads) >> 5;
@@ -377,14 +511,19 @@ __global__ void __launch_bounds__(kRopeThreads, 5) mxfp8_insert_kernel(RopeParam
         if (i < 0) break;
         const int64_t pg = __shfl_sync(0xFFFFFFFFu, page_off, i);
         const int64_t slot_in_page = __shfl_sync(0xFFFFFFFFu, in_page, i);
-        float f0[8], f1[8];
-        rotate_row<kSanitize>(w ? xb0 : xa0, w ? xb1 : xa1, w ? cb : ca, w ? snb : sna, lane, f0,
-                              f1);
         uint8_t* page = p.cache + pg;
-        uint8_t* values = page + slot_in_page * 512;
-        uint8_t* scales = page + p.cache_block * 512 + slot_in_page * 16;
-        mxfp8_half<kSanitize>(f0, values, scales, lane);
-        mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
+        if constexpr (kL == Layout::kMxfp8) {
+          float f0[8], f1[8];
+          rotate_row<kSanitize>(w ? xb0 : xa0, w ? xb1 : xa1, w ? cb : ca, w ? snb : sna, lane,
+                                f0, f1);
+          uint8_t* values = page + slot_in_page * 512;
+          uint8_t* scales = page + p.cache_block * 512 + slot_in_page * 16;
+          mxfp8_half<kSanitize>(f0, values, scales, lane);
+          mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
+        } else {
+          write_other<kL, kSanitize>(p, w ? xb0 : xa0, w ? xb1 : xa1, w ? cb : ca, w ? snb : sna,
+                                     page, slot_in_page, lane);
+        }
       }
     }
   }
@@ -450,7 +589,7 @@ __global__ void __launch_bounds__(kRopeThreads, 5) nvfp4_insert_kernel(RopeParam
   }
 }
 
-int g_rope_occupancy[3][64];
+int g_rope_occupancy[8][64];
 
 template <typename Kernel>
 int launch(Kernel k, int* occupancy, const RopeParams& p, cudaStream_t stream) {
@@ -462,30 +601,26 @@ int launch(Kernel k, int* occupancy, const RopeParams& p, cudaStream_t stream) {
   return launch_status();
 }
 
-int rope_insert(bool nvfp4, const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
+enum class Kind { kMxfp8, kNvfp4, kV4, kPlainBf16, kPlainFp8 };
+
+// Checks shared by every insert; fills the fields of `p` that do not depend
+// on the cache layout. KVQ_OK, or KVQ_EINVAL.
+int common_args(const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
                 const int64_t* positions, const float* cos_sin, int64_t cos_stride,
-                int64_t cos_sin_rows, uint8_t* cache, const int64_t* cache_slots,
-                int64_t num_pages, int64_t cache_block, int64_t page_stride_bytes,
-                int32_t compress_ratio, int32_t sanitize_nans, cudaStream_t stream) {
-  const int64_t record = nvfp4 ? kNvfp4Record : kMxfp8Record;
+                int64_t cos_sin_rows, const void* cache, const int64_t* cache_slots,
+                int64_t num_pages, int64_t cache_block, int32_t compress_ratio, RopeParams& p) {
   if (num_tokens < 0 || row_stride_elems < kLatent || row_stride_elems % 8 != 0) return KVQ_EINVAL;
   if (cos_stride < 64 || cos_stride % 4 != 0 || cos_sin_rows < 1) return KVQ_EINVAL;
   if (num_pages < 1 || cache_block < 1 || compress_ratio < 1) return KVQ_EINVAL;
-  if (sanitize_nans != 0 && sanitize_nans != 1) return KVQ_EINVAL;
-  if (cache_block > INT64_MAX / record || page_stride_bytes < cache_block * record ||
-      page_stride_bytes % 16 != 0)
-    return KVQ_EINVAL;
-  if (num_pages > INT64_MAX / page_stride_bytes || num_pages > INT64_MAX / cache_block)
-    return KVQ_EINVAL;
+  if (num_pages > INT64_MAX / cache_block) return KVQ_EINVAL;
   if (cos_sin_rows > INT64_MAX / cos_stride) return KVQ_EINVAL;
   if (num_tokens > INT64_MAX / 2 / row_stride_elems) return KVQ_EINVAL;
-  if (num_tokens == 0) return KVQ_OK;
-  if (!latent_bf16 || !positions || !cos_sin || !cache || !cache_slots) return KVQ_EINVAL;
-  if (!aligned(latent_bf16, 16) || !aligned(cos_sin, 16) || !aligned(cache, 16) ||
-      !aligned(positions, 8) || !aligned(cache_slots, 8))
-    return KVQ_EINVAL;
-
-  RopeParams p;
+  if (num_tokens > 0) {
+    if (!latent_bf16 || !positions || !cos_sin || !cache || !cache_slots) return KVQ_EINVAL;
+    if (!aligned(latent_bf16, 16) || !aligned(cos_sin, 16) || !aligned(cache, 16) ||
+        !aligned(positions, 8) || !aligned(cache_slots, 8))
+      return KVQ_EINVAL;
+  }
   p.latent = static_cast<const uint8_t*>(latent_bf16);
   p.row_pitch = row_stride_elems * 2;
   p.num_tokens = num_tokens;
@@ -493,15 +628,62 @@ int rope_insert(bool nvfp4, const void* latent_bf16, int64_t num_tokens, int64_t
   p.cos_sin = cos_sin;
   p.cos_stride = cos_stride;
   p.cos_rows = cos_sin_rows;
-  p.cache = cache;
+  p.cache = static_cast<uint8_t*>(const_cast<void*>(cache));
   p.slots = cache_slots;
   p.num_slots = num_pages * cache_block;
   p.cache_block = cache_block;
-  p.page_stride = page_stride_bytes;
   p.ratio = compress_ratio;
-  if (nvfp4) return launch(nvfp4_insert_kernel, g_rope_occupancy[2], p, stream);
-  return sanitize_nans ? launch(mxfp8_insert_kernel<true>, g_rope_occupancy[1], p, stream)
-                       : launch(mxfp8_insert_kernel<false>, g_rope_occupancy[0], p, stream);
+  p.slot_pitch = 0;
+  p.fp8_scale = 1.0f;
+  return KVQ_OK;
+}
+
+int dispatch(Kind kind, bool sanitize, const RopeParams& p, cudaStream_t stream) {
+  if (p.num_tokens == 0) return KVQ_OK;
+  switch (kind) {
+    case Kind::kNvfp4:
+      return launch(nvfp4_insert_kernel, g_rope_occupancy[2], p, stream);
+    case Kind::kMxfp8:
+      return sanitize
+                 ? launch(fp8_family_insert_kernel<Layout::kMxfp8, true>, g_rope_occupancy[1], p,
+                          stream)
+                 : launch(fp8_family_insert_kernel<Layout::kMxfp8, false>, g_rope_occupancy[0], p,
+                          stream);
+    case Kind::kV4:
+      return sanitize
+                 ? launch(fp8_family_insert_kernel<Layout::kV4, true>, g_rope_occupancy[4], p,
+                          stream)
+                 : launch(fp8_family_insert_kernel<Layout::kV4, false>, g_rope_occupancy[3], p,
+                          stream);
+    case Kind::kPlainBf16:
+      return launch(fp8_family_insert_kernel<Layout::kPlainBf16, false>, g_rope_occupancy[5], p,
+                    stream);
+    default:
+      return launch(fp8_family_insert_kernel<Layout::kPlainFp8, false>, g_rope_occupancy[6], p,
+                    stream);
+  }
+}
+
+// The paged records (MXFP8 528 B, NVFP4 288 B, V4 584 B): value bytes of the
+// page's slots, then their scale bytes; pages page_stride_bytes apart.
+int record_insert(Kind kind, const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
+                  const int64_t* positions, const float* cos_sin, int64_t cos_stride,
+                  int64_t cos_sin_rows, uint8_t* cache, const int64_t* cache_slots,
+                  int64_t num_pages, int64_t cache_block, int64_t page_stride_bytes,
+                  int32_t compress_ratio, int32_t sanitize_nans, cudaStream_t stream) {
+  const int64_t record =
+      kind == Kind::kNvfp4 ? kNvfp4Record : (kind == Kind::kV4 ? kV4Record : kMxfp8Record);
+  RopeParams p;
+  int st = common_args(latent_bf16, num_tokens, row_stride_elems, positions, cos_sin, cos_stride,
+                       cos_sin_rows, cache, cache_slots, num_pages, cache_block, compress_ratio, p);
+  if (st != KVQ_OK) return st;
+  if (sanitize_nans != 0 && sanitize_nans != 1) return KVQ_EINVAL;
+  if (cache_block > INT64_MAX / record || page_stride_bytes < cache_block * record ||
+      page_stride_bytes % 16 != 0)
+    return KVQ_EINVAL;
+  if (num_pages > INT64_MAX / page_stride_bytes) return KVQ_EINVAL;
+  p.page_stride = page_stride_bytes;
+  return dispatch(kind, sanitize_nans != 0, p, stream);
 }
 
 }  // namespace
@@ -515,9 +697,10 @@ extern "C" int rope_quant_insert_mxfp8(const void* latent_bf16, int64_t num_toke
                                        int64_t cache_block, int64_t page_stride_bytes,
                                        int32_t compress_ratio, int32_t sanitize_nans,
                                        cudaStream_t stream) {
-  return kvq::rope_insert(false, latent_bf16, num_tokens, row_stride_elems, positions, cos_sin,
-                          cos_stride, cos_sin_rows, cache, cache_slots, num_pages, cache_block,
-                          page_stride_bytes, compress_ratio, sanitize_nans, stream);
+  return kvq::record_insert(kvq::Kind::kMxfp8, latent_bf16, num_tokens, row_stride_elems,
+                            positions, cos_sin, cos_stride, cos_sin_rows, cache, cache_slots,
+                            num_pages, cache_block, page_stride_bytes, compress_ratio,
+                            sanitize_nans, stream);
 }
 
 extern "C" int rope_quant_insert_nvfp4(const void* latent_bf16, int64_t num_tokens,
@@ -528,7 +711,46 @@ extern "C" int rope_quant_insert_nvfp4(const void* latent_bf16, int64_t num_toke
                                        int64_t cache_block, int64_t page_stride_bytes,
                                        int32_t compress_ratio, int32_t sanitize_nans,
                                        cudaStream_t stream) {
-  return kvq::rope_insert(true, latent_bf16, num_tokens, row_stride_elems, positions, cos_sin,
-                          cos_stride, cos_sin_rows, cache, cache_slots, num_pages, cache_block,
-                          page_stride_bytes, compress_ratio, sanitize_nans, stream);
+  return kvq::record_insert(kvq::Kind::kNvfp4, latent_bf16, num_tokens, row_stride_elems,
+                            positions, cos_sin, cos_stride, cos_sin_rows, cache, cache_slots,
+                            num_pages, cache_block, page_stride_bytes, compress_ratio,
+                            sanitize_nans, stream);
+}
+
+extern "C" int rope_quant_insert_v4(const void* latent_bf16, int64_t num_tokens,
+                                    int64_t row_stride_elems, const int64_t* positions,
+                                    const float* cos_sin, int64_t cos_stride, int64_t cos_sin_rows,
+                                    uint8_t* cache, const int64_t* cache_slots, int64_t num_pages,
+                                    int64_t cache_block, int64_t page_stride_bytes,
+                                    int32_t compress_ratio, int32_t sanitize_nans,
+                                    cudaStream_t stream) {
+  return kvq::record_insert(kvq::Kind::kV4, latent_bf16, num_tokens, row_stride_elems, positions,
+                            cos_sin, cos_stride, cos_sin_rows, cache, cache_slots, num_pages,
+                            cache_block, page_stride_bytes, compress_ratio, sanitize_nans, stream);
+}
+
+extern "C" int rope_plain_insert(const void* latent_bf16, int64_t num_tokens,
+                                 int64_t row_stride_elems, const int64_t* positions,
+                                 const float* cos_sin, int64_t cos_stride, int64_t cos_sin_rows,
+                                 void* cache, const int64_t* cache_slots, int64_t num_pages,
+                                 int64_t cache_block, int64_t page_stride_elems,
+                                 int64_t slot_stride_elems, int32_t compress_ratio, int32_t fp8,
+                                 float fp8_scale, cudaStream_t stream) {
+  using namespace kvq;
+  RopeParams p;
+  int st = common_args(latent_bf16, num_tokens, row_stride_elems, positions, cos_sin, cos_stride,
+                       cos_sin_rows, cache, cache_slots, num_pages, cache_block, compress_ratio, p);
+  if (st != KVQ_OK) return st;
+  if (fp8 != 0 && fp8 != 1) return KVQ_EINVAL;
+  if (fp8 && !(fp8_scale > 0.0f && fp8_scale <= 3.0e38f)) return KVQ_EINVAL;
+  const int64_t es = fp8 ? 1 : 2;  // bytes per element
+  if (slot_stride_elems < kLatent || slot_stride_elems % 8 != 0 || page_stride_elems % 8 != 0)
+    return KVQ_EINVAL;
+  if (cache_block - 1 > (INT64_MAX / 4 - kLatent) / slot_stride_elems) return KVQ_EINVAL;
+  if (page_stride_elems < (cache_block - 1) * slot_stride_elems + kLatent) return KVQ_EINVAL;
+  if (num_pages > INT64_MAX / 4 / page_stride_elems) return KVQ_EINVAL;
+  p.page_stride = page_stride_elems * es;
+  p.slot_pitch = slot_stride_elems * es;
+  p.fp8_scale = fp8 ? fp8_scale : 1.0f;
+  return dispatch(fp8 ? Kind::kPlainFp8 : Kind::kPlainBf16, false, p, stream);
 }

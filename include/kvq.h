@@ -1,7 +1,9 @@
 /*
  * kvq.h — C ABI of the GB300 (sm_103a) quantize-and-scatter library for a
- * paged MLA KV cache: MXFP4 store, V4.1 RoPE-then-quantize inserts (MXFP8 and
- * NVFP4 records), and the MXFP4 gather-and-dequantize read.
+ * paged MLA KV cache: MXFP4 store, RoPE-then-quantize inserts (V4.1 MXFP8
+ * and NVFP4 records, the V4 record, plain bf16 / fp8 rows), the compressor's
+ * ring-state save, the MXFP4 gather-and-dequantize read and sparse MLA
+ * attention on the packed cache.
  *
  * Pages this interface follows (cited by title and section):
  *   [store] "vllm.v1.attention.ops.mxfp4_mla.store" (vLLM API docs):
@@ -9,7 +11,8 @@
  *           store_mxfp4_mla.
  *   [v41]   "vllm.models.deepseek_v41.common.ops.fused_compress_quant_cache"
  *           (vLLM API docs): _rope_quant_insert_mxfp8_kernel,
- *           _rope_quant_insert_nvfp4_kernel, rope_quant_insert.
+ *           _rope_quant_insert_nvfp4_kernel, rope_quant_insert (and its
+ *           docstring on the V4 record and the plain rows), save_ring_rows.
  *   [pr]    "[ROCm][Attention] Add an mxfp4_mla KV cache for rope-free sparse
  *           MLA (read/write path)", vLLM pull request 60321: Overview, Claims,
  *           Details (format and write path; read path).
@@ -183,6 +186,86 @@ int rope_quant_insert_nvfp4(const void* latent_bf16, int64_t num_tokens, int64_t
                             int64_t cos_sin_rows, uint8_t* cache, const int64_t* cache_slots,
                             int64_t num_pages, int64_t cache_block, int64_t page_stride_bytes,
                             int32_t compress_ratio, int32_t sanitize_nans, cudaStream_t stream);
+
+/*
+ * rope_quant_insert_v4 — the V4 584-byte record: GPT-J RoPE, then 448 E4M3
+ * values in seven tiles of 64 and 64 bf16 rotary values. [v41]
+ * rope_quant_insert (docstring: 576 value bytes, eight UE8M0 scale bytes of
+ * which one is a zero pad; the kernel itself is not printed).
+ *
+ * Gates, rotation and sanitising as rope_quant_insert_mxfp8. Elements
+ * 0..447 form tiles g = 0..6 of 64 quantized by the MXFP8 rule of
+ * rope_quant_insert_mxfp8 (1e-4 amax floor, scale byte capped at 254 when
+ * sanitising, 255 otherwise); elements 448..511 (the rotated pairs) are
+ * stored as bf16, nearest even, every NaN as 0x7FC0. Page P = s / cache_block
+ * at cache + P*page_stride_bytes: value bytes at page + (s % cache_block)*576
+ * ([448 E4M3 | 64 bf16 little-endian]), scale bytes at
+ * page + cache_block*576 + (s % cache_block)*8 (bytes 0..6 the tiles', byte 7
+ * always 0).
+ * page_stride_bytes must be >= cache_block*584 and a multiple of 16; other
+ * arguments as rope_quant_insert_mxfp8.
+ */
+int rope_quant_insert_v4(const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
+                         const int64_t* positions, const float* cos_sin, int64_t cos_stride,
+                         int64_t cos_sin_rows, uint8_t* cache, const int64_t* cache_slots,
+                         int64_t num_pages, int64_t cache_block, int64_t page_stride_bytes,
+                         int32_t compress_ratio, int32_t sanitize_nans, cudaStream_t stream);
+
+/*
+ * rope_plain_insert — a plain [448 NoPE | 64 RoPE] row of bf16, or of E4M3
+ * with a per-tensor scale, for readers that take unquantized rows. [v41]
+ * rope_quant_insert (docstring: bfloat16 and float8_e4m3fn caches of shape
+ * [pages, CACHE_BLOCK, 512] with their own strides; the kernel is not
+ * printed).
+ *
+ * Gates and table row as rope_quant_insert_mxfp8 (no sanitising). Rotary
+ * pairs i = 224..255 (elements 448..511) are rotated in binary32 as there.
+ *   fp8 == 0: elements 0..447 are the latent's bf16 patterns copied bit for
+ *             bit; 448..511 are the rotated values rounded to bf16 (nearest
+ *             even, every NaN as 0x7FC0).
+ *   fp8 == 1: every element x (the latent's value, or the rotated value)
+ *             becomes E4M3(clamp(RN(x / fp8_scale), -448, 448)), nearest
+ *             even, NaN -> 0x7F.
+ * Element j of slot s sits at element
+ *   (s / cache_block)*page_stride_elems + (s % cache_block)*slot_stride_elems + j
+ * of `cache` (2-byte elements for bf16, 1-byte for fp8).
+ *
+ * cache              bf16 or E4M3, 16-byte aligned
+ * page_stride_elems  multiple of 8, >= (cache_block-1)*slot_stride_elems + 512
+ * slot_stride_elems  multiple of 8, >= 512
+ * fp8                0 (bf16 cache) or 1 (E4M3 cache)
+ * fp8_scale          fp8 == 1 only: finite and > 0 (the dequantizing factor)
+ * Other arguments as rope_quant_insert_mxfp8.
+ */
+int rope_plain_insert(const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
+                      const int64_t* positions, const float* cos_sin, int64_t cos_stride,
+                      int64_t cos_sin_rows, void* cache, const int64_t* cache_slots,
+                      int64_t num_pages, int64_t cache_block, int64_t page_stride_elems,
+                      int64_t slot_stride_elems, int32_t compress_ratio, int32_t fp8,
+                      float fp8_scale, cudaStream_t stream);
+
+/*
+ * save_ring_rows — store the compressor's fp32 [kv | score] rows of 1024
+ * values into their slots of the paged ring state. [v41] save_ring_rows.
+ *
+ * For each row t with s = slot_mapping[t]: if 0 <= s < num_blocks*state_block
+ * the 1024 floats at rows + t*row_stride_elems are copied bit for bit to
+ *   state + (s / state_block)*state_stride_elems + (s % state_block)*state_row_stride_elems;
+ * otherwise (-1, or outside the state) the row is skipped.
+ *
+ * rows                    fp32 [num_rows, row_stride_elems], 16-byte aligned
+ * row_stride_elems        >= 1024, multiple of 4
+ * slot_mapping            int64 [num_rows]
+ * state                   fp32, 16-byte aligned
+ * num_blocks, state_block >= 1
+ * state_row_stride_elems  >= 1024, multiple of 4
+ * state_stride_elems      multiple of 4,
+ *                         >= (state_block-1)*state_row_stride_elems + 1024
+ */
+int save_ring_rows(const float* rows, int64_t num_rows, int64_t row_stride_elems,
+                   const int64_t* slot_mapping, float* state, int64_t num_blocks,
+                   int64_t state_block, int64_t state_stride_elems,
+                   int64_t state_row_stride_elems, cudaStream_t stream);
 
 /*
  * mxfp4_mla_gather_dequant — read packed MXFP4 rows back to bf16.

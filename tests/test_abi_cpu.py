@@ -31,6 +31,7 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) == {"kvq_strerror", "kvq_row_bytes", "mxfp4_mla_store",
                           "mxfp4_mla_rmsnorm_store",
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
+                          "rope_quant_insert_v4", "rope_plain_insert", "save_ring_rows",
                           "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention"}
     for n in names:
         assert hasattr(L, n), n
@@ -87,7 +88,8 @@ def test_rmsnorm_store_validation_on_host(L):
 
 
 def test_insert_validation_on_host(L):
-    for f, rec in ((L.rope_quant_insert_mxfp8, 528), (L.rope_quant_insert_nvfp4, 288)):
+    for f, rec in ((L.rope_quant_insert_mxfp8, 528), (L.rope_quant_insert_nvfp4, 288),
+                   (L.rope_quant_insert_v4, 584)):
         ok = [A16, 4, 512, A8, A16, 64, 10, A16, A8, 2, 64, 64 * rec, 4, 0, None]
         empty = list(ok); empty[1] = 0; empty[0] = None
         assert f(*empty) == 0
@@ -96,6 +98,36 @@ def test_insert_validation_on_host(L):
         for k, v in bad.items():
             a = list(ok); a[int(k)] = v
             assert f(*a) == -1, (rec, k, v)
+
+
+def test_plain_insert_validation_on_host(L):
+    f = L.rope_plain_insert
+    ok = [A16, 4, 512, A8, A16, 64, 10, A16, A8, 2, 64, 64 * 512, 512, 4, 1, 0.5, None]
+    empty = list(ok); empty[1] = 0; empty[0] = None
+    assert f(*empty) == 0
+    bad = {1: -3, 2: 500, 5: 62, 6: 0, 9: 0, 10: 0, 11: 63 * 512 + 504, 11.1: 64 * 512 + 4,
+           12: 504, 12.1: 516, 13: 0, 14: 2, 15: 0.0, 15.1: -1.0, 15.2: float("nan"),
+           15.3: float("inf"), 0: A16 + 8, 7: A16 + 8, 3: A8 + 4}
+    for k, v in bad.items():
+        a = list(ok); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
+    # a bf16 cache ignores the scale; 0 is accepted there (empty batch: no launch)
+    a = list(empty); a[14] = 0; a[15] = 0.0
+    assert f(*a) == 0
+
+
+def test_ring_rows_validation_on_host(L):
+    f = L.save_ring_rows
+    ok = [A16, 4, 1024, A8, A16, 2, 8, 8 * 1024, 1024, None]
+    empty = list(ok); empty[1] = 0; empty[0] = None
+    assert f(*empty) == 0
+    bad = {1: -1, 2: 1020, 2.1: 1026, 5: 0, 6: 0, 7: 8 * 1024 - 4, 7.1: 8 * 1024 + 2, 8: 1020,
+           8.1: 1030, 0: A16 + 4, 4: A16 + 8, 3: A8 + 4}
+    for k, v in bad.items():
+        a = list(ok); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
+    a = list(ok); a[0] = None
+    assert f(*a) == -1
 
 
 def test_gather_validation_on_host(L):
@@ -127,6 +159,7 @@ def test_attention_validation_on_host(L):
 
 def test_binding_has_the_abi_names():
     for n in ("mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
-              "rope_quant_insert_nvfp4", "mxfp4_mla_gather_dequant",
+              "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
+              "save_ring_rows", "mxfp4_mla_gather_dequant",
               "mxfp4_mla_sparse_attention"):
         assert callable(getattr(kvq, n))

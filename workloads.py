@@ -16,7 +16,9 @@ the recipe and shrink the counts for fast tests):
   store_small   64 tokens, contiguous 128-slot cache, injected edge groups
   store_paged   16,384 tokens, 2048 blocks x 64 slots, block stride 192 rows
   store_large   4,300,000 tokens, source row stride 576, 8,388,608 slots
-  rope_insert   65,536 tokens (or 4,194,304 for the large variant), R = 4
+  rope_insert   65,536 tokens (or 4,194,304 for the large variant), R = 4;
+                records mxfp8 / nvfp4 / v4, or plain bf16 / fp8 rows
+  ring_rows     fp32 [kv | score] rows of 1024 values into a paged ring state
   gather        1,048,576-slot packed cache, 128 queries x 2048 indices
   sparse_attention  the gather's cache and indices + 128 heads of bf16 queries
 """
@@ -30,6 +32,10 @@ LATENT = 512
 ROW_BYTES_MXFP4 = 272          # 512/2 code bytes + 512/32 scale bytes
 RECORD_BYTES_MXFP8 = 528       # 512 value bytes + 16 scale bytes
 RECORD_BYTES_NVFP4 = 288       # 256 code bytes + 32 scale bytes
+RECORD_BYTES_V4 = 584          # 576 value bytes + 8 scale bytes
+PLAIN_FP8_SCALE = 0.0125       # per-tensor scale of the plain fp8 rows (not a power of two)
+RING_ROW = 1024                # fp32 values per compressor row ([kv | score])
+RING_POISON_BITS = 0x7FBADBAD  # fill of the ring state before a save (a NaN pattern)
 POISON = 0xAA                  # fill of this layer's cache rows before a store
 OTHER_LAYER_POISON = 0x5A      # fill of interleaved pages of other layers
 BF16_MAX_BITS = 0x7F7F         # fill of source columns past the latent
@@ -216,12 +222,51 @@ def rope_insert(seed: int = 0, num_tokens: int = 65536, num_pages: int = 1024,
     positions = rng.integers(0, table_rows, size=num_tokens, dtype=np.int64)
     num_slots = num_pages * cache_block
     slots = _slots_with_pads(rng, num_slots, num_tokens, pad_count)
-    record_bytes = {"mxfp8": RECORD_BYTES_MXFP8, "nvfp4": RECORD_BYTES_NVFP4}[record]
+    if record in ("bf16", "fp8"):
+        # plain [pages, cache_block, 512] rows; strides in elements
+        esize = 2 if record == "bf16" else 1
+        page_elems = cache_block * LATENT
+        cache = np.full(num_pages * page_elems * esize, POISON, dtype=np.uint8)
+        return dict(latent=latent, positions=positions, cos_sin=rope_cos_sin_table(table_rows),
+                    cache=cache, cache_slots=slots, num_pages=num_pages,
+                    cache_block=cache_block, page_stride_elems=page_elems,
+                    slot_stride_elems=LATENT, compress_ratio=compress_ratio, record=record,
+                    fp8=record == "fp8", fp8_scale=PLAIN_FP8_SCALE)
+    record_bytes = {"mxfp8": RECORD_BYTES_MXFP8, "nvfp4": RECORD_BYTES_NVFP4,
+                    "v4": RECORD_BYTES_V4}[record]
     page_stride = cache_block * record_bytes
     cache = np.full(num_pages * page_stride, POISON, dtype=np.uint8)
     return dict(latent=latent, positions=positions, cos_sin=rope_cos_sin_table(table_rows),
                 cache=cache, cache_slots=slots, num_pages=num_pages, cache_block=cache_block,
                 page_stride_bytes=page_stride, compress_ratio=compress_ratio, record=record)
+
+
+# -------------------------------------------------------------- ring_rows ---
+
+def ring_rows(seed: int = 0, num_rows: int = 65536, num_blocks: int = 512,
+              state_block: int = 128, pad_fraction: float = 0.05) -> dict:
+    """fp32 rows [num_rows, 1024] ~N(0,1) (the [kv | score] halves drawn
+    alike); slots a random injection into num_blocks * state_block ring rows
+    with ``pad_fraction`` set to -1; the state [num_blocks, state_block, 1024]
+    filled with the RING_POISON_BITS pattern."""
+    rng = np.random.default_rng([seed, 7])
+    rows = np.empty((num_rows, RING_ROW), dtype=np.float32)
+    n_chunks = max(1, math.ceil(num_rows / CHUNK_ROWS))
+    children = np.random.SeedSequence([seed, 8]).spawn(n_chunks)
+
+    def one(c):
+        lo, hi = c * CHUNK_ROWS, min(num_rows, (c + 1) * CHUNK_ROWS)
+        rows[lo:hi] = np.random.default_rng(children[c]).standard_normal(
+            (hi - lo, RING_ROW), dtype=np.float32)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, range(n_chunks)))
+    slots = _slots_with_pads(rng, num_blocks * state_block, num_rows,
+                             int(round(pad_fraction * num_rows)))
+    state = np.empty((num_blocks, state_block, RING_ROW), dtype=np.float32)
+    state.view(np.uint32)[...] = RING_POISON_BITS
+    return dict(rows=rows, slot_mapping=slots, state=state, num_blocks=num_blocks,
+                state_block=state_block)
 
 
 # ----------------------------------------------------------------- gather ---
