@@ -115,6 +115,57 @@ def attention_case(torch, kvq, dev, cache, idx, valid):
     return call, flops, hbm, status
 
 
+RECORD_WIDTH = {"mxfp8": 528, "nvfp4": 288, "v4": 584}
+
+
+def rope_inputs(torch, dev, n, pages):
+    """Device copies of the rope_insert workload's latent, positions, table
+    and slots (the same for every layout), plus the writer count."""
+    w = workloads.rope_insert(seed=0, num_tokens=n, num_pages=pages, record="mxfp8")
+    writers = int(np.sum((w["cache_slots"] >= 0) & ((w["positions"] + 1) % 4 == 0)))
+    return dict(lat=torch.from_numpy(w["latent"].view(np.int16)).to(dev).view(torch.bfloat16),
+                pos=torch.from_numpy(w["positions"]).to(dev),
+                tab=torch.from_numpy(w["cos_sin"]).to(dev),
+                slots=torch.from_numpy(w["cache_slots"]).to(dev), n=n, pages=pages,
+                writers=writers)
+
+
+def rope_case(torch, kvq, dev, layout, inputs):
+    """(call, algorithmic bytes) of one insert of the inputs' tokens into a
+    poisoned cache of the layout (pages of 64 slots, R = 4). Per token 16
+    bytes of position and slot; per writer the 1024-byte latent row, the
+    256-byte table row and the record or row written."""
+    lat, pos, tab, slots = inputs["lat"], inputs["pos"], inputs["tab"], inputs["slots"]
+    pages = inputs["pages"]
+    if layout in RECORD_WIDTH:
+        width = RECORD_WIDTH[layout]
+        cache = torch.full((pages, 64, width), workloads.POISON, dtype=torch.uint8, device=dev)
+        fn = getattr(kvq, f"rope_quant_insert_{layout}")
+        call = lambda: fn(lat, pos, tab, cache, slots, 4)  # noqa: E731
+    else:
+        width = 1024 if layout == "bf16" else 512
+        raw = torch.full((pages * 64 * width,), workloads.POISON, dtype=torch.uint8, device=dev)
+        cache = raw.view(torch.bfloat16 if layout == "bf16" else torch.float8_e4m3fn)
+        cache = cache.view(pages, 64, 512)
+        scale = workloads.PLAIN_FP8_SCALE if layout == "fp8" else None
+        call = lambda: kvq.rope_plain_insert(lat, pos, tab, cache, slots, 4,  # noqa: E731
+                                             fp8_scale=scale)
+    return call, 16 * inputs["n"] + inputs["writers"] * (1024 + 256 + width)
+
+
+def ring_case(torch, kvq, dev, n, blocks):
+    """(call, algorithmic bytes, saved rows) of save_ring_rows on `n` rows
+    into `blocks` blocks of 128: 8 bytes of slot per row, 4096 read and 4096
+    written per saved row."""
+    w = workloads.ring_rows(seed=0, num_rows=n, num_blocks=blocks, state_block=128)
+    rows = torch.from_numpy(w["rows"]).to(dev)
+    slots = torch.from_numpy(w["slot_mapping"]).to(dev)
+    state = torch.from_numpy(w["state"]).to(dev)
+    saved = int(np.sum(w["slot_mapping"] >= 0))
+    call = lambda: kvq.save_ring_rows(rows, slots, state)  # noqa: E731
+    return call, 8 * n + 8192 * saved, saved
+
+
 def store_bytes(num_tokens, valid):
     read = 8 * num_tokens + 1024 * valid
     write = ROW * valid
@@ -270,9 +321,11 @@ def time_events(torch, fn, reps, stream, flush=None):
 
 
 def secondary_paths(torch, kvq, dev, peak, store_inputs):
-    """The RMSNorm-fused store on the headline workload, the RoPE inserts on
-    4,194,304 tokens and the 128 x 2048 gather: mean of CUDA-event times over
-    20 reps each (L2 flushed before each gather rep)."""
+    """The RMSNorm-fused store on the headline workload, the RoPE inserts
+    (every layout) on 4,194,304 tokens, the ring-row save on 1,048,576 rows,
+    the 128 x 2048 gather and the sparse attention: mean of CUDA-event times
+    over 20 reps each (L2 flushed before each gather and attention rep; the
+    other inputs are larger than L2)."""
     out = {}
     stream = torch.cuda.current_stream()
     flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
@@ -294,28 +347,32 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
         "tokens_per_s": N_TOKENS / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
         "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak}
 
-    for record, width in (("mxfp8", 528), ("nvfp4", 288)):
-        w = workloads.rope_insert(seed=0, num_tokens=4_194_304, num_pages=65_536, record=record)
-        lat = torch.from_numpy(w["latent"].view(np.int16)).to(dev).view(torch.bfloat16)
-        pos = torch.from_numpy(w["positions"]).to(dev)
-        tab = torch.from_numpy(w["cos_sin"]).to(dev)
-        slots = torch.from_numpy(w["cache_slots"]).to(dev)
-        cache = torch.from_numpy(w["cache"]).to(dev).view(w["num_pages"], 64, width)
-        fn = getattr(kvq, f"rope_quant_insert_{record}")
-        pos_np, slot_np = w["positions"], w["cache_slots"]
-        writers = int(np.sum((slot_np >= 0) & ((pos_np + 1) % 4 == 0)))
-        n = pos_np.size
-        algo = 16 * n + writers * (1024 + 256 + width)
-        call = lambda: fn(lat, pos, tab, cache, slots, 4)  # noqa: E731
+    inputs = rope_inputs(torch, dev, 4_194_304, 65_536)
+    n, writers = inputs["n"], inputs["writers"]
+    for layout in ("mxfp8", "nvfp4", "v4", "bf16", "fp8"):
+        call, algo = rope_case(torch, kvq, dev, layout, inputs)
         for _ in range(3):
             call()
         ms, _ = time_events(torch, call, 20, stream)
-        out[f"rope_quant_insert_{record}"] = {
+        name = (f"rope_quant_insert_{layout}" if layout in RECORD_WIDTH
+                else f"rope_plain_insert_{layout}")
+        out[name] = {
             "workload": "4,194,304 tokens, R=4, 65,536 pages x 64, 0.05% NaN",
             "tokens_per_s": n / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
             "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
             "writers": writers}
-        del lat, pos, tab, slots, cache
+        del call
+    del inputs
+    call, algo, saved = ring_case(torch, kvq, dev, 1_048_576, 8192)
+    for _ in range(3):
+        call()
+    ms, _ = time_events(torch, call, 20, stream)
+    out["save_ring_rows"] = {
+        "workload": "1,048,576 fp32 rows of 1024 (5% pads) into 8,192 blocks x 128",
+        "rows_per_s": 1_048_576 / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
+        "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
+        "saved": saved}
+    del call
     g = workloads.gather(seed=0)
     lat = torch.from_numpy(g["fill_latent"].view(np.int16)).to(dev).view(torch.bfloat16)
     slots = torch.from_numpy(g["fill_slots"]).to(dev)
@@ -496,19 +553,11 @@ def run_profile(args):
             call = lambda: kvq.mxfp4_mla_rmsnorm_store(  # noqa: E731
                 lat_d, weight, 1e-6, slots_d, cache)
             algo += 1024
-    elif args.profile in ("rope_mxfp8", "rope_nvfp4"):
-        record = args.profile[5:]
-        width = 528 if record == "mxfp8" else 288
-        w = workloads.rope_insert(seed=0, num_tokens=n, num_pages=n // 64, record=record)
-        lat_d = torch.from_numpy(w["latent"].view(np.int16)).to(dev).view(torch.bfloat16)
-        pos = torch.from_numpy(w["positions"]).to(dev)
-        tab = torch.from_numpy(w["cos_sin"]).to(dev)
-        sl = torch.from_numpy(w["cache_slots"]).to(dev)
-        cache = torch.from_numpy(w["cache"]).to(dev).view(n // 64, 64, width)
-        fn = getattr(kvq, f"rope_quant_insert_{record}")
-        call = lambda: fn(lat_d, pos, tab, cache, sl, 4)  # noqa: E731
-        writers = int(np.sum((w["cache_slots"] >= 0) & ((w["positions"] + 1) % 4 == 0)))
-        algo = 16 * n + writers * (1024 + 256 + width)
+    elif args.profile.startswith("rope_"):
+        call, algo = rope_case(torch, kvq, dev, args.profile[5:],
+                               rope_inputs(torch, dev, n, n // 64))
+    elif args.profile == "ring":
+        call, algo, _ = ring_case(torch, kvq, dev, n, -(-n // 128))
     else:  # gather, attention
         g = workloads.gather(seed=0)
         lat_d = torch.from_numpy(g["fill_latent"].view(np.int16)).to(dev).view(torch.bfloat16)
@@ -541,7 +590,8 @@ def main():
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the secondary RoPE-insert and gather measurements")
     ap.add_argument("--profile", choices=["store", "rmsnorm_store", "rope_mxfp8", "rope_nvfp4",
-                                         "gather", "attention"],
+                                         "rope_v4", "rope_bf16", "rope_fp8", "ring", "gather",
+                                         "attention"],
                     help="run one kernel on a reduced case (for Nsight Compute) and exit")
     ap.add_argument("--profile-tokens", type=int, default=400_000)
     ap.add_argument("--profile-slots", type=int, default=0,
