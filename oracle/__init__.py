@@ -16,6 +16,12 @@ encoder, the NVFP4 division, the RoPE rotation and the gather are pinned by the
 tests in tests/test_oracle_pins*.py. The treatment of NaN inputs by the V4.1
 inserts (NaN-ignoring amax, NaN kept through the clamp as E4M3 0x7F) is pinned
 only by the reading stated in kvq_oracle.c: the pages do not fix it.
+
+Two modules hold float64 oracles of operations whose kernels use
+transcendental or reduced-precision arithmetic, checked within derived
+bounds rather than bit for bit: attention.py (sparse MLA attention over the
+packed cache) and compress.py (fused_save_compress_norm: group pooling,
+RMSNorm and the ring save).
 """
 import ctypes
 import os

@@ -107,6 +107,35 @@ MUTANTS = [
      "test_oracle_pins_attention.py::test_single_valid_key_returns_its_row", "attention.py"),
     ("attn_abs_values", "out[n] = (p @ k) / l", "out[n] = (p @ np.abs(k)) / l",
      "test_oracle_pins_attention.py::test_single_valid_key_returns_its_row", "attention.py"),
+    # fused_save_compress_norm (oracle/compress.py)
+    ("fscn_ring_row_of_p", "state[s // cap, (int(pos[i]) - 1) % cap, :2 * LATENT]",
+     "state[s // cap, int(pos[i]) % cap, :2 * LATENT]",
+     "test_oracle_pins_compress.py::test_cr2_equals_streaming_model_and_is_invariant_to_chunking",
+     "compress.py"),
+    ("fscn_softmax_sign", "e0, e1 = np.exp(s0 - m), np.exp(s1 - m)",
+     "e0, e1 = np.exp(m - s0), np.exp(m - s1)",
+     "test_oracle_pins_compress.py::test_cr2_score_gap_sets_the_weights", "compress.py"),
+    ("fscn_saves_first_rows", "for i in range(max(qs, qe - cap), qe):",
+     "for i in range(qs, min(qe, qs + cap)):",
+     "test_oracle_pins_compress.py::"
+     "test_ring_save_takes_only_the_last_capacity_rows_and_skips_with_prev_rows", "compress.py"),
+    ("fscn_saves_with_prev_rows", "if R == 2 and prev_rows is None:", "if R == 2:",
+     "test_oracle_pins_compress.py::"
+     "test_ring_save_takes_only_the_last_capacity_rows_and_skips_with_prev_rows", "compress.py"),
+    ("fscn_prev_row_off_by_one", "j = int(prev_row_indices[k])",
+     "j = int(prev_row_indices[k]) - 1",
+     "test_oracle_pins_compress.py::test_prev_rows_select_the_predecessor", "compress.py"),
+    ("fscn_eps_outside_root",
+     "r = 1.0 / np.sqrt(np.mean(pooled * pooled, axis=1) + eps)",
+     "r = 1.0 / (np.sqrt(np.mean(pooled * pooled, axis=1)) + eps)",
+     "test_oracle_pins_compress.py::test_cr1_constant_row_closed_form", "compress.py"),
+    ("fscn_closes_even_positions", "written = (slot >= 0) & (pos >= 0) & ((pos + 1) % R == 0)",
+     "written = (slot >= 0) & (pos >= 0) & (pos % R == 0)",
+     "test_oracle_pins_compress.py::test_cr2_equals_streaming_model_and_is_invariant_to_chunking",
+     "compress.py"),
+    ("fscn_weight_dropped", "latent = pooled * r[:, None] * w[None, :]",
+     "latent = pooled * r[:, None]",
+     "test_oracle_pins_compress.py::test_cr1_weight_and_alternating_signs", "compress.py"),
 ]
 
 

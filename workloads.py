@@ -19,6 +19,8 @@ the recipe and shrink the counts for fast tests):
   rope_insert   65,536 tokens (or 4,194,304 for the large variant), R = 4;
                 records mxfp8 / nvfp4 / v4, or plain bf16 / fp8 rows
   ring_rows     fp32 [kv | score] rows of 1024 values into a paged ring state
+  compress      fused_save_compress_norm batches: packed request chunks of
+                fp32 [kv | score] rows (R = 2) or kv rows (R = 1)
   gather        1,048,576-slot packed cache, 128 queries x 2048 indices
   sparse_attention  the gather's cache and indices + 128 heads of bf16 queries
 """
@@ -308,3 +310,68 @@ def sparse_attention(seed: int = 0, num_queries: int = 128, num_heads: int = 128
     d["q"] = attention_queries(seed, num_queries, num_heads)
     d["sm_scale"] = 1.0 / math.sqrt(LATENT)
     return d
+
+
+# --------------------------------------------------------------- compress ---
+
+def compress(seed: int = 0, compress_ratio: int = 2, num_reqs: int = 256, max_chunk: int = 511,
+             decode_fraction: float = 0.25, capacity: int = 4, pad_tokens: int = 16,
+             prev_rows: bool = False) -> dict:
+    """A packed batch for fused_save_compress_norm. Each request's chunk has
+    length 1 with probability ``decode_fraction``, else U{2..max_chunk}, and
+    starts at a position U[0, 100000) (either parity); its tokens are
+    consecutive positions, packed request after request, then ``pad_tokens``
+    padding tokens (slot -1). Rows: kv ~N(0,1), scores ~N(0,1) x 2 (fp32).
+    R = 2: request k owns ring block perm[k] of num_reqs + 8 blocks of
+    ``capacity`` rows, slot = block * capacity + p % capacity; the ring holds
+    N(0,1) rows (the predecessors of chunks that start at odd positions).
+    R = 1: slots are distinct random values in [0, 2T), 5% of them -1.
+    prev_rows (R = 2): [num_reqs, 1024] N(0,1) rows, prev_row_indices a
+    permutation with a quarter of the entries -1. Weight bf16 U(0.5, 1.5),
+    eps 1e-6."""
+    rng = np.random.default_rng([seed, 11, compress_ratio])
+    lens = np.where(rng.random(num_reqs) < decode_fraction, 1,
+                    rng.integers(2, max_chunk + 1, size=num_reqs))
+    starts = rng.integers(0, 100_000, size=num_reqs)
+    qsl = np.zeros(num_reqs + 1, np.int64)
+    qsl[1:] = np.cumsum(lens)
+    n_real = int(qsl[-1])
+    T = n_real + pad_tokens
+    t2r = np.zeros(T, np.int64)
+    t2r[:n_real] = np.repeat(np.arange(num_reqs), lens)
+    positions = np.zeros(T, np.int64)
+    positions[:n_real] = starts[t2r[:n_real]] + (np.arange(n_real) - qsl[t2r[:n_real]])
+    width = LATENT * compress_ratio
+    rows = np.empty((T, width), np.float32)
+    n_chunks = max(1, math.ceil(T / CHUNK_ROWS))
+    children = np.random.SeedSequence([seed, 12, compress_ratio]).spawn(n_chunks)
+
+    def one(c):
+        lo, hi = c * CHUNK_ROWS, min(T, (c + 1) * CHUNK_ROWS)
+        g = np.random.default_rng(children[c])
+        rows[lo:hi] = g.standard_normal((hi - lo, width), dtype=np.float32)
+        if compress_ratio == 2:
+            rows[lo:hi, LATENT:] *= 2.0
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, range(n_chunks)))
+    weight = f32_to_bf16_bits(rng.uniform(0.5, 1.5, LATENT).astype(np.float32))
+    out = dict(kv_score=rows, positions=positions, query_start_loc=qsl, token_to_req=t2r,
+               weight=weight, eps=1e-6, compress_ratio=compress_ratio, num_reqs=num_reqs,
+               num_real=n_real)
+    if compress_ratio == 1:
+        slots = _slots_with_pads(rng, 2 * T, T, int(round(0.05 * T)))
+        slots[n_real:] = -1
+        out.update(slot_mapping=slots, state=None)
+        return out
+    blocks = rng.permutation(num_reqs + 8)[:num_reqs]
+    slots = np.full(T, -1, np.int64)
+    slots[:n_real] = blocks[t2r[:n_real]] * capacity + positions[:n_real] % capacity
+    state = rng.standard_normal((num_reqs + 8, capacity, 2 * LATENT), dtype=np.float32)
+    out.update(slot_mapping=slots, state=state, capacity=capacity)
+    if prev_rows:
+        idx = rng.permutation(num_reqs).astype(np.int64)
+        idx[rng.random(num_reqs) < 0.25] = -1
+        out.update(prev_rows=rng.standard_normal((num_reqs, 2 * LATENT), dtype=np.float32),
+                   prev_row_indices=idx)
+    return out
