@@ -166,6 +166,34 @@ def ring_case(torch, kvq, dev, n, blocks):
     return call, 8 * n + 8192 * saved, saved
 
 
+def compress_case(torch, kvq, dev, num_reqs=2048, max_chunk=1023):
+    """(call, algorithmic bytes, tokens, groups) of fused_save_compress_norm
+    on a prefill batch (R = 2, capacity 4, chunk lengths U{2..max_chunk}).
+    Per token 24 B (slot, position, request); per request 16 B of chunk
+    bounds; the 1 KiB weight; per group its two 4096-byte rows (the chunk's
+    first group reads its predecessor from the ring) and the 1024-byte latent
+    written; per saved ring row 4096 B read and 4096 B written."""
+    w = workloads.compress(seed=0, compress_ratio=2, num_reqs=num_reqs, max_chunk=max_chunk,
+                           decode_fraction=0.0, capacity=4, pad_tokens=0)
+    T = w["slot_mapping"].size
+    pos, qsl = w["positions"], w["query_start_loc"]
+    groups = int(np.sum((pos % 2) == 1))
+    lens = np.diff(qsl)
+    saved = int(np.sum(np.minimum(lens, 4)))
+    algo = 24 * T + 16 * num_reqs + 1024 + groups * (2 * 4096 + 1024) + saved * 8192
+    kv = torch.from_numpy(w["kv_score"]).to(dev)
+    pos_d = torch.from_numpy(pos).to(dev)
+    st = torch.from_numpy(w["state"]).to(dev)
+    sl = torch.from_numpy(w["slot_mapping"]).to(dev)
+    q = torch.from_numpy(qsl).to(dev)
+    t2r = torch.from_numpy(w["token_to_req"]).to(dev)
+    wt = torch.from_numpy(w["weight"].view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty((T, 512), dtype=torch.bfloat16, device=dev)
+    call = lambda: kvq.fused_save_compress_norm(kv, pos_d, st, sl, q, t2r, wt,  # noqa: E731
+                                                w["eps"], 2, out)
+    return call, algo, T, groups
+
+
 def store_bytes(num_tokens, valid):
     read = 8 * num_tokens + 1024 * valid
     write = ROW * valid
@@ -363,6 +391,15 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
             "writers": writers}
         del call
     del inputs
+    call, algo, n, groups = compress_case(torch, kvq, dev)
+    for _ in range(3):
+        call()
+    ms, _ = time_events(torch, call, 20, stream)
+    out["fused_save_compress_norm"] = {
+        "workload": f"{n:,} tokens in 2,048 prefill chunks (R=2, capacity 4), {groups:,} groups",
+        "tokens_per_s": n / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
+        "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak}
+    del call
     call, algo, saved = ring_case(torch, kvq, dev, 1_048_576, 8192)
     for _ in range(3):
         call()
@@ -556,6 +593,8 @@ def run_profile(args):
     elif args.profile.startswith("rope_"):
         call, algo = rope_case(torch, kvq, dev, args.profile[5:],
                                rope_inputs(torch, dev, n, n // 64))
+    elif args.profile == "compress":
+        call, algo, n, _ = compress_case(torch, kvq, dev, num_reqs=max(1, n // 512), max_chunk=1023)
     elif args.profile == "ring":
         call, algo, _ = ring_case(torch, kvq, dev, n, -(-n // 128))
     else:  # gather, attention
@@ -590,7 +629,8 @@ def main():
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the secondary RoPE-insert and gather measurements")
     ap.add_argument("--profile", choices=["store", "rmsnorm_store", "rope_mxfp8", "rope_nvfp4",
-                                         "rope_v4", "rope_bf16", "rope_fp8", "ring", "gather",
+                                         "rope_v4", "rope_bf16", "rope_fp8", "ring", "compress",
+                                         "gather",
                                          "attention"],
                     help="run one kernel on a reduced case (for Nsight Compute) and exit")
     ap.add_argument("--profile-tokens", type=int, default=400_000)

@@ -20,7 +20,7 @@ import torch
 
 __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
            "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
-           "save_ring_rows",
+           "save_ring_rows", "fused_save_compress_norm",
            "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "row_bytes",
            "cache_view", "KvqError", "lib",
            "LIBRARY_PATH"]
@@ -65,6 +65,10 @@ def lib() -> ctypes.CDLL:
         L.rope_plain_insert.restype = ctypes.c_int
         L.rope_plain_insert.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _p, _p, _i64, _i64,
                                         _i64, _i64, _i32, _i32, ctypes.c_float, _p]
+        L.fused_save_compress_norm.restype = ctypes.c_int
+        L.fused_save_compress_norm.argtypes = [_p, _i64, _i64, _p, _p, _i32, _p, _p, _i64, _p,
+                                               _i64, _i64, _i64, _i64, _p, ctypes.c_float, _p,
+                                               _i64, _i64, _p, _p, _i64, _p]
         L.save_ring_rows.restype = ctypes.c_int
         L.save_ring_rows.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _i64, _i64, _p]
         L.mxfp4_mla_gather_dequant.restype = ctypes.c_int
@@ -250,6 +254,66 @@ def save_ring_rows(rows: torch.Tensor, slot_mapping: torch.Tensor, state: torch.
         rows.data_ptr(), slot_mapping.numel(), rows.stride(0), slot_mapping.data_ptr(),
         state.data_ptr(), state.shape[0], state.shape[1], state.stride(0), state.stride(1),
         _stream(stream)))
+
+
+def fused_save_compress_norm(kv_score, positions, state_cache, slot_mapping, query_start_loc,
+                             token_to_req_indices, rms_norm_weight, rms_norm_eps: float,
+                             compress_ratio: int, latent_out, prev_rows=None,
+                             prev_row_indices=None, stream=None) -> None:
+    """kv_score: fp32 [tokens, 512 * R] (unit column stride); state_cache: fp32
+    [blocks, capacity, >= 1024] with unit last stride (R = 2); slot_mapping,
+    positions, query_start_loc [num_reqs + 1] and token_to_req_indices: int64
+    contiguous; rms_norm_weight: bf16 [512]; latent_out: bf16 [tokens, 512]
+    with unit last stride; prev_rows: fp32 [rows, >= 1024] with
+    prev_row_indices int64 [num_reqs], or neither."""
+    R = int(compress_ratio)
+    _need(kv_score, torch.float32, "kv_score")
+    _need(positions, torch.int64, "positions")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(rms_norm_weight, torch.bfloat16, "rms_norm_weight")
+    _need(latent_out, torch.bfloat16, "latent_out")
+    if kv_score.dim() != 2 or kv_score.shape[1] != 512 * R or kv_score.stride(1) != 1:
+        raise ValueError("kv_score must be [tokens, 512 * compress_ratio] with unit column stride")
+    if latent_out.dim() != 2 or latent_out.shape[1] != 512 or latent_out.stride(1) != 1:
+        raise ValueError("latent_out must be [tokens, 512] with unit column stride")
+    if rms_norm_weight.numel() != 512 or not rms_norm_weight.is_contiguous():
+        raise ValueError("rms_norm_weight must be a contiguous [512] tensor")
+    n = slot_mapping.numel()
+    if n > min(kv_score.shape[0], positions.numel(), latent_out.shape[0]) or \
+            not slot_mapping.is_contiguous() or not positions.is_contiguous():
+        raise ValueError("slot_mapping / positions must be contiguous and cover the tokens")
+    qsl = t2r = st = prev = pidx = None
+    nreq = nb = cap = sst = srs = nprev = pst = 0
+    if R == 2:
+        _need(query_start_loc, torch.int64, "query_start_loc")
+        _need(token_to_req_indices, torch.int64, "token_to_req_indices")
+        _need(state_cache, torch.float32, "state_cache")
+        if not query_start_loc.is_contiguous() or not token_to_req_indices.is_contiguous() or \
+                token_to_req_indices.numel() < n:
+            raise ValueError("query_start_loc / token_to_req_indices must be contiguous")
+        if state_cache.dim() != 3 or state_cache.shape[2] < 1024 or state_cache.stride(2) != 1:
+            raise ValueError("state_cache must be [blocks, capacity, >= 1024] with unit last stride")
+        nreq = query_start_loc.numel() - 1
+        qsl, t2r, st = query_start_loc.data_ptr(), token_to_req_indices.data_ptr(), \
+            state_cache.data_ptr()
+        nb, cap = state_cache.shape[0], state_cache.shape[1]
+        sst, srs = state_cache.stride(0), state_cache.stride(1)
+        if prev_rows is not None:
+            _need(prev_rows, torch.float32, "prev_rows")
+            _need(prev_row_indices, torch.int64, "prev_row_indices")
+            if prev_rows.dim() != 2 or prev_rows.shape[1] < 1024 or prev_rows.stride(1) != 1:
+                raise ValueError("prev_rows must be [rows, >= 1024] with unit column stride")
+            if prev_row_indices.numel() < nreq or not prev_row_indices.is_contiguous():
+                raise ValueError("prev_row_indices must be contiguous and cover the requests")
+            prev, pidx = prev_rows.data_ptr(), prev_row_indices.data_ptr()
+            nprev, pst = prev_rows.shape[0], prev_rows.stride(0)
+    elif R != 1:
+        raise ValueError("compress_ratio must be 1 or 2")
+    _check("fused_save_compress_norm", lib().fused_save_compress_norm(
+        kv_score.data_ptr(), n, kv_score.stride(0), positions.data_ptr(), slot_mapping.data_ptr(),
+        R, qsl, t2r, nreq, st, nb, cap, sst, srs, rms_norm_weight.data_ptr(),
+        float(rms_norm_eps), prev, nprev, pst, pidx, latent_out.data_ptr(),
+        latent_out.stride(0), _stream(stream)))
 
 
 def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor = None,

@@ -2,8 +2,8 @@
  * kvq.h — C ABI of the GB300 (sm_103a) quantize-and-scatter library for a
  * paged MLA KV cache: MXFP4 store, RoPE-then-quantize inserts (V4.1 MXFP8
  * and NVFP4 records, the V4 record, plain bf16 / fp8 rows), the compressor's
- * ring-state save, the MXFP4 gather-and-dequantize read and sparse MLA
- * attention on the packed cache.
+ * ring-state save, the compressor's pooling + RMSNorm step, the MXFP4
+ * gather-and-dequantize read and sparse MLA attention on the packed cache.
  *
  * Pages this interface follows (cited by title and section):
  *   [store] "vllm.v1.attention.ops.mxfp4_mla.store" (vLLM API docs):
@@ -12,7 +12,8 @@
  *   [v41]   "vllm.models.deepseek_v41.common.ops.fused_compress_quant_cache"
  *           (vLLM API docs): _rope_quant_insert_mxfp8_kernel,
  *           _rope_quant_insert_nvfp4_kernel, rope_quant_insert (and its
- *           docstring on the V4 record and the plain rows), save_ring_rows.
+ *           docstring on the V4 record and the plain rows), save_ring_rows,
+ *           fused_save_compress_norm.
  *   [pr]    "[ROCm][Attention] Add an mxfp4_mla KV cache for rope-free sparse
  *           MLA (read/write path)", vLLM pull request 60321: Overview, Claims,
  *           Details (format and write path; read path).
@@ -266,6 +267,69 @@ int save_ring_rows(const float* rows, int64_t num_rows, int64_t row_stride_elems
                    const int64_t* slot_mapping, float* state, int64_t num_blocks,
                    int64_t state_block, int64_t state_stride_elems,
                    int64_t state_row_stride_elems, cudaStream_t stream);
+
+/*
+ * fused_save_compress_norm — pool each closed group of compressor rows into
+ * an RMS-normalised bf16 latent, and keep the ring rows the next chunk needs.
+ * [v41] fused_save_compress_norm (docstring and Args; its kernel is not
+ * printed, so the pooling below is this library's reading).
+ *
+ * A group is compress_ratio (R, 1 or 2) consecutive positions and closes at
+ * the token t with position p >= 0, (p + 1) % R == 0 and slot s =
+ * slot_mapping[t] >= 0. Only closing tokens write latent row t.
+ *   R = 1: kv_score rows are 512 kv values; pooled = the row.
+ *   R = 2: rows are [512 kv | 512 score]. Token t (request k =
+ *          token_to_req_indices[t], 0 <= k < num_reqs, with
+ *          query_start_loc[k] <= t < query_start_loc[k+1] and
+ *          s < num_blocks*capacity; otherwise skipped) closes the group
+ *          (predecessor, t): the predecessor is row t-1 if t is not its
+ *          chunk's first token; else prev_rows[prev_row_indices[k]] when
+ *          prev_rows is given and that index is >= 0 (an index >=
+ *          num_prev_rows skips the group); else the ring row
+ *          (p - 1) % capacity of block s / capacity. Per channel d:
+ *            m = max(s0[d], s1[d]),  e_i = exp(s_i[d] - m),
+ *            pooled[d] = (e0*kv0[d] + e1*kv1[d]) / (e0 + e1).
+ *          After the groups, unless prev_rows is given, each request's
+ *          last min(capacity, chunk length) tokens with a slot in
+ *          [0, num_blocks*capacity) are copied (1024 floats, bit for bit)
+ *          to ring row s % capacity of block s / capacity. Ring rows are
+ *          read as they were before the call.
+ *   latent[t][d] = bf16(pooled[d] * w[d] / sqrt(mean(pooled^2) + eps)),
+ *   computed in fp32 (exp by expf, correctly rounded sqrt, reciprocal and
+ *   division, the final bf16 rounding to nearest even): |latent - exact| <=
+ *   2^-7 |exact| + 2^-18 * r * |w[d]| * sum_i w_i |kv_i[d]| (r the exact
+ *   1/sqrt(mean + eps)). A row whose pooled values overflow binary32 when
+ *   squared (|x| >= 2^63) is outside that bound.
+ *
+ * kv_score               fp32 [num_tokens, row_stride_elems], 512*R used,
+ *                        16-byte aligned; row_stride_elems multiple of 4
+ * positions, slot_mapping int64 [num_tokens]
+ * query_start_loc        R = 2: int64 [num_reqs + 1], non-decreasing
+ * token_to_req_indices   R = 2: int64 [num_tokens]
+ * state                  R = 2: fp32 [num_blocks, capacity, >= 1024], block
+ *                        stride state_stride_elems, row stride
+ *                        state_row_stride_elems (multiples of 4, rows >= 1024
+ *                        apart, blocks not overlapping); each request owns
+ *                        its block (two requests sharing one race)
+ * weight_bf16            bf16 [512], 8-byte aligned; eps finite, >= 0
+ * prev_rows              R = 2, optional: fp32 [num_prev_rows, >= 1024],
+ *                        row stride prev_row_stride_elems (multiple of 4);
+ *                        prev_row_indices int64 [num_reqs] (both or neither)
+ * latent_out_bf16        bf16 [num_tokens, out_row_stride_elems] (>= 512,
+ *                        multiple of 8), 16-byte aligned; rows of tokens
+ *                        that close no group are not written
+ * For R = 1 the request, ring and prev_rows arguments are ignored.
+ */
+int fused_save_compress_norm(const float* kv_score, int64_t num_tokens, int64_t row_stride_elems,
+                             const int64_t* positions, const int64_t* slot_mapping,
+                             int32_t compress_ratio, const int64_t* query_start_loc,
+                             const int64_t* token_to_req_indices, int64_t num_reqs, float* state,
+                             int64_t num_blocks, int64_t capacity, int64_t state_stride_elems,
+                             int64_t state_row_stride_elems, const void* weight_bf16, float eps,
+                             const float* prev_rows, int64_t num_prev_rows,
+                             int64_t prev_row_stride_elems, const int64_t* prev_row_indices,
+                             void* latent_out_bf16, int64_t out_row_stride_elems,
+                             cudaStream_t stream);
 
 /*
  * mxfp4_mla_gather_dequant — read packed MXFP4 rows back to bf16.

@@ -32,6 +32,7 @@ def test_every_declared_symbol_is_exported(L):
                           "mxfp4_mla_rmsnorm_store",
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
                           "rope_quant_insert_v4", "rope_plain_insert", "save_ring_rows",
+                          "fused_save_compress_norm",
                           "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention"}
     for n in names:
         assert hasattr(L, n), n
@@ -130,6 +131,37 @@ def test_ring_rows_validation_on_host(L):
     assert f(*a) == -1
 
 
+def test_compress_validation_on_host(L):
+    f = L.fused_save_compress_norm
+    # kv, T, stride, pos, slots, R, qsl, t2r, nreq, state, nb, cap, sst, srs, w, eps,
+    # prev, nprev, pst, pidx, out, ostride, stream
+    ok2 = [A16, 4, 1024, A8, A8, 2, A8, A8, 2, A16, 4, 4, 4 * 1024, 1024, A8, 1e-6,
+           None, 0, 0, None, A16, 512, None]
+    empty = list(ok2); empty[1] = 0; empty[0] = None
+    assert f(*empty) == 0
+    bad = {5: 3, 5.1: 0, 1: -1, 2: 1020, 2.1: 1026, 21: 500, 21.1: 516, 15: -1.0,
+           15.1: float("nan"), 15.2: float("inf"), 8: -1, 10: 0, 11: 0, 13: 1020, 13.1: 1030,
+           12: 4 * 1024 - 4, 12.1: 4 * 1024 + 2, 0: A16 + 4, 3: A8 + 4, 4: A8 + 2, 14: A8 + 2,
+           20: A16 + 8, 6: None, 7: None, 9: None, 9.1: A16 + 4}
+    for k, v in bad.items():
+        a = list(ok2); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
+    a = list(ok2); a[16] = A16                               # prev_rows without indices
+    assert f(*a) == -1
+    a = list(ok2); a[16], a[17], a[18], a[19] = A16, 3, 1020, A8   # prev row stride < 1024
+    assert f(*a) == -1
+    a = list(ok2); a[16], a[17], a[18], a[19] = A16 + 4, 3, 1024, A8
+    assert f(*a) == -1
+    # R = 1 ignores the request and ring arguments (only shapes are checked)
+    ok1 = [A16, 4, 512, A8, A8, 1, None, None, 0, None, 0, 0, 0, 0, A8, 1e-6,
+           None, 0, 0, None, A16, 512, None]
+    e1 = list(ok1); e1[1] = 0
+    assert f(*e1) == 0
+    for k, v in {2: 508, 2.1: 514, 0: None, 20: None}.items():
+        a = list(ok1); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
+
+
 def test_gather_validation_on_host(L):
     f = L.mxfp4_mla_gather_dequant
     ok = [A16, 1, 8, 8, 512, A8, 4, A16, 512, None]
@@ -160,6 +192,6 @@ def test_attention_validation_on_host(L):
 def test_binding_has_the_abi_names():
     for n in ("mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
               "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
-              "save_ring_rows", "mxfp4_mla_gather_dequant",
+              "save_ring_rows", "fused_save_compress_norm", "mxfp4_mla_gather_dequant",
               "mxfp4_mla_sparse_attention"):
         assert callable(getattr(kvq, n))
