@@ -10,7 +10,9 @@ of 272-byte rows, 1% pad slots. One step = one store of the whole batch.
              written per valid token) / mean kernel time, against the measured
              HBM copy bandwidth; traffic from the committed ncu summary
   e2e        the same metric through the public API from pinned host buffers:
-             each step copies the latent and slots in and the cache back out
+             each step copies the latent and slots in and the cache back out;
+             step k's download overlaps step k+1's upload (two streams,
+             double-buffered device buffers)
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
   paths      the other hot-path rows measured in the same run: the
              RMSNorm-fused store on the same batch, the V4.1 RoPE inserts
@@ -506,25 +508,44 @@ def run_ours(args):
         clocks = sampler.summary(t_wall0, t_wall1)
     gpu_launches = args.steps
 
-    # end to end: pinned host in, cache back to pinned host, every step
+    # end to end: every step copies its whole pinned host source and slots in
+    # and the whole cache back out. Device buffers are doubled so that step
+    # k's download (on a second stream, the other copy direction) overlaps
+    # step k + 1's upload and store; a store waits until the download of the
+    # cache it is about to rewrite has finished.
     e2e_steps = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    lat_e = [torch.empty_like(lat_h, device=dev) for _ in range(2)]
+    slots_e = [torch.empty_like(slots_h, device=dev) for _ in range(2)]
+    cache_e = [cache_d, torch.full_like(cache_d, 0xAA)]
+    d2h_stream = torch.cuda.Stream(device=dev)
+    downloaded = [None, None]
     torch.cuda.synchronize()
     barrier(dist)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    lat_full_d = torch.empty_like(lat_h, device=dev)
     a.record(stream)
-    for _ in range(e2e_steps):
-        lat_full_d.copy_(lat_h, non_blocking=True)
-        slots_d.copy_(slots_h, non_blocking=True)
-        kvq.mxfp4_mla_store(lat_full_d.view(torch.bfloat16)[:, :512], slots_d, cache_d)
-        cache_h.copy_(cache_d, non_blocking=True)
+    for k in range(e2e_steps):
+        i = k % 2
+        lat_e[i].copy_(lat_h, non_blocking=True)
+        slots_e[i].copy_(slots_h, non_blocking=True)
+        if downloaded[i] is not None:
+            stream.wait_event(downloaded[i])
+        kvq.mxfp4_mla_store(lat_e[i].view(torch.bfloat16)[:, :512], slots_e[i], cache_e[i])
+        stored = torch.cuda.Event()
+        stored.record(stream)
+        d2h_stream.wait_event(stored)
+        with torch.cuda.stream(d2h_stream):
+            cache_h.copy_(cache_e[i], non_blocking=True)
+        downloaded[i] = torch.cuda.Event()
+        downloaded[i].record(d2h_stream)
+    stream.wait_stream(d2h_stream)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, a.elapsed_time(b))
     h2d = lat_h.numel() * 2 + slots_h.numel() * 8
     d2h = cache_h.numel()
-    del lat_full_d
+    del lat_e, slots_e, cache_e
 
     paths = secondary_paths(torch, kvq, dev, peak, (lat_d, slots_d, cache_d, valid)) \
         if (rank == 0 and not args.no_paths) else None
