@@ -10,27 +10,30 @@
 // Work decomposition. One CTA per (query, half of the 512 value columns): the
 // two CTAs of a query both form the full scores q.k (512-deep) and each
 // accumulates 256 output columns. Tensor memory (512 columns x 128 lanes,
-// lane = head) holds the output accumulator (256 columns), two 64-key score
-// buffers (128) and the first 256 dims of Q as bf16 pairs (128): the q.k
-// products over those dims take Q from tensor memory and read only the key
-// tile from shared memory, which halves their shared-memory traffic (a
-// 128 x 64 x 16 product that reads both operands from shared memory is bound
-// by it). The other 256 dims of Q stay in shared memory. Keys go in tiles of
-// 64, and three groups of warps run as a pipeline through mbarriers:
-//   - producers (warps 4-11, lane = key, two warps per quarter of the row):
-//     load the packed rows two tiles ahead into registers (pads and
+// lane = head) holds the output accumulator (256 columns), four 32-key score
+// buffers (128; softmax writes the bf16 probabilities P back over the scores
+// of the same buffer, and p.v takes P from there as its A operand) and the
+// first 256 dims of Q as bf16 pairs (128): the q.k products over those dims
+// take Q from tensor memory and read only the key tile from shared memory.
+// The other 256 dims of Q stay in shared memory next to four 32 KB key tiles
+// of 32 keys (a ring of four stages). Three groups of warps run as a
+// pipeline through mbarriers:
+//   - producers (warps 4-11, lane = key, warp 4+e = dims [64e, 64e + 64)):
+//     load the packed rows three tiles ahead into registers (pads and
 //     out-of-range indices load nothing and decode to zero rows),
 //     dequantize them with byte permutes into a 128-byte-swizzled K-major
-//     bf16 key tile (two buffers), and arrive on its "full" barrier;
-//   - the issuer (warp 12, one thread): S(t) = Q K^T (M 128, N 64, K 512)
-//     into one of two score buffers once the tile and the buffer are free,
-//     then O += P(t-1) V(t-1) (M 128, N 256, K 64; V is the same key tile read
-//     MN-major) once softmax has written P; tcgen05.commit on mbarriers
-//     tracks completion;
-//   - softmax (warps 0-3, one head per thread): read S(t), release its
-//     buffer, run the online softmax in fp32 (exp2, running max with a
-//     rescale of the output only when the max grows by more than 2**8), and
-//     write P (bf16, two buffers) to shared memory.
+//     bf16 key tile, and arrive on its "full" barrier; a stage is reused once
+//     the p.v that last read it has completed;
+//   - the issuer (warp 12, one thread), event-driven: O += P(u) V(u)
+//     (M 128, N 256, K 32; V is the key tile read MN-major) as soon as
+//     softmax has written P(u), else S(t) = Q K(t)^T (M 128, N 32, K 512)
+//     once K(t) is written and p.v(t - 4), the last reader of the stage's
+//     tensor-memory columns, has been issued (MMAs from one thread run in
+//     order); tcgen05.commit on mbarriers tracks completion;
+//   - softmax (warps 0-3, one head per thread): read S(t), run the online
+//     softmax in fp32 (exp2, running max with a rescale of the output only
+//     when the max grows by more than 2**8), and store P (bf16 pairs) into
+//     tensor memory.
 // Every wait is bounded; a timeout sets a CTA-wide abort flag that ends the
 // other roles' waits, and the CTA reports through an optional status word.
 //
@@ -50,32 +53,31 @@ namespace {
 
 constexpr int kHeads = 128;     // MMA M: rows = heads of one query
 constexpr int kDim = 512;       // latent width (score depth)
-constexpr int kTileKeys = 64;   // MMA N of q.k, K of p.v
+constexpr int kTileKeys = 32;   // MMA N of q.k, K of p.v
+constexpr int kStages = 4;      // key tiles (and score / probability buffers) in the ring
 constexpr int kHalf = 256;      // output columns per CTA
 constexpr int kThreads = 416;   // softmax warps 0-3, producers 4-11, issuer 12
 constexpr int kIssuerWarp = 12;
 constexpr int kRow = 272;       // packed row bytes
-constexpr int kDepth = 2;       // tiles a producer has in flight
+constexpr int kDepth = 3;       // tiles a producer has in flight
 
 constexpr uint32_t kQhiBytes = kHeads * 256 * 2;         // dims 256..511: 4 K-blocks x 128 rows
-constexpr uint32_t kKBytes = kTileKeys * kDim * 2;       // 8 K-blocks x 64 rows x 128 B
+constexpr uint32_t kKBytes = kTileKeys * kDim * 2;       // 8 K-blocks x 32 rows x 128 B
 constexpr uint32_t kKBlock = kTileKeys * 128;            // bytes of one K-block of a key tile
-constexpr uint32_t kPBytes = kHeads * kTileKeys * 2;     // 16 row groups x 8 core matrices
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQhiBytes;            // two buffers
-constexpr uint32_t kOffP = kOffK + 2 * kKBytes;          // two buffers
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;        // ten mbarriers
+constexpr uint32_t kOffK = kOffQ + kQhiBytes;            // kStages buffers
+constexpr uint32_t kOffBar = kOffK + kStages * kKBytes;  // sixteen mbarriers
 constexpr uint32_t kOffTmemSlot = kOffBar + 128;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 16;
 constexpr uint32_t kSmemUsed = kOffAbort + 16;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
 
-// mbarriers, two of each (buffer t & 1)
-constexpr uint32_t kBarKFull = 0, kBarSFull = 16, kBarSEmpty = 32, kBarPFull = 48, kBarPvDone = 64;
+// mbarriers, one of each per stage (tile t uses stage t % kStages)
+constexpr uint32_t kBarKFull = 0, kBarSFull = 32, kBarPFull = 64, kBarPvDone = 96;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
-constexpr uint32_t kColS = 256;   // two buffers of 64 columns
+constexpr uint32_t kColS = 256;   // kStages buffers of 32 columns: scores, then P over them
 constexpr uint32_t kColQ = 384;   // Q dims 0..255 as 128 columns of bf16 pairs
 
 constexpr uint32_t kWaitPolls = 1u << 22;
@@ -121,11 +123,6 @@ __device__ __forceinline__ uint4 ld_issue_v4(const void* p) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t ld_issue_u32(const void* p) {
-  uint32_t r;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -250,6 +247,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -283,12 +292,12 @@ constexpr uint32_t kIdescPV = instr_desc(kHeads, kHalf, true);
 
 // --------------------------------------------------------------- producer ---
 
-// One producer thread's share of a key row: the 64 code bytes of dims
-// [128q, 128q + 128) and the four scale bytes of those groups. A pad or an
-// out-of-range index loads nothing: zero codes decode to +0.0 under any
-// scale byte in [2, 252].
+// One producer thread's share of a key row: the 32 code bytes of dims
+// [64e, 64e + 64) and the two scale bytes of those groups (low 16 bits of s).
+// A pad or an out-of-range index loads nothing: zero codes decode to +0.0
+// under any scale byte in [2, 252].
 struct Packed {
-  uint4 c[4];
+  uint4 c[2];
   uint32_t s;
 };
 
@@ -297,85 +306,96 @@ __device__ __forceinline__ int64_t key_index(const AttnParams& p, const int64_t*
   return k < p.topk ? ld_once_i64(idx_row + k) : -1;
 }
 
-__device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, int q) {
+__device__ __forceinline__ uint32_t ld_issue_u16(const void* p) {
+  uint16_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, int e) {
   Packed r;
   if (s >= 0 && s < p.num_slots) {
     int64_t blk, in_blk;
     divmod_pos(s, p.block_size, blk, in_blk);
     const uint8_t* row = p.cache + (blk * p.block_stride_rows + in_blk) * kRow;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) r.c[g] = ld_issue_v4(row + 64 * q + 16 * g);
-    r.s = ld_issue_u32(row + 256 + 4 * q);
+    r.c[0] = ld_issue_v4(row + 32 * e);
+    r.c[1] = ld_issue_v4(row + 32 * e + 16);
+    r.s = ld_issue_u16(row + 256 + 2 * e);
   } else {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) r.c[g] = make_uint4(0, 0, 0, 0);
-    r.s = 0x7F7F7F7Fu;
+    r.c[0] = make_uint4(0, 0, 0, 0);
+    r.c[1] = r.c[0];
+    r.s = 0x7F7Fu;
   }
   return r;
 }
 
-// Dims [128q, 128q + 128) of key j into key buffer `kbuf`, 128-byte-swizzled
-// K-major: element (key j, dim d) at kb*kKBlock + j*128 + ((c ^ (j & 7)) << 4)
-// + 2*(d & 7), kb = d / 64, c = (d % 64) / 8. With lane = key, each 8-lane
-// phase of a 16-byte store covers eight keys and all eight bank groups.
-__device__ __forceinline__ void dequant_share(const Packed& x, uint32_t kbuf, int j, int q) {
-  const uint32_t kdst = kbuf + (uint32_t)j * 128;
+// Dims [64e, 64e + 64) (K-block e) of key j into key buffer `kbuf`,
+// 128-byte-swizzled K-major: element (key j, dim d) at
+// kb*kKBlock + j*128 + ((c ^ (j & 7)) << 4) + 2*(d & 7), kb = d / 64,
+// c = (d % 64) / 8. With lane = key, each 8-lane phase of a 16-byte store
+// covers eight keys and all eight bank groups.
+__device__ __forceinline__ void dequant_share(const Packed& x, uint32_t kbuf, int j, int e) {
+  const uint32_t row = kbuf + (uint32_t)e * kKBlock + (uint32_t)j * 128;
   const uint32_t swz = (uint32_t)(j & 7);
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < 2; ++g) {
     const uint32_t sb = (x.s >> (8 * g)) & 0xFFu;
     const ByteTables tb = make_tables(sb);
     const uint32_t words[4] = {x.c[g].x, x.c[g].y, x.c[g].z, x.c[g].w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int i = 4 * g + u;  // chunk of 8 dims within the thread's 128
-      const uint4 v = decode8_direct(words[u], sb, tb);
-      sts_v4(kdst + (uint32_t)(2 * q + (i >> 3)) * kKBlock + ((((uint32_t)i & 7) ^ swz) << 4),
-             v);
+      const uint32_t c = (uint32_t)(4 * g + u);  // chunk of 8 dims within the K-block
+      sts_v4(row + ((c ^ swz) << 4), decode8_direct(words[u], sb, tb));
     }
   }
 }
 
 // --------------------------------------------------------------- issuer ---
 
-// S(t) = Q K(t)^T into score buffer t & 1: dims 0..255 with Q from TMEM
-// (16 steps of 8 columns), dims 256..511 with Q from shared memory.
-__device__ __forceinline__ void issue_qk(int64_t t, uint32_t q_base, uint32_t k_base,
+// Descriptors are built once per tile: a descriptor's start address field
+// holds address >> 4 in its low 14 bits, and shared-memory addresses stay
+// below 2**18, so adding a byte offset / 16 to a base descriptor moves the
+// start without carrying into the other fields (fewer instructions in the
+// issuing thread, which shares its SMSP with busy warps).
+__device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t byte_offset) {
+  return base_desc + (uint64_t)(byte_offset >> 4);
+}
+
+// S(t) = Q K(t)^T into score buffer t % kStages: dims 0..255 with Q from
+// TMEM (16 steps of 8 columns), dims 256..511 with Q from shared memory.
+__device__ __forceinline__ void issue_qk(int64_t t, uint64_t q_desc, uint32_t k_base,
                                          uint32_t tmem) {
-  const uint32_t kb_base = k_base + (uint32_t)(t & 1) * kKBytes;
-  const uint32_t d = tmem + kColS + (uint32_t)(t & 1) * kTileKeys;
+  const uint32_t st = (uint32_t)(t % kStages);
+  const uint64_t k_desc = smem_desc(k_base + st * kKBytes, 16, 1024, 2);
+  const uint32_t d = tmem + kColS + st * kTileKeys;
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t b = smem_desc(kb_base + kb * kKBlock + ks * 32, 16, 1024, 2);
-      mma_bf16_ta(d, tmem + kColQ + (uint32_t)(8 * (4 * kb + ks)), b, kIdescQK, (kb | ks) != 0);
-    }
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16_ta(d, tmem + kColQ + (uint32_t)(8 * (4 * kb + ks)),
+                  desc_at(k_desc, kb * kKBlock + ks * 32), kIdescQK, (kb | ks) != 0);
   }
 #pragma unroll
   for (int kb = 4; kb < 8; ++kb) {
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t a = smem_desc(q_base + (kb - 4) * (kHeads * 128) + ks * 32, 16, 1024, 2);
-      const uint64_t b = smem_desc(kb_base + kb * kKBlock + ks * 32, 16, 1024, 2);
-      mma_bf16(d, a, b, kIdescQK, 1);
-    }
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(d, desc_at(q_desc, (kb - 4) * (kHeads * 128) + ks * 32),
+               desc_at(k_desc, kb * kKBlock + ks * 32), kIdescQK, 1);
   }
 }
 
-// O (+)= P(t) V(t), V = key buffer t & 1 read MN-major from column block 4v
-// (LBO: next 64 columns, SBO: next 8 keys), P K-major without swizzle
-// (8x16-byte core matrices; LBO: next 8 keys, SBO: next 8 heads).
-__device__ __forceinline__ void issue_pv(int64_t t, int v, uint32_t p_base, uint32_t k_base,
-                                         uint32_t tmem) {
-  const uint32_t pb = p_base + (uint32_t)(t & 1) * kPBytes;
-  const uint32_t vb = k_base + (uint32_t)(t & 1) * kKBytes + (uint32_t)v * 4 * kKBlock;
+// O (+)= P(t) V(t): P (bf16 pairs, written by softmax over the score
+// columns of stage t % kStages) is the TMEM A operand, 8 columns per step of
+// 16 keys; V is key buffer t % kStages read MN-major from column block 4v
+// (LBO: next 64 columns, SBO: next 8 keys).
+__device__ __forceinline__ void issue_pv(int64_t t, int v, uint32_t k_base, uint32_t tmem) {
+  const uint32_t st = (uint32_t)(t % kStages);
+  const uint64_t v_desc =
+      smem_desc(k_base + st * kKBytes + (uint32_t)v * 4 * kKBlock, kKBlock, 1024, 2);
+  const uint32_t pa = tmem + kColS + st * kTileKeys;
 #pragma unroll
-  for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-    const uint64_t a = smem_desc(pb + ks * 256, 128, 1024, 0);
-    const uint64_t b = smem_desc(vb + ks * 2048, kKBlock, 1024, 2);
-    mma_bf16(tmem + kColO, a, b, kIdescPV, (t | ks) != 0);
-  }
+  for (int ks = 0; ks < kTileKeys / 16; ++ks)
+    mma_bf16_ta(tmem + kColO, pa + 8 * ks, desc_at(v_desc, ks * 2048), kIdescPV, (t | ks) != 0);
 }
 
 // ---------------------------------------------------------------- kernel ---
@@ -388,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t n = blockIdx.x >> 1;
   const int v = blockIdx.x & 1;
-  const uint32_t q_base = base + kOffQ, k_base = base + kOffK, p_base = base + kOffP;
+  const uint32_t q_base = base + kOffQ, k_base = base + kOffK;
   const uint32_t bars = base + kOffBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
@@ -398,10 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   if (warp == kIssuerWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   if (tid == 0) {
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kStages; ++b) {
       mbar_init(bars + kBarKFull + 8 * b, 256);
       mbar_init(bars + kBarSFull + 8 * b, 1);
-      mbar_init(bars + kBarSEmpty + 8 * b, 128);
       mbar_init(bars + kBarPFull + 8 * b, 128);
       mbar_init(bars + kBarPvDone + 8 * b, 1);
     }
@@ -453,11 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
 
   if (warp >= 4 && warp < kIssuerWarp) {
     // ------------------------------------------------------------ producers
-    const int j = lane + 32 * (warp & 1), q = (warp - 4) >> 1;
+    // Lane = key of the tile, warp 4 + e = dims [64e, 64e + 64). Key buffer
+    // t % kStages is free once PV(t - kStages) has completed.
+    const int e = warp - 4, j = lane;
     Packed buf[kDepth];
 #pragma unroll
     for (int u = 0; u < kDepth; ++u)
-      buf[u] = load_packed(p, key_index(p, idx_row, (int64_t)u * kTileKeys + j), q);
+      buf[u] = load_packed(p, key_index(p, idx_row, (int64_t)u * kTileKeys + j), e);
     int64_t s_next = key_index(p, idx_row, (int64_t)kDepth * kTileKeys + j);
     bool live = true;
     for (int64_t t0 = 0; t0 < num_tiles && live; t0 += kDepth) {
@@ -466,16 +487,16 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
         const int64_t t = t0 + u;
         if (t < num_tiles && live) {
           const Packed cur = buf[u];
-          buf[u] = load_packed(p, s_next, q);  // tile t + kDepth
+          buf[u] = load_packed(p, s_next, e);  // tile t + kDepth
           s_next = key_index(p, idx_row, (t + kDepth + 1) * kTileKeys + j);
-          // key buffer t & 1 is free once PV(t-2) has completed
-          if (t >= 2 && !mbar_wait(bars + kBarPvDone + 8 * (t & 1), (uint32_t)(((t - 2) >> 1) & 1),
-                                   abort)) {
+          const uint32_t st = (uint32_t)(t % kStages);
+          if (t >= kStages &&
+              !mbar_wait(bars + kBarPvDone + 8 * st, (uint32_t)(((t / kStages) - 1) & 1), abort)) {
             live = false;
           } else {
-            dequant_share(cur, k_base + (uint32_t)(t & 1) * kKBytes, j, q);
+            dequant_share(cur, k_base + st * kKBytes, j, e);
             fence_proxy_async();
-            mbar_arrive(bars + kBarKFull + 8 * (t & 1));
+            mbar_arrive(bars + kBarKFull + 8 * st);
           }
         }
       }
@@ -483,22 +504,35 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   } else if (warp == kIssuerWarp) {
     // --------------------------------------------------------------- issuer
     if (lane == 0) {
-      for (int64_t t = 0; t <= num_tiles; ++t) {
-        if (t < num_tiles) {
-          if (!mbar_wait(bars + kBarKFull + 8 * (t & 1), (uint32_t)((t >> 1) & 1), abort)) break;
-          if (t >= 2 && !mbar_wait(bars + kBarSEmpty + 8 * (t & 1),
-                                   (uint32_t)(((t - 2) >> 1) & 1), abort))
-            break;
+      const uint64_t q_desc = smem_desc(q_base, 16, 1024, 2);
+      // Event-driven: O += P(u) V(u) as soon as softmax has written P(u) (it
+      // frees key buffer u % kStages, so it goes first), else S(t) = Q K(t)^T
+      // once K(t) is written and PV(t - kStages), the last reader of the
+      // stage's TMEM columns, has been issued (MMAs from this thread run in
+      // order). Polls without progress are bounded.
+      int64_t t = 0, u = 0;
+      uint32_t idle = 0;
+      while (u < num_tiles) {
+        if (u < t && mbar_test(bars + kBarPFull + 8 * (uint32_t)(u % kStages),
+                               (uint32_t)((u / kStages) & 1))) {
           tc_fence_after();
-          issue_qk(t, q_base, k_base, tmem);
-          mma_commit(bars + kBarSFull + 8 * (t & 1));
-        }
-        if (t >= 1) {
-          const int64_t u = t - 1;
-          if (!mbar_wait(bars + kBarPFull + 8 * (u & 1), (uint32_t)((u >> 1) & 1), abort)) break;
+          issue_pv(u, v, k_base, tmem);
+          mma_commit(bars + kBarPvDone + 8 * (uint32_t)(u % kStages));
+          ++u;
+          idle = 0;
+        } else if (t < num_tiles && t - u < kStages &&
+                   mbar_test(bars + kBarKFull + 8 * (uint32_t)(t % kStages),
+                             (uint32_t)((t / kStages) & 1))) {
           tc_fence_after();
-          issue_pv(u, v, p_base, k_base, tmem);
-          mma_commit(bars + kBarPvDone + 8 * (u & 1));
+          issue_qk(t, q_desc, k_base, tmem);
+          mma_commit(bars + kBarSFull + 8 * (uint32_t)(t % kStages));
+          ++t;
+          idle = 0;
+        } else if (++idle >= kWaitPolls) {
+          *abort = 1;
+          break;
+        } else if ((idle & 31u) == 31u && *abort) {
+          break;
         }
       }
     }
@@ -509,36 +543,35 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     float m_ref = -__int_as_float(0x7F800000);  // reference max (log2 units)
     float l = 0.0f;                              // sum of p against m_ref
     bool live = true;
-    int64_t s_lo = key_index(p, idx_row, lane), s_hi = key_index(p, idx_row, 32 + lane);
+    int64_t s_key = key_index(p, idx_row, lane);
     for (int64_t t = 0; t < num_tiles && live; ++t) {
-      const uint32_t mask_lo = __ballot_sync(0xFFFFFFFFu, s_lo >= 0 && s_lo < p.num_slots);
-      const uint32_t mask_hi = __ballot_sync(0xFFFFFFFFu, s_hi >= 0 && s_hi < p.num_slots);
-      s_lo = key_index(p, idx_row, (t + 1) * kTileKeys + lane);
-      s_hi = key_index(p, idx_row, (t + 1) * kTileKeys + 32 + lane);
-      if (!warp_wait(bars + kBarSFull + 8 * (t & 1), (uint32_t)((t >> 1) & 1), abort)) {
+      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, s_key >= 0 && s_key < p.num_slots);
+      s_key = key_index(p, idx_row, (t + 1) * kTileKeys + lane);
+      const uint32_t st = (uint32_t)(t % kStages);
+      if (!warp_wait(bars + kBarSFull + 8 * st, (uint32_t)((t / kStages) & 1), abort)) {
         live = false;
         break;
       }
       tc_fence_after();
-      const uint32_t scol = lane_base + kColS + (uint32_t)(t & 1) * kTileKeys;
-      // Pass 1: the tile max (scores in log2 units, -inf for dropped keys).
-      float mt = -__int_as_float(0x7F800000);
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[32];
-        tmem_ld32(scol + 32 * hf, sr);
-        const uint32_t m = hf ? mask_hi : mask_lo;
+      const uint32_t scol = lane_base + kColS + st * kTileKeys;
+      uint32_t sr[32];
+      tmem_ld32(scol, sr);
+      // the tile max (log2 units, -inf for dropped keys), four chains
+      float mc[4] = {-__int_as_float(0x7F800000), -__int_as_float(0x7F800000),
+                     -__int_as_float(0x7F800000), -__int_as_float(0x7F800000)};
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if ((m >> k) & 1u) mt = fmaxf(mt, __fmul_rn(__uint_as_float(sr[k]), p.scale_log2));
-      }
+      for (int k = 0; k < 32; ++k)
+        if ((mask >> k) & 1u)
+          mc[k & 3] = fmaxf(mc[k & 3], __fmul_rn(__uint_as_float(sr[k]), p.scale_log2));
+      const float mt = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
       const bool need = mt > m_ref + 8.0f;
       if (__any_sync(0xFFFFFFFFu, need)) {
         const float f = need ? ex2(m_ref - mt) : 1.0f;  // ex2(-inf) = 0
         if (t > 0) {
           // O may be touched only once PV(t-1) has completed
-          if (!warp_wait(bars + kBarPvDone + 8 * ((t - 1) & 1), (uint32_t)(((t - 1) >> 1) & 1),
-                         abort)) {
+          const int64_t w = t - 1;
+          if (!warp_wait(bars + kBarPvDone + 8 * (uint32_t)(w % kStages),
+                         (uint32_t)((w / kStages) & 1), abort)) {
             live = false;
             break;
           }
@@ -556,50 +589,30 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
         if (need) m_ref = mt;
       }
       const float mu = m_ref == -__int_as_float(0x7F800000) ? 0.0f : m_ref;
-      // P buffer t & 1 is free once PV(t-2) has completed
-      if (t >= 2 && !warp_wait(bars + kBarPvDone + 8 * (t & 1), (uint32_t)(((t - 2) >> 1) & 1),
-                               abort)) {
-        live = false;
-        break;
-      }
-      // Pass 2: probabilities, their sum, and P (bf16) for this head's row.
-      const uint32_t prow = p_base + (uint32_t)(t & 1) * kPBytes + (uint32_t)(tid >> 3) * 1024 +
-                            (uint32_t)(tid & 7) * 16;
+      // probabilities, their sum, and P (bf16 pairs) over the score columns
       float lsum0 = 0.0f, lsum1 = 0.0f;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[32];
-        tmem_ld32(scol + 32 * hf, sr);
-        const uint32_t m = hf ? mask_hi : mask_lo;
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float x0 = ((m >> (2 * k)) & 1u)
-                               ? __fmul_rn(__uint_as_float(sr[2 * k]), p.scale_log2)
-                               : -__int_as_float(0x7F800000);
-          const float x1 = ((m >> (2 * k + 1)) & 1u)
-                               ? __fmul_rn(__uint_as_float(sr[2 * k + 1]), p.scale_log2)
-                               : -__int_as_float(0x7F800000);
-          const float p0 = ex2(x0 - mu), p1 = ex2(x1 - mu);
-          lsum0 += p0;
-          lsum1 += p1;
-          pk[k] = pack_bf16x2(p0, p1);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          sts_v4(prow + 128 * (4 * hf + c),
-                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+      for (int k = 0; k < 16; ++k) {
+        const float x0 = ((mask >> (2 * k)) & 1u)
+                             ? __fmul_rn(__uint_as_float(sr[2 * k]), p.scale_log2)
+                             : -__int_as_float(0x7F800000);
+        const float x1 = ((mask >> (2 * k + 1)) & 1u)
+                             ? __fmul_rn(__uint_as_float(sr[2 * k + 1]), p.scale_log2)
+                             : -__int_as_float(0x7F800000);
+        const float p0 = ex2(x0 - mu), p1 = ex2(x1 - mu);
+        lsum0 += p0;
+        lsum1 += p1;
+        pk[k] = pack_bf16x2(p0, p1);
       }
+      tmem_st16(scol, pk);
       l += lsum0 + lsum1;
       tc_fence_before();
-      mbar_arrive(bars + kBarSEmpty + 8 * (t & 1));
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(bars + kBarPFull + 8 * (t & 1));
+      mbar_arrive(bars + kBarPFull + 8 * st);
     }
     if (live && num_tiles > 0 &&
-        !warp_wait(bars + kBarPvDone + 8 * ((num_tiles - 1) & 1),
-                   (uint32_t)(((num_tiles - 1) >> 1) & 1), abort))
+        !warp_wait(bars + kBarPvDone + 8 * (uint32_t)((num_tiles - 1) % kStages),
+                   (uint32_t)(((num_tiles - 1) / kStages) & 1), abort))
       live = false;
     live = __all_sync(0xFFFFFFFFu, live && !*abort);
     if (live) {
