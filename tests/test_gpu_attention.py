@@ -101,7 +101,7 @@ def test_small_two_tiles_with_pads():
 
 
 @pytest.mark.parametrize("heads", [1, 64, 127, 128])
-@pytest.mark.parametrize("topk", [1, 31, 33, 100])
+@pytest.mark.parametrize("topk", [1, 31, 33, 100, 161])
 def test_ragged_heads_and_topk(heads, topk):
     cache = _fill_cache(2048, seed=4)
     q = _queries(5 + heads, 2, heads)
