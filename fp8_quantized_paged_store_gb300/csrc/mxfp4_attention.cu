@@ -26,10 +26,12 @@
 //     the p.v that last read it has completed;
 //   - the issuer (warp 12, one thread), event-driven: O += P(u) V(u)
 //     (M 128, N 256, K 32; V is the key tile read MN-major) as soon as
-//     softmax has written P(u), else S(t) = Q K(t)^T (M 128, N 32, K 512)
-//     once K(t) is written and p.v(t - 4), the last reader of the stage's
-//     tensor-memory columns, has been issued (MMAs from one thread run in
-//     order); tcgen05.commit on mbarriers tracks completion;
+//     softmax has written P(u), else S = Q K^T over two tiles at once
+//     (M 128, N 64, K 512: the ring is laid out K-block-major, so the same
+//     K-block of two neighbouring stages is one 64-row operand) once both
+//     are written and the p.v that last read their tensor-memory columns has
+//     been issued (MMAs from one thread run in order); tcgen05.commit on
+//     mbarriers tracks completion;
 //   - softmax (warps 0-3, one head per thread): read S(t), run the online
 //     softmax in fp32 (exp2, running max with a rescale of the output only
 //     when the max grows by more than 2**8), and store P (bf16 pairs) into
@@ -64,6 +66,10 @@ constexpr int kDepth = 3;       // tiles a producer has in flight
 constexpr uint32_t kQhiBytes = kHeads * 256 * 2;         // dims 256..511: 4 K-blocks x 128 rows
 constexpr uint32_t kKBytes = kTileKeys * kDim * 2;       // 8 K-blocks x 32 rows x 128 B
 constexpr uint32_t kKBlock = kTileKeys * 128;            // bytes of one K-block of a key tile
+// The ring is laid out K-block-major: K-block kb of stage s at
+// (kb * kStages + s) * kKBlock, so the same K-block of stages s and s + 1
+// (s even) is one 64-row block and q.k runs at N = 64 over a pair of stages.
+constexpr uint32_t kKBlockStride = kStages * kKBlock;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQhiBytes;            // kStages buffers
 constexpr uint32_t kOffBar = kOffK + kStages * kKBytes;  // sixteen mbarriers
@@ -287,7 +293,7 @@ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major) {
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-constexpr uint32_t kIdescQK = instr_desc(kHeads, kTileKeys, false);
+constexpr uint32_t kIdescQK = instr_desc(kHeads, 2 * kTileKeys, false);
 constexpr uint32_t kIdescPV = instr_desc(kHeads, kHalf, true);
 
 // --------------------------------------------------------------- producer ---
@@ -329,13 +335,13 @@ __device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, in
   return r;
 }
 
-// Dims [64e, 64e + 64) (K-block e) of key j into key buffer `kbuf`,
-// 128-byte-swizzled K-major: element (key j, dim d) at
-// kb*kKBlock + j*128 + ((c ^ (j & 7)) << 4) + 2*(d & 7), kb = d / 64,
+// Dims [64e, 64e + 64) (K-block e) of key j into the stage whose K-block 0
+// is at `kbuf`, 128-byte-swizzled K-major: element (key j, dim d) at
+// kb*kKBlockStride + j*128 + ((c ^ (j & 7)) << 4) + 2*(d & 7), kb = d / 64,
 // c = (d % 64) / 8. With lane = key, each 8-lane phase of a 16-byte store
 // covers eight keys and all eight bank groups.
 __device__ __forceinline__ void dequant_share(const Packed& x, uint32_t kbuf, int j, int e) {
-  const uint32_t row = kbuf + (uint32_t)e * kKBlock + (uint32_t)j * 128;
+  const uint32_t row = kbuf + (uint32_t)e * kKBlockStride + (uint32_t)j * 128;
   const uint32_t swz = (uint32_t)(j & 7);
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
@@ -361,37 +367,39 @@ __device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t byte_of
   return base_desc + (uint64_t)(byte_offset >> 4);
 }
 
-// S(t) = Q K(t)^T into score buffer t % kStages: dims 0..255 with Q from
-// TMEM (16 steps of 8 columns), dims 256..511 with Q from shared memory.
+// S(t), S(t+1) = Q K^T over the pair of stages t % kStages (even) and the
+// next, into their score columns (N = 64): dims 0..255 with Q from TMEM (16
+// steps of 8 columns), dims 256..511 with Q from shared memory. When t is the
+// last tile, the second half computes scores of a stage no tile reads.
 __device__ __forceinline__ void issue_qk(int64_t t, uint64_t q_desc, uint32_t k_base,
                                          uint32_t tmem) {
   const uint32_t st = (uint32_t)(t % kStages);
-  const uint64_t k_desc = smem_desc(k_base + st * kKBytes, 16, 1024, 2);
+  const uint64_t k_desc = smem_desc(k_base + st * kKBlock, 16, 1024, 2);
   const uint32_t d = tmem + kColS + st * kTileKeys;
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
       mma_bf16_ta(d, tmem + kColQ + (uint32_t)(8 * (4 * kb + ks)),
-                  desc_at(k_desc, kb * kKBlock + ks * 32), kIdescQK, (kb | ks) != 0);
+                  desc_at(k_desc, kb * kKBlockStride + ks * 32), kIdescQK, (kb | ks) != 0);
   }
 #pragma unroll
   for (int kb = 4; kb < 8; ++kb) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
       mma_bf16(d, desc_at(q_desc, (kb - 4) * (kHeads * 128) + ks * 32),
-               desc_at(k_desc, kb * kKBlock + ks * 32), kIdescQK, 1);
+               desc_at(k_desc, kb * kKBlockStride + ks * 32), kIdescQK, 1);
   }
 }
 
 // O (+)= P(t) V(t): P (bf16 pairs, written by softmax over the score
 // columns of stage t % kStages) is the TMEM A operand, 8 columns per step of
-// 16 keys; V is key buffer t % kStages read MN-major from column block 4v
-// (LBO: next 64 columns, SBO: next 8 keys).
+// 16 keys; V is the stage's key rows read MN-major from column block 4v
+// (LBO: the stage's next K-block, SBO: next 8 keys).
 __device__ __forceinline__ void issue_pv(int64_t t, int v, uint32_t k_base, uint32_t tmem) {
   const uint32_t st = (uint32_t)(t % kStages);
-  const uint64_t v_desc =
-      smem_desc(k_base + st * kKBytes + (uint32_t)v * 4 * kKBlock, kKBlock, 1024, 2);
+  const uint64_t v_desc = smem_desc(k_base + ((uint32_t)v * 4 * kStages + st) * kKBlock,
+                                    kKBlockStride, 1024, 2);
   const uint32_t pa = tmem + kColS + st * kTileKeys;
 #pragma unroll
   for (int ks = 0; ks < kTileKeys / 16; ++ks)
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
               !mbar_wait(bars + kBarPvDone + 8 * st, (uint32_t)(((t / kStages) - 1) & 1), abort)) {
             live = false;
           } else {
-            dequant_share(cur, k_base + st * kKBytes, j, e);
+            dequant_share(cur, k_base + st * kKBlock, j, e);
             fence_proxy_async();
             mbar_arrive(bars + kBarKFull + 8 * st);
           }
@@ -506,10 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     if (lane == 0) {
       const uint64_t q_desc = smem_desc(q_base, 16, 1024, 2);
       // Event-driven: O += P(u) V(u) as soon as softmax has written P(u) (it
-      // frees key buffer u % kStages, so it goes first), else S(t) = Q K(t)^T
-      // once K(t) is written and PV(t - kStages), the last reader of the
-      // stage's TMEM columns, has been issued (MMAs from this thread run in
-      // order). Polls without progress are bounded.
+      // frees key stage u % kStages, so it goes first), else q.k over the
+      // pair of tiles t, t + 1 (t even) once both are written and PV(t - 3),
+      // the last reader of their TMEM columns, has been issued (MMAs from
+      // this thread run in order). Polls without progress are bounded.
       int64_t t = 0, u = 0;
       uint32_t idle = 0;
       while (u < num_tiles) {
@@ -520,13 +528,17 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
           mma_commit(bars + kBarPvDone + 8 * (uint32_t)(u % kStages));
           ++u;
           idle = 0;
-        } else if (t < num_tiles && t - u < kStages &&
+        } else if (t < num_tiles && t + 1 - u < kStages &&
                    mbar_test(bars + kBarKFull + 8 * (uint32_t)(t % kStages),
-                             (uint32_t)((t / kStages) & 1))) {
+                             (uint32_t)((t / kStages) & 1)) &&
+                   (t + 1 >= num_tiles ||
+                    mbar_test(bars + kBarKFull + 8 * (uint32_t)((t + 1) % kStages),
+                              (uint32_t)(((t + 1) / kStages) & 1)))) {
           tc_fence_after();
           issue_qk(t, q_desc, k_base, tmem);
           mma_commit(bars + kBarSFull + 8 * (uint32_t)(t % kStages));
-          ++t;
+          if (t + 1 < num_tiles) mma_commit(bars + kBarSFull + 8 * (uint32_t)((t + 1) % kStages));
+          t += 2;
           idle = 0;
         } else if (++idle >= kWaitPolls) {
           *abort = 1;
