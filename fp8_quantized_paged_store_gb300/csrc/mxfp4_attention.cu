@@ -321,9 +321,14 @@ __device__ __forceinline__ uint32_t ld_issue_u16(const void* p) {
 __device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, int e) {
   Packed r;
   if (s >= 0 && s < p.num_slots) {
-    int64_t blk, in_blk;
-    divmod_pos(s, p.block_size, blk, in_blk);
-    const uint8_t* row = p.cache + (blk * p.block_stride_rows + in_blk) * kRow;
+    // blocks laid end to end (stride = block size): the row is the slot
+    int64_t row_index = s;
+    if (p.block_stride_rows != p.block_size) {
+      int64_t blk, in_blk;
+      divmod_pos(s, p.block_size, blk, in_blk);
+      row_index = blk * p.block_stride_rows + in_blk;
+    }
+    const uint8_t* row = p.cache + row_index * kRow;
     r.c[0] = ld_issue_v4(row + 32 * e);
     r.c[1] = ld_issue_v4(row + 32 * e + 16);
     r.s = ld_issue_u16(row + 256 + 2 * e);
