@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(kCompressThreads) compress_norm_kernel(Compres
           closes = req >= 0 && req < p.num_reqs && s < p.num_state_slots;
           if (closes) {
             const int64_t qs = ld_i64(p.qsl + req), qe = ld_i64(p.qsl + req + 1);
-            closes = qs < t && t < qe;  // the chunk's first token is the request role's
+            // the chunk's first token (a start below 0 reads as 0) is the request role's
+            closes = (qs > 0 ? qs : 0) < t && t < qe;
           }
         }
       }

@@ -304,7 +304,9 @@ int save_ring_rows(const float* rows, int64_t num_rows, int64_t row_stride_elems
  * kv_score               fp32 [num_tokens, row_stride_elems], 512*R used,
  *                        16-byte aligned; row_stride_elems multiple of 4
  * positions, slot_mapping int64 [num_tokens]
- * query_start_loc        R = 2: int64 [num_reqs + 1], non-decreasing
+ * query_start_loc        R = 2: int64 [num_reqs + 1], non-decreasing; a
+ *                        chunk is cut to [0, num_tokens) (a start below 0
+ *                        reads as 0, an end past num_tokens as num_tokens)
  * token_to_req_indices   R = 2: int64 [num_tokens]
  * state                  R = 2: fp32 [num_blocks, capacity, >= 1024], block
  *                        stride state_stride_elems, row stride

@@ -29,6 +29,8 @@ Readings where the page is silent (the kernel itself is not printed):
     its slot is >= 0 (and, for R = 2, its ring slot lies inside the state)
     and its position is >= 0; a token whose request index or chunk range is
     inconsistent is skipped, as is a prev_rows index past the rows given;
+  * a request's chunk is query_start_loc[k] .. query_start_loc[k + 1] cut to
+    the batch's rows [0, T): a start below 0 reads as 0, an end past T as T;
   * the ring rows saved are bit copies of the tokens' 1024 floats.
 
 Written out here in float64 (the exact value of the definition before the
@@ -78,9 +80,10 @@ def fused_save_compress_norm(kv_score: np.ndarray, positions: np.ndarray, state,
         t = np.arange(T)
         req_ok = (req >= 0) & (req < num_reqs)
         r_safe = np.where(req_ok, req, 0)
-        in_chunk = req_ok & (qsl[r_safe] <= t) & (t < qsl[r_safe + 1])
+        qs_t = np.maximum(qsl[r_safe], 0)
+        in_chunk = req_ok & (qs_t <= t) & (t < qsl[r_safe + 1])
         written &= in_chunk & (slot < blocks * cap)
-        first = t == qsl[r_safe]
+        first = t == qs_t
         # the predecessor row of each written token's group
         pred = np.full((T, 2 * LATENT), np.nan)
         inner = written & ~first
@@ -114,7 +117,7 @@ def fused_save_compress_norm(kv_score: np.ndarray, positions: np.ndarray, state,
 
     if R == 2 and prev_rows is None:
         for k in range(num_reqs):
-            qs, qe = int(qsl[k]), min(int(qsl[k + 1]), T)
+            qs, qe = max(int(qsl[k]), 0), min(int(qsl[k + 1]), T)
             for i in range(max(qs, qe - cap), qe):
                 s = int(slot[i])
                 if 0 <= s < blocks * cap:

@@ -204,3 +204,27 @@ def test_empty_batch():
         torch.ones(512, dtype=torch.bfloat16, device=G.DEV), 1e-6, 2, out[:0])
     torch.cuda.synchronize()
     assert bool((out == 0).all())
+
+
+def test_cr2_inconsistent_inputs_are_skipped_like_the_oracle():
+    """Request indices outside [0, num_reqs), an empty chunk, a token outside
+    its request's chunk, chunk bounds outside the batch, a prev_rows index
+    past the rows given, a ring slot past the state, padding tokens: the
+    kernel skips what the oracle skips and writes the same rows and ring
+    state."""
+    w = workloads.compress(seed=6, compress_ratio=2, num_reqs=12, max_chunk=9,
+                           decode_fraction=0.2, capacity=2, pad_tokens=6, prev_rows=True)
+    qsl = w["query_start_loc"].copy()
+    t2r = w["token_to_req"].copy()
+    slots = w["slot_mapping"].copy()
+    qsl[0] = -4                              # a chunk start below 0 (reads as 0)
+    qsl[5] = qsl[4]                          # request 4 becomes empty (its tokens now belong nowhere)
+    qsl[-1] = 10 ** 6                        # a chunk end past the batch
+    t2r[0] = 99                              # a request index past num_reqs
+    t2r[w["num_real"]:] = -3                 # padding tokens with a negative request index
+    slots[2] = w["state"].shape[0] * 2 + 1   # a ring slot past the state
+    idx = w["prev_row_indices"].copy()
+    idx[7] = 10 ** 6                         # a prev_rows index past the rows given
+    w.update(query_start_loc=qsl, token_to_req=t2r, slot_mapping=slots, prev_row_indices=idx)
+    _run(w, prev=True)
+    _run(w)

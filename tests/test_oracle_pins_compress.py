@@ -263,3 +263,24 @@ def test_cr2_gates_and_inconsistent_requests():
     slots_oob = np.array([0, 1, 4, 1, 0, 1])           # 4 = blocks * capacity: outside the ring
     written, _, _ = fscn(rows[:4], pos[:4], state, slots_oob[:4], [0, 4], [0] * 4, ONE, 0.0, 2)
     assert list(written) == [True, False, False, False]
+
+
+def test_cr2_chunk_bounds_are_cut_to_the_batch():
+    """A chunk given as [-3, 9) over a 4-token batch is the chunk [0, 4):
+    same rows written, same latent, same ring."""
+    rng = np.random.default_rng(9)
+    rows = rng.standard_normal((4, 2 * L)).astype(np.float32)
+    pos = np.array([3, 4, 5, 6])
+    ring0 = rng.standard_normal((1, 2, 2 * L)).astype(np.float32)
+    out = []
+    for qsl in ([0, 4], [-3, 4], [0, 9], [-3, 9]):
+        state = ring0.copy()
+        written, lat, _ = fscn(rows, pos, state, pos % 2, qsl, [0] * 4, ONE, 1e-6, 2)
+        out.append((written, lat, state))
+    assert list(out[0][0]) == [True, False, True, False]
+    # the last two tokens (positions 5 and 6) land in ring rows 1 and 0
+    assert np.array_equal(out[0][2][0, 1], rows[2]) and np.array_equal(out[0][2][0, 0], rows[3])
+    for written, lat, state in out[1:]:
+        assert np.array_equal(written, out[0][0])
+        assert np.array_equal(lat, out[0][1])
+        assert np.array_equal(state, out[0][2])
