@@ -33,7 +33,7 @@
 // j (4 bytes) with its own cos and sin, so the rotation and the exact quotient
 // of the 64 rotated values are spread over the whole warp instead of 8 lanes.
 // The other 448 values are bf16 numbers and take the cheaper exact code rule
-// of nvfp4_code_value (two fused products, no ALU work).
+// of nvfp4_code_value2 (two fused products, no ALU work).
 //
 // The pages evaluate the rotation formula on all 256 pairs, with cos 1 and
 // sin 0 outside the rotary range. There it is the identity except for NaN,
@@ -152,6 +152,38 @@ __device__ __forceinline__ float abs_max8(const float f[8]) {
 
 // ------------------------------------------------------------------ MXFP8 ---
 
+// Packed binary32 pairs: one instruction rounds two IEEE products or fused
+// multiply-adds to nearest, each result equal to the scalar one. Only for
+// products that no later addition consumes: the compiler may fuse a packed
+// product into a packed sum, which the scalar __fmul_rn never allows.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mov.b64 c, {%6, %7};\n fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// Eight values times the power of two `inv` as E4M3 (clamped to +-448,
+// NaN -> 0x7F), two per packed product; a product by a power of two is exact
+// unless it leaves the normal range, where it rounds like the scalar one.
+__device__ __forceinline__ uint2 e4m3x8_scaled(const float f[8], float inv) {
+  const float2 i2 = make_float2(inv, inv);
+  const float2 p0 = mul2_rn(make_float2(f[0], f[1]), i2), p1 = mul2_rn(make_float2(f[2], f[3]), i2);
+  const float2 p2 = mul2_rn(make_float2(f[4], f[5]), i2), p3 = mul2_rn(make_float2(f[6], f[7]), i2);
+  return make_uint2(cvt_e4m3x2(p0.x, p0.y) | (cvt_e4m3x2(p1.x, p1.y) << 16),
+                    cvt_e4m3x2(p2.x, p2.y) | (cvt_e4m3x2(p3.x, p3.y) << 16));
+}
+
+
 template <bool kSanitize>
 __device__ __forceinline__ void mxfp8_half(const float f[8], uint8_t* values, uint8_t* scales,
                                            int lane) {
@@ -162,10 +194,8 @@ __device__ __forceinline__ void mxfp8_half(const float f[8], uint8_t* values, ui
   const int e = ceil_pow2_exponent(__fmul_rn(amax, 1.0f / 448.0f));  // -22..128
   const float inv = exp2_neg(e);
   // clamp to +-448 and E4M3 rounding are exactly cvt.rn.satfinite; NaN -> 0x7F
-  const uint32_t a = cvt_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
-                     (cvt_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
-  const uint32_t b = cvt_e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
-                     (cvt_e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
+  const uint2 ab = e4m3x8_scaled(f, inv);
+  const uint32_t a = ab.x, b = ab.y;
   st_v2(values + 8 * lane, a, b);
   if ((lane & 3) == 0) {
     const int cap = kSanitize ? 254 : 255;
@@ -190,10 +220,8 @@ __device__ __forceinline__ void v4_nope_half(const float f[8], uint8_t* values, 
   amax = fmaxf(amax, 1e-4f);
   const int e = ceil_pow2_exponent(__fmul_rn(amax, 1.0f / 448.0f));
   const float inv = exp2_neg(e);
-  const uint32_t a = cvt_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
-                     (cvt_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
-  const uint32_t b = cvt_e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
-                     (cvt_e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
+  const uint2 ab = e4m3x8_scaled(f, inv);
+  const uint32_t a = ab.x, b = ab.y;
   if (store) {
     st_v2(values, a, b);
     if ((lane & 7) == 0) {
@@ -302,7 +330,7 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
 
 // Per E4M3 byte b (0..127), built once per block: s = value(b), y = RN(1/s)
 // for the corrected quotient, and the two-term reciprocal yh = RD(1/s),
-// yl = RN((1 - s*yh) * yh) >= 0 for nvfp4_code_value.
+// yl = RN((1 - s*yh) * yh) >= 0 for nvfp4_code_value2.
 struct ScaleEntry {
   float s, y, yh, yl;
 };
@@ -345,8 +373,11 @@ __device__ __forceinline__ uint32_t nvfp4_scale(float amax, const float4* table,
 // and an infinite quotient rather than NaN. An exhaustive check over all 126
 // positive scales and every non-NaN bf16 x (both infinities with s = 448)
 // found the E2M1 codes equal to those of RN(x / s) everywhere.
-__device__ __forceinline__ float nvfp4_code_value(float x, const ScaleEntry& e) {
-  return __fmaf_rn(x, e.yh, __fmul_rn(x, e.yl));
+// Both bf16 halves of `w` (low element first) go through one packed pair of
+// these steps.
+__device__ __forceinline__ float2 nvfp4_code_value2(uint32_t w, const ScaleEntry& e) {
+  const float2 x = make_float2(bf16_lo(w), bf16_hi(w));
+  return fma2_rn(x, make_float2(e.yh, e.yh), mul2_rn(x, make_float2(e.yl, e.yl)));
 }
 
 // Correctly rounded binary32 x / s for a tile's E4M3 scale s, given
@@ -371,7 +402,7 @@ __device__ __forceinline__ bool markstein_ok(float x, float q0) {
 // Eight bf16-exact values of one NoPE half (four bf16x2 words): the NoPE
 // formula, NaN and -0.0 to +0.0 (both encode as code 0 and NaN never raises
 // the amax), the tile amax over this lane and its partner, then the codes by
-// nvfp4_code_value. Lanes with `store` false compute but write nothing.
+// nvfp4_code_value2. Lanes with `store` false compute but write nothing.
 __device__ __forceinline__ void nvfp4_nope_half(uint4 w, uint8_t* codes, uint8_t* scales, int lane,
                                                 const float4* table, bool store) {
   auto clean = [](uint32_t v) {
@@ -387,11 +418,9 @@ __device__ __forceinline__ void nvfp4_nope_half(uint4 w, uint8_t* codes, uint8_t
   const float amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
   ScaleEntry e;
   const uint32_t sbyte = nvfp4_scale(amax, table, e);
-  const uint32_t c = cvt_e2m1x8(
-      nvfp4_code_value(bf16_lo(w.x), e), nvfp4_code_value(bf16_hi(w.x), e),
-      nvfp4_code_value(bf16_lo(w.y), e), nvfp4_code_value(bf16_hi(w.y), e),
-      nvfp4_code_value(bf16_lo(w.z), e), nvfp4_code_value(bf16_hi(w.z), e),
-      nvfp4_code_value(bf16_lo(w.w), e), nvfp4_code_value(bf16_hi(w.w), e));
+  const float2 q0 = nvfp4_code_value2(w.x, e), q1 = nvfp4_code_value2(w.y, e);
+  const float2 q2 = nvfp4_code_value2(w.z, e), q3 = nvfp4_code_value2(w.w, e);
+  const uint32_t c = cvt_e2m1x8(q0.x, q0.y, q1.x, q1.y, q2.x, q2.y, q3.x, q3.y);
   if (store) {
     st_u32(codes + 4 * lane, c);
     if ((lane & 1) == 0) st_u8(scales + (lane >> 1), sbyte);
@@ -417,12 +446,16 @@ __device__ __forceinline__ void nvfp4_rotary_pair(uint32_t xr, float c, float sn
   ScaleEntry sc;
   const uint32_t sbyte = nvfp4_scale(amax, table, sc);
   const float s = sc.s, y = sc.y;
-  const float qe0 = __fmul_rn(re, y), qo0 = __fmul_rn(ro, y);
+  const float2 r2 = make_float2(re, ro), y2 = make_float2(y, y);
+  const float2 q0 = mul2_rn(r2, y2);
+  const float qe0 = q0.x, qo0 = q0.y;
   const bool ok = __fmul_rn(amax, y) < 0x1p61f && markstein_ok(re, qe0) && markstein_ok(ro, qo0);
   float qe, qo;
   if (__all_sync(0xFFFFFFFFu, ok)) {
-    qe = __fmaf_rn(__fmaf_rn(-qe0, s, re), y, qe0);
-    qo = __fmaf_rn(__fmaf_rn(-qo0, s, ro), y, qo0);
+    // RN(r - q0 s) is exact; -s q0 == -(q0 s)
+    const float2 q1 = fma2_rn(fma2_rn(q0, make_float2(-s, -s), r2), y2, q0);
+    qe = q1.x;
+    qo = q1.y;
   } else {
     qe = nvfp4_quotient_ieee(re, s);
     qo = nvfp4_quotient_ieee(ro, s);
