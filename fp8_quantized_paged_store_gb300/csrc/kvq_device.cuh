@@ -141,6 +141,26 @@ __device__ __forceinline__ uint32_t lds_u8(const void* p) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Packed binary32 pairs: one instruction rounds two IEEE products or fused
+// multiply-adds to nearest, each result equal to the scalar one. Only for
+// products that no later addition consumes: the compiler may fuse a packed
+// product into a packed sum, which the scalar __fmul_rn never allows.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mov.b64 c, {%6, %7};\n fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 // Per-half max of |a|, |b| (NaN ignored unless both are NaN); the sign bits of
 // the result are the XOR of the inputs' and carry no meaning here.
 __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
