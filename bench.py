@@ -9,10 +9,12 @@ of 272-byte rows, 1% pad slots. One step = one store of the whole batch.
   roofline   algorithmic bytes (8 B slot per token + 1024 B read and 272 B
              written per valid token) / mean kernel time, against the measured
              HBM copy bandwidth; traffic from the committed ncu summary
-  e2e        the same metric through the public API from pinned host buffers:
-             each step copies the latent and slots in and the cache back out;
-             step k's download overlaps step k+1's upload (two streams,
-             double-buffered device buffers)
+  e2e        the same metric through the public API with pinned HOST
+             buffers: each step's store reads the latent rows and slots from
+             host memory and writes its rows into a host cache over the
+             host-device link; beside it (copy_engines) the same steps with
+             the latent and slots copied in and the whole cache copied out,
+             step k's download overlapping step k+1's upload
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
   paths      the other hot-path rows measured in the same run: the
              RMSNorm-fused store on the same batch, the V4.1 RoPE inserts
@@ -514,12 +516,32 @@ def run_ours(args):
         clocks = sampler.summary(t_wall0, t_wall1)
     gpu_launches = args.steps
 
-    # end to end: every step copies its whole pinned host source and slots in
-    # and the whole cache back out. Device buffers are doubled so that step
-    # k's download (on a second stream, the other copy direction) overlaps
-    # step k + 1's upload and store; a store waits until the download of the
-    # cache it is about to rewrite has finished.
+    # end to end, through the same call with HOST buffers: each step's store
+    # reads the latent rows and slots from pinned host memory and writes its
+    # rows into a pinned host cache over the host-device link (NVLink-C2C);
+    # the C ABI takes any memory the device addresses. Over the link per
+    # step: 8 B per slot and 1024 B per valid row in, 272 B per valid row out.
     e2e_steps = max(1, min(args.steps, 10))
+    lat_hv = lat_h.view(torch.bfloat16)[:, :512]
+    kvq.mxfp4_mla_store(lat_hv, slots_h, cache_h)  # one untimed pass
+    torch.cuda.synchronize()
+    barrier(dist)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        kvq.mxfp4_mla_store(lat_hv, slots_h, cache_h)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, a.elapsed_time(b))
+    h2d = 8 * N_TOKENS + 1024 * valid
+    d2h = ROW * valid
+
+    # the same, with copy engines instead: every step copies its whole pinned
+    # host source and slots in and the whole cache back out. Device buffers
+    # are doubled so that step k's download (on a second stream, the other
+    # copy direction) overlaps step k + 1's upload and store; a store waits
+    # until the download of the cache it is about to rewrite has finished.
     torch.cuda.synchronize()
     lat_e = [torch.empty_like(lat_h, device=dev) for _ in range(2)]
     slots_e = [torch.empty_like(slots_h, device=dev) for _ in range(2)]
@@ -528,8 +550,6 @@ def run_ours(args):
     downloaded = [None, None]
     torch.cuda.synchronize()
     barrier(dist)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for k in range(e2e_steps):
         i = k % 2
@@ -548,9 +568,9 @@ def run_ours(args):
     stream.wait_stream(d2h_stream)
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(dist, a.elapsed_time(b))
-    h2d = lat_h.numel() * 2 + slots_h.numel() * 8
-    d2h = cache_h.numel()
+    copy_ms = max_over_ranks(dist, a.elapsed_time(b))
+    copy_h2d = lat_h.numel() * 2 + slots_h.numel() * 8
+    copy_d2h = cache_h.numel()
     del lat_e, slots_e, cache_e
 
     paths = secondary_paths(torch, kvq, dev, peak, (lat_d, slots_d, cache_d, valid)) \
@@ -581,7 +601,13 @@ def run_ours(args):
                      "peak_source": peak_src, "traffic_note": traffic_note},
         "cpu_baseline": cpu,
         "e2e": {"value": world * N_TOKENS * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "mode": "host buffers: the store reads pinned host latent rows and slots and "
+                        "writes rows into a pinned host cache over NVLink-C2C",
+                "copy_engines": {
+                    "value": world * N_TOKENS * e2e_steps / (copy_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": copy_h2d, "d2h_bytes_per_step": copy_d2h,
+                    "mode": "whole source copied in, whole cache copied out, overlapped"}},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "paths": paths,

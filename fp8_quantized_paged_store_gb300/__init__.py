@@ -4,7 +4,9 @@ Python binding of the C ABI in include/kvq.h. Every function here only
 marshals torch tensors into pointers, sizes and the current CUDA stream and
 calls the same-named entry point of libkvq.so; all work runs in the CUDA
 kernels. There is no fallback: if the library is not built, importing the
-functions works but every call raises.
+functions works but every call raises. Tensors are CUDA tensors, or pinned
+CPU tensors that the device addresses at the same pointer (the kernels then
+read and write host memory over the host-device link, with no copies).
 
   mxfp4_mla_store            quantize bf16 latent rows to 272-byte MXFP4 rows
   mxfp4_mla_rmsnorm_store    RMSNorm (bf16 weight, eps) then the MXFP4 store, one pass
@@ -22,7 +24,7 @@ __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp
            "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
            "save_ring_rows", "fused_save_compress_norm",
            "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "row_bytes",
-           "cache_view", "KvqError", "lib",
+           "cache_view", "KvqError", "lib", "KVQ_PTR_DEVICE", "KVQ_PTR_HOST_MAPPED",
            "LIBRARY_PATH"]
 
 LIBRARY_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
@@ -51,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.kvq_strerror.argtypes = [ctypes.c_int]
         L.kvq_row_bytes.restype = _i64
         L.kvq_row_bytes.argtypes = [_i64, _i64]
+        L.kvq_pointer_kind.restype = ctypes.c_int
+        L.kvq_pointer_kind.argtypes = [_p]
         L.mxfp4_mla_store.restype = ctypes.c_int
         L.mxfp4_mla_store.argtypes = [_p, _i64, _i64, _i64, _p, _p, _i64, _i64, _i64, _i32, _p]
         L.mxfp4_mla_rmsnorm_store.restype = ctypes.c_int
@@ -92,9 +96,27 @@ def _check(name, status):
         raise KvqError(name, status)
 
 
+KVQ_PTR_DEVICE, KVQ_PTR_HOST_MAPPED = 1, 2
+
+
+def _host_mapped(t: torch.Tensor) -> bool:
+    """A CPU tensor in page-locked memory that the device addresses at the
+    same pointer (the library checks; pageable memory never qualifies)."""
+    try:
+        pinned = t.is_pinned()
+    except RuntimeError:
+        return False
+    if not pinned or t.numel() == 0:
+        return False
+    return lib().kvq_pointer_kind(t.data_ptr()) == KVQ_PTR_HOST_MAPPED
+
+
 def _need(t: torch.Tensor, dtype, what):
-    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda:
-        raise TypeError(f"{what} must be a CUDA {dtype} tensor")
+    """A CUDA tensor of `dtype`, or a pinned CPU one the device addresses."""
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or \
+            not (t.is_cuda or (t.device.type == "cpu" and _host_mapped(t))):
+        raise TypeError(f"{what} must be a CUDA {dtype} tensor, or a pinned CPU one mapped "
+                        f"into the device's address space")
 
 
 def row_bytes(latent_dim: int = 512, group: int = 32) -> int:
@@ -226,8 +248,9 @@ def rope_plain_insert(latent, positions, cos_sin, kv_cache, slot_mapping, compre
         fp8, scale = 1, float(fp8_scale)
     else:
         raise TypeError(f"kv_cache must be bfloat16 or float8_e4m3fn, got {kv_cache.dtype}")
-    if not kv_cache.is_cuda:
-        raise ValueError("kv_cache must be a CUDA tensor")
+    if not (kv_cache.is_cuda or (kv_cache.device.type == "cpu" and _host_mapped(kv_cache))):
+        raise TypeError("kv_cache must be a CUDA tensor, or a pinned CPU one mapped into the "
+                        "device's address space")
     if kv_cache.dim() != 3 or kv_cache.shape[2] != 512 or kv_cache.stride(2) != 1:
         raise ValueError("kv_cache must be [pages, cache_block, 512] with unit last stride")
     _check("rope_plain_insert", lib().rope_plain_insert(
@@ -326,7 +349,7 @@ def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: to
     nb, bs, bsr = cache_view(cache, row_bytes(latent_dim, 32))
     if out is None:
         out = torch.empty((*indices.shape, latent_dim), dtype=torch.bfloat16,
-                          device=indices.device)
+                          device=indices.device, pin_memory=not indices.is_cuda)
     _need(out, torch.bfloat16, "out")
     flat = out.view(-1, latent_dim) if out.is_contiguous() else out.reshape(-1, latent_dim)
     if flat.data_ptr() != out.data_ptr() or flat.stride(1) != 1:
@@ -354,7 +377,8 @@ def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: to
         raise ValueError("indices must be a contiguous [num_queries, topk] tensor")
     nb, bs, bsr = cache_view(cache, row_bytes(512, 32))
     if out is None:
-        out = torch.empty((nq, nh, 512), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((nq, nh, 512), dtype=torch.bfloat16, device=q.device,
+                          pin_memory=not q.is_cuda)
     _need(out, torch.bfloat16, "out")
     if out.dim() != 3 or tuple(out.shape) != (nq, nh, 512) or out.stride(2) != 1:
         raise ValueError("out must be [num_queries, num_heads, 512] with unit last stride")

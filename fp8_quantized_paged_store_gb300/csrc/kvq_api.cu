@@ -1,6 +1,8 @@
 // kvq_api.cu — the small host-only entry points of the C ABI.
 #include <cstdint>
 
+#include <cuda_runtime.h>
+
 #include "kvq.h"
 
 extern "C" const char* kvq_strerror(int status) {
@@ -21,4 +23,30 @@ extern "C" const char* kvq_strerror(int status) {
 extern "C" int64_t kvq_row_bytes(int64_t latent_dim, int64_t group) {
   if (latent_dim <= 0 || group <= 0 || group % 2 != 0 || latent_dim % group != 0) return -1;
   return latent_dim / 2 + latent_dim / group;
+}
+
+// Where `ptr` lives, as far as a kernel launched on the current device can
+// reach it under that same address.
+extern "C" int kvq_pointer_kind(const void* ptr) {
+  if (ptr == nullptr) return KVQ_EINVAL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ECUDA;
+  }
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ECUDA;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      return a.device == dev ? KVQ_PTR_DEVICE : KVQ_PTR_UNADDRESSABLE;
+    case cudaMemoryTypeManaged:
+      return KVQ_PTR_DEVICE;
+    case cudaMemoryTypeHost:
+      return a.devicePointer == ptr ? KVQ_PTR_HOST_MAPPED : KVQ_PTR_UNADDRESSABLE;
+    default:
+      return KVQ_PTR_UNADDRESSABLE;
+  }
 }

@@ -23,6 +23,12 @@
  *     any memory the GPU can address). The library allocates nothing, keeps
  *     no pointer past the call, and never synchronises: work is enqueued on
  *     `stream` (0 = the legacy default stream) and the call returns.
+ *     Page-locked host memory that the device addresses under the same
+ *     pointer (cudaHostAlloc / cudaMallocHost under unified addressing;
+ *     kvq_pointer_kind() tells) is such memory: the kernels then read their
+ *     inputs from, and write their rows into, host memory over the
+ *     host-device link (NVLink-C2C on a GB300 node), with no copy before or
+ *     after the call; the call is then bound by the link's bandwidth.
  *   - bf16 data is passed as raw 16-bit patterns (`const void*`).
  *   - Status: 0 (KVQ_OK) on success; KVQ_EINVAL (-1) when an argument is
  *     rejected before anything is launched (nothing is written); KVQ_ECUDA
@@ -64,6 +70,22 @@ const char* kvq_strerror(int status);
  * kvq_row_bytes(512, 32) == 272. Returns -1 unless latent_dim > 0,
  * group > 0, group even and latent_dim a multiple of group. */
 int64_t kvq_row_bytes(int64_t latent_dim, int64_t group);
+
+#define KVQ_PTR_UNADDRESSABLE 0
+#define KVQ_PTR_DEVICE 1
+#define KVQ_PTR_HOST_MAPPED 2
+
+/* Where `ptr` lives, for a kernel launched on the current device under that
+ * same address (a helper of this library; the pages have no counterpart):
+ *   KVQ_PTR_DEVICE          memory of the current device, or managed memory;
+ *   KVQ_PTR_HOST_MAPPED     page-locked host memory mapped into the device's
+ *                           address space at the same address;
+ *   KVQ_PTR_UNADDRESSABLE   anything else (pageable host memory, another
+ *                           device's memory, host memory registered at a
+ *                           different device address): not to be passed;
+ *   KVQ_EINVAL for a null pointer, KVQ_ECUDA when the CUDA runtime cannot
+ *   answer (no device). Host-only: launches nothing, never synchronises. */
+int kvq_pointer_kind(const void* ptr);
 
 /*
  * mxfp4_mla_store — quantize MLA latent rows to MXFP4 and scatter them into a

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(L):
     names = declared_functions()
-    assert set(names) == {"kvq_strerror", "kvq_row_bytes", "mxfp4_mla_store",
+    assert set(names) == {"kvq_strerror", "kvq_row_bytes", "kvq_pointer_kind", "mxfp4_mla_store",
                           "mxfp4_mla_rmsnorm_store",
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
                           "rope_quant_insert_v4", "rope_plain_insert", "save_ring_rows",
@@ -195,3 +195,16 @@ def test_binding_has_the_abi_names():
               "save_ring_rows", "fused_save_compress_norm", "mxfp4_mla_gather_dequant",
               "mxfp4_mla_sparse_attention"):
         assert callable(getattr(kvq, n))
+
+
+def test_binding_refuses_pageable_host_tensors():
+    """A CPU tensor reaches the library only when it is pinned and mapped at
+    the same device address; a pageable one is refused before any call."""
+    import torch
+    lat = torch.zeros((4, 512), dtype=torch.bfloat16)
+    slots = torch.zeros(4, dtype=torch.int64)
+    cache = torch.zeros(8 * 272, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        kvq.mxfp4_mla_store(lat, slots, cache)
+    with pytest.raises(TypeError):
+        kvq.mxfp4_mla_gather_dequant(cache, slots)

@@ -1,0 +1,98 @@
+"""Entry points on pinned HOST buffers: the kernels read their inputs from,
+and write their rows into, page-locked host memory that the device addresses
+at the same pointer, with no copy before or after the call. Compared byte for
+byte with the CPU oracle (store) or with the same call on device buffers."""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import fp8_quantized_paged_store_gb300 as kvq
+import oracle
+import workloads
+from tests import _gpu as G
+
+pytestmark = pytest.mark.gpu
+ROW = 272
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    __graft_entry__.build()
+
+
+def _pinned(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+
+def test_pointer_kind():
+    L = kvq.lib()
+    d = torch.zeros(64, device=G.DEV)
+    h = torch.zeros(64).pin_memory()
+    pageable = torch.zeros(64)
+    assert L.kvq_pointer_kind(d.data_ptr()) == kvq.KVQ_PTR_DEVICE
+    assert L.kvq_pointer_kind(d[17:].data_ptr()) == kvq.KVQ_PTR_DEVICE
+    assert L.kvq_pointer_kind(h.data_ptr()) == kvq.KVQ_PTR_HOST_MAPPED
+    assert L.kvq_pointer_kind(h[17:].data_ptr()) == kvq.KVQ_PTR_HOST_MAPPED
+    assert L.kvq_pointer_kind(pageable.data_ptr()) == 0
+    assert L.kvq_pointer_kind(None) == kvq.KVQ_EINVAL
+
+
+def test_pageable_host_tensor_is_refused():
+    lat = torch.zeros((4, 512), dtype=torch.bfloat16)
+    slots = torch.zeros(4, dtype=torch.int64, device=G.DEV)
+    cache = torch.zeros(8 * ROW, dtype=torch.uint8, device=G.DEV)
+    with pytest.raises(TypeError):
+        kvq.mxfp4_mla_store(lat, slots, cache)
+
+
+@pytest.mark.parametrize("where", ["all_host", "host_inputs", "host_cache"])
+def test_store_paged_on_host_buffers(where):
+    """The paged workload (16,384 tokens, block stride 192 rows with other
+    layers' rows poisoned, 5% pads): latent, slots and cache on the host in
+    any mix with the device."""
+    w = workloads.store_paged(seed=7)
+    nb, bs, bsr, off = w["num_blocks"], w["block_size"], w["block_stride_rows"], w["cache_offset"]
+    want = w["cache"].copy()
+    oracle.mxfp4_mla_store(w["latent"], w["slot_mapping"], want, nb, bs, bsr, cache_offset=off)
+    host_in = where in ("all_host", "host_inputs")
+    host_out = where in ("all_host", "host_cache")
+    lat = (_pinned(w["latent"].view(np.int16)) if host_in
+           else G.to_dev(w["latent"].view(np.int16))).view(torch.bfloat16)
+    slots = _pinned(w["slot_mapping"]) if host_in else G.to_dev(w["slot_mapping"])
+    buf = _pinned(w["cache"]) if host_out else G.to_dev(w["cache"])
+    view = buf[off:].as_strided((nb, bs, ROW), (bsr * ROW, ROW, 1))
+    kvq.mxfp4_mla_store(lat, slots, view)
+    torch.cuda.synchronize()
+    got = buf.numpy() if host_out else buf.cpu().numpy()
+    assert G.first_diff(got, want) is None, G.first_diff(got, want)
+
+
+def test_store_strided_latent_from_host():
+    """200,000 tokens read through a 576-element row stride from pinned host
+    memory into a pinned host cache of 400,000 slots (1% pads)."""
+    lat_full = workloads.store_large_latent(seed=3, num_tokens=200_000, row_stride=576)
+    slots = workloads.store_large_slots(seed=3, num_tokens=200_000, num_slots=400_000)
+    want = np.full(400_000 * ROW, 0xAA, dtype=np.uint8)
+    oracle.mxfp4_mla_store(lat_full[:, :512], slots, want, 1, 400_000, 400_000,
+                           threads=oracle.default_threads())
+    lat_h = _pinned(lat_full.view(np.int16)).view(torch.bfloat16)[:, :512]
+    cache_h = _pinned(np.full(400_000 * ROW, 0xAA, dtype=np.uint8))
+    kvq.mxfp4_mla_store(lat_h, _pinned(slots), cache_h)
+    torch.cuda.synchronize()
+    assert G.first_diff(cache_h.numpy(), want) is None, G.first_diff(cache_h.numpy(), want)
+
+
+def test_gather_into_host_output():
+    """The gather reads a device cache and writes its bf16 rows into pinned
+    host memory; the indices come from the host too. Same bits as the gather
+    into device memory."""
+    w = workloads.gather(seed=2, num_slots=65_536, num_queries=16, topk=512)
+    cache = torch.zeros(65_536 * ROW, dtype=torch.uint8, device=G.DEV)
+    kvq.mxfp4_mla_store(G.bf16_dev(w["fill_latent"]), G.to_dev(w["fill_slots"]), cache)
+    idx_d = G.to_dev(w["indices"])
+    dev_out = kvq.mxfp4_mla_gather_dequant(cache, idx_d)
+    host_out = kvq.mxfp4_mla_gather_dequant(cache, _pinned(w["indices"]))
+    torch.cuda.synchronize()
+    assert not host_out.is_cuda and host_out.is_pinned()
+    assert torch.equal(host_out.view(torch.int16), dev_out.view(torch.int16).cpu())
