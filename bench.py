@@ -288,12 +288,13 @@ def run_reference(args):
     slots = workloads.store_large_slots(seed=0)[:per_step].copy()
     valid = int(np.sum(slots >= 0))
     cache = np.full(N_SLOTS * ROW, 0xAA, dtype=np.uint8)
-    for _ in range(args.warmup):
-        oracle.mxfp4_mla_store(lat[:, :512], slots, cache, 1, N_SLOTS, N_SLOTS)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.mxfp4_mla_store(lat[:, :512], slots, cache, 1, N_SLOTS, N_SLOTS)
-    dt = time.perf_counter() - t0
+    with OneCore() as pin:
+        for _ in range(args.warmup):
+            oracle.mxfp4_mla_store(lat[:, :512], slots, cache, 1, N_SLOTS, N_SLOTS)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.mxfp4_mla_store(lat[:, :512], slots, cache, 1, N_SLOTS, N_SLOTS)
+        dt = time.perf_counter() - t0
     value = per_step * args.steps / dt
     cores = 1
     sample = (f"{per_step} tokens of the 4.3M-token workload per step (same generator, "
@@ -308,7 +309,7 @@ def run_reference(args):
                        "group": 32, "sample_tokens_per_step": per_step},
             "gbs": (rd + wr) * args.steps / dt / 1e9,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "host": oracle_host(pin.core)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -317,6 +318,48 @@ def run_reference(args):
 
 # ------------------------------------------------------------------- ours ---
 
+def host_cpu():
+    """(logical CPUs, CPU identification from /proc/cpuinfo) of this host."""
+    n = os.cpu_count() or 0
+    ident = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k = k.strip().lower()
+                if k in ("model name", "cpu implementer", "cpu part") and k not in ident:
+                    ident[k] = v.strip()
+    except OSError:
+        pass
+    if "model name" in ident:
+        return n, ident["model name"]
+    return n, " ".join(f"{k} {v}" for k, v in ident.items()) or "unknown"
+
+
+class OneCore:
+    """The calling thread pinned to one CPU (the lowest it may run on) for the
+    duration of the block; the previous affinity is restored afterwards."""
+
+    def __enter__(self):
+        self.old, self.core = None, None
+        if hasattr(os, "sched_getaffinity"):
+            self.old = os.sched_getaffinity(0)
+            self.core = min(self.old)
+            os.sched_setaffinity(0, {self.core})
+        return self
+
+    def __exit__(self, *exc):
+        if self.old is not None:
+            os.sched_setaffinity(0, self.old)
+        return False
+
+
+def oracle_host(core):
+    n, ident = host_cpu()
+    return f"1 core of {n} ({ident}), pinned to CPU {core}" if core is not None else \
+        f"1 core of {n} ({ident})"
+
+
 def cpu_baseline_sample(lat_host, slots_host, seconds=10.0):
     """Oracle (single thread, as it stands) on consecutive 50,000-token chunks
     of the same host inputs until ~`seconds` of CPU work."""
@@ -324,16 +367,36 @@ def cpu_baseline_sample(lat_host, slots_host, seconds=10.0):
     oracle.lib()
     chunk = 50_000
     cache = np.full(N_SLOTS * ROW, 0xAA, dtype=np.uint8)
-    done, t0 = 0, time.perf_counter()
-    while done < lat_host.shape[0] and time.perf_counter() - t0 < seconds:
-        n = min(chunk, lat_host.shape[0] - done)
-        oracle.mxfp4_mla_store(lat_host[done:done + n, :512], slots_host[done:done + n], cache,
-                               1, N_SLOTS, N_SLOTS)
-        done += n
-    dt = time.perf_counter() - t0
+    with OneCore() as pin:
+        done, t0 = 0, time.perf_counter()
+        while done < lat_host.shape[0] and time.perf_counter() - t0 < seconds:
+            n = min(chunk, lat_host.shape[0] - done)
+            oracle.mxfp4_mla_store(lat_host[done:done + n, :512], slots_host[done:done + n],
+                                   cache, 1, N_SLOTS, N_SLOTS)
+            done += n
+        dt = time.perf_counter() - t0
     return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"first {done} tokens of the same 4.3M-token workload ({dt:.1f} s, "
-                      f"single thread)"}
+                      f"single thread)", "host": oracle_host(pin.core)}
+
+
+def live_copy_gbs(torch, src, stream, reps=5):
+    """Device-to-device copy (cudaMemcpyAsync) of `src` into a fresh buffer:
+    read + write bytes over the best of `reps` CUDA-event times, in GB/s."""
+    dst = torch.empty_like(src)
+    for _ in range(2):
+        dst.copy_(src)
+    best = float("inf")
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src)
+        b.record(stream)
+        b.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del dst
+    return 2 * src.numel() * src.element_size() / (best * 1e-3) / 1e9
 
 
 def time_events(torch, fn, reps, stream, flush=None):
@@ -477,7 +540,8 @@ def run_ours(args):
     slots_h = torch.from_numpy(slots_np).pin_memory()
     cache_h = torch.empty(N_SLOTS * ROW, dtype=torch.uint8).pin_memory()
 
-    lat_d = lat_h.to(dev).view(torch.bfloat16)[:, :512]
+    lat_full_d = lat_h.to(dev)
+    lat_d = lat_full_d.view(torch.bfloat16)[:, :512]
     slots_d = slots_h.to(dev)
     cache_d = torch.full((N_SLOTS * ROW,), 0xAA, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -515,6 +579,8 @@ def run_ours(args):
         sampler.stop()
         clocks = sampler.summary(t_wall0, t_wall1)
     gpu_launches = args.steps
+
+    copy_gbs = live_copy_gbs(torch, lat_full_d, stream)  # this rank's GPU
 
     # end to end, through the same call with HOST buffers: each step's store
     # reads the latent rows and slots from pinned host memory and writes its
@@ -598,7 +664,10 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": rd + wr,
-                     "peak_source": peak_src, "traffic_note": traffic_note},
+                     "peak_source": peak_src, "traffic_note": traffic_note,
+                     "live_copy_gbs": copy_gbs, "frac_of_live_copy": achieved / copy_gbs,
+                     "live_copy": "device-to-device cudaMemcpyAsync of the 4.95 GB source in "
+                                  "the same run (read + write bytes, best of 5)"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * N_TOKENS * e2e_steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
