@@ -136,6 +136,8 @@ MUTANTS = [
     ("fscn_weight_dropped", "latent = pooled * r[:, None] * w[None, :]",
      "latent = pooled * r[:, None]",
      "test_oracle_pins_compress.py::test_cr1_weight_and_alternating_signs", "compress.py"),
+    ("fscn_chunk_start_not_cut", "qs_t = np.maximum(qsl[r_safe], 0)", "qs_t = qsl[r_safe]",
+     "test_oracle_pins_compress.py::test_cr2_chunk_bounds_are_cut_to_the_batch", "compress.py"),
 ]
 
 
