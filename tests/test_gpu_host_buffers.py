@@ -96,3 +96,62 @@ def test_gather_into_host_output():
     torch.cuda.synchronize()
     assert not host_out.is_cuda and host_out.is_pinned()
     assert torch.equal(host_out.view(torch.int16), dev_out.view(torch.int16).cpu())
+
+
+@pytest.mark.parametrize("record", ["mxfp8", "nvfp4"])
+def test_rope_insert_on_host_buffers(record):
+    """A V4.1 insert (65,536 tokens, R = 4, 0.05% NaN) with the latent,
+    positions, cos/sin table, slots and paged cache all in pinned host
+    memory: byte for byte the oracle's cache."""
+    fo, fk, width = {"mxfp8": (oracle.rope_quant_insert_mxfp8, kvq.rope_quant_insert_mxfp8, 528),
+                     "nvfp4": (oracle.rope_quant_insert_nvfp4, kvq.rope_quant_insert_nvfp4,
+                               288)}[record]
+    w = workloads.rope_insert(seed=11, record=record)
+    np_, cb = w["num_pages"], w["cache_block"]
+    want = w["cache"].copy()
+    fo(w["latent"], w["positions"], w["cos_sin"], want, w["cache_slots"], np_, cb, cb * width,
+       w["compress_ratio"], False)
+    cache_h = _pinned(w["cache"])
+    view = cache_h.as_strided((np_, cb, width), (cb * width, width, 1))
+    fk(_pinned(w["latent"].view(np.int16)).view(torch.bfloat16), _pinned(w["positions"]),
+       _pinned(w["cos_sin"]), view, _pinned(w["cache_slots"]), w["compress_ratio"])
+    torch.cuda.synchronize()
+    assert G.first_diff(cache_h.numpy(), want) is None, G.first_diff(cache_h.numpy(), want)
+
+
+def test_ring_rows_into_host_state():
+    """save_ring_rows from pinned host rows into a pinned host ring state:
+    bit copies, pads skipped, the rest of the state untouched."""
+    w = workloads.ring_rows(seed=5, num_rows=4096, num_blocks=64, state_block=128)
+    want = w["state"].copy()
+    nb, sb = want.shape[0], want.shape[1]
+    oracle.save_ring_rows(w["rows"], w["slot_mapping"], want, nb, sb, sb * 1024, 1024)
+    state_h = _pinned(w["state"])
+    kvq.save_ring_rows(_pinned(w["rows"]), _pinned(w["slot_mapping"]), state_h)
+    torch.cuda.synchronize()
+    assert np.array_equal(state_h.numpy().view(np.uint32), want.view(np.uint32))
+
+
+def test_attention_query_and_output_on_host():
+    """Sparse attention with the queries read from and the output and lse
+    written to pinned host memory (packed cache and indices on the device):
+    the same bits as with every buffer on the device."""
+    w = workloads.sparse_attention(seed=3, num_queries=8, num_heads=128, topk=256,
+                                   num_slots=16_384)
+    cache = torch.zeros(16_384 * ROW, dtype=torch.uint8, device=G.DEV)
+    kvq.mxfp4_mla_store(G.bf16_dev(w["fill_latent"]), G.to_dev(w["fill_slots"]), cache)
+    idx = G.to_dev(w["indices"])
+    q_np = w["q"].reshape(8, 128, 512)
+    status = torch.zeros(1, dtype=torch.int32, device=G.DEV)
+    lse_d = torch.empty((8, 128), dtype=torch.float32, device=G.DEV)
+    out_d, _ = kvq.mxfp4_mla_sparse_attention(G.bf16_dev(q_np), cache, idx, w["sm_scale"],
+                                              lse=lse_d, status=status)
+    q_h = _pinned(q_np.view(np.int16)).view(torch.bfloat16)
+    lse_h = torch.empty((8, 128), dtype=torch.float32).pin_memory()
+    out_h, _ = kvq.mxfp4_mla_sparse_attention(q_h, cache, idx, w["sm_scale"], lse=lse_h,
+                                              status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "a kernel wait timed out"
+    assert not out_h.is_cuda
+    assert torch.equal(out_h.view(torch.int16), out_d.view(torch.int16).cpu())
+    assert torch.equal(lse_h, lse_d.cpu())
