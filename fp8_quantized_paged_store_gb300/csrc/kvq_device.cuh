@@ -35,6 +35,16 @@ __device__ __forceinline__ uint4 ld_once_v4(const void* p) {
   return r;
 }
 
+// Read-only 16-byte load that allocates in L1: for sectors that the next
+// load of the same warp touches again.
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ int64_t ld_once_i64(const int64_t* p) {
   int64_t r;
   asm("ld.global.nc.L1::no_allocate.s64 %0, [%1];" : "=l"(r) : "l"(p));
