@@ -20,27 +20,30 @@
 // quantized: with two writers in flight per warp and 40 warps per SM, loads
 // stay in flight while other warps compute (a shared-memory cp.async ring
 // measured slower here, the gate and ballot work per window then sitting on
-// the critical path). A row is held as lane l: elements 8l..8l+7 (half 0) and
-// 256+8l..256+8l+7 (half 1), each 16-byte load of the warp covering 512
-// contiguous bytes. Rotary pairs 224..255 are elements 448..511.
+// the critical path). Rotary pairs 224..255 are elements 448..511.
 //
-// MXFP8, V4 and plain rows: the rotary elements are half 1 of lanes 24..31,
-// which alone read the table row (lane l: cos and sin 4(l-24)..4(l-24)+3, two
-// 16-byte loads). A V4 tile of 64 is eight lanes' halves, so its amax takes
-// three xor-shuffles; lanes 24..31 write their rotated half 1 as bf16.
+// The records (MXFP8, NVFP4, V4): lane l < 28 holds a run of 16 NoPE
+// elements, 16l..16l+15 (two 16-byte loads at bytes 32l and 32l+16; the
+// second hits the sectors the first brought into L1), and every lane j
+// rotates rotary pair j with its own cos and sin (4 bytes of the row, one
+// cos and one sin). An NVFP4 tile is one lane's run (no amax shuffle), an
+// MXFP8 tile of 32 two (one shuffle), a V4 tile of 64 four (two); a run's
+// E4M3 values leave in one 16-byte store, its E2M1 codes in one 8-byte
+// store. Against holding elements 8l..8l+7 and 256+8l..256+8l+7 (two
+// half-row passes, every tile shared by more lanes) this measured 0.345 ->
+// 0.310 ms (NVFP4), 0.351 -> 0.329 ms (MXFP8) and 0.379 -> 0.375 ms (V4) on
+// 4,194,304 tokens, and removed the spills those kernels had at 48
+// registers. The rotary values are spread over the whole warp: the NVFP4
+// exact quotients, the MXFP8 tiles 14 and 15 (16 lanes each) and the V4 bf16
+// values all run one pair per lane. The 448 NVFP4 NoPE values are bf16
+// numbers and take the cheaper exact code rule of nvfp4_code_value2 (two
+// fused products, no ALU work).
 //
-// NVFP4: lane l < 28 holds one whole NoPE tile, elements 16l..16l+15 (two
-// 16-byte loads at bytes 32l and 32l+16; the second hits the sectors the
-// first brought into L1), so its amax needs no shuffle, one scale is computed
-// per tile rather than once by each of two lanes, and its eight code bytes
-// leave in one store. Every lane j also loads rotary pair j (4 bytes) with
-// its own cos and sin, so the rotation and the exact quotient of the 64
-// rotated values are spread over the whole warp instead of 4 lanes. The 448
-// NoPE values are bf16 numbers and take the cheaper exact code rule of
-// nvfp4_code_value2 (two fused products, no ALU work). Against a lane pair
-// per tile (8 values each, two half-row passes) this measured 0.345 ->
-// 0.310 ms on 4,194,304 tokens, without the spills the pair version had at
-// 48 registers.
+// Plain rows keep the half-row mapping: lane l holds elements 8l..8l+7
+// (half 0) and 256+8l..256+8l+7 (half 1), each 16-byte load of the warp
+// covering 512 contiguous bytes; the rotary elements are half 1 of lanes
+// 24..31, which alone read the table row (cos and sin 4(l-24)..4(l-24)+3,
+// two 16-byte loads each).
 //
 // The pages evaluate the rotation formula on all 256 pairs, with cos 1 and
 // sin 0 outside the rotary range. There it is the identity except for NaN,
@@ -82,8 +85,8 @@ struct RopeParams {
   float fp8_scale;      // plain fp8 rows: the per-tensor scale
 };
 
-// Layouts written by fp8_family_insert_kernel (the MXFP8 record and the ones
-// that share its structure).
+// E4M3-family layouts: the MXFP8 and V4 records (record_run_insert_kernel)
+// and the plain rows (fp8_family_insert_kernel).
 enum class Layout { kMxfp8, kV4, kPlainBf16, kPlainFp8 };
 constexpr int kV4Record = 584;   // 576 value bytes (448 E4M3 + 64 bf16) + 8 scale bytes
 
@@ -108,55 +111,6 @@ __device__ __forceinline__ void widen8(uint4 w, float f[8]) {
   f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
 }
 
-// Rotated (or identity) binary32 values of the lane's two halves. With
-// kZeroNan, NaN results become +0.0 (the sanitising step): on NoPE words by a
-// bf16x2 mask (the NoPE formula's result is already exact in bf16), on the
-// rotary values by a binary32 select.
-template <bool kZeroNan>
-__device__ __forceinline__ void rotate_row(uint4 x0, uint4 x1, float4 c, float4 s, int lane,
-                                           float f0[8], float f1[8]) {
-  auto nope = [](uint32_t w) {
-    const uint32_t r = nope_pair(w);
-    return kZeroNan ? (r & bf16x2_number_mask(r)) : r;
-  };
-  x0.x = nope(x0.x);
-  x0.y = nope(x0.y);
-  x0.z = nope(x0.z);
-  x0.w = nope(x0.w);
-  widen8(x0, f0);
-  if (lane < 24) {
-    x1.x = nope(x1.x);
-    x1.y = nope(x1.y);
-    x1.z = nope(x1.z);
-    x1.w = nope(x1.w);
-    widen8(x1, f1);
-  } else {
-    float v[8];
-    widen8(x1, v);
-    const float cc[4] = {c.x, c.y, c.z, c.w};
-    const float ss[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float e = v[2 * k], o = v[2 * k + 1];
-      float re = __fsub_rn(__fmul_rn(e, cc[k]), __fmul_rn(o, ss[k]));
-      float ro = __fadd_rn(__fmul_rn(o, cc[k]), __fmul_rn(e, ss[k]));
-      if (kZeroNan) {
-        re = (re == re) ? re : 0.0f;
-        ro = (ro == ro) ? ro : 0.0f;
-      }
-      f1[2 * k] = re;
-      f1[2 * k + 1] = ro;
-    }
-  }
-}
-
-__device__ __forceinline__ float abs_max8(const float f[8]) {
-  float m = 0.0f;  // fmaxf ignores NaN
-#pragma unroll
-  for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
-  return m;
-}
-
 // ------------------------------------------------------------------ MXFP8 ---
 
 // Eight values times the power of two `inv` as E4M3 (clamped to +-448,
@@ -171,53 +125,7 @@ __device__ __forceinline__ uint2 e4m3x8_scaled(const float f[8], float inv) {
 }
 
 
-template <bool kSanitize>
-__device__ __forceinline__ void mxfp8_half(const float f[8], uint8_t* values, uint8_t* scales,
-                                           int lane) {
-  float amax = abs_max8(f);
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-  amax = fmaxf(amax, 1e-4f);
-  const int e = ceil_pow2_exponent(__fmul_rn(amax, 1.0f / 448.0f));  // -22..128
-  const float inv = exp2_neg(e);
-  // clamp to +-448 and E4M3 rounding are exactly cvt.rn.satfinite; NaN -> 0x7F
-  const uint2 ab = e4m3x8_scaled(f, inv);
-  const uint32_t a = ab.x, b = ab.y;
-  st_v2(values + 8 * lane, a, b);
-  if ((lane & 3) == 0) {
-    const int cap = kSanitize ? 254 : 255;
-    const int enc = e + 127;  // >= 105
-    st_u8(scales + (lane >> 2), (uint32_t)(enc < cap ? enc : cap));
-  }
-}
-
 // ------------------------------------------------------------ V4 and plain ---
-
-// V4 record, one NoPE half of the row held by this lane (8 values): tiles of
-// 64 values span eight lanes (tile = lane / 8, plus 4 for half 1), each under
-// the MXFP8 scale rule; lanes with `store` false (the rotary lanes of half 1)
-// take part in the shuffles only.
-template <bool kSanitize>
-__device__ __forceinline__ void v4_nope_half(const float f[8], uint8_t* values, uint8_t* scales,
-                                             int tile, int lane, bool store) {
-  float amax = abs_max8(f);
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-  amax = fmaxf(amax, 1e-4f);
-  const int e = ceil_pow2_exponent(__fmul_rn(amax, 1.0f / 448.0f));
-  const float inv = exp2_neg(e);
-  const uint2 ab = e4m3x8_scaled(f, inv);
-  const uint32_t a = ab.x, b = ab.y;
-  if (store) {
-    st_v2(values, a, b);
-    if ((lane & 7) == 0) {
-      const int cap = kSanitize ? 254 : 255;
-      const int enc = e + 127;
-      st_u8(scales + tile, (uint32_t)(enc < cap ? enc : cap));
-    }
-  }
-}
 
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t d;
@@ -266,22 +174,14 @@ __device__ __forceinline__ void rotate_pairs(uint4 x1, float4 c, float4 s, float
   }
 }
 
-// One writer row of a layout other than the MXFP8 record. `page` points at
-// the slot's page, `slot_in_page` is its row there.
-template <Layout kL, bool kSanitize>
-__device__ __forceinline__ void write_other(const RopeParams& p, uint4 x0, uint4 x1, float4 c,
+// One writer row of a plain layout. `page` points at the slot's page,
+// `slot_in_page` is its row there.
+template <Layout kL>
+__device__ __forceinline__ void write_plain(const RopeParams& p, uint4 x0, uint4 x1, float4 c,
                                             float4 s, uint8_t* page, int64_t slot_in_page,
                                             int lane) {
-  if constexpr (kL == Layout::kV4) {
-    float f0[8], f1[8];
-    rotate_row<kSanitize>(x0, x1, c, s, lane, f0, f1);
-    uint8_t* values = page + slot_in_page * 576;
-    uint8_t* scales = page + p.cache_block * 576 + slot_in_page * 8;
-    v4_nope_half<kSanitize>(f0, values + 8 * lane, scales, lane >> 3, lane, true);
-    v4_nope_half<kSanitize>(f1, values + 256 + 8 * lane, scales, 4 + (lane >> 3), lane, lane < 24);
-    if (lane >= 24) st_v4(values + 448 + 16 * (lane - 24), bf16x8_rn(f1));
-    if (lane == 24) st_u8(scales + 7, 0u);
-  } else if constexpr (kL == Layout::kPlainBf16) {
+  static_assert(kL == Layout::kPlainBf16 || kL == Layout::kPlainFp8, "plain rows only");
+  if constexpr (kL == Layout::kPlainBf16) {
     uint8_t* row = page + slot_in_page * p.slot_pitch;
     st_v4(row + 16 * lane, x0);
     if (lane < 24) {
@@ -509,12 +409,10 @@ __device__ __forceinline__ void token_gates(const RopeParams& p, TokenIds id, in
 
 // ---------------------------------------------------------------- kernels ---
 
-// The MXFP8 record and the layouts that share its structure (V4 record, plain
-// bf16 and fp8 rows). Five resident blocks (40 warps) per SM: the 48-register
-// cap costs a few spilled words in the MXFP8 kernel, but the extra writers in
-// flight lifted it
-// by 7 % (4,194,304-token insert: 5292 -> 5680 GB/s; six blocks at 40
-// registers lose it again).
+// The plain bf16 and fp8 rows. Five resident blocks (40 warps) per SM: the
+// 48-register cap costs a few spilled words, but the extra writers in flight
+// lifted the inserts by 7 % when measured on the MXFP8 record (4,194,304
+// tokens: 5292 -> 5680 GB/s; six blocks at 40 registers lose it again).
 template <Layout kL, bool kSanitize>
 __global__ void __launch_bounds__(kRopeThreads, 5) fp8_family_insert_kernel(RopeParams p) {
   const int lane = threadIdx.x & 31;
@@ -561,19 +459,146 @@ __global__ void __launch_bounds__(kRopeThreads, 5) fp8_family_insert_kernel(Rope
         if (i < 0) break;
         const int64_t pg = __shfl_sync(0xFFFFFFFFu, page_off, i);
         const int64_t slot_in_page = __shfl_sync(0xFFFFFFFFu, in_page, i);
-        uint8_t* page = p.cache + pg;
-        if constexpr (kL == Layout::kMxfp8) {
-          float f0[8], f1[8];
-          rotate_row<kSanitize>(w ? xb0 : xa0, w ? xb1 : xa1, w ? cb : ca, w ? snb : sna, lane,
-                                f0, f1);
-          uint8_t* values = page + slot_in_page * 512;
-          uint8_t* scales = page + p.cache_block * 512 + slot_in_page * 16;
-          mxfp8_half<kSanitize>(f0, values, scales, lane);
-          mxfp8_half<kSanitize>(f1, values + 256, scales + 8, lane);
-        } else {
-          write_other<kL, kSanitize>(p, w ? xb0 : xa0, w ? xb1 : xa1, w ? cb : ca, w ? snb : sna,
-                                     page, slot_in_page, lane);
+        write_plain<kL>(p, w ? xb0 : xa0, w ? xb1 : xa1, w ? cb : ca, w ? snb : sna,
+                        p.cache + pg, slot_in_page, lane);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void st_u16(void* p, uint32_t v) {
+  asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)v) : "memory");
+}
+
+// One writer of the MXFP8 or V4 record, one run per lane: lane l < 28 holds
+// NoPE elements 16l..16l+15 (`a`, `b`), and every lane rotates rotary pair l
+// (`xr`, with its own cos `c` and sin `sn`). An MXFP8 tile of 32 is two
+// lanes' runs (one xor-shuffle), a V4 tile of 64 four (two); the NoPE run
+// leaves as one 16-byte store. The MXFP8 rotary tiles 14 and 15 are 16 lanes
+// each (four xor-shuffles, two code bytes per lane); the V4 rotary values
+// are bf16, four bytes per lane.
+template <Layout kL, bool kSanitize>
+__device__ __forceinline__ void record_run(const RopeParams& p, uint4 a, uint4 b, uint32_t xr,
+                                           float c, float sn, uint8_t* page,
+                                           int64_t slot_in_page, int lane) {
+  constexpr int kValueBytes = kL == Layout::kV4 ? 576 : 512;
+  constexpr int kScaleBytes = kL == Layout::kV4 ? 8 : 16;
+  constexpr int kCap = kSanitize ? 254 : 255;
+  uint8_t* values = page + slot_in_page * kValueBytes;
+  uint8_t* scales = page + p.cache_block * kValueBytes + slot_in_page * kScaleBytes;
+  auto nope = [](uint32_t w) {
+    const uint32_t r = nope_pair(w);
+    return kSanitize ? (r & bf16x2_number_mask(r)) : r;
+  };
+  a.x = nope(a.x);
+  a.y = nope(a.y);
+  a.z = nope(a.z);
+  a.w = nope(a.w);
+  b.x = nope(b.x);
+  b.y = nope(b.y);
+  b.z = nope(b.z);
+  b.w = nope(b.w);
+  // NaN is ignored by the maxima (a tile of NaN alone ends at the 1e-4 floor)
+  const uint32_t m = bf16x2_maxabs(bf16x2_maxabs(bf16x2_maxabs(a.x, a.y), bf16x2_maxabs(a.z, a.w)),
+                                   bf16x2_maxabs(bf16x2_maxabs(b.x, b.y), bf16x2_maxabs(b.z, b.w)));
+  float amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  if (kL == Layout::kV4) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  amax = fmaxf(amax, 1e-4f);
+  const int e = ceil_pow2_exponent(__fmul_rn(amax, 1.0f / 448.0f));
+  const float inv = exp2_neg(e);
+  float f[8];
+  widen8(a, f);
+  const uint2 lo = e4m3x8_scaled(f, inv);
+  widen8(b, f);
+  const uint2 hi = e4m3x8_scaled(f, inv);
+  if (lane < 28) {
+    st_v4(values + 16 * lane, make_uint4(lo.x, lo.y, hi.x, hi.y));
+    const int enc = e + 127;
+    if (kL == Layout::kV4 ? (lane & 3) == 0 : (lane & 1) == 0)
+      st_u8(scales + (kL == Layout::kV4 ? lane >> 2 : lane >> 1),
+            (uint32_t)(enc < kCap ? enc : kCap));
+  }
+  // rotary pair `lane`: elements 448 + 2*lane and 449 + 2*lane
+  const float ev = bf16_lo(xr), od = bf16_hi(xr);
+  float re = __fsub_rn(__fmul_rn(ev, c), __fmul_rn(od, sn));
+  float ro = __fadd_rn(__fmul_rn(od, c), __fmul_rn(ev, sn));
+  if (kSanitize) {
+    re = (re == re) ? re : 0.0f;
+    ro = (ro == ro) ? ro : 0.0f;
+  }
+  if constexpr (kL == Layout::kV4) {
+    st_u32(values + 448 + 4 * lane, bf16x2_rn_nan(re, ro));
+    if (lane == 0) st_u8(scales + 7, 0u);
+  } else {
+    float ramax = fmaxf(fmaxf(fabsf(re), fabsf(ro)), 0.0f);
+    ramax = fmaxf(ramax, __shfl_xor_sync(0xFFFFFFFFu, ramax, 1));
+    ramax = fmaxf(ramax, __shfl_xor_sync(0xFFFFFFFFu, ramax, 2));
+    ramax = fmaxf(ramax, __shfl_xor_sync(0xFFFFFFFFu, ramax, 4));
+    ramax = fmaxf(ramax, __shfl_xor_sync(0xFFFFFFFFu, ramax, 8));
+    ramax = fmaxf(ramax, 1e-4f);
+    const int er = ceil_pow2_exponent(__fmul_rn(ramax, 1.0f / 448.0f));
+    const float rinv = exp2_neg(er);
+    st_u16(values + 448 + 2 * lane, cvt_e4m3x2(__fmul_rn(re, rinv), __fmul_rn(ro, rinv)));
+    if ((lane & 15) == 0) {
+      const int enc = er + 127;
+      st_u8(scales + 14 + (lane >> 4), (uint32_t)(enc < kCap ? enc : kCap));
+    }
+  }
+}
+
+// The MXFP8 and V4 records (record_run per writer), with the token loop of
+// the NVFP4 kernel: the next chunk's slots and positions in flight while
+// this chunk's writers are stored.
+template <Layout kL, bool kSanitize>
+__global__ void __launch_bounds__(kRopeThreads, 5) record_run_insert_kernel(RopeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kRopeThreads + threadIdx.x) >> 5;
+  const int64_t num_warps = ((int64_t)gridDim.x * kRopeThreads) >> 5;
+
+  TokenIds ids = token_ids(p, warp * 32 + lane);
+  for (int64_t base = warp * 32; base < p.num_tokens; base += num_warps * 32) {
+    int64_t page_off, table_off, in_page;
+    token_gates(p, ids, page_off, table_off, in_page);
+    ids = token_ids(p, base + num_warps * 32 + lane);
+    uint32_t todo = __ballot_sync(0xFFFFFFFFu, page_off >= 0);
+    while (todo) {
+      const int ia = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int ib = todo ? __ffs(todo) - 1 : -1;
+      if (todo) todo &= todo - 1;
+      const uint8_t* sa = p.latent + (base + ia) * p.row_pitch;
+      const int64_t ta = __shfl_sync(0xFFFFFFFFu, table_off, ia);
+      uint4 xa0 = make_uint4(0, 0, 0, 0), xa1 = xa0;
+      if (lane < 28) {
+        xa0 = ld_nc_v4(sa + 32 * lane);
+        xa1 = ld_nc_v4(sa + 32 * lane + 16);
+      }
+      const uint32_t ra = ld_once_u32(sa + 896 + 4 * lane);
+      const float ca = ld_f32(p.cos_sin + ta + lane);
+      const float sna = ld_f32(p.cos_sin + ta + 32 + lane);
+      uint4 xb0 = make_uint4(0, 0, 0, 0), xb1 = xb0;
+      uint32_t rb = 0;
+      float cb = 1.0f, snb = 0.0f;
+      if (ib >= 0) {
+        const uint8_t* sb = p.latent + (base + ib) * p.row_pitch;
+        const int64_t tb = __shfl_sync(0xFFFFFFFFu, table_off, ib);
+        if (lane < 28) {
+          xb0 = ld_nc_v4(sb + 32 * lane);
+          xb1 = ld_nc_v4(sb + 32 * lane + 16);
         }
+        rb = ld_once_u32(sb + 896 + 4 * lane);
+        cb = ld_f32(p.cos_sin + tb + lane);
+        snb = ld_f32(p.cos_sin + tb + 32 + lane);
+      }
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const int i = w ? ib : ia;
+        if (i < 0) break;
+        const int64_t pg = __shfl_sync(0xFFFFFFFFu, page_off, i);
+        const int64_t slot_in_page = __shfl_sync(0xFFFFFFFFu, in_page, i);
+        record_run<kL, kSanitize>(p, w ? xb0 : xa0, w ? xb1 : xa1, w ? rb : ra, w ? cb : ca,
+                                  w ? snb : sna, p.cache + pg, slot_in_page, lane);
       }
     }
   }
@@ -705,15 +730,15 @@ int dispatch(Kind kind, bool sanitize, const RopeParams& p, cudaStream_t stream)
       return launch(nvfp4_insert_kernel, g_rope_occupancy[2], p, stream);
     case Kind::kMxfp8:
       return sanitize
-                 ? launch(fp8_family_insert_kernel<Layout::kMxfp8, true>, g_rope_occupancy[1], p,
+                 ? launch(record_run_insert_kernel<Layout::kMxfp8, true>, g_rope_occupancy[1], p,
                           stream)
-                 : launch(fp8_family_insert_kernel<Layout::kMxfp8, false>, g_rope_occupancy[0], p,
+                 : launch(record_run_insert_kernel<Layout::kMxfp8, false>, g_rope_occupancy[0], p,
                           stream);
     case Kind::kV4:
       return sanitize
-                 ? launch(fp8_family_insert_kernel<Layout::kV4, true>, g_rope_occupancy[4], p,
+                 ? launch(record_run_insert_kernel<Layout::kV4, true>, g_rope_occupancy[4], p,
                           stream)
-                 : launch(fp8_family_insert_kernel<Layout::kV4, false>, g_rope_occupancy[3], p,
+                 : launch(record_run_insert_kernel<Layout::kV4, false>, g_rope_occupancy[3], p,
                           stream);
     case Kind::kPlainBf16:
       return launch(fp8_family_insert_kernel<Layout::kPlainBf16, false>, g_rope_occupancy[5], p,
