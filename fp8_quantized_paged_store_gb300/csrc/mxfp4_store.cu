@@ -14,16 +14,20 @@
 //     with 32 KiB of ring per block, six blocks (48 warps, ~144 KiB of loads
 //     in flight) fit an SM, which measured faster than four rows ahead with
 //     five blocks, or two rows ahead;
-//   * one row is 1 KiB read as two fully coalesced 512-byte warp copies: lane
-//     l holds elements 8l..8l+7 (half 0, groups 0..7) and 256+8l..256+8l+7
-//     (half 1, groups 8..15), so a 32-element group spans four lanes;
+//   * one row is 1 KiB; in the store lane l holds the run of elements
+//     16l..16l+15 (two 16-byte copies, bytes 32l and 32l+16), so a group of
+//     32 is two lanes' runs; the RMSNorm-fused store holds elements 8l..8l+7
+//     (half 0, groups 0..7) and 256+8l..256+8l+7 (half 1, groups 8..15),
+//     the order its sum of squares is defined in, a group over four lanes;
 //   * group amax: bf16x2 max-of-magnitudes (NaN ignored) within the lane, then
-//     two xor-shuffles across the four lanes, both halves packed in one word;
+//     one xor-shuffle (runs) or two across four lanes with both halves packed
+//     in one word (halves);
 //   * the E8M0 exponent comes from the amax bits without a division;
 //   * values are scaled by the exact power 2**-e in binary32 and converted
 //     by cvt.rn.satfinite.e2m1x2.f32 (NaN and -0.0 are cleared first);
-//   * each lane stores two 4-byte code words (two coalesced 128-byte warp
-//     stores) and four lanes store the two scale bytes of their groups.
+//   * each lane stores its eight code bytes in one store and every other lane
+//     its group's scale byte (runs), or two 4-byte code words and every
+//     fourth lane two scale bytes (halves).
 #include <cmath>
 #include <cstdint>
 
@@ -109,6 +113,23 @@ __device__ __forceinline__ uint32_t group_amax2(uint4 x0, uint4 x1) {
   return g & 0x7FFF7FFFu;
 }
 
+// |amax| of this lane's group as bf16 bits (low 16 bits) when the lane holds a
+// run of 16 consecutive values (x0, x1) and a group of 32 is two lanes' runs:
+// the maximum over the run, then one xor-shuffle.
+template <bool kNanPropagating>
+__device__ __forceinline__ uint32_t run_group_amax(uint4 x0, uint4 x1) {
+  auto mx = [](uint32_t a, uint32_t b) {
+    return kNanPropagating ? bf16x2_maxabs_nan(a, b) : bf16x2_maxabs(a, b);
+  };
+  uint32_t m = mx(mx(mx(x0.x, x0.y), mx(x0.z, x0.w)), mx(mx(x1.x, x1.y), mx(x1.z, x1.w)));
+  m = mx(m, __byte_perm(m, m, 0x1032)) & 0x7FFF7FFFu;
+  auto mg = [](uint32_t a, uint32_t b) {
+    return kNanPropagating ? bf16x2_maxabs_nan(a, b) : bf16x2_max(a, b);
+  };
+  m = mg(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  return m & 0x7FFFu;
+}
+
 // Group exponent for a finite amax (bf16 bits a < 0x7F80): the closed form of
 // mxfp4_group_exponent without its NaN and infinity cases. (a + 0x3F) >> 7
 // adds 1 to the exponent field exactly when the 7-bit mantissa exceeds 0x40.
@@ -117,12 +138,8 @@ __device__ __forceinline__ int finite_group_exponent(uint32_t a) {
   return a == 0u ? 0 : (e < -126 ? -126 : e);
 }
 
-// Quantize one row held by the warp (x0: half 0, x1: half 1) and write its 272
-// bytes at dst. kPacked: the fast path scales two values per packed fused
-// multiply-add (same results); the plain store runs faster with it, the
-// RMSNorm-fused store faster without (1.065 vs 1.082 ms and 1.115 vs
-// 1.086 ms on 4,300,000 rows).
-template <bool kPacked>
+// Quantize one row held by the warp as halves (x0: half 0, x1: half 1; the
+// RMSNorm-fused store) and write its 272 bytes at dst.
 __device__ __forceinline__ void quantize_store_row(uint4 x0, uint4 x1, uint8_t* dst, int lane) {
   const uint32_t g = group_amax2<true>(x0, x1);
   const uint32_t a0 = g & 0xFFFFu, a1 = g >> 16;
@@ -137,8 +154,8 @@ __device__ __forceinline__ void quantize_store_row(uint4 x0, uint4 x1, uint8_t* 
     c0 = encode8<true, false>(x0, exp2_neg(e0));
     c1 = encode8<true, false>(x1, exp2_neg(e1));
   } else {
-    c0 = encode8<false, kPacked>(x0, __uint_as_float((uint32_t)(127 - e0) << 23));
-    c1 = encode8<false, kPacked>(x1, __uint_as_float((uint32_t)(127 - e1) << 23));
+    c0 = encode8<false, false>(x0, __uint_as_float((uint32_t)(127 - e0) << 23));
+    c1 = encode8<false, false>(x1, __uint_as_float((uint32_t)(127 - e1) << 23));
   }
   st_u32(dst + 4 * lane, c0);
   st_u32(dst + 128 + 4 * lane, c1);
@@ -146,6 +163,33 @@ __device__ __forceinline__ void quantize_store_row(uint4 x0, uint4 x1, uint8_t* 
     st_u8(dst + 256 + (lane >> 2), (uint32_t)(e0 + 127));
     st_u8(dst + 264 + (lane >> 2), (uint32_t)(e1 + 127));
   }
+}
+
+// Quantize one row held by the warp as runs (lane l: elements 16l..16l+15 in
+// x0, x1; group l/2) and write its 272 bytes at dst: eight code bytes per
+// lane in one store, one scale byte per even lane. The fast path scales two
+// values per packed fused multiply-add. Against the halves mapping (a group
+// over four lanes, two shuffles, two code stores per lane; scalar products)
+// this measured 1.082 -> 1.065 ms (packed products) and 1.040 -> 1.017 ms
+// (runs) on 4,300,000 rows; the RMSNorm-fused store measured slower with
+// packed products (1.086 -> 1.115 ms) and keeps the halves, the order its
+// sum of squares is defined in.
+__device__ __forceinline__ void quantize_store_run(uint4 x0, uint4 x1, uint8_t* dst, int lane) {
+  const uint32_t a = run_group_amax<true>(x0, x1);
+  int e = finite_group_exponent(a);
+  uint32_t c0, c1;
+  if (__any_sync(0xFFFFFFFFu, (a >= 0x7F80u) | (e > 16))) {
+    e = mxfp4_group_exponent(run_group_amax<false>(x0, x1));  // NaN ignored
+    const float inv = exp2_neg(e);
+    c0 = encode8<true, false>(x0, inv);
+    c1 = encode8<true, false>(x1, inv);
+  } else {
+    const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+    c0 = encode8<false, true>(x0, inv);
+    c1 = encode8<false, true>(x1, inv);
+  }
+  st_v2(dst + 8 * lane, c0, c1);
+  if ((lane & 1) == 0) st_u8(dst + 256 + (lane >> 1), (uint32_t)(e + 127));
 }
 
 // RMSNorm of one row held by the warp (fused variant), in the order this
@@ -218,9 +262,10 @@ __device__ __forceinline__ uint32_t row_index(const StoreParams& p, int64_t t, i
 
 // Each warp owns a contiguous token range and streams its rows through a
 // per-warp shared-memory ring with cp.async, kPrefetch rows ahead of the row
-// it quantizes. Lane l copies, and later reads back, only bytes 16l..16l+15
-// and 512+16l..512+16l+15 of each row, so the per-thread commit groups alone
-// order the ring: no barrier and no spin-wait. Row indices come 32 tokens at
+// it quantizes. Lane l copies, and later reads back, only its own bytes of
+// each row (32l..32l+31 for runs; 16l..16l+15 and 512+16l..512+16l+15 for
+// halves), so the per-thread commit groups alone order the ring: no barrier
+// and no spin-wait. Row indices come 32 tokens at
 // a time (lane i holds token base+i); the window after the current one is
 // loaded early so that prefetches crossing into it find their indices ready.
 // The loop is unrolled over the ring's stages so that stage offsets are
@@ -230,14 +275,18 @@ __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams 
   extern __shared__ uint4 smem[];
   const int lane = threadIdx.x & 31;
   const int warp_in_block = threadIdx.x >> 5;
-  uint4* ring = smem + warp_in_block * (kStages * kStageVecs) + lane;
+  // the plain store holds runs (lane l: bytes 32l..32l+31 of a row); the
+  // RMSNorm-fused one halves (bytes 16l..16l+15 and 512+16l..512+16l+15), the
+  // order its sum of squares is defined in
+  constexpr bool kRuns = !kNorm;
+  uint4* ring = smem + warp_in_block * (kStages * kStageVecs) + (kRuns ? 2 * lane : lane);
   const int64_t warp = (int64_t)blockIdx.x * kStoreWarps + warp_in_block;
   const int64_t num_warps = (int64_t)gridDim.x * kStoreWarps;
   const int64_t t_begin = p.num_tokens * warp / num_warps;
   const int64_t t_end = p.num_tokens * (warp + 1) / num_warps;
   const int n = (int)(t_end - t_begin);  // < 2**31, checked at launch
   if (n <= 0) return;
-  const uint8_t* src = p.latent + t_begin * p.row_pitch + 16 * lane;
+  const uint8_t* src = p.latent + t_begin * p.row_pitch + (kRuns ? 32 : 16) * lane;
   const uint32_t pitch = (uint32_t)p.row_pitch;
   uint4 wt0 = make_uint4(0, 0, 0, 0), wt1 = wt0;  // the lane's RMSNorm weights
   if (kNorm) {
@@ -252,7 +301,7 @@ __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams 
     if (row != 0xFFFFFFFFu) {
       const uint8_t* s = src + (size_t)i * pitch;
       cp_async_16(ring + stage * kStageVecs, s);
-      cp_async_16(ring + stage * kStageVecs + 32, s + 512);
+      cp_async_16(ring + stage * kStageVecs + (kRuns ? 1 : 32), s + (kRuns ? 16 : 512));
     }
     cp_async_commit();
   };
@@ -277,9 +326,13 @@ __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams 
         cp_async_wait<kPrefetch>();  // row i has landed
         const uint32_t row = __shfl_sync(0xFFFFFFFFu, w0, k);
         if (row != 0xFFFFFFFFu) {
-          uint4 x0 = lds_v4(ring + u * kStageVecs), x1 = lds_v4(ring + u * kStageVecs + 32);
+          uint4 x0 = lds_v4(ring + u * kStageVecs);
+          uint4 x1 = lds_v4(ring + u * kStageVecs + (kRuns ? 1 : 32));
           if (kNorm) rmsnorm_row(x0, x1, wt0, wt1, p.eps);
-          quantize_store_row<!kNorm>(x0, x1, p.cache + (size_t)row * kMxfp4RowBytes, lane);
+          if (kRuns)
+            quantize_store_run(x0, x1, p.cache + (size_t)row * kMxfp4RowBytes, lane);
+          else
+            quantize_store_row(x0, x1, p.cache + (size_t)row * kMxfp4RowBytes, lane);
         }
       }
     }
