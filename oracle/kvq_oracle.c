@@ -477,7 +477,7 @@ void oracle_rope_quant_insert_nvfp4(const uint16_t* latent, int64_t num_tokens, 
  * epsilon into a bf16 latent. The pages fix neither the summation order nor
  * how the reciprocal square root is formed, so this reading fixes both in a
  * form that can be reproduced exactly:
- *   partial[l] = x[16l]^2 + x[16l+1]^2 + ... + x[16l+15]^2
+ *   partial[l] = x[8l]^2 + ... + x[8l+7]^2 + x[256+8l]^2 + ... + x[256+8l+7]^2
  *                (l = 0..31, accumulated left to right, each square and sum
  *                rounded to binary32),
  *   S = pairwise tree over l: partial[l] + partial[l ^ 1], then the pairs of
@@ -490,10 +490,12 @@ static void rmsnorm_row_512(const uint16_t* x, const uint16_t* w, float eps, uin
     float partial[32];
     for (int l = 0; l < 32; ++l) {
         float acc = 0.0f;
-        for (int k = 0; k < 16; ++k) {
-            float v = bf16_to_f32(x[16 * l + k]);
-            float sq = v * v;
-            acc = acc + sq;
+        for (int h = 0; h < 2; ++h) {
+            for (int k = 0; k < 8; ++k) {
+                float v = bf16_to_f32(x[256 * h + 8 * l + k]);
+                float sq = v * v;
+                acc = acc + sq;
+            }
         }
         partial[l] = acc;
     }
