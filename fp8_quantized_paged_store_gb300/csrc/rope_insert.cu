@@ -55,7 +55,10 @@
 // pairs use the binary32 formula with every product and sum rounded
 // separately (no fused multiply-add). Plain rows take the 448 NoPE values as
 // they are (bit for bit in bf16, divided by the scale in fp8).
+#include <atomic>
+#include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "kvq.h"
 #include "kvq_device.cuh"
@@ -83,7 +86,19 @@ struct RopeParams {
   int64_t ratio;
   int64_t slot_pitch;   // plain rows: bytes between the rows of a page
   float fp8_scale;      // plain fp8 rows: the per-tensor scale
+  int32_t fp8_mode;     // plain fp8 rows: how x / fp8_scale is formed (Fp8Quotient)
+  float fp8_yh, fp8_yl;  // plain fp8 rows: RD(1/scale) and RN((1 - scale*yh) * yh)
 };
+
+// How the plain fp8 rows form the E4M3 code of RN(x / scale):
+//   kDivide   every value by a correctly rounded division;
+//   kTwoTerm  the bf16 NoPE values by RN(x*yh + RN(x*yl)), a two-term
+//             reciprocal that the host found to give the division's code for
+//             every one of the 65,536 bf16 patterns at this scale; the binary32
+//             rotary values by division;
+//   kProduct  scale a power of two with a normal reciprocal: every value by
+//             RN(x * yh), the same rounding of the same exact quotient.
+enum Fp8Quotient : int32_t { kDivide = 0, kTwoTerm = 1, kProduct = 2 };
 
 // E4M3-family layouts: the MXFP8 and V4 records (record_run_insert_kernel)
 // and the plain rows (fp8_family_insert_kernel).
@@ -159,6 +174,22 @@ __device__ __forceinline__ uint2 e4m3x8_div(const float f[8], float scale) {
   return make_uint2(w[0], w[1]);
 }
 
+// Eight values as E4M3 of RN(x*yh + RN(x*yl)) (kTwoTerm) or of RN(x*yh)
+// (kProduct, yl unused), two per packed instruction. The product feeds only
+// the fused multiply-add's addend, which no instruction can absorb.
+template <bool kTwoTerm>
+__device__ __forceinline__ uint2 e4m3x8_recip(const float f[8], float yh, float yl) {
+  const float2 h2 = make_float2(yh, yh), l2 = make_float2(yl, yl);
+  uint32_t c[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 x = make_float2(f[2 * k], f[2 * k + 1]);
+    const float2 q = kTwoTerm ? fma2_rn(x, h2, mul2_rn(x, l2)) : mul2_rn(x, h2);
+    c[k] = cvt_e4m3x2(q.x, q.y);
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 // The rotary values of the lane's half 1 (lanes 24..31), binary32 formula
 // without contraction and without sanitising.
 __device__ __forceinline__ void rotate_pairs(uint4 x1, float4 c, float4 s, float f[8]) {
@@ -200,7 +231,17 @@ __device__ __forceinline__ void write_plain(const RopeParams& p, uint4 x0, uint4
     } else {
       rotate_pairs(x1, c, s, f1);
     }
-    const uint2 a = e4m3x8_div(f0, p.fp8_scale), b = e4m3x8_div(f1, p.fp8_scale);
+    uint2 a, b;
+    if (p.fp8_mode == kTwoTerm) {
+      a = e4m3x8_recip<true>(f0, p.fp8_yh, p.fp8_yl);
+      b = lane < 24 ? e4m3x8_recip<true>(f1, p.fp8_yh, p.fp8_yl) : e4m3x8_div(f1, p.fp8_scale);
+    } else if (p.fp8_mode == kProduct) {
+      a = e4m3x8_recip<false>(f0, p.fp8_yh, 0.0f);
+      b = e4m3x8_recip<false>(f1, p.fp8_yh, 0.0f);
+    } else {
+      a = e4m3x8_div(f0, p.fp8_scale);
+      b = e4m3x8_div(f1, p.fp8_scale);
+    }
     st_v2(row + 8 * lane, a.x, a.y);
     st_v2(row + 256 + 8 * lane, b.x, b.y);
   }
@@ -688,6 +729,60 @@ int launch(Kernel k, int* occupancy, const RopeParams& p, cudaStream_t stream) {
 
 enum class Kind { kMxfp8, kNvfp4, kV4, kPlainBf16, kPlainFp8 };
 
+// E4M3 byte of a binary32 value as the satfinite conversion gives it: round
+// to nearest even on a 3-bit fraction (subnormal step 2^-9), NaN -> 0x7F,
+// magnitudes that reach 448 or beyond (infinities included) -> +-448.
+inline uint32_t host_e4m3(float f) {
+  if (f != f) return 0x7Fu;
+  const uint32_t sign = std::signbit(f) ? 0x80u : 0u;
+  const double a = std::fabs((double)f);
+  if (a >= 448.0) return sign | 0x7Eu;
+  if (a < 0.015625) return sign | (uint32_t)std::nearbyint(a * 512.0);  // 0..8
+  int ex = 0;
+  std::frexp(a, &ex);
+  int e = ex - 1;                                      // a in [2^e, 2^(e+1))
+  double m = std::nearbyint(std::ldexp(a, 3 - e));     // 8..16
+  if (m == 16.0) {
+    m = 8.0;
+    e += 1;
+  }
+  return sign | (uint32_t)(((e + 7) << 3) | ((int)m - 8));
+}
+
+// How the plain fp8 rows divide by `scale` (Fp8Quotient), with yh and yl set
+// for the product modes. A power of two with a normal reciprocal takes the
+// product. Otherwise yh = RD(1/scale), yl = RN((1 - scale*yh) * yh) (the
+// residual is exact), and the two-term rule is used only if it gives the
+// division's E4M3 code for every bf16 pattern: an exhaustive check, run once
+// per distinct scale (the last answer is cached).
+inline int32_t fp8_quotient_mode(float scale, float& yh, float& yl) {
+  int ex = 0;
+  if (std::frexp(scale, &ex) == 0.5f && ex >= -124 && ex <= 127) {
+    yh = std::ldexp(1.0f, 1 - ex);
+    yl = 0.0f;
+    return kProduct;
+  }
+  yh = 1.0f / scale;
+  if (std::fmaf(-scale, yh, 1.0f) < 0.0f) yh = std::nextafterf(yh, 0.0f);
+  yl = std::fmaf(-scale, yh, 1.0f) * yh;
+  uint32_t bits = 0;
+  std::memcpy(&bits, &scale, 4);
+  static std::atomic<uint64_t> last{0};  // (scale bits << 2) | (mode + 1)
+  const uint64_t seen = last.load(std::memory_order_relaxed);
+  if (seen != 0 && (seen >> 2) == bits) return (int32_t)(seen & 3u) - 1;
+  int32_t mode = kTwoTerm;
+  for (uint32_t b = 0; b < 65536u && mode == kTwoTerm; ++b) {
+    const uint32_t w = b << 16;
+    float x = 0.0f;
+    std::memcpy(&x, &w, 4);
+    const float q = x / scale;
+    volatile float t = x * yl;
+    if (host_e4m3(q) != host_e4m3(std::fmaf(x, yh, t))) mode = kDivide;
+  }
+  last.store(((uint64_t)bits << 2) | (uint64_t)(mode + 1), std::memory_order_relaxed);
+  return mode;
+}
+
 // Checks shared by every insert; fills the fields of `p` that do not depend
 // on the cache layout. KVQ_OK, or KVQ_EINVAL.
 int common_args(const void* latent_bf16, int64_t num_tokens, int64_t row_stride_elems,
@@ -720,6 +815,9 @@ int common_args(const void* latent_bf16, int64_t num_tokens, int64_t row_stride_
   p.ratio = compress_ratio;
   p.slot_pitch = 0;
   p.fp8_scale = 1.0f;
+  p.fp8_mode = kDivide;
+  p.fp8_yh = 1.0f;
+  p.fp8_yl = 0.0f;
   return KVQ_OK;
 }
 
@@ -837,5 +935,6 @@ extern "C" int rope_plain_insert(const void* latent_bf16, int64_t num_tokens,
   p.page_stride = page_stride_elems * es;
   p.slot_pitch = slot_stride_elems * es;
   p.fp8_scale = fp8 ? fp8_scale : 1.0f;
+  if (fp8) p.fp8_mode = fp8_quotient_mode(fp8_scale, p.fp8_yh, p.fp8_yl);
   return dispatch(fp8 ? Kind::kPlainFp8 : Kind::kPlainBf16, false, p, stream);
 }

@@ -164,6 +164,27 @@ def test_fp8_scales(scale):
     assert G.first_diff(got, want) is None, G.first_diff(got, want)
 
 
+@pytest.mark.parametrize("scale", [0.0125, 0.9375, 0.5, 2.0 ** -126, 3.0e38])
+def test_fp8_every_bf16_nope_value(scale):
+    """All 65,536 bf16 patterns (NaN, infinities, zeros, subnormals included)
+    as NoPE values at scales that take each way of forming the quotient: the
+    two-term reciprocal (0.0125, 0.9375; verified for every pattern at the
+    scale), the exact product by a power of two (0.5), and the division (a
+    power of two whose reciprocal is not normal, and 3e38 with a subnormal
+    reciprocal)."""
+    rows = -(-65536 // 448)
+    nope = np.zeros(rows * 448, np.uint16)
+    nope[:65536] = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    lat = np.zeros((rows, 512), np.uint16)
+    lat[:, :448] = nope.reshape(rows, 448)
+    lat[:, 448:] = 0x3F80
+    table = workloads.rope_cos_sin_table(rows=rows)
+    cache = np.full(3 * 64 * 512, 0xAA, dtype=np.uint8)
+    got, want = _run("fp8", lat, np.arange(rows), table, cache, np.arange(rows), 3, 64, 1,
+                     fp8_scale=scale)
+    assert G.first_diff(got, want) is None, G.first_diff(got, want)
+
+
 def test_fp8_division_ties():
     """Rotated values x = M*s with M an E4M3 midpoint: x / s is the tie M and
     rounds to the even code, where x * RN(1/s) would round up."""
