@@ -208,3 +208,12 @@ def test_binding_refuses_pageable_host_tensors():
         kvq.mxfp4_mla_store(lat, slots, cache)
     with pytest.raises(TypeError):
         kvq.mxfp4_mla_gather_dequant(cache, slots)
+
+
+def test_pointer_kind_host_side(L):
+    """kvq_pointer_kind needs no launch: a null pointer is EINVAL; pageable
+    host memory is never reported addressable (KVQ_ECUDA where no device is
+    present, KVQ_PTR_UNADDRESSABLE where one is)."""
+    assert L.kvq_pointer_kind(None) == -1
+    buf = ctypes.create_string_buffer(64)
+    assert L.kvq_pointer_kind(ctypes.addressof(buf)) in (-2, 0)
