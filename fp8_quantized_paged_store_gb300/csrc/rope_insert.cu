@@ -205,14 +205,14 @@ __device__ __forceinline__ void rotate_pairs(uint4 x1, float4 c, float4 s, float
   }
 }
 
-// One writer row of a plain layout. `page` points at the slot's page,
+// One writer row of the plain bf16 layout. `page` points at the slot's page,
 // `slot_in_page` is its row there.
 template <Layout kL>
 __device__ __forceinline__ void write_plain(const RopeParams& p, uint4 x0, uint4 x1, float4 c,
                                             float4 s, uint8_t* page, int64_t slot_in_page,
                                             int lane) {
-  static_assert(kL == Layout::kPlainBf16 || kL == Layout::kPlainFp8, "plain rows only");
-  if constexpr (kL == Layout::kPlainBf16) {
+  static_assert(kL == Layout::kPlainBf16, "plain bf16 rows only");
+  {
     uint8_t* row = page + slot_in_page * p.slot_pitch;
     st_v4(row + 16 * lane, x0);
     if (lane < 24) {
@@ -222,28 +222,6 @@ __device__ __forceinline__ void write_plain(const RopeParams& p, uint4 x0, uint4
       rotate_pairs(x1, c, s, f1);
       st_v4(row + 512 + 16 * lane, bf16x8_rn(f1));
     }
-  } else {  // kPlainFp8
-    uint8_t* row = page + slot_in_page * p.slot_pitch;
-    float f0[8], f1[8];
-    widen8(x0, f0);
-    if (lane < 24) {
-      widen8(x1, f1);
-    } else {
-      rotate_pairs(x1, c, s, f1);
-    }
-    uint2 a, b;
-    if (p.fp8_mode == kTwoTerm) {
-      a = e4m3x8_recip<true>(f0, p.fp8_yh, p.fp8_yl);
-      b = lane < 24 ? e4m3x8_recip<true>(f1, p.fp8_yh, p.fp8_yl) : e4m3x8_div(f1, p.fp8_scale);
-    } else if (p.fp8_mode == kProduct) {
-      a = e4m3x8_recip<false>(f0, p.fp8_yh, 0.0f);
-      b = e4m3x8_recip<false>(f1, p.fp8_yh, 0.0f);
-    } else {
-      a = e4m3x8_div(f0, p.fp8_scale);
-      b = e4m3x8_div(f1, p.fp8_scale);
-    }
-    st_v2(row + 8 * lane, a.x, a.y);
-    st_v2(row + 256 + 8 * lane, b.x, b.y);
   }
 }
 
@@ -522,6 +500,38 @@ template <Layout kL, bool kSanitize>
 __device__ __forceinline__ void record_run(const RopeParams& p, uint4 a, uint4 b, uint32_t xr,
                                            float c, float sn, uint8_t* page,
                                            int64_t slot_in_page, int lane) {
+  if constexpr (kL == Layout::kPlainFp8) {
+    // plain fp8 row: E4M3 of x / scale, the quotient formed as the host chose
+    uint8_t* row = page + slot_in_page * p.slot_pitch;
+    float f[8];
+    uint2 lo, hi;
+    widen8(a, f);
+    if (p.fp8_mode == kTwoTerm) {
+      lo = e4m3x8_recip<true>(f, p.fp8_yh, p.fp8_yl);
+      widen8(b, f);
+      hi = e4m3x8_recip<true>(f, p.fp8_yh, p.fp8_yl);
+    } else if (p.fp8_mode == kProduct) {
+      lo = e4m3x8_recip<false>(f, p.fp8_yh, 0.0f);
+      widen8(b, f);
+      hi = e4m3x8_recip<false>(f, p.fp8_yh, 0.0f);
+    } else {
+      lo = e4m3x8_div(f, p.fp8_scale);
+      widen8(b, f);
+      hi = e4m3x8_div(f, p.fp8_scale);
+    }
+    if (lane < 28) {  // rows are 8-byte aligned
+      st_v2(row + 16 * lane, lo.x, lo.y);
+      st_v2(row + 16 * lane + 8, hi.x, hi.y);
+    }
+    const float ev = bf16_lo(xr), od = bf16_hi(xr);
+    const float re = __fsub_rn(__fmul_rn(ev, c), __fmul_rn(od, sn));
+    const float ro = __fadd_rn(__fmul_rn(od, c), __fmul_rn(ev, sn));
+    const uint32_t two = p.fp8_mode == kProduct
+                             ? cvt_e4m3x2(__fmul_rn(re, p.fp8_yh), __fmul_rn(ro, p.fp8_yh))
+                             : cvt_e4m3x2(__fdiv_rn(re, p.fp8_scale), __fdiv_rn(ro, p.fp8_scale));
+    st_u16(row + 448 + 2 * lane, two);
+    return;
+  }
   constexpr int kValueBytes = kL == Layout::kV4 ? 576 : 512;
   constexpr int kScaleBytes = kL == Layout::kV4 ? 8 : 16;
   constexpr int kCap = kSanitize ? 254 : 255;
@@ -842,7 +852,7 @@ int dispatch(Kind kind, bool sanitize, const RopeParams& p, cudaStream_t stream)
       return launch(fp8_family_insert_kernel<Layout::kPlainBf16, false>, g_rope_occupancy[5], p,
                     stream);
     default:
-      return launch(fp8_family_insert_kernel<Layout::kPlainFp8, false>, g_rope_occupancy[6], p,
+      return launch(record_run_insert_kernel<Layout::kPlainFp8, false>, g_rope_occupancy[6], p,
                     stream);
   }
 }
