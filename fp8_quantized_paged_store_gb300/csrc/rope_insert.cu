@@ -39,11 +39,13 @@
 // numbers and take the cheaper exact code rule of nvfp4_code_value2 (two
 // fused products, no ALU work).
 //
-// Plain rows keep the half-row mapping: lane l holds elements 8l..8l+7
-// (half 0) and 256+8l..256+8l+7 (half 1), each 16-byte load of the warp
-// covering 512 contiguous bytes; the rotary elements are half 1 of lanes
-// 24..31, which alone read the table row (cos and sin 4(l-24)..4(l-24)+3,
-// two 16-byte loads each).
+// Plain fp8 rows use the run mapping too (their rotary quotients then run
+// two per lane). Plain bf16 rows keep the half-row mapping, which measured
+// faster for them (0.389 against 0.397 ms with runs: their NoPE part is a
+// plain copy, best done as fully coalesced 512-byte warp stores): lane l
+// holds elements 8l..8l+7 (half 0) and 256+8l..256+8l+7 (half 1), and the
+// rotary elements are half 1 of lanes 24..31, which alone read the table row
+// (cos and sin 4(l-24)..4(l-24)+3, two 16-byte loads each).
 //
 // The pages evaluate the rotation formula on all 256 pairs, with cos 1 and
 // sin 0 outside the rotary range. There it is the identity except for NaN,
@@ -100,8 +102,8 @@ struct RopeParams {
 //             RN(x * yh), the same rounding of the same exact quotient.
 enum Fp8Quotient : int32_t { kDivide = 0, kTwoTerm = 1, kProduct = 2 };
 
-// E4M3-family layouts: the MXFP8 and V4 records (record_run_insert_kernel)
-// and the plain rows (fp8_family_insert_kernel).
+// Layouts besides NVFP4: the MXFP8 and V4 records and the plain fp8 rows
+// (record_run_insert_kernel), the plain bf16 rows (fp8_family_insert_kernel).
 enum class Layout { kMxfp8, kV4, kPlainBf16, kPlainFp8 };
 constexpr int kV4Record = 584;   // 576 value bytes (448 E4M3 + 64 bf16) + 8 scale bytes
 
@@ -428,7 +430,7 @@ __device__ __forceinline__ void token_gates(const RopeParams& p, TokenIds id, in
 
 // ---------------------------------------------------------------- kernels ---
 
-// The plain bf16 and fp8 rows. Five resident blocks (40 warps) per SM: the
+// The plain bf16 rows. Five resident blocks (40 warps) per SM: the
 // 48-register cap costs a few spilled words, but the extra writers in flight
 // lifted the inserts by 7 % when measured on the MXFP8 record (4,194,304
 // tokens: 5292 -> 5680 GB/s; six blocks at 40 registers lose it again).
