@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.kvq_row_bytes.argtypes = [_i64, _i64]
         L.kvq_pointer_kind.restype = ctypes.c_int
         L.kvq_pointer_kind.argtypes = [_p]
+        L.kvq_plain_fp8_quotient_mode.restype = ctypes.c_int
+        L.kvq_plain_fp8_quotient_mode.argtypes = [ctypes.c_float]
         L.mxfp4_mla_store.restype = ctypes.c_int
         L.mxfp4_mla_store.argtypes = [_p, _i64, _i64, _i64, _p, _p, _i64, _i64, _i64, _i32, _p]
         L.mxfp4_mla_rmsnorm_store.restype = ctypes.c_int

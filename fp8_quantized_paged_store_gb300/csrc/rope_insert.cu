@@ -924,6 +924,13 @@ extern "C" int rope_quant_insert_v4(const void* latent_bf16, int64_t num_tokens,
                             cache_block, page_stride_bytes, compress_ratio, sanitize_nans, stream);
 }
 
+extern "C" int kvq_plain_fp8_quotient_mode(float fp8_scale) {
+  using namespace kvq;
+  if (!(fp8_scale > 0.0f && fp8_scale <= 3.0e38f)) return KVQ_EINVAL;
+  float yh = 1.0f, yl = 0.0f;
+  return fp8_quotient_mode(fp8_scale, yh, yl);
+}
+
 extern "C" int rope_plain_insert(const void* latent_bf16, int64_t num_tokens,
                                  int64_t row_stride_elems, const int64_t* positions,
                                  const float* cos_sin, int64_t cos_stride, int64_t cos_sin_rows,

@@ -267,6 +267,21 @@ int rope_plain_insert(const void* latent_bf16, int64_t num_tokens, int64_t row_s
                       int64_t slot_stride_elems, int32_t compress_ratio, int32_t fp8,
                       float fp8_scale, cudaStream_t stream);
 
+/* How rope_plain_insert forms the E4M3 code of RN(x / fp8_scale) for an fp8
+ * cache at this scale (a query of this library; the pages have no
+ * counterpart). The codes are those of the correctly rounded quotient in
+ * every mode; only the arithmetic differs:
+ *   0  every value by a correctly rounded division;
+ *   1  the bf16 NoPE values by RN(x*yh + RN(x*yl)), yh = RD(1/scale) and
+ *      yl = RN((1 - scale*yh) * yh), because an exhaustive host check found
+ *      that rule giving the division's code for all 65,536 bf16 patterns at
+ *      this scale; the binary32 rotary values by division;
+ *   2  scale a power of two with a normal reciprocal: every value by
+ *      RN(x * (1/scale)), the same rounding of the same exact quotient.
+ * The check runs once per distinct scale (the last answer is cached).
+ * KVQ_EINVAL unless 0 < fp8_scale <= 3e38. Host-only: launches nothing. */
+int kvq_plain_fp8_quotient_mode(float fp8_scale);
+
 /*
  * save_ring_rows — store the compressor's fp32 [kv | score] rows of 1024
  * values into their slots of the paged ring state. [v41] save_ring_rows.

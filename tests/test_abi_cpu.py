@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(L):
     names = declared_functions()
-    assert set(names) == {"kvq_strerror", "kvq_row_bytes", "kvq_pointer_kind", "mxfp4_mla_store",
+    assert set(names) == {"kvq_strerror", "kvq_row_bytes", "kvq_pointer_kind",
+                          "kvq_plain_fp8_quotient_mode", "mxfp4_mla_store",
                           "mxfp4_mla_rmsnorm_store",
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
                           "rope_quant_insert_v4", "rope_plain_insert", "save_ring_rows",

@@ -7,6 +7,8 @@ NVFP4 codes of bf16 values (rope_quant_insert_nvfp4, NoPE elements): the
 kernel decides the E2M1 code of RN(x / s) from RN(x*yh + RN(x*yl)) with
 yh = RD(1/s), yl = RN((1 - s*yh) * yh).
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -59,3 +61,72 @@ def test_nvfp4_plain_reciprocal_is_not_enough():
     assert oracle.e2m1_code(np.array([x / s], np.float32))[0] == 2
     y = np.float32(1) / s
     assert oracle.e2m1_code(np.array([x * y], np.float32))[0] == 3
+
+
+# ---------------------------------------------------------------------------
+# Plain fp8 rows: the library's per-scale choice of quotient rule
+# (kvq_plain_fp8_quotient_mode), against an independent numpy restatement.
+
+def _e4m3_codes(q: np.ndarray) -> np.ndarray:
+    """E4M3 bytes of binary32 values: nearest even on a 3-bit fraction
+    (subnormal step 2^-9), NaN -> 0x7F, magnitudes >= 448 -> +-448."""
+    q64 = q.astype(np.float64)
+    sign = np.signbit(q64).astype(np.int64) << 7
+    a = np.abs(q64)
+    with np.errstate(all="ignore"):
+        _, ex = np.frexp(np.where(a > 0, a, 1.0))
+        e = ex - 1
+        m = np.rint(np.ldexp(a, 3 - e))
+        bump = m == 16
+        e = np.where(bump, e + 1, e)
+        m = np.where(bump, 8, m)
+        normal = ((e + 7) << 3) | (m.astype(np.int64) - 8)
+        sub = np.rint(a * 512.0).astype(np.int64)
+    codes = np.where(a < 2.0 ** -6, sub, normal)
+    codes = np.where(a >= 448.0, 0x7E, codes) | sign
+    return np.where(np.isnan(q64), 0x7F, codes)
+
+
+def _expected_mode(scale: float) -> int:
+    s = np.float32(scale)
+    frac, ex = math.frexp(float(s))
+    if frac == 0.5 and -124 <= ex <= 127:
+        return 2
+    yh = np.float32(1.0) / s
+    if np.float64(1.0) - np.float64(s) * np.float64(yh) < 0:
+        yh = np.nextafter(yh, np.float32(0))
+    yl = np.float32(np.float32(np.float64(1.0) - np.float64(s) * np.float64(yh)) * yh)
+    x = _bf16_values_all()
+    with np.errstate(all="ignore"):
+        q = x / s
+        t = (x * yl).astype(np.float32)
+        fast = (x.astype(np.float64) * np.float64(yh) + t.astype(np.float64)).astype(np.float32)
+    return 1 if np.array_equal(_e4m3_codes(q), _e4m3_codes(fast)) else 0
+
+
+def _bf16_values_all() -> np.ndarray:
+    return (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+
+
+def test_e4m3_restatement_on_known_bytes():
+    vals = np.array([0.0, -0.0, 448.0, 464.0, 1e9, np.inf, -np.inf, np.nan, 2.0 ** -9,
+                     2.0 ** -10, 3 * 2.0 ** -11, 1.0, 1.0625, 1.1875, 240.0, -0.75],
+                    np.float32)
+    # 2^-10 is half the subnormal step (tie to 0), 3*2^-11 three quarters
+    # of it (rounds to 1), 1.0625 and 1.1875 ties to the even fraction
+    want = [0x00, 0x80, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7F, 0x01,
+            0x00, 0x01, 0x38, 0x38, 0x3A, 0x77, 0xB4]
+    assert _e4m3_codes(vals).tolist() == want
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.5, 4.0, 2.0 ** -126, 0.0125, 0.1, 0.9375, 3.7, 1e-3,
+                                   1e-30, 1.5e-38, 1e38, 3.0e38])
+def test_plain_fp8_quotient_mode_matches_an_independent_check(scale):
+    import fp8_quantized_paged_store_gb300 as kvq
+    assert kvq.lib().kvq_plain_fp8_quotient_mode(scale) == _expected_mode(scale)
+
+
+def test_plain_fp8_quotient_mode_rejects_bad_scales():
+    import fp8_quantized_paged_store_gb300 as kvq
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert kvq.lib().kvq_plain_fp8_quotient_mode(bad) == -1
