@@ -136,6 +136,12 @@ MUTANTS = [
     ("fscn_weight_dropped", "latent = pooled * r[:, None] * w[None, :]",
      "latent = pooled * r[:, None]",
      "test_oracle_pins_compress.py::test_cr1_weight_and_alternating_signs", "compress.py"),
+    ("bf16_nan_keeps_sign", "if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;",
+     "if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u);",
+     "test_oracle_pins_inserts.py::test_rotated_nan_is_stored_as_the_canonical_bf16_nan"),
+    ("bf16_ties_away", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;",
+     "if (lower >= 0x8000u) upper += 1u;",
+     "test_oracle_pins_rmsnorm.py::test_rmsnorm_matches_float64_within_one_ulp"),
     ("fscn_chunk_start_not_cut", "qs_t = np.maximum(qsl[r_safe], 0)", "qs_t = qsl[r_safe]",
      "test_oracle_pins_compress.py::test_cr2_chunk_bounds_are_cut_to_the_batch", "compress.py"),
 ]
