@@ -249,3 +249,21 @@ def test_nvfp4_division_ties():
     codes[0::2], codes[1::2] = c[:16] & 0xF, c[:16] >> 4
     assert codes[:14].tolist() == [7, 0, 2, 2, 4, 4, 6, 6, 8, 10, 10, 12, 12, 14]
     assert codes[16:23].tolist() == [7, 2, 4, 6, 10, 12, 14]
+
+
+def test_nvfp4_scale_clamps_to_448():
+    """A tile whose amax * fl32(1/6) exceeds 448 takes the largest E4M3 scale,
+    448 (byte 0x7E): with amax 6144 a member 896 is 896 / 448 = 2 exactly
+    (code 4), and the amax itself saturates at 6 (code 7)."""
+    table = _identity_table(rows=2)
+    row = np.zeros(512, np.uint16)
+    vals = np.array([6144.0, 896.0, -896.0, 224.0], np.float32)
+    row[:4] = workloads.f32_to_bf16_bits(vals)
+    assert np.array_equal(ind.bf16_bits_to_f32(row[:4]), vals)   # exact in bf16
+    cache = _run("nvfp4", row[None], [0], table, [0], num_pages=1)
+    c, s = _nvfp4_slot(cache, 0)
+    assert s[0] == 0x7E
+    codes = np.empty(32, np.uint8)
+    codes[0::2], codes[1::2] = c[:16] & 0xF, c[:16] >> 4
+    # 224 / 448 = 0.5 (code 1); the other twelve members are +0 (code 0)
+    assert codes[:16].tolist() == [7, 4, 12, 1] + [0] * 12
