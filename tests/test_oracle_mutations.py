@@ -144,6 +144,9 @@ MUTANTS = [
      "test_oracle_pins_rmsnorm.py::test_rmsnorm_matches_float64_within_one_ulp"),
     ("nvfp4_scale_cap_240", "const float kMaxScale = 448.0f;", "const float kMaxScale = 240.0f;",
      "test_oracle_pins_rope.py::test_nvfp4_scale_clamps_to_448"),
+    ("mxfp8_value_clamp_dropped", "        if (y > 448.0f) y = 448.0f;\n        if (y < -448.0f) y = -448.0f;\n        values[j] = oracle_e4m3_encode(y);",
+     "        values[j] = oracle_e4m3_encode(y);",
+     "test_oracle_pins_rope.py::test_mxfp8_scale_cap_depends_on_sanitising"),
     ("fscn_chunk_start_not_cut", "qs_t = np.maximum(qsl[r_safe], 0)", "qs_t = qsl[r_safe]",
      "test_oracle_pins_compress.py::test_cr2_chunk_bounds_are_cut_to_the_batch", "compress.py"),
 ]
