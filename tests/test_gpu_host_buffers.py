@@ -155,3 +155,46 @@ def test_attention_query_and_output_on_host():
     assert not out_h.is_cuda
     assert torch.equal(out_h.view(torch.int16), out_d.view(torch.int16).cpu())
     assert torch.equal(lse_h, lse_d.cpu())
+
+
+def test_rmsnorm_store_on_host_buffers():
+    """The RMSNorm-fused store with the latent, weight, slots and paged cache
+    in pinned host memory: byte for byte the oracle's cache."""
+    w = workloads.store_paged(seed=8)
+    nb, bs, bsr, off = w["num_blocks"], w["block_size"], w["block_stride_rows"], w["cache_offset"]
+    rng = np.random.default_rng(8)
+    weight = workloads.f32_to_bf16_bits(rng.uniform(0.5, 1.5, 512).astype(np.float32))
+    want = w["cache"].copy()
+    oracle.mxfp4_mla_rmsnorm_store(w["latent"], weight, 1e-6, w["slot_mapping"], want, nb, bs,
+                                   bsr, cache_offset=off)
+    buf = _pinned(w["cache"])
+    view = buf[off:].as_strided((nb, bs, ROW), (bsr * ROW, ROW, 1))
+    kvq.mxfp4_mla_rmsnorm_store(_pinned(w["latent"].view(np.int16)).view(torch.bfloat16),
+                                _pinned(weight.view(np.int16)).view(torch.bfloat16), 1e-6,
+                                _pinned(w["slot_mapping"]), view)
+    torch.cuda.synchronize()
+    assert G.first_diff(buf.numpy(), want) is None, G.first_diff(buf.numpy(), want)
+
+
+def test_compressor_on_host_buffers():
+    """fused_save_compress_norm with every argument in pinned host memory
+    gives the same latent rows and ring state, bit for bit, as with every
+    argument on the device."""
+    w = workloads.compress(seed=3, compress_ratio=2, num_reqs=64, max_chunk=100)
+    T = w["slot_mapping"].size
+    args = [w["kv_score"], w["positions"], w["state"], w["slot_mapping"], w["query_start_loc"],
+            w["token_to_req"]]
+    outs = []
+    for where in ("device", "host"):
+        put = G.to_dev if where == "device" else _pinned
+        kv, pos, st, sl, qsl, t2r = (put(a) for a in args)
+        wt = put(w["weight"].view(np.int16)).view(torch.bfloat16)
+        out = (torch.zeros((T, 512), dtype=torch.int16, device=G.DEV) if where == "device"
+               else torch.zeros((T, 512), dtype=torch.int16).pin_memory())
+        kvq.fused_save_compress_norm(kv, pos, st, sl, qsl, t2r, wt, w["eps"], 2,
+                                     out.view(torch.bfloat16))
+        torch.cuda.synchronize()
+        outs.append((out.cpu().numpy(), st.cpu().numpy().view(np.uint32)))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+    assert np.any(outs[0][0] != 0)
