@@ -192,15 +192,17 @@ __device__ __forceinline__ void quantize_store_run(uint4 x0, uint4 x1, uint8_t* 
   if ((lane & 1) == 0) st_u8(dst + 256 + (lane >> 1), (uint32_t)(e + 127));
 }
 
-// RMSNorm of one row held by the warp (fused variant), in the order this
-// library fixes so that the result is reproducible bit for bit: lane l sums
-// the squares of its 16 values (half 0 then half 1, left to right, each
-// square and sum rounded to binary32), an xor-butterfly over strides 1, 2, 4,
-// 8, 16 adds the lane sums (every lane ends with the same bits, since each
-// step adds the same two operands), then r = RN(1 / RN(sqrt(S / 512 + eps)))
-// with correctly rounded square root and reciprocal, y = bf16(x * r) and
-// z = bf16(y * w). A bf16 product is exact in binary32, so mul.rn.bf16x2
-// rounds it once.
+// RMSNorm of one row held by the warp (fused variant), in the order the
+// library's interface fixes: block k = elements 8k..8k+7 then
+// 256+8k..256+8k+7, its squares summed left to right, then a balanced
+// pairwise tree over the 32 block sums in block order; every square and sum
+// rounded to binary32. Here block k is exactly lane k's two 16-byte pieces,
+// and the xor-butterfly over strides 1, 2, 4, 8, 16 adds the same operands
+// as that tree (each step's two addends are the sums of neighbouring
+// subtrees, and the addition commutes, so every lane ends with the tree's
+// bits). Then r = RN(1 / RN(sqrt(S / 512 + eps))) with correctly rounded
+// square root and reciprocal, y = bf16(x * r) and z = bf16(y * w). A bf16
+// product is exact in binary32, so mul.rn.bf16x2 rounds it once.
 __device__ __forceinline__ uint32_t bf16x2_from_f32(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));

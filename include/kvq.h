@@ -134,13 +134,21 @@ int mxfp4_mla_store(const void* latent_bf16, int64_t num_tokens, int64_t latent_
  *
  * Per token with a valid slot: the RMSNorm below, then exactly what
  * mxfp4_mla_store does with the normalised bf16 row. The pages fix neither
- * the summation order nor the reciprocal square root; this library fixes
- * both so the result is reproducible bit for bit:
- *   lane sums  p_l = sum of x^2 over elements 8l..8l+7 then 256+8l..256+8l+7
- *              (l = 0..31, left to right, every square and sum in binary32),
- *   S          = xor-butterfly over l with strides 1, 2, 4, 8, 16,
- *   r          = RN(1 / RN(sqrt(RN(RN(S / 512) + eps)))),
+ * the summation order nor the reciprocal square root. This library fixes
+ * both as part of its interface, in element terms, so the result is
+ * reproducible bit for bit by any implementation:
+ *   blocks     block k (k = 0..31) = elements 8k..8k+7 followed by
+ *              256+8k..256+8k+7,
+ *   B_k        = the squares of block k's elements added left to right in
+ *              that order (every square and every sum rounded to binary32),
+ *   S          = balanced pairwise tree over B_0..B_31 in block order
+ *              ((B_0+B_1), (B_2+B_3), ..., then neighbouring pairs of those,
+ *              five levels),
+ *   r          = RN(1 / RN(sqrt(RN(S / 512 + eps)))),
  *   y          = bf16(RN(x * r)),   z = bf16(y * w).
+ * Any other order changes some outputs: a row on which this order, sixteen
+ * consecutive elements per block, and a plain left-to-right sum give three
+ * different results is among the library's tests.
  *
  * weight_bf16  bf16 [512], 16-byte aligned
  * eps          >= 0 and finite

@@ -474,37 +474,39 @@ void oracle_rope_quant_insert_nvfp4(const uint16_t* latent, int64_t num_tokens, 
 
 /* [store] store_mxfp4_mla takes "the post-RMSNorm latent"; the V4.1 page's
  * fused_save_compress_norm normalises with a bf16 [512] weight and an fp32
- * epsilon into a bf16 latent. The pages fix neither the summation order nor
- * how the reciprocal square root is formed, so this reading fixes both in a
- * form that can be reproduced exactly:
- *   partial[l] = x[8l]^2 + ... + x[8l+7]^2 + x[256+8l]^2 + ... + x[256+8l+7]^2
- *                (l = 0..31, accumulated left to right, each square and sum
- *                rounded to binary32),
- *   S = pairwise tree over l: partial[l] + partial[l ^ 1], then the pairs of
- *       those (l ^ 2), then l ^ 4, l ^ 8, l ^ 16,
+ * epsilon into a bf16 latent. The pages fix neither the order of the sum of
+ * squares nor how the reciprocal square root is formed. This library fixes
+ * both as part of its interface, in element terms:
+ *   blocks: the 512 elements form 32 blocks of sixteen; block k holds
+ *     elements 8k, 8k+1, ..., 8k+7 followed by 256+8k, ..., 256+8k+7;
+ *   B[k] = the squares of block k's elements added left to right in that
+ *     listed order, from +0 (every square and every sum rounded to binary32);
+ *   S = a balanced pairwise tree over B[0..31] in block order: B[0]+B[1],
+ *     B[2]+B[3], ..., then neighbouring results added pairwise again, five
+ *     levels in all;
  *   r = RN(1 / RN(sqrt(RN(S / 512 + eps)))),      (S / 512 is exact scaling)
  *   y = bf16(RN(x * r)),   z = bf16(y * w)        (y * w is exact in binary32).
  * The row is normalised when latent_dim is 512; z is then quantized exactly
  * as by oracle_mxfp4_mla_store. */
-static void rmsnorm_row_512(const uint16_t* x, const uint16_t* w, float eps, uint16_t* z) {
-    float partial[32];
-    for (int l = 0; l < 32; ++l) {
+static int rmsnorm_block_element(int k, int i) { return i < 8 ? 8 * k + i : 256 + 8 * k + (i - 8); }
+
+static float rmsnorm_sum_of_squares(const uint16_t* x) {
+    float sums[32];
+    for (int k = 0; k < 32; ++k) {
         float acc = 0.0f;
-        for (int h = 0; h < 2; ++h) {
-            for (int k = 0; k < 8; ++k) {
-                float v = bf16_to_f32(x[256 * h + 8 * l + k]);
-                float sq = v * v;
-                acc = acc + sq;
-            }
+        for (int i = 0; i < 16; ++i) {
+            float v = bf16_to_f32(x[rmsnorm_block_element(k, i)]);
+            acc = acc + v * v;
         }
-        partial[l] = acc;
+        sums[k] = acc;
     }
-    for (int stride = 1; stride < 32; stride *= 2) {
-        float next[32];
-        for (int l = 0; l < 32; ++l) next[l] = partial[l] + partial[l ^ stride];
-        memcpy(partial, next, sizeof next);
-    }
-    float mean = partial[0] / 512.0f;
+    for (int n = 32; n > 1; n /= 2)
+        for (int k = 0; k < n / 2; ++k) sums[k] = sums[2 * k] + sums[2 * k + 1];
+    return sums[0];
+}
+
+static void rmsnorm_row_512(const uint16_t* x, const uint16_t* w, float eps, uint16_t* z) {
+    float mean = rmsnorm_sum_of_squares(x) / 512.0f;
     float var = mean + eps;
     float root = sqrtf(var);
     float r = 1.0f / root;

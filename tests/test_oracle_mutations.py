@@ -56,7 +56,8 @@ MUTANTS = [
      "    return lower + 1.0f;", "test_oracle_pins_formats.py::test_e4m3_named_values"),
     ("rmsnorm_eps_dropped", "float var = mean + eps;", "float var = mean;",
      "test_oracle_pins_rmsnorm.py::test_rmsnorm_eps_sits_inside_the_root"),
-    ("rmsnorm_mean_511", "float mean = partial[0] / 512.0f;", "float mean = partial[0] / 511.0f;",
+    ("rmsnorm_mean_511", "float mean = rmsnorm_sum_of_squares(x) / 512.0f;",
+     "float mean = rmsnorm_sum_of_squares(x) / 511.0f;",
      "test_oracle_pins_rmsnorm.py::test_rmsnorm_matches_float64_within_one_ulp"),
     ("rmsnorm_weight_dropped", "float yw = bf16_to_f32(y) * bf16_to_f32(w[j]);",
      "float yw = bf16_to_f32(y);",
@@ -64,6 +65,15 @@ MUTANTS = [
     ("rmsnorm_y_unrounded", "float yw = bf16_to_f32(y) * bf16_to_f32(w[j]);",
      "float yw = xr * bf16_to_f32(w[j]); (void)y;",
      "test_oracle_pins_rmsnorm.py::test_rmsnorm_matches_float64_within_one_ulp"),
+    ("rmsnorm_runs_of_16",
+     "static int rmsnorm_block_element(int k, int i) { return i < 8 ? 8 * k + i : 256 + 8 * k + (i - 8); }",
+     "static int rmsnorm_block_element(int k, int i) { return 16 * k + i; }",
+     "test_oracle_pins_rmsnorm.py::test_rmsnorm_summation_order_golden"),
+    ("rmsnorm_left_to_right",
+     "        for (int k = 0; k < n / 2; ++k) sums[k] = sums[2 * k] + sums[2 * k + 1];\n    return sums[0];",
+     "        ;\n    { float a = 0.0f; for (int j = 0; j < 512; ++j) { float v = bf16_to_f32(x[j]); "
+     "a = a + v * v; } return a; }",
+     "test_oracle_pins_rmsnorm.py::test_rmsnorm_summation_order_golden"),
     ("gather_scale_byte", "uint8_t scale_byte = row[latent_dim / 2 + j / group];",
      "uint8_t scale_byte = row[latent_dim / 2 + j / group] + 1;",
      "test_oracle_pins_store.py::test_gather_equals_independent_decode"),

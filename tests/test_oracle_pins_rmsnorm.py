@@ -3,10 +3,17 @@
 Pages: 'vllm.v1.attention.ops.mxfp4_mla.store' (store_mxfp4_mla takes the
 post-RMSNorm latent) and 'vllm.models.deepseek_v41.common.ops.
 fused_compress_quant_cache' (fused_save_compress_norm: bf16 [512] weight, fp32
-epsilon, bf16 latent out). The summation order and the reciprocal square root
-are this build's reading (kvq_oracle.c); the pins below check the formula
-against float64 and against cases where the result is exact whatever the order.
+epsilon, bf16 latent out). The pages fix no summation order: the library fixes
+one as part of its interface (block k = elements 8k..8k+7 then
+256+8k..256+8k+7, summed left to right; the 32 block sums added as a balanced
+pairwise tree). The pins below check the formula against float64, against
+cases where the result is exact whatever the order, and the order itself
+against a hand-derived row on which three different orders give three
+different outputs (tests/golden/rmsnorm_order_worked.json).
 """
+import json
+import os
+
 import numpy as np
 
 import oracle
@@ -92,3 +99,53 @@ def test_fused_store_equals_rmsnorm_then_store():
     oracle.mxfp4_mla_rmsnorm_store(x, w, 1e-5, slots, a, 1, 128, 128)
     oracle.mxfp4_mla_store(oracle.rmsnorm_rows(x, w, 1e-5), slots, b, 1, 128, 128)
     assert np.array_equal(a, b)
+
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "rmsnorm_order_worked.json")
+
+
+def _order_row():
+    g = json.load(open(GOLDEN))
+    x = np.full(512, 0x3F80, np.uint16)                     # ones
+    x[6:8] = 0
+    x[256:264] = 0
+    for j, v in g["row"]["values"].items():
+        x[int(j)] = _bf16(np.float32([v]))[0]
+    eps = float(np.array([int(g["row"]["eps_f32_hex"], 16)], np.uint32).view(np.float32)[0])
+    return g, x, eps
+
+
+def _expected(spec):
+    want = np.full(512, int(spec["ones"], 16), np.uint16)
+    want[6:8] = int(spec["zeros"], 16)
+    want[256:264] = int(spec["zeros"], 16)
+    for j in range(6):
+        want[j] = int(spec[str(j)], 16)
+    return want
+
+
+def test_rmsnorm_summation_order_golden():
+    """The library's order (blocks of 8k..8k+7, 256+8k..256+8k+7, then a
+    pairwise tree) gives the hand-derived row; the run-of-16 order and a
+    left-to-right sum would give other rows."""
+    g, x, eps = _order_row()
+    assert eps == np.float32(1e-6)
+    w = np.full(512, 0x3F80, np.uint16)
+    rows = {k: _expected(v) for k, v in g["expected_bf16_hex"].items()}
+    assert not np.array_equal(rows["contract"], rows["run16"])
+    assert not np.array_equal(rows["run16"], rows["sequential"])
+    assert not np.array_equal(rows["contract"], rows["sequential"])
+    got = oracle.rmsnorm_rows(x[None, :], w, eps)[0]
+    assert np.array_equal(got, rows["contract"]), [
+        (j, hex(got[j]), hex(rows["contract"][j])) for j in np.nonzero(got != rows["contract"])[0]]
+
+
+def test_rmsnorm_order_golden_row_is_what_the_derivation_says():
+    """The fixture's own arithmetic, checked with exact integers: the three
+    sums of squares and the fact that eps vanishes next to S/512."""
+    g, x, eps = _order_row()
+    v = ind.bf16_bits_to_f32(x).astype(np.float64)
+    assert np.sum(v != 0) == 502 and np.sum(v == 1.0) == 496
+    exact = int(np.sum(v * v))
+    assert exact == 2 ** 24 + 213344 + 496
+    assert eps < 2.0 ** -9   # below half the binary32 spacing at S/512 ~ 33185
