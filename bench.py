@@ -104,17 +104,24 @@ def bf16_peak():
         return 1900.0, "fallback (1.9 PFLOP/s)"
 
 
-def attention_case(torch, kvq, dev, cache, idx, valid):
+def attention_case(torch, kvq, dev, cache, idx, valid, split=True):
     """(call, flops, hbm bytes, status tensor) of sparse attention over the
-    gather workload's cache and indices: 128 queries x 128 heads."""
+    gather workload's cache and indices: 128 queries x 128 heads. ``split``:
+    the key tiles split evenly over the SMs with a preallocated workspace
+    (the attention kernel and the merge of split units, both timed), else one
+    CTA per (query, value half)."""
     q = torch.from_numpy(workloads.attention_queries(0, 128, 128).view(np.int16)).to(dev)
     q = q.view(torch.bfloat16)
     idx2 = idx.view(128, -1)
     outa = torch.empty((128, 128, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((128, 128), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = False
+    if split:
+        ws = torch.empty(max(1, kvq.attention_workspace_size(128, 128, idx2.shape[1])),
+                         dtype=torch.uint8, device=dev)
     call = lambda: kvq.mxfp4_mla_sparse_attention(  # noqa: E731
-        q, cache, idx2, 1.0 / 512 ** 0.5, out=outa, lse=lse, status=status)
+        q, cache, idx2, 1.0 / 512 ** 0.5, out=outa, lse=lse, status=status, workspace=ws)
     flops = 4.0 * 128 * valid * 512            # q.k and p.v over the valid keys, 128 heads
     hbm = ROW * valid + 8 * idx.numel() + 2 * 128 * 128 * 1024 + 4 * 128 * 128
     return call, flops, hbm, status
@@ -518,7 +525,12 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
         "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
         "l2": "flushed before each rep (512 MB written, then 1 GiB read)"}
 
-    # sparse MLA decode attention on the same packed cache and indices
+    # sparse MLA decode attention on the same packed cache and indices: one
+    # CTA per (query, value half), then the split-K schedule (reported)
+    call, _, _, status0 = attention_case(torch, kvq, dev, cache, idx, valid, split=False)
+    for _ in range(3):
+        call()
+    ms_unsplit, _ = time_events(torch, call, 20, stream, flush=flush)
     call, flops, hbm, status = attention_case(torch, kvq, dev, cache, idx, valid)
     for _ in range(3):
         call()
@@ -529,7 +541,10 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
         "ms": ms, "algorithmic_flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
         "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tpeak, "bf16_peak_tflops": tpeak,
         "bf16_peak_source": tpeak_src, "hbm_bytes": hbm, "gbs": hbm / (ms * 1e-3) / 1e9,
-        "wait_status": int(status.item()),
+        "wait_status": int(status.item()) | int(status0.item()),
+        "schedule": "split-K: key tiles split evenly over one CTA per SM, partials merged by "
+                    "log-sum-exp (both kernels timed)",
+        "unsplit_ms": ms_unsplit, "unsplit_tflops": flops / (ms_unsplit * 1e-3) / 1e12,
         "l2": "flushed before each rep (512 MB written, then 1 GiB read)"}
     return out
 

@@ -15,6 +15,7 @@ read and write host memory over the host-device link, with no copies).
   mxfp4_mla_gather_dequant   gather packed rows back to bf16
   mxfp4_mla_sparse_attention sparse MLA decode attention on the packed cache
 """
+import contextlib
 import ctypes
 import os
 
@@ -23,12 +24,14 @@ import torch
 __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
            "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
            "save_ring_rows", "fused_save_compress_norm",
-           "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "row_bytes",
+           "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "attention_workspace_size",
+           "row_bytes",
            "cache_view", "KvqError", "lib", "KVQ_PTR_DEVICE", "KVQ_PTR_HOST_MAPPED",
            "LIBRARY_PATH"]
 
 LIBRARY_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
 KVQ_OK, KVQ_EINVAL, KVQ_ECUDA = 0, -1, -2
+KVQ_ETIMEOUT = -3  # raised by the binding only: a kernel's status word was set
 
 _i64, _i32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
 _LIB = None
@@ -37,7 +40,9 @@ _LIB = None
 class KvqError(RuntimeError):
     def __init__(self, name, status):
         self.status = status
-        super().__init__(f"{name} failed: {lib().kvq_strerror(status).decode()} (status {status})")
+        what = ("an internal wait of the kernel timed out; the output is undefined"
+                if status == KVQ_ETIMEOUT else lib().kvq_strerror(status).decode())
+        super().__init__(f"{name} failed: {what} (status {status})")
 
 
 def lib() -> ctypes.CDLL:
@@ -82,7 +87,9 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_mla_sparse_attention.restype = ctypes.c_int
         L.mxfp4_mla_sparse_attention.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64, _i64,
                                                  _p, _i64, ctypes.c_float, _p, _i64, _i64, _p, _p,
-                                                 _p]
+                                                 _p, _i64, _p]
+        L.mxfp4_mla_sparse_attention_workspace_size.restype = _i64
+        L.mxfp4_mla_sparse_attention_workspace_size.argtypes = [_i64, _i64, _i64]
         _LIB = L
     return _LIB
 
@@ -96,6 +103,35 @@ def _stream(stream):
 def _check(name, status):
     if status != KVQ_OK:
         raise KvqError(name, status)
+
+
+def _device(name, tensors, stream=None):
+    """The index of the one CUDA device that every CUDA tensor in `tensors`
+    (and a torch stream, if given) lives on, or None when all are pinned host
+    tensors. Kernels run on the current device and take raw pointers, so a
+    tensor of another GPU would be an illegal address there: raise instead."""
+    dev = None
+    for t in tensors:
+        if t is None or not t.is_cuda:
+            continue
+        i = t.device.index if t.device.index is not None else torch.cuda.current_device()
+        if dev is None:
+            dev = i
+        elif i != dev:
+            raise TypeError(f"{name}: tensors on cuda:{dev} and cuda:{i}; all CUDA arguments must "
+                            "be on one device")
+    if isinstance(stream, torch.cuda.Stream) and dev is not None and stream.device.index != dev:
+        raise TypeError(f"{name}: the stream belongs to cuda:{stream.device.index}, the tensors "
+                        f"to cuda:{dev}")
+    return dev
+
+
+def _launch(name, tensors, stream, call):
+    """Run `call(stream_handle)` with the tensors' device current (so the
+    default stream is that device's) and raise on a nonzero status."""
+    dev = _device(name, tensors, stream)
+    with torch.cuda.device(dev) if dev is not None else contextlib.nullcontext():
+        _check(name, call(_stream(stream)))
 
 
 KVQ_PTR_DEVICE, KVQ_PTR_HOST_MAPPED = 1, 2
@@ -156,9 +192,9 @@ def mxfp4_mla_store(latent: torch.Tensor, slot_mapping: torch.Tensor, cache: tor
             not slot_mapping.is_contiguous():
         raise ValueError("slot_mapping must be a contiguous [tokens] tensor")
     nb, bs, bsr = cache_view(cache, row_bytes(latent.shape[1], group))
-    _check("mxfp4_mla_store", lib().mxfp4_mla_store(
+    _launch("mxfp4_mla_store", (latent, slot_mapping, cache), stream, lambda s: lib().mxfp4_mla_store(
         latent.data_ptr(), latent.shape[0], latent.shape[1], latent.stride(0),
-        slot_mapping.data_ptr(), cache.data_ptr(), nb, bs, bsr, group, _stream(stream)))
+        slot_mapping.data_ptr(), cache.data_ptr(), nb, bs, bsr, group, s))
 
 
 def mxfp4_mla_rmsnorm_store(latent: torch.Tensor, weight: torch.Tensor, eps: float,
@@ -177,10 +213,11 @@ def mxfp4_mla_rmsnorm_store(latent: torch.Tensor, weight: torch.Tensor, eps: flo
             not slot_mapping.is_contiguous():
         raise ValueError("slot_mapping must be a contiguous [tokens] tensor")
     nb, bs, bsr = cache_view(cache, row_bytes(latent.shape[1], group))
-    _check("mxfp4_mla_rmsnorm_store", lib().mxfp4_mla_rmsnorm_store(
-        latent.data_ptr(), latent.shape[0], latent.shape[1], latent.stride(0), weight.data_ptr(),
-        float(eps), slot_mapping.data_ptr(), cache.data_ptr(), nb, bs, bsr, group,
-        _stream(stream)))
+    _launch("mxfp4_mla_rmsnorm_store", (latent, weight, slot_mapping, cache), stream,
+            lambda s: lib().mxfp4_mla_rmsnorm_store(
+                latent.data_ptr(), latent.shape[0], latent.shape[1], latent.stride(0),
+                weight.data_ptr(), float(eps), slot_mapping.data_ptr(), cache.data_ptr(), nb, bs,
+                bsr, group, s))
 
 
 def _rope_inputs(latent, positions, cos_sin, slot_mapping):
@@ -205,11 +242,12 @@ def _rope(name, record, latent, positions, cos_sin, kv_cache, slot_mapping, comp
     _need(kv_cache, torch.uint8, "kv_cache")
     if kv_cache.dim() != 3 or kv_cache.shape[-1] != record or not kv_cache[0].is_contiguous():
         raise ValueError(f"kv_cache must be [pages, cache_block, {record}] with contiguous pages")
-    _check(name, getattr(lib(), name)(
-        latent.data_ptr(), n, latent.stride(0), positions.data_ptr(), cos_sin.data_ptr(),
-        cos_sin.stride(0), cos_sin.shape[0], kv_cache.data_ptr(), slot_mapping.data_ptr(),
-        kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), int(compress_ratio),
-        1 if sanitize_nans else 0, _stream(stream)))
+    _launch(name, (latent, positions, cos_sin, kv_cache, slot_mapping), stream,
+            lambda s: getattr(lib(), name)(
+                latent.data_ptr(), n, latent.stride(0), positions.data_ptr(), cos_sin.data_ptr(),
+                cos_sin.stride(0), cos_sin.shape[0], kv_cache.data_ptr(), slot_mapping.data_ptr(),
+                kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), int(compress_ratio),
+                1 if sanitize_nans else 0, s))
 
 
 def rope_quant_insert_mxfp8(latent, positions, cos_sin, kv_cache, slot_mapping, compress_ratio,
@@ -255,11 +293,12 @@ def rope_plain_insert(latent, positions, cos_sin, kv_cache, slot_mapping, compre
                         "device's address space")
     if kv_cache.dim() != 3 or kv_cache.shape[2] != 512 or kv_cache.stride(2) != 1:
         raise ValueError("kv_cache must be [pages, cache_block, 512] with unit last stride")
-    _check("rope_plain_insert", lib().rope_plain_insert(
-        latent.data_ptr(), n, latent.stride(0), positions.data_ptr(), cos_sin.data_ptr(),
-        cos_sin.stride(0), cos_sin.shape[0], kv_cache.data_ptr(), slot_mapping.data_ptr(),
-        kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1),
-        int(compress_ratio), fp8, scale, _stream(stream)))
+    _launch("rope_plain_insert", (latent, positions, cos_sin, kv_cache, slot_mapping), stream,
+            lambda s: lib().rope_plain_insert(
+                latent.data_ptr(), n, latent.stride(0), positions.data_ptr(), cos_sin.data_ptr(),
+                cos_sin.stride(0), cos_sin.shape[0], kv_cache.data_ptr(), slot_mapping.data_ptr(),
+                kv_cache.shape[0], kv_cache.shape[1], kv_cache.stride(0), kv_cache.stride(1),
+                int(compress_ratio), fp8, scale, s))
 
 
 def save_ring_rows(rows: torch.Tensor, slot_mapping: torch.Tensor, state: torch.Tensor,
@@ -275,10 +314,9 @@ def save_ring_rows(rows: torch.Tensor, slot_mapping: torch.Tensor, state: torch.
         raise ValueError("state must be [blocks, state_block, >= 1024] with unit last stride")
     if slot_mapping.numel() > rows.shape[0] or not slot_mapping.is_contiguous():
         raise ValueError("slot_mapping must be contiguous and cover the rows")
-    _check("save_ring_rows", lib().save_ring_rows(
+    _launch("save_ring_rows", (rows, slot_mapping, state), stream, lambda s: lib().save_ring_rows(
         rows.data_ptr(), slot_mapping.numel(), rows.stride(0), slot_mapping.data_ptr(),
-        state.data_ptr(), state.shape[0], state.shape[1], state.stride(0), state.stride(1),
-        _stream(stream)))
+        state.data_ptr(), state.shape[0], state.shape[1], state.stride(0), state.stride(1), s))
 
 
 def fused_save_compress_norm(kv_score, positions, state_cache, slot_mapping, query_start_loc,
@@ -334,11 +372,14 @@ def fused_save_compress_norm(kv_score, positions, state_cache, slot_mapping, que
             nprev, pst = prev_rows.shape[0], prev_rows.stride(0)
     elif R != 1:
         raise ValueError("compress_ratio must be 1 or 2")
-    _check("fused_save_compress_norm", lib().fused_save_compress_norm(
+    args = (kv_score, positions, slot_mapping, rms_norm_weight, latent_out) + (
+        (query_start_loc, token_to_req_indices, state_cache, prev_rows, prev_row_indices)
+        if R == 2 else ())
+    _launch("fused_save_compress_norm", args, stream, lambda s: lib().fused_save_compress_norm(
         kv_score.data_ptr(), n, kv_score.stride(0), positions.data_ptr(), slot_mapping.data_ptr(),
         R, qsl, t2r, nreq, st, nb, cap, sst, srs, rms_norm_weight.data_ptr(),
         float(rms_norm_eps), prev, nprev, pst, pidx, latent_out.data_ptr(),
-        latent_out.stride(0), _stream(stream)))
+        latent_out.stride(0), s))
 
 
 def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor = None,
@@ -356,20 +397,30 @@ def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: to
     flat = out.view(-1, latent_dim) if out.is_contiguous() else out.reshape(-1, latent_dim)
     if flat.data_ptr() != out.data_ptr() or flat.stride(1) != 1:
         raise ValueError("out must be viewable as [num_indices, latent_dim] without a copy")
-    _check("mxfp4_mla_gather_dequant", lib().mxfp4_mla_gather_dequant(
-        cache.data_ptr(), nb, bs, bsr, latent_dim, indices.data_ptr(), indices.numel(),
-        out.data_ptr(), flat.stride(0), _stream(stream)))
+    _launch("mxfp4_mla_gather_dequant", (cache, indices, out), stream,
+            lambda s: lib().mxfp4_mla_gather_dequant(
+                cache.data_ptr(), nb, bs, bsr, latent_dim, indices.data_ptr(), indices.numel(),
+                out.data_ptr(), flat.stride(0), s))
     return out
 
 
 def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tensor,
                                sm_scale: float, out: torch.Tensor = None, lse: torch.Tensor = None,
-                               status: torch.Tensor = None, stream=None):
+                               status: torch.Tensor = None, workspace=True, stream=None):
     """q: bf16 [num_queries, num_heads <= 128, 512] (unit last stride, strides
     multiples of 8); cache: uint8 paged view (see cache_view) of 272-byte rows;
     indices: int64 [num_queries, topk] (contiguous; -1 pads). Returns (out bf16
     [num_queries, num_heads, 512], lse fp32 [num_queries, num_heads] or None).
-    ``status`` (int32, one element) is set nonzero if a kernel wait timed out."""
+
+    ``workspace``: True (default) splits the key tiles evenly over the SMs
+    with a workspace allocated here, False runs one CTA per (query, value
+    half) with none, or a uint8 device tensor of at least
+    ``attention_workspace_size(...)`` bytes to use.
+    ``status``: an int32 device tensor of one element that the kernel sets
+    nonzero if an internal wait timed out (the output is then undefined); the
+    caller reads it. Without one, a status word is made here and read back
+    after the launch (this synchronises the stream) and KvqError is raised
+    if it is set."""
     _need(q, torch.bfloat16, "q")
     _need(indices, torch.int64, "indices")
     if q.dim() != 3 or q.shape[2] != 512 or q.stride(2) != 1:
@@ -378,6 +429,8 @@ def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: to
     if indices.dim() != 2 or indices.shape[0] != nq or not indices.is_contiguous():
         raise ValueError("indices must be a contiguous [num_queries, topk] tensor")
     nb, bs, bsr = cache_view(cache, row_bytes(512, 32))
+    dev = _device("mxfp4_mla_sparse_attention", (q, cache, indices, out, lse, status), stream)
+    cuda_dev = torch.device("cuda", dev if dev is not None else torch.cuda.current_device())
     if out is None:
         out = torch.empty((nq, nh, 512), dtype=torch.bfloat16, device=q.device,
                           pin_memory=not q.is_cuda)
@@ -388,11 +441,35 @@ def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: to
         _need(lse, torch.float32, "lse")
         if tuple(lse.shape) != (nq, nh) or not lse.is_contiguous():
             raise ValueError("lse must be a contiguous [num_queries, num_heads] tensor")
-    if status is not None:
+    own_status = status is None
+    with torch.cuda.device(cuda_dev):
+        if own_status:
+            status = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
         _need(status, torch.int32, "status")
-    _check("mxfp4_mla_sparse_attention", lib().mxfp4_mla_sparse_attention(
-        q.data_ptr(), nq, nh, q.stride(0), q.stride(1), cache.data_ptr(), nb, bs, bsr,
-        indices.data_ptr(), indices.shape[1], float(sm_scale), out.data_ptr(), out.stride(0),
-        out.stride(1), lse.data_ptr() if lse is not None else None,
-        status.data_ptr() if status is not None else None, _stream(stream)))
+        if workspace is True:
+            nbytes = attention_workspace_size(nq, nh, indices.shape[1])
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=cuda_dev) \
+                if nbytes > 0 else None
+        elif workspace is False:
+            workspace = None
+        if workspace is not None:
+            _need(workspace, torch.uint8, "workspace")
+    _launch("mxfp4_mla_sparse_attention", (q, cache, indices, out, lse, status, workspace), stream,
+            lambda s: lib().mxfp4_mla_sparse_attention(
+                q.data_ptr(), nq, nh, q.stride(0), q.stride(1), cache.data_ptr(), nb, bs, bsr,
+                indices.data_ptr(), indices.shape[1], float(sm_scale), out.data_ptr(),
+                out.stride(0), out.stride(1), lse.data_ptr() if lse is not None else None,
+                status.data_ptr(), workspace.data_ptr() if workspace is not None else None,
+                workspace.numel() if workspace is not None else 0, s))
+    if own_status and int(status.item()) != 0:
+        raise KvqError("mxfp4_mla_sparse_attention", KVQ_ETIMEOUT)
     return out, lse
+
+
+def attention_workspace_size(num_queries: int, num_heads: int, topk: int) -> int:
+    """Workspace bytes mxfp4_mla_sparse_attention needs to split these shapes
+    over the current device's SMs (0: nothing to split)."""
+    n = int(lib().mxfp4_mla_sparse_attention_workspace_size(num_queries, num_heads, topk))
+    if n < 0:
+        raise KvqError("mxfp4_mla_sparse_attention_workspace_size", n)
+    return n

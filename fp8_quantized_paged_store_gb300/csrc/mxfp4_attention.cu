@@ -7,9 +7,23 @@
 // attention over the dequantized bf16 values). For the rope-free latent the
 // key and the value of a token are the same 512-wide row.
 //
-// Work decomposition. One CTA per (query, half of the 512 value columns): the
-// two CTAs of a query both form the full scores q.k (512-deep) and each
-// accumulates 256 output columns. Tensor memory (512 columns x 128 lanes,
+// Work decomposition. A unit of work is (query, half of the 512 value
+// columns): the two units of a query both form the full scores q.k
+// (512-deep) and each accumulates 256 output columns. A unit is a run of
+// 32-key tiles; the units' tiles laid end to end (query-major, half 0 before
+// half 1) are cut into one contiguous range per CTA of a grid of one CTA per
+// SM, so that every SM gets the same number of tiles whatever the number of
+// units (the split-K of the read path). A CTA walks its range as segments,
+// one per unit it touches: a segment that covers its whole unit writes the
+// output; one that covers part of a unit writes an fp32 partial (the output
+// normalised by the piece's own softmax sum, and that sum's log-sum-exp)
+// into a caller-provided workspace, and a second, small kernel combines the
+// pieces of each split unit by their log-sum-exps. Between segments the CTA
+// reads the output accumulator out and, when the query changes, reloads Q;
+// the producers keep streaming the next segment's keys meanwhile. Without a
+// workspace the grid has one CTA per unit and nothing is split.
+//
+// Each CTA: tensor memory (512 columns x 128 lanes,
 // lane = head) holds the output accumulator (256 columns), four 32-key score
 // buffers (128; softmax writes the bf16 probabilities P back over the scores
 // of the same buffer, and p.v takes P from there as its A operand) and the
@@ -38,6 +52,9 @@
 //     tensor memory.
 // Every wait is bounded; a timeout sets a CTA-wide abort flag that ends the
 // other roles' waits, and the CTA reports through an optional status word.
+// Before tensor memory is released, the issuing thread waits (bounded, abort
+// or not) for every MMA it issued, so that none writes released tensor
+// memory or arrives on a released barrier.
 //
 // Numerics: scores and the output accumulate in fp32 on the tensor core from
 // exact bf16 inputs (the dequantized rows are exact); the probabilities are
@@ -72,14 +89,18 @@ constexpr uint32_t kKBlock = kTileKeys * 128;            // bytes of one K-block
 constexpr uint32_t kKBlockStride = kStages * kKBlock;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQhiBytes;            // kStages buffers
-constexpr uint32_t kOffBar = kOffK + kStages * kKBytes;  // sixteen mbarriers
-constexpr uint32_t kOffTmemSlot = kOffBar + 128;
+constexpr uint32_t kOffBar = kOffK + kStages * kKBytes;  // eighteen mbarriers
+constexpr uint32_t kOffTmemSlot = kOffBar + 160;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 16;
 constexpr uint32_t kSmemUsed = kOffAbort + 16;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
 
-// mbarriers, one of each per stage (tile t uses stage t % kStages)
+// mbarriers, one of each per stage (the CTA's i-th tile uses stage i % kStages),
+// then one that softmax completes at every segment boundary (the output
+// accumulator has been read out and, for a new query, Q reloaded), and one
+// the issuer commits its last MMAs to before tensor memory is released
 constexpr uint32_t kBarKFull = 0, kBarSFull = 32, kBarPFull = 64, kBarPvDone = 96;
+constexpr uint32_t kBarSeg = 128, kBarDrain = 136;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
@@ -101,6 +122,19 @@ struct AttnParams {
   int64_t o_qstride, o_hstride;
   float* lse;              // [num_queries, num_heads] or null
   int32_t* status;         // or null
+  // Schedule: unit k = (query k / 2, value half k % 2) is `tiles` tiles of
+  // 32 keys; the units' tiles laid end to end (`total` of them) are split
+  // into `grid` contiguous ranges, CTA b taking [total*b/grid,
+  // total*(b+1)/grid).
+  int64_t tiles, units, total;
+  int64_t grid;
+  // Partial results of units split between CTAs (null when grid is one CTA
+  // per unit, so that nothing is split): piece slot 2b (CTA b's first
+  // segment) or 2b + 1 (its last), [2 * grid][num_heads][256] fp32 outputs
+  // normalised by the piece's softmax sum, and [2 * grid][num_heads] that
+  // sum's log-sum-exp in log2 units (-inf for a piece without valid keys).
+  float* part_o;
+  float* part_lse;
 };
 
 // ------------------------------------------------------------------ PTX ---
@@ -294,6 +328,7 @@ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major) {
 }
 
 constexpr uint32_t kIdescQK = instr_desc(kHeads, 2 * kTileKeys, false);
+constexpr uint32_t kIdescQK1 = instr_desc(kHeads, kTileKeys, false);
 constexpr uint32_t kIdescPV = instr_desc(kHeads, kHalf, true);
 
 // --------------------------------------------------------------- producer ---
@@ -307,9 +342,22 @@ struct Packed {
   uint32_t s;
 };
 
-__device__ __forceinline__ int64_t key_index(const AttnParams& p, const int64_t* idx_row,
-                                             int64_t k) {
-  return k < p.topk ? ld_once_i64(idx_row + k) : -1;
+// Position in a CTA's run of tiles: unit (query << 1 | value half) and the
+// tile within the unit.
+struct Cursor {
+  int64_t unit, t;
+  __device__ __forceinline__ void next(int64_t tiles) {
+    if (++t == tiles) {
+      t = 0;
+      ++unit;
+    }
+  }
+};
+
+// Slot index of key j of the cursor's tile, or -1 past the query's top-k.
+__device__ __forceinline__ int64_t key_index(const AttnParams& p, const Cursor& c, int j) {
+  const int64_t k = c.t * kTileKeys + j;
+  return k < p.topk ? ld_once_i64(p.indices + (c.unit >> 1) * p.topk + k) : -1;
 }
 
 __device__ __forceinline__ uint32_t ld_issue_u16(const void* p) {
@@ -372,13 +420,14 @@ __device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t byte_of
   return base_desc + (uint64_t)(byte_offset >> 4);
 }
 
-// S(t), S(t+1) = Q K^T over the pair of stages t % kStages (even) and the
-// next, into their score columns (N = 64): dims 0..255 with Q from TMEM (16
-// steps of 8 columns), dims 256..511 with Q from shared memory. When t is the
-// last tile, the second half computes scores of a stage no tile reads.
-__device__ __forceinline__ void issue_qk(int64_t t, uint64_t q_desc, uint32_t k_base,
+// S = Q K^T into the score columns of stage `st` (N = 32), or of the pair of
+// stages st (even) and st + 1 (N = 64: the ring is K-block-major, so the
+// same K-block of the two stages is one 64-row operand): dims 0..255 with Q
+// from TMEM (16 steps of 8 columns), dims 256..511 with Q from shared memory.
+template <bool kPair>
+__device__ __forceinline__ void issue_qk(uint32_t st, uint64_t q_desc, uint32_t k_base,
                                          uint32_t tmem) {
-  const uint32_t st = (uint32_t)(t % kStages);
+  constexpr uint32_t idesc = kPair ? kIdescQK : kIdescQK1;
   const uint64_t k_desc = smem_desc(k_base + st * kKBlock, 16, 1024, 2);
   const uint32_t d = tmem + kColS + st * kTileKeys;
 #pragma unroll
@@ -386,64 +435,46 @@ __device__ __forceinline__ void issue_qk(int64_t t, uint64_t q_desc, uint32_t k_
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
       mma_bf16_ta(d, tmem + kColQ + (uint32_t)(8 * (4 * kb + ks)),
-                  desc_at(k_desc, kb * kKBlockStride + ks * 32), kIdescQK, (kb | ks) != 0);
+                  desc_at(k_desc, kb * kKBlockStride + ks * 32), idesc, (kb | ks) != 0);
   }
 #pragma unroll
   for (int kb = 4; kb < 8; ++kb) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
       mma_bf16(d, desc_at(q_desc, (kb - 4) * (kHeads * 128) + ks * 32),
-               desc_at(k_desc, kb * kKBlockStride + ks * 32), kIdescQK, 1);
+               desc_at(k_desc, kb * kKBlockStride + ks * 32), idesc, 1);
   }
 }
 
-// O (+)= P(t) V(t): P (bf16 pairs, written by softmax over the score
-// columns of stage t % kStages) is the TMEM A operand, 8 columns per step of
-// 16 keys; V is the stage's key rows read MN-major from column block 4v
-// (LBO: the stage's next K-block, SBO: next 8 keys).
-__device__ __forceinline__ void issue_pv(int64_t t, int v, uint32_t k_base, uint32_t tmem) {
-  const uint32_t st = (uint32_t)(t % kStages);
+// O (+)= P V of the tile in stage `st`: P (bf16 pairs, written by softmax
+// over the stage's score columns) is the TMEM A operand, 8 columns per step
+// of 16 keys; V is the stage's key rows read MN-major from column block 4v
+// (LBO: the stage's next K-block, SBO: next 8 keys). `first` starts a new
+// accumulation (the first tile of a segment).
+__device__ __forceinline__ void issue_pv(uint32_t st, int v, bool first, uint32_t k_base,
+                                         uint32_t tmem) {
   const uint64_t v_desc = smem_desc(k_base + ((uint32_t)v * 4 * kStages + st) * kKBlock,
                                     kKBlockStride, 1024, 2);
   const uint32_t pa = tmem + kColS + st * kTileKeys;
 #pragma unroll
   for (int ks = 0; ks < kTileKeys / 16; ++ks)
-    mma_bf16_ta(tmem + kColO, pa + 8 * ks, desc_at(v_desc, ks * 2048), kIdescPV, (t | ks) != 0);
+    mma_bf16_ta(tmem + kColO, pa + 8 * ks, desc_at(v_desc, ks * 2048), kIdescPV,
+                !(first && ks == 0));
 }
 
 // ---------------------------------------------------------------- kernel ---
 
-__global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sm = smem_raw + (base - raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t n = blockIdx.x >> 1;
-  const int v = blockIdx.x & 1;
-  const uint32_t q_base = base + kOffQ, k_base = base + kOffK;
-  const uint32_t bars = base + kOffBar;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
-  volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
-  const int64_t num_tiles = (p.topk + kTileKeys - 1) / kTileKeys;
-  const int64_t* idx_row = p.indices + n * p.topk;
-
-  if (warp == kIssuerWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-  if (tid == 0) {
-#pragma unroll
-    for (int b = 0; b < kStages; ++b) {
-      mbar_init(bars + kBarKFull + 8 * b, 256);
-      mbar_init(bars + kBarSFull + 8 * b, 1);
-      mbar_init(bars + kBarPFull + 8 * b, 128);
-      mbar_init(bars + kBarPvDone + 8 * b, 1);
-    }
-    *abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  // Q dims 256..511 of head r into the swizzled K-major layout (zero rows past
-  // num_heads), 16 bytes per cp.async.
+// Q of query n into the operand buffers (not inlined: they run once per query
+// change, and inlined into the softmax loop they made its live state spill):
+// dims 256..511 of head r into the
+// swizzled K-major shared-memory layout (zero rows past num_heads), 16 bytes
+// per cp.async by threads [0, nthreads); then, by the 128 softmax threads
+// only (warps 0-3, head = thread), dims 0..255 into TMEM lane `head`,
+// columns kColQ.. as bf16 pairs (the A operand of the first 16 q.k steps).
+__device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_t q_base,
+                                            int tid, int nthreads) {
   const uint8_t* qn = p.q + n * p.q_qstride;
-  for (int id = tid; id < kHeads * 32; id += kThreads) {
+  for (int id = tid; id < kHeads * 32; id += nthreads) {
     const int r = id >> 5, c32 = id & 31;
     const uint32_t dst = q_base + (uint32_t)(c32 >> 3) * (kHeads * 128) + (uint32_t)r * 128 +
                          ((((uint32_t)c32 & 7) ^ ((uint32_t)r & 7)) << 4);
@@ -455,56 +486,176 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   cp_async_commit();
   cp_async_wait<0>();
   fence_proxy_async();
+}
+
+__device__ __noinline__ void load_q_tmem(const AttnParams& p, int64_t n, uint32_t tmem,
+                                            int tid) {
+  const uint32_t lane_base = tmem + ((uint32_t)((tid >> 5) * 32) << 16);
+  const uint8_t* qrow = p.q + n * p.q_qstride + (int64_t)tid * p.q_hstride;
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 x =
+          tid < p.num_heads ? ld_once_v4(qrow + 64 * c + 16 * k) : make_uint4(0, 0, 0, 0);
+      w[4 * k] = x.x;
+      w[4 * k + 1] = x.y;
+      w[4 * k + 2] = x.z;
+      w[4 * k + 3] = x.w;
+    }
+    tmem_st16(lane_base + kColQ + 16 * c, w);
+  }
+}
+
+// Bounded wait for the completion of every MMA issued so far by the calling
+// thread (commit to the drain barrier, then poll it): runs whether or not
+// the CTA is aborting, so that no MMA still writes tensor memory or arrives
+// on an mbarrier once the CTA releases them.
+__device__ __forceinline__ bool drain_mmas(uint32_t bar) {
+  mma_commit(bar);
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_test(bar, 0)) return true;
+  return false;
+}
+
+// One head's result for the segment just finished (thread = head, O in TMEM
+// lanes of this warp): the bf16 output row half, or for a unit split between
+// CTAs the fp32 output normalised by this piece's softmax sum and that sum's
+// log-sum-exp (log2 units) in piece slot `slot`.
+__device__ __forceinline__ void write_segment(const AttnParams& p, int64_t unit, bool whole,
+                                              int64_t slot, uint32_t lane_base, int h,
+                                              float m_ref, float l) {
+  const bool store = h < p.num_heads;
+  const int64_t n = unit >> 1;
+  const int v = (int)(unit & 1);
+  const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+  uint8_t* orow = p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
+  float* prow = whole ? nullptr : p.part_o + (slot * p.num_heads + h) * kHalf;
+#pragma unroll 1
+  for (int c = 0; c < kHalf / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(lane_base + kColO + 32 * c, o);
+    if (whole) {
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        w[k] = l > 0.0f ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv,
+                                      __uint_as_float(o[2 * k + 1]) * inv)
+                        : 0u;
+      if (store) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_v4(orow + 64 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                    w[4 * u + 3]));
+      }
+    } else if (store) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_v4(prow + 32 * c + 4 * u,
+              make_uint4(__float_as_uint(__uint_as_float(o[4 * u]) * inv),
+                         __float_as_uint(__uint_as_float(o[4 * u + 1]) * inv),
+                         __float_as_uint(__uint_as_float(o[4 * u + 2]) * inv),
+                         __float_as_uint(__uint_as_float(o[4 * u + 3]) * inv)));
+    }
+  }
+  if (!store) return;
+  const float lse2 = l > 0.0f ? m_ref + log2f(l) : -__int_as_float(0x7F800000);
+  if (!whole)
+    p.part_lse[slot * p.num_heads + h] = lse2;
+  else if (v == 0 && p.lse)
+    p.lse[n * p.num_heads + h] =
+        l > 0.0f ? lse2 * 0.69314718055994531f : -__int_as_float(0x7F800000);
+}
+
+// First tile of CTA b's range. One CTA per unit: the unit's tiles; split
+// (at most 1023 CTAs, total * 1024 in range): total * b / grid.
+__device__ __forceinline__ int64_t range_begin(const AttnParams& p, int64_t b) {
+  return p.grid == p.units ? b * p.tiles : p.total * b / p.grid;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t b = blockIdx.x;
+  if (p.tiles == 0) {
+    // no keys at all: every output row is zero and every log-sum-exp -inf
+    // (one CTA per unit)
+    const int64_t n = b >> 1;
+    const int v = (int)(b & 1);
+    for (int id = tid; id < p.num_heads * 32; id += kThreads)
+      st_v4(p.out + n * p.o_qstride + (int64_t)(id >> 5) * p.o_hstride + v * kHalf * 2 +
+                (id & 31) * 16,
+            make_uint4(0, 0, 0, 0));
+    if (v == 0 && p.lse)
+      for (int h = tid; h < p.num_heads; h += kThreads)
+        p.lse[n * p.num_heads + h] = -__int_as_float(0x7F800000);
+    return;
+  }
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  const uint32_t q_base = base + kOffQ, k_base = base + kOffK;
+  const uint32_t bars = base + kOffBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
+  // this CTA's run of tiles [g0, g1) and where it starts
+  const int64_t g0 = range_begin(p, b), g1 = range_begin(p, b + 1);
+  const int64_t n_tiles = g1 - g0;  // >= 1: grid <= total
+  const int64_t u_first = g0 / p.tiles;
+  const Cursor start{u_first, g0 - u_first * p.tiles};
+
+  if (warp == kIssuerWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bars + kBarKFull + 8 * s, 256);
+      mbar_init(bars + kBarSFull + 8 * s, 1);
+      mbar_init(bars + kBarPFull + 8 * s, 128);
+      mbar_init(bars + kBarPvDone + 8 * s, 1);
+    }
+    mbar_init(bars + kBarSeg, 128);
+    mbar_init(bars + kBarDrain, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  load_q_smem(p, u_first >> 1, q_base, tid, kThreads);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) {
-    // Q dims 0..255 of head `tid` into TMEM lane `tid`, columns kColQ.. as
-    // bf16 pairs (the A operand of the first 16 q.k steps).
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint8_t* qrow = qn + (int64_t)tid * p.q_hstride;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t w[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 x = tid < p.num_heads ? ld_once_v4(qrow + 128 * c + 16 * k)
-                                          : make_uint4(0, 0, 0, 0);
-        w[4 * k] = x.x;
-        w[4 * k + 1] = x.y;
-        w[4 * k + 2] = x.z;
-        w[4 * k + 3] = x.w;
-      }
-      tmem_st32(lane_base + kColQ + 32 * c, w);
-    }
-  }
+  if (warp < 4) load_q_tmem(p, u_first >> 1, tmem, tid);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
   if (warp >= 4 && warp < kIssuerWarp) {
     // ------------------------------------------------------------ producers
-    // Lane = key of the tile, warp 4 + e = dims [64e, 64e + 64). Key buffer
-    // t % kStages is free once PV(t - kStages) has completed.
+    // Lane = key of the tile, warp 4 + e = dims [64e, 64e + 64). The CTA's
+    // i-th tile goes to stage i % kStages, free once the p.v of tile
+    // i - kStages has completed; rows are loaded kDepth tiles ahead.
     const int e = warp - 4, j = lane;
+    Cursor cl = start;  // the tile whose rows are loaded next
     Packed buf[kDepth];
 #pragma unroll
-    for (int u = 0; u < kDepth; ++u)
-      buf[u] = load_packed(p, key_index(p, idx_row, (int64_t)u * kTileKeys + j), e);
-    int64_t s_next = key_index(p, idx_row, (int64_t)kDepth * kTileKeys + j);
+    for (int u = 0; u < kDepth; ++u) {
+      buf[u] = load_packed(p, u < n_tiles ? key_index(p, cl, j) : -1, e);
+      cl.next(p.tiles);
+    }
+    int64_t s_next = kDepth < n_tiles ? key_index(p, cl, j) : -1;
     bool live = true;
-    for (int64_t t0 = 0; t0 < num_tiles && live; t0 += kDepth) {
+    for (int64_t i0 = 0; i0 < n_tiles && live; i0 += kDepth) {
 #pragma unroll
       for (int u = 0; u < kDepth; ++u) {
-        const int64_t t = t0 + u;
-        if (t < num_tiles && live) {
+        const int64_t i = i0 + u;
+        if (i < n_tiles && live) {
           const Packed cur = buf[u];
-          buf[u] = load_packed(p, s_next, e);  // tile t + kDepth
-          s_next = key_index(p, idx_row, (t + kDepth + 1) * kTileKeys + j);
-          const uint32_t st = (uint32_t)(t % kStages);
-          if (t >= kStages &&
-              !mbar_wait(bars + kBarPvDone + 8 * st, (uint32_t)(((t / kStages) - 1) & 1), abort)) {
+          buf[u] = load_packed(p, s_next, e);  // tile i + kDepth
+          cl.next(p.tiles);
+          s_next = i + kDepth + 1 < n_tiles ? key_index(p, cl, j) : -1;
+          const uint32_t st = (uint32_t)(i % kStages);
+          if (i >= kStages &&
+              !mbar_wait(bars + kBarPvDone + 8 * st, (uint32_t)(((i / kStages) - 1) & 1), abort)) {
             live = false;
           } else {
             dequant_share(cur, k_base + st * kKBlock, j, e);
@@ -518,32 +669,70 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     // --------------------------------------------------------------- issuer
     if (lane == 0) {
       const uint64_t q_desc = smem_desc(q_base, 16, 1024, 2);
-      // Event-driven: O += P(u) V(u) as soon as softmax has written P(u) (it
-      // frees key stage u % kStages, so it goes first), else q.k over the
-      // pair of tiles t, t + 1 (t even) once both are written and PV(t - 3),
-      // the last reader of their TMEM columns, has been issued (MMAs from
-      // this thread run in order). Polls without progress are bounded.
-      int64_t t = 0, u = 0;
+      // Event-driven over the CTA's tiles: O += P(pi) V(pi) as soon as
+      // softmax has written P(pi) (it frees a key stage, so it goes first);
+      // else q.k of tile qi (with tile qi + 1 when qi's stage is even and
+      // both tiles belong to the same query) once its keys are written and
+      // the p.v that last read its tensor-memory columns has been issued
+      // (MMAs from this thread run in order). The first p.v of a segment
+      // waits for softmax to have read out the previous segment's output;
+      // the first q.k of a new query waits for softmax to have loaded its Q.
+      // Segment boundaries are observed one at a time, in order.
+      Cursor cq = start, cp = start;
+      int64_t qi = 0, pi = 0, seen = 0;
       uint32_t idle = 0;
-      while (u < num_tiles) {
-        if (u < t && mbar_test(bars + kBarPFull + 8 * (uint32_t)(u % kStages),
-                               (uint32_t)((u / kStages) & 1))) {
-          tc_fence_after();
-          issue_pv(u, v, k_base, tmem);
-          mma_commit(bars + kBarPvDone + 8 * (uint32_t)(u % kStages));
-          ++u;
-          idle = 0;
-        } else if (t < num_tiles && t + 1 - u < kStages &&
-                   mbar_test(bars + kBarKFull + 8 * (uint32_t)(t % kStages),
-                             (uint32_t)((t / kStages) & 1)) &&
-                   (t + 1 >= num_tiles ||
-                    mbar_test(bars + kBarKFull + 8 * (uint32_t)((t + 1) % kStages),
-                              (uint32_t)(((t + 1) / kStages) & 1)))) {
-          tc_fence_after();
-          issue_qk(t, q_desc, k_base, tmem);
-          mma_commit(bars + kBarSFull + 8 * (uint32_t)(t % kStages));
-          if (t + 1 < num_tiles) mma_commit(bars + kBarSFull + 8 * (uint32_t)((t + 1) % kStages));
-          t += 2;
+      auto seg_ready = [&](int64_t k) -> bool {
+        while (seen < k) {
+          if (!mbar_test(bars + kBarSeg, (uint32_t)(seen & 1))) return false;
+          ++seen;
+        }
+        return true;
+      };
+      while (pi < n_tiles) {
+        bool progress = false;
+        if (pi < qi && mbar_test(bars + kBarPFull + 8 * (uint32_t)(pi % kStages),
+                                 (uint32_t)((pi / kStages) & 1))) {
+          const bool first = pi == 0 || cp.t == 0;
+          if (!first || pi == 0 || seg_ready(cp.unit - u_first)) {
+            tc_fence_after();
+            issue_pv((uint32_t)(pi % kStages), (int)(cp.unit & 1), first, k_base, tmem);
+            mma_commit(bars + kBarPvDone + 8 * (uint32_t)(pi % kStages));
+            ++pi;
+            cp.next(p.tiles);
+            progress = true;
+          }
+        }
+        if (!progress && qi < n_tiles) {
+          const uint32_t st = (uint32_t)(qi % kStages);
+          Cursor c2 = cq;
+          c2.next(p.tiles);
+          const bool pair =
+              (st & 1u) == 0 && qi + 1 < n_tiles && (c2.unit >> 1) == (cq.unit >> 1);
+          const int64_t q_unit0 = cq.unit & ~(int64_t)1;  // first unit of the tile's query
+          const int64_t q_seg = (q_unit0 > u_first ? q_unit0 : u_first) - u_first;
+          if (qi + (pair ? 1 : 0) - pi < kStages &&
+              mbar_test(bars + kBarKFull + 8 * st, (uint32_t)((qi / kStages) & 1)) &&
+              (!pair || mbar_test(bars + kBarKFull + 8 * (st + 1),
+                                  (uint32_t)(((qi + 1) / kStages) & 1))) &&
+              seg_ready(q_seg)) {
+            tc_fence_after();
+            if (pair) {
+              issue_qk<true>(st, q_desc, k_base, tmem);
+              mma_commit(bars + kBarSFull + 8 * st);
+              mma_commit(bars + kBarSFull + 8 * (st + 1));
+              qi += 2;
+              cq = c2;
+              cq.next(p.tiles);
+            } else {
+              issue_qk<false>(st, q_desc, k_base, tmem);
+              mma_commit(bars + kBarSFull + 8 * st);
+              qi += 1;
+              cq = c2;
+            }
+            progress = true;
+          }
+        }
+        if (progress) {
           idle = 0;
         } else if (++idle >= kWaitPolls) {
           *abort = 1;
@@ -552,20 +741,31 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
           break;
         }
       }
+      if (!drain_mmas(bars + kBarDrain)) *abort = 1;
     }
     __syncwarp();
   } else {
     // -------------------------------------------------------------- softmax
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_ref = -__int_as_float(0x7F800000);  // reference max (log2 units)
-    float l = 0.0f;                              // sum of p against m_ref
+    const float kNegInf = -__int_as_float(0x7F800000);
+    float m_ref = kNegInf;  // reference max of the segment (log2 units)
+    float l = 0.0f;         // sum of p against m_ref
     bool live = true;
-    int64_t s_key = key_index(p, idx_row, lane);
-    for (int64_t t = 0; t < num_tiles && live; ++t) {
+    Cursor c = start;
+    int64_t s_key = key_index(p, c, lane);
+    for (int64_t i = 0; i < n_tiles && live; ++i) {
+      const bool seg_first = i == 0 || c.t == 0;
+      const bool seg_last = i == n_tiles - 1 || c.t == p.tiles - 1;
+      if (seg_first) {
+        m_ref = kNegInf;
+        l = 0.0f;
+      }
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, s_key >= 0 && s_key < p.num_slots);
-      s_key = key_index(p, idx_row, (t + 1) * kTileKeys + lane);
-      const uint32_t st = (uint32_t)(t % kStages);
-      if (!warp_wait(bars + kBarSFull + 8 * st, (uint32_t)((t / kStages) & 1), abort)) {
+      Cursor cn = c;
+      cn.next(p.tiles);
+      s_key = i + 1 < n_tiles ? key_index(p, cn, lane) : -1;
+      const uint32_t st = (uint32_t)(i % kStages);
+      if (!warp_wait(bars + kBarSFull + 8 * st, (uint32_t)((i / kStages) & 1), abort)) {
         live = false;
         break;
       }
@@ -574,8 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       uint32_t sr[32];
       tmem_ld32(scol, sr);
       // the tile max (log2 units, -inf for dropped keys), four chains
-      float mc[4] = {-__int_as_float(0x7F800000), -__int_as_float(0x7F800000),
-                     -__int_as_float(0x7F800000), -__int_as_float(0x7F800000)};
+      float mc[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
       for (int k = 0; k < 32; ++k)
         if ((mask >> k) & 1u)
@@ -584,9 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       const bool need = mt > m_ref + 8.0f;
       if (__any_sync(0xFFFFFFFFu, need)) {
         const float f = need ? ex2(m_ref - mt) : 1.0f;  // ex2(-inf) = 0
-        if (t > 0) {
-          // O may be touched only once PV(t-1) has completed
-          const int64_t w = t - 1;
+        if (!seg_first) {
+          // O may be touched only once the p.v of tile i - 1 has completed
+          const int64_t w = i - 1;
           if (!warp_wait(bars + kBarPvDone + 8 * (uint32_t)(w % kStages),
                          (uint32_t)((w / kStages) & 1), abort)) {
             live = false;
@@ -594,18 +793,18 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < kHalf / 32; ++c) {
+          for (int cc = 0; cc < kHalf / 32; ++cc) {
             uint32_t o[32];
-            tmem_ld32(lane_base + kColO + 32 * c, o);
+            tmem_ld32(lane_base + kColO + 32 * cc, o);
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-            tmem_st32(lane_base + kColO + 32 * c, o);
+            tmem_st32(lane_base + kColO + 32 * cc, o);
           }
         }
         l *= f;
         if (need) m_ref = mt;
       }
-      const float mu = m_ref == -__int_as_float(0x7F800000) ? 0.0f : m_ref;
+      const float mu = m_ref == kNegInf ? 0.0f : m_ref;
       // probabilities, their sum, and P (bf16 pairs) over the score columns
       float lsum0 = 0.0f, lsum1 = 0.0f;
       uint32_t pk[16];
@@ -613,10 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       for (int k = 0; k < 16; ++k) {
         const float x0 = ((mask >> (2 * k)) & 1u)
                              ? __fmul_rn(__uint_as_float(sr[2 * k]), p.scale_log2)
-                             : -__int_as_float(0x7F800000);
+                             : kNegInf;
         const float x1 = ((mask >> (2 * k + 1)) & 1u)
                              ? __fmul_rn(__uint_as_float(sr[2 * k + 1]), p.scale_log2)
-                             : -__int_as_float(0x7F800000);
+                             : kNegInf;
         const float p0 = ex2(x0 - mu), p1 = ex2(x1 - mu);
         lsum0 += p0;
         lsum1 += p1;
@@ -626,44 +825,30 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       l += lsum0 + lsum1;
       tc_fence_before();
       mbar_arrive(bars + kBarPFull + 8 * st);
-    }
-    if (live && num_tiles > 0 &&
-        !warp_wait(bars + kBarPvDone + 8 * (uint32_t)((num_tiles - 1) % kStages),
-                   (uint32_t)(((num_tiles - 1) / kStages) & 1), abort))
-      live = false;
-    live = __all_sync(0xFFFFFFFFu, live && !*abort);
-    if (live) {
-      tc_fence_after();
-      const int h = tid;
-      const bool store = h < p.num_heads;
-      uint8_t* orow =
-          p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-#pragma unroll 1
-      for (int c = 0; c < kHalf / 32; ++c) {
-        uint32_t o[32];
-        if (num_tiles > 0) {
-          tmem_ld32(lane_base + kColO + 32 * c, o);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0;
+      if (seg_last) {
+        // the segment's output: wait for its last p.v, read O out, then (if
+        // another segment follows) load Q of a new query and release O
+        if (!warp_wait(bars + kBarPvDone + 8 * st, (uint32_t)((i / kStages) & 1), abort)) {
+          live = false;
+          break;
         }
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          w[k] = l > 0.0f ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv,
-                                        __uint_as_float(o[2 * k + 1]) * inv)
-                          : 0u;
-        if (store) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_v4(orow + 64 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                                      w[4 * u + 3]));
+        tc_fence_after();
+        // whole: the segment runs from the unit's first tile to its last
+        // (recomputed here rather than kept live through the loop)
+        const int64_t cta = blockIdx.x, r0 = range_begin(p, cta), uf = r0 / p.tiles;
+        const bool whole = c.t + 1 == p.tiles && (c.unit > uf || r0 == uf * p.tiles);
+        write_segment(p, c.unit, whole, 2 * cta + (c.unit == uf ? 0 : 1), lane_base, tid, m_ref,
+                      l);
+        if (i + 1 < n_tiles) {
+          if ((cn.unit >> 1) != (c.unit >> 1)) {
+            load_q_smem(p, cn.unit >> 1, q_base, tid, 128);
+            load_q_tmem(p, cn.unit >> 1, tmem, tid);
+          }
+          tc_fence_before();
+          mbar_arrive(bars + kBarSeg);
         }
       }
-      if (v == 0 && store && p.lse)
-        p.lse[n * p.num_heads + h] = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f
-                                              : -__int_as_float(0x7F800000);
+      c = cn;
     }
   }
   tc_fence_before();
@@ -675,42 +860,92 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   }
 }
 
+// Combines the pieces of every unit split between CTAs. Block j looks at the
+// boundary between CTAs j and j + 1; the unit it falls inside (if any) is
+// merged by the block of its first boundary, over the pieces of CTAs
+// b_first..b_last: out = sum_b 2**(lse_b - L) o_b / sum_b 2**(lse_b - L),
+// L = max_b lse_b, and the unit's log-sum-exp L + log2(sum) (in natural
+// log units, half 0 only). A unit without any valid key gets zeros and -inf.
+// Thread t: head t / 64 + 4k, columns 4 (t % 64) .. 4 (t % 64) + 3.
+__global__ void __launch_bounds__(256) mxfp4_attention_merge_kernel(AttnParams p) {
+  const int64_t j = blockIdx.x;
+  const int64_t gb = p.total * (j + 1) / p.grid;
+  const int64_t unit = gb / p.tiles;
+  if (gb == unit * p.tiles) return;  // the boundary lies between units
+  const int64_t g0 = p.total * j / p.grid;
+  if (g0 > unit * p.tiles) return;   // merged by the block of an earlier boundary
+  const int64_t b_last = ((unit + 1) * p.tiles * p.grid - 1) / p.total;
+  const int64_t n = unit >> 1;
+  const int v = (int)(unit & 1);
+  const int c4 = threadIdx.x & 63;
+  const float kNegInf = -__int_as_float(0x7F800000);
+  for (int64_t h = threadIdx.x >> 6; h < p.num_heads; h += 4) {
+    float L = kNegInf;
+    for (int64_t bb = j; bb <= b_last; ++bb) {
+      const int64_t slot = 2 * bb + ((p.total * bb / p.grid) / p.tiles == unit ? 0 : 1);
+      L = fmaxf(L, p.part_lse[slot * p.num_heads + h]);
+    }
+    float W = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (L != kNegInf) {
+      for (int64_t bb = j; bb <= b_last; ++bb) {
+        const int64_t slot = 2 * bb + ((p.total * bb / p.grid) / p.tiles == unit ? 0 : 1);
+        const float w = exp2f(p.part_lse[slot * p.num_heads + h] - L);
+        const float4 o = *reinterpret_cast<const float4*>(
+            p.part_o + (slot * p.num_heads + h) * kHalf + 4 * c4);
+        W += w;
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+    }
+    const float inv = W > 0.0f ? 1.0f / W : 0.0f;
+    st_v2(p.out + n * p.o_qstride + h * p.o_hstride + (int64_t)(v * kHalf + 4 * c4) * 2,
+          pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (v == 0 && p.lse && c4 == 0)
+      p.lse[n * p.num_heads + h] = W > 0.0f ? (L + log2f(W)) * 0.69314718055994531f : kNegInf;
+  }
+}
+
 }  // namespace
 }  // namespace kvq
 
-extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries,
-                                          int64_t num_heads, int64_t q_query_stride,
-                                          int64_t q_head_stride, const uint8_t* cache,
-                                          int64_t num_blocks, int64_t block_size,
-                                          int64_t block_stride_rows, const int64_t* indices,
-                                          int64_t topk, float sm_scale, void* out_bf16,
-                                          int64_t out_query_stride, int64_t out_head_stride,
-                                          float* lse, int32_t* status, cudaStream_t stream) {
+namespace {
+
+// CTAs of the split schedule: one per SM (each holds all of tensor memory),
+// at most one per tile.
+int64_t split_grid(int64_t total) {
+  int64_t sms = kvq::sm_count();
+  if (sms > 1023) sms = 1023;
+  return total < sms ? total : sms;
+}
+
+// Checks shared by the entry points; fills `p` (without workspace).
+int attention_params(const void* q_bf16, int64_t num_queries, int64_t num_heads,
+                     int64_t q_query_stride, int64_t q_head_stride, const uint8_t* cache,
+                     int64_t num_blocks, int64_t block_size, int64_t block_stride_rows,
+                     const int64_t* indices, int64_t topk, float sm_scale, void* out_bf16,
+                     int64_t out_query_stride, int64_t out_head_stride, float* lse,
+                     int32_t* status, kvq::AttnParams& p) {
   using namespace kvq;
   if (num_queries < 0 || num_heads < 1 || num_heads > kHeads || topk < 0) return KVQ_EINVAL;
   if (num_blocks < 1 || block_size < 1 || block_stride_rows < block_size) return KVQ_EINVAL;
   if (num_blocks > INT64_MAX / block_size) return KVQ_EINVAL;
+  if (num_blocks > INT64_MAX / block_stride_rows / kRow) return KVQ_EINVAL;
   if (!(sm_scale == sm_scale) || sm_scale < 0.0f || sm_scale > 3.0e38f) return KVQ_EINVAL;
   if (q_head_stride < kDim || q_head_stride % 8 || q_query_stride % 8) return KVQ_EINVAL;
   if (out_head_stride < kDim || out_head_stride % 8 || out_query_stride % 8) return KVQ_EINVAL;
   if (num_queries > INT64_MAX / 2 / (topk > 0 ? topk : 1)) return KVQ_EINVAL;
+  if (num_queries > 0x7FFFFFFF / 2) return KVQ_EINVAL;
+  const int64_t tiles = (topk + kTileKeys - 1) / kTileKeys;
+  // the schedule's products total * (grid + 1) stay in range
+  if (tiles > 0 && 2 * num_queries > INT64_MAX / 1024 / tiles) return KVQ_EINVAL;
   if (num_queries == 0) return KVQ_OK;
   if (!q_bf16 || !cache || !out_bf16 || (topk > 0 && !indices)) return KVQ_EINVAL;
   if (!aligned(q_bf16, 16) || !aligned(cache, 16) || !aligned(out_bf16, 16) ||
       !aligned(indices, 8) || (lse && !aligned(lse, 4)) || (status && !aligned(status, 4)))
     return KVQ_EINVAL;
-  if (num_queries > 0x7FFFFFFF / 2) return KVQ_EINVAL;
-
-  static int attr_done[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ECUDA;
-  if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(mxfp4_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return KVQ_ECUDA;
-    attr_done[dev] = 1;
-  }
-  AttnParams p;
   p.q = static_cast<const uint8_t*>(q_bf16);
   p.q_qstride = q_query_stride * 2;
   p.q_hstride = q_head_stride * 2;
@@ -727,6 +962,78 @@ extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_querie
   p.o_hstride = out_head_stride * 2;
   p.lse = lse;
   p.status = status;
-  mxfp4_attention_kernel<<<(unsigned)(2 * num_queries), kThreads, kSmemBytes, stream>>>(p);
+  p.tiles = tiles;
+  p.units = 2 * num_queries;
+  p.total = 2 * num_queries * tiles;
+  p.grid = 2 * num_queries;  // one CTA per unit unless split
+  p.part_o = nullptr;
+  p.part_lse = nullptr;
+  return KVQ_OK;
+}
+
+// Bytes of the split schedule's partial results (0 without keys).
+int64_t split_bytes(int64_t grid, int64_t num_heads) {
+  return 2 * grid * num_heads * (int64_t)(kvq::kHalf * 4 + 4);
+}
+
+// Lays the partial results out in `ws` (256-byte aligned) for `grid` CTAs.
+void split_layout(kvq::AttnParams& p, int64_t grid, void* ws) {
+  p.grid = grid;
+  p.part_o = static_cast<float*>(ws);
+  p.part_lse = p.part_o + 2 * grid * p.num_heads * kvq::kHalf;
+}
+
+int launch_attention(const kvq::AttnParams& p, cudaStream_t stream) {
+  using namespace kvq;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ECUDA;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(mxfp4_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return KVQ_ECUDA;
+    attr_done[dev] = 1;
+  }
+  mxfp4_attention_kernel<<<(unsigned)p.grid, kThreads, kSmemBytes, stream>>>(p);
+  int rc = launch_status();
+  if (rc != KVQ_OK || !p.part_o || p.grid < 2) return rc;
+  mxfp4_attention_merge_kernel<<<(unsigned)(p.grid - 1), 256, 0, stream>>>(p);
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries,
+                                                             int64_t num_heads, int64_t topk) {
+  if (num_queries < 0 || num_heads < 1 || num_heads > kvq::kHeads || topk < 0) return KVQ_EINVAL;
+  if (num_queries > 0x7FFFFFFF / 2 || num_queries > INT64_MAX / 2 / (topk > 0 ? topk : 1))
+    return KVQ_EINVAL;
+  const int64_t tiles = (topk + kvq::kTileKeys - 1) / kvq::kTileKeys;
+  if (tiles > 0 && 2 * num_queries > INT64_MAX / 1024 / tiles) return KVQ_EINVAL;
+  if (tiles == 0 || num_queries == 0) return 0;
+  return split_bytes(split_grid(2 * num_queries * tiles), num_heads);
+}
+
+extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries,
+                                          int64_t num_heads, int64_t q_query_stride,
+                                          int64_t q_head_stride, const uint8_t* cache,
+                                          int64_t num_blocks, int64_t block_size,
+                                          int64_t block_stride_rows, const int64_t* indices,
+                                          int64_t topk, float sm_scale, void* out_bf16,
+                                          int64_t out_query_stride, int64_t out_head_stride,
+                                          float* lse, int32_t* status, void* workspace,
+                                          int64_t workspace_bytes, cudaStream_t stream) {
+  using namespace kvq;
+  AttnParams p;
+  int rc = attention_params(q_bf16, num_queries, num_heads, q_query_stride, q_head_stride, cache,
+                            num_blocks, block_size, block_stride_rows, indices, topk, sm_scale,
+                            out_bf16, out_query_stride, out_head_stride, lse, status, p);
+  if (rc != KVQ_OK || num_queries == 0) return rc;
+  if (workspace && p.tiles > 0) {
+    const int64_t grid = split_grid(p.total);
+    if (workspace_bytes < split_bytes(grid, num_heads) || !aligned(workspace, 256))
+      return KVQ_EINVAL;
+    split_layout(p, grid, workspace);
+  }
+  return launch_attention(p, stream);
 }

@@ -432,7 +432,24 @@ int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks, int64_t b
  * lse              fp32 [num_queries, num_heads] or NULL
  * status           device int32 or NULL: set to a nonzero value if an
  *                  internal wait of the kernel timed out (the output is then
- *                  undefined); never written otherwise
+ *                  undefined); never written otherwise. Without a status
+ *                  word such a timeout is reported nowhere and the output
+ *                  is undefined: pass one to be told.
+ * workspace        device memory of at least workspace_bytes >=
+ *                  mxfp4_mla_sparse_attention_workspace_size(num_queries,
+ *                  num_heads, topk) bytes, 256-byte aligned, or NULL.
+ *                  With a workspace the queries' key tiles are split evenly
+ *                  over one CTA per SM (the split-K of the read path [pr]:
+ *                  a ragged sparse-attention kernel plus a split-K partial
+ *                  kernel): pieces of a (query, value half) cut between two
+ *                  CTAs are written there as fp32 partial outputs with their
+ *                  log-sum-exps and merged by a second kernel launched on
+ *                  the same stream. Its contents need no initialisation and
+ *                  are garbage afterwards; two calls in flight at once must
+ *                  not share it. Without one, one CTA takes each (query,
+ *                  value half) whole (no second kernel). Both give results
+ *                  within the bound above; they may differ in the last bits.
+ *                  KVQ_EINVAL if the workspace is too small or misaligned.
  * The library allocates nothing and keeps no pointer after the call.
  */
 int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries, int64_t num_heads,
@@ -441,7 +458,19 @@ int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries, int64_t 
                                int64_t block_stride_rows, const int64_t* indices, int64_t topk,
                                float sm_scale, void* out_bf16, int64_t out_query_stride,
                                int64_t out_head_stride, float* lse, int32_t* status,
+                               void* workspace, int64_t workspace_bytes,
                                cudaStream_t stream);
+
+/*
+ * mxfp4_mla_sparse_attention_workspace_size — bytes of workspace that
+ * mxfp4_mla_sparse_attention needs to split these shapes over the current
+ * device's SMs: 2 x CTAs x num_heads x (256 x 4 + 4) (CTAs = min(SMs,
+ * 2 x num_queries x ceil(topk / 32))), 0 when there is nothing to split
+ * (num_queries or topk 0), KVQ_EINVAL for shapes the attention rejects.
+ * No page counterpart: a host query of this library.
+ */
+int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries, int64_t num_heads,
+                                                  int64_t topk);
 
 #ifdef __cplusplus
 }

@@ -34,7 +34,8 @@ def test_every_declared_symbol_is_exported(L):
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
                           "rope_quant_insert_v4", "rope_plain_insert", "save_ring_rows",
                           "fused_save_compress_norm",
-                          "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention"}
+                          "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention",
+                          "mxfp4_mla_sparse_attention_workspace_size"}
     for n in names:
         assert hasattr(L, n), n
     # exported with C linkage from the shared object itself
@@ -177,7 +178,7 @@ def test_gather_validation_on_host(L):
 def test_attention_validation_on_host(L):
     f = L.mxfp4_mla_sparse_attention
     ok = [A16, 2, 128, 128 * 512, 512, A16, 1, 8, 8, A8, 16, 0.05, A16, 128 * 512, 512, None,
-          None, None]
+          None, None, 0, None]
     empty = list(ok); empty[1] = 0; empty[0] = None
     assert f(*empty) == 0
     bad = {1: -1, 2: 0, 2.1: 129, 4: 256, 4.1: 516, 3: 12, 6: 0, 7: 0, 8: 7, 10: -1,
@@ -188,13 +189,55 @@ def test_attention_validation_on_host(L):
         assert f(*a) == -1, (k, v)
     a = list(ok); a[0] = None
     assert f(*a) == -1
+    # cache rows whose byte offsets leave int64: rejected like the store's
+    a = list(ok); a[6] = 1 << 40; a[8] = 1 << 30
+    assert f(*a) == -1
+    # a workspace that is misaligned or smaller than the query says
+    need = L.mxfp4_mla_sparse_attention_workspace_size(2, 128, 16)
+    assert need > 0
+    a = list(ok); a[17] = A16 + 16; a[18] = need
+    assert f(*a) == -1
+    a = list(ok); a[17] = A16; a[18] = need - 1
+    assert f(*a) == -1
+
+
+def test_attention_workspace_size(L):
+    """2 x CTAs x heads x (256 fp32 + one log-sum-exp), CTAs = min(SMs,
+    2 x queries x tiles of 32 keys); 0 when nothing can be split; -1 for
+    shapes the attention rejects."""
+    g = L.mxfp4_mla_sparse_attention_workspace_size
+    assert g(0, 128, 2048) == 0 and g(3, 128, 0) == 0
+    assert g(-1, 128, 16) == -1 and g(2, 0, 16) == -1 and g(2, 129, 16) == -1
+    assert g(2, 128, -1) == -1
+    per_cta = 2 * 128 * (256 * 4 + 4)
+    big = g(128, 128, 2048)
+    assert big % per_cta == 0 and 1 <= big // per_cta <= 2 * 128 * 64
+    # one query, one tile per unit: two CTAs at most
+    assert g(1, 128, 32) == 2 * per_cta and g(1, 64, 1) == 2 * 2 * 64 * (256 * 4 + 4)
+
+
+def test_tensors_on_two_devices_are_refused_before_any_launch():
+    """Every CUDA argument must be on one device (raw pointers of another GPU
+    would be illegal addresses on the launching one); checked before the
+    library is called."""
+    import types
+    import torch
+    a = types.SimpleNamespace(is_cuda=True, device=torch.device("cuda", 0))
+    b = types.SimpleNamespace(is_cuda=True, device=torch.device("cuda", 1))
+    host = types.SimpleNamespace(is_cuda=False, device=torch.device("cpu"))
+    calls = []
+    with pytest.raises(TypeError):
+        kvq._launch("x", (a, host, b), None, lambda s: calls.append(s) or 0)
+    assert calls == []
+    assert kvq._device("x", (a, host, None, a)) == 0
+    assert kvq._device("x", (host,)) is None
 
 
 def test_binding_has_the_abi_names():
     for n in ("mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp8",
               "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
               "save_ring_rows", "fused_save_compress_norm", "mxfp4_mla_gather_dequant",
-              "mxfp4_mla_sparse_attention"):
+              "mxfp4_mla_sparse_attention", "attention_workspace_size"):
         assert callable(getattr(kvq, n))
 
 

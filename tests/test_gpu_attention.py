@@ -11,6 +11,10 @@ covers the fp32 floor: exp2 flushes probabilities below 2**-126 of the
 running maximum to zero, and at most 2**11 keys with |k| < 2**14 can lose
 less than 2**-101 that way (an exact output of 6e-50 comes out as 0).
 lse: |lse - exact| <= 2e-3.
+Both schedules are checked: key tiles split evenly over the SMs (pieces of a
+(query, value half) cut between CTAs merged by log-sum-exp; the default), and
+one CTA per (query, value half). The bound holds for both: a split piece's
+output is kept in fp32 and the merge rounds to bf16 once.
 The packed cache is written by the oracle's store, never by the CUDA path.
 """
 import numpy as np
@@ -44,7 +48,8 @@ def _fill_cache(num_slots, seed, num_blocks=1, block_size=None, block_stride_row
     return cache
 
 
-def _run(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full=None):
+def _run(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full=None,
+         split=True):
     """Kernel on the GPU; q_full (optional) is a wider buffer q is a view of."""
     dev = torch.device("cuda", 0)
     src = q if q_full is None else q_full
@@ -59,15 +64,18 @@ def _run(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_f
     idd = torch.from_numpy(np.ascontiguousarray(idx)).to(dev)
     lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    out, _ = kvq.mxfp4_mla_sparse_attention(qd, cd, idd, sm_scale, lse=lse, status=status)
+    out, _ = kvq.mxfp4_mla_sparse_attention(qd, cd, idd, sm_scale, lse=lse, status=status,
+                                            workspace=split)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "a kernel wait timed out"
     o = out.float().cpu().numpy().astype(np.float64)
     return o, lse.cpu().numpy().astype(np.float64)
 
 
-def _check(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full=None):
-    out, lse = _run(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full)
+def _check(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full=None,
+           split=True):
+    out, lse = _run(q, cache, idx, sm_scale, num_blocks, block_size, block_stride_rows, q_full,
+                    split)
     want, want_lse, mass = attn_oracle(q, cache, num_blocks, block_size, block_stride_rows, idx,
                                        sm_scale)
     err = np.abs(out - want)
@@ -89,7 +97,8 @@ def _queries(seed, nq, nh, scale=1.0):
                                       .astype(np.float32))
 
 
-def test_small_two_tiles_with_pads():
+@pytest.mark.parametrize("split", [True, False])
+def test_small_two_tiles_with_pads(split):
     cache = _fill_cache(4096, seed=1)
     q = _queries(2, 3, 128)
     rng = np.random.default_rng(3)
@@ -97,7 +106,7 @@ def test_small_two_tiles_with_pads():
     idx[0, 60:] = -1
     idx[1, 5] = 4096                         # outside the cache: dropped
     idx[2, ::7] = -1
-    _check(q, cache, idx, 1 / np.sqrt(512), 1, 4096, 4096)
+    _check(q, cache, idx, 1 / np.sqrt(512), 1, 4096, 4096, split=split)
 
 
 @pytest.mark.parametrize("heads", [1, 64, 127, 128])
@@ -119,6 +128,7 @@ def test_paged_cache_with_block_stride_and_strided_query():
     q = np.ascontiguousarray(q_full[:, :128, :512])
     idx = np.stack([rng.permutation(nb * bs)[:256] for _ in range(4)]).astype(np.int64)
     _check(q, cache, idx, 0.04, nb, bs, bsr, q_full=q_full)
+    _check(q, cache, idx, 0.04, nb, bs, bsr, q_full=q_full, split=False)
 
 
 def test_queries_without_valid_keys_and_empty_topk():
@@ -127,8 +137,9 @@ def test_queries_without_valid_keys_and_empty_topk():
     idx = np.array([[-1] * 40, [300] * 40, list(range(40))], np.int64)
     out, _ = _check(q, cache, idx, 0.05, 1, 256, 256)
     assert np.all(out[:2] == 0)
-    out0, lse0 = _run(q, cache, np.zeros((3, 0), np.int64), 0.05, 1, 256, 256)
-    assert np.all(out0 == 0) and np.all(np.isneginf(lse0))
+    for split in (True, False):
+        out0, lse0 = _run(q, cache, np.zeros((3, 0), np.int64), 0.05, 1, 256, 256, split=split)
+        assert np.all(out0 == 0) and np.all(np.isneginf(lse0))
 
 
 def test_growing_scores_exercise_the_output_rescale():
@@ -142,16 +153,46 @@ def test_growing_scores_exercise_the_output_rescale():
     order = np.argsort(k @ qd[0, 0])           # ascending for head 0
     idx = order[None, -512:].astype(np.int64)
     _check(q, cache, idx, 2.0, 1, 1024, 1024)
+    _check(q, cache, idx, 2.0, 1, 1024, 1024, split=False)
 
 
-def test_full_workload_128_queries_2048_keys():
+@pytest.mark.parametrize("split", [True, False])
+def test_full_workload_128_queries_2048_keys(split):
     """The benchmark workload: 1,048,576-slot cache, 128 queries x 128 heads x
     2048 top-k indices with trailing pads; every output compared."""
     w = workloads.sparse_attention(seed=0)
     cache = np.zeros(w["num_slots"] * 272, np.uint8)
     oracle.mxfp4_mla_store(w["fill_latent"], w["fill_slots"], cache, 1, w["num_slots"],
                            w["num_slots"], threads=oracle.default_threads())
-    _check(w["q"], cache, w["indices"], w["sm_scale"], 1, w["num_slots"], w["num_slots"])
+    _check(w["q"], cache, w["indices"], w["sm_scale"], 1, w["num_slots"], w["num_slots"],
+           split=split)
+
+
+@pytest.mark.parametrize("nq,topk,heads", [(1, 4096, 128), (1, 8192, 64), (5, 2048, 128),
+                                           (3, 333, 128), (77, 64, 16), (200, 96, 128)])
+def test_split_schedules(nq, topk, heads):
+    """Shapes whose units are cut into many pieces (one query: each value
+    half spread over ~76 CTAs, up to ~77 pieces merged), into a few, or not
+    at all (more units than SMs, tiles per unit small), with ragged top-k
+    and pads; both schedules against the oracle."""
+    cache = _fill_cache(8192, seed=20 + nq)
+    q = _queries(21 + topk, nq, heads)
+    rng = np.random.default_rng(22 + heads)
+    idx = np.stack([rng.integers(-1, 8192, topk) for _ in range(nq)]).astype(np.int64)
+    idx[:, :3] = rng.integers(0, 8192, (nq, 3))
+    _check(q, cache, idx, 0.06, 1, 8192, 8192)
+    _check(q, cache, idx, 0.06, 1, 8192, 8192, split=False)
+
+
+def test_split_workspace_too_small_is_refused():
+    dev = torch.device("cuda", 0)
+    q = torch.zeros((2, 128, 512), dtype=torch.bfloat16, device=dev)
+    cache = torch.zeros(64 * 272, dtype=torch.uint8, device=dev)
+    idx = torch.zeros((2, 64), dtype=torch.int64, device=dev)
+    need = kvq.attention_workspace_size(2, 128, 64)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device=dev)
+    with pytest.raises(kvq.KvqError):
+        kvq.mxfp4_mla_sparse_attention(q, cache, idx, 0.1, workspace=ws)
 
 
 def test_rejects_bad_arguments_on_gpu():
