@@ -50,7 +50,7 @@ ROW = 272
 N_TOKENS = 4_300_000
 ROW_STRIDE = 576
 N_SLOTS = 8_388_608
-PROFILE = os.path.join(ROOT, "profiles", "mxfp4_mla_store_4300000tok.md")
+PROFILE = os.path.join(ROOT, "profiles", "mxfp4_mla_store_400000tok.md")
 STORE_SOURCES = ["csrc/mxfp4_store.cu", "csrc/kvq_device.cuh", "csrc/kvq_host.h"]
 
 
@@ -220,9 +220,12 @@ def source_sha256():
     return h.hexdigest()
 
 
-def profiled_traffic():
-    """(bytes per launch, note) from the committed ncu summary, or (None, why)
-    when there is none or the kernel source changed since it was taken."""
+def profiled_traffic(valid):
+    """(DRAM bytes per launch, note) for the full workload with `valid` stored
+    rows, scaled from the committed ncu capture of a reduced case (DRAM bytes
+    per stored row there x valid rows: the traffic is the rows' own, so it
+    grows with them), or (None, why) when there is no capture or the kernel
+    source changed since it was taken."""
     try:
         text = open(PROFILE).read()
     except OSError:
@@ -232,7 +235,7 @@ def profiled_traffic():
             rec = json.loads(line[len("<!-- bench:"):line.rindex("-->")])
             if rec.get("source_sha256") != source_sha256():
                 return None, "kernel changed since the ncu capture"
-            return float(rec["traffic_bytes_per_launch"]), rec.get("note", "")
+            return float(rec["traffic_bytes_per_valid_row"]) * valid, rec.get("note", "")
     return None, "ncu summary has no bench record"
 
 
@@ -692,7 +695,7 @@ def run_ours(args):
     rd, wr = store_bytes(N_TOKENS, valid)
     mean_launch_ms = statistics.mean(per_launch)
     achieved = (rd + wr) / (mean_launch_ms * 1e-3) / 1e9
-    traffic, traffic_note = profiled_traffic()
+    traffic, traffic_note = profiled_traffic(valid)
     value = world * N_TOKENS * args.steps / (total_ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -31,7 +31,7 @@ __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp
 
 LIBRARY_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
 KVQ_OK, KVQ_EINVAL, KVQ_ECUDA = 0, -1, -2
-KVQ_ETIMEOUT = -3  # raised by the binding only: a kernel's status word was set
+KVQ_ETIMEOUT = -1000  # the binding's own: a kernel's status word was set (not a C status)
 
 _i64, _i32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
 _LIB = None
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.kvq_pointer_kind.argtypes = [_p]
         L.kvq_plain_fp8_quotient_mode.restype = ctypes.c_int
         L.kvq_plain_fp8_quotient_mode.argtypes = [ctypes.c_float]
+        L.kvq_plain_fp8_checks_run.restype = _i64
+        L.kvq_plain_fp8_checks_run.argtypes = []
         L.mxfp4_mla_store.restype = ctypes.c_int
         L.mxfp4_mla_store.argtypes = [_p, _i64, _i64, _i64, _p, _p, _i64, _i64, _i64, _i32, _p]
         L.mxfp4_mla_rmsnorm_store.restype = ctypes.c_int

@@ -13,8 +13,11 @@ inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
 
-// Number of SMs of the current device (queried once per device).
-inline int sm_count() {
+// Number of SMs of the current device (queried once per device). Internal
+// linkage: as a plain inline function its cache would be one STB_GNU_UNIQUE
+// object that the dynamic linker shares among every copy of the library
+// loaded into a process; static keeps one per translation unit instead.
+static inline int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;

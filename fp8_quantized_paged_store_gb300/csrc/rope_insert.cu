@@ -236,17 +236,16 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
             : __uint_as_float(0x3B000000u) * (float)man;  // man * 2**-9, exact
 }
 
-// Per E4M3 byte b (0..127), built once per block: s = value(b), y = RN(1/s)
-// for the corrected quotient, and the two-term reciprocal yh = RD(1/s),
-// yl = RN((1 - s*yh) * yh) >= 0 for nvfp4_code_value2.
+// Per E4M3 byte b (0..127), built once per block: s = value(b) and the
+// two-term reciprocal yh = RD(1/s), yl = RN((1 - s*yh) * yh) >= 0 that
+// nvfp4_code_value2 and nvfp4_rotary_code_value2 divide by.
 struct ScaleEntry {
-  float s, y, yh, yl;
+  float s, yh, yl;
 };
 
 __device__ __forceinline__ ScaleEntry make_scale_entry(uint32_t b) {
   ScaleEntry e;
   e.s = e4m3_value(b);
-  e.y = __frcp_rn(e.s);
   e.yh = __frcp_rd(e.s);
   e.yl = __fmul_rn(__fmaf_rn(-e.s, e.yh, 1.0f), e.yh);  // 1 - s*yh is exact
   return e;
@@ -260,9 +259,8 @@ __device__ __forceinline__ uint32_t nvfp4_scale(float amax, const float4* table,
   const uint32_t sbyte = cvt_e4m3x2(target, 0.0f) & 0xFFu;  // 0x01..0x7E
   const float4 t = table[sbyte];
   e.s = t.x;
-  e.y = t.y;
-  e.yh = t.z;
-  e.yl = t.w;
+  e.yh = t.y;
+  e.yl = t.z;
   return sbyte;
 }
 
@@ -288,23 +286,26 @@ __device__ __forceinline__ float2 nvfp4_code_value2(uint32_t w, const ScaleEntry
   return fma2_rn(x, make_float2(e.yh, e.yh), mul2_rn(x, make_float2(e.yl, e.yl)));
 }
 
-// Correctly rounded binary32 x / s for a tile's E4M3 scale s, given
-// y = RN(1/s): the product q0 = RN(x * y) is corrected once,
-// q1 = RN(q0 + (x - q0 * s) * y), both steps fused (Markstein's correction).
-// A GB300 check over every E4M3 significand and every binary32 significand
-// of x, both signs, found q1 == RN(x / s) in all 2**29 cases. Scaling x or s
-// by powers of two scales every step exactly while all intermediates stay
-// normal, which |q0| in [2**-60, 2**61) ensures for s in [2**-9, 448] (the
-// remainder is then >= 2**-115). x = +-0 gives q0 = +-0 and q1 = +0. Values
-// outside that range (tiny nonzero, or a tile whose amax * y reaches 2**61,
-// which includes infinite amax) make the whole warp take the IEEE division,
-// followed by +0.0 to turn a -0.0 quotient into +0.0.
-__device__ __noinline__ float nvfp4_quotient_ieee(float x, float s) {
-  return __fadd_rn(__fdiv_rn(x, s), 0.0f);
-}
-
-__device__ __forceinline__ bool markstein_ok(float x, float q0) {
-  return fabsf(q0) >= 0x1p-60f || x == 0.0f;
+// Code-deciding stand-in for RN(r / s) when r is a binary32 rotary value
+// (NaN already cleared): q = RN(r*yh + RN(r*yl)) + 0.0, with yh and yl the
+// two-term reciprocal of nvfp4_code_value2. The E2M1 code of a quotient
+// depends only on which side of each midpoint M (0.25, 0.75, ..., 5) it lies
+// and on ties at M itself; q and RN(r / s) can differ only if r / s lies
+// within about 2**-44 (relative) of a binary32 rounding boundary, and can
+// then change the code only if that boundary is next to some M. A boundary
+// B next to M has 25 significant bits with an odd last one, and s at most 4,
+// so B*s is never a binary32 value: the binary32 r nearest B*s keeps r / s
+// more than 2**-28 (relative) away from B, far outside the 2**-44 above. Where r /
+// s is exactly M, r*yh + RN(r*yl) is within 2**-44 of M and rounds to M. Far
+// from the midpoints (tiny, huge, or infinite r, the last only with s = 448
+// where yl > 0) the two agree on the code without any range check. The
+// final +0.0 turns a -0.0 result (from r = -0 or a quotient that underflows)
+// into +0.0, whose code is 0 as the oracle's sign rule gives. A CPU check
+// over every E4M3 scale, every midpoint and the binary32 values around each
+// adjacent boundary confirms the codes and the margin.
+__device__ __forceinline__ float2 nvfp4_rotary_code_value2(float2 r, const ScaleEntry& e) {
+  const float2 t = mul2_rn(r, make_float2(e.yl, e.yl));
+  return add2_rn(fma2_rn(r, make_float2(e.yh, e.yh), t), make_float2(0.0f, 0.0f));
 }
 
 // One NoPE tile of the record (16 bf16-exact values, elements 16*lane ..
@@ -314,21 +315,32 @@ __device__ __forceinline__ bool markstein_ok(float x, float q0) {
 __device__ __forceinline__ void nvfp4_nope_tile(uint4 a, uint4 b, uint8_t* codes,
                                                 uint8_t* scales, int lane, const float4* table,
                                                 bool store) {
-  auto clean = [](uint32_t v) {
-    const uint32_t r = nope_pair(v);
-    return r & bf16x2_nonzero_number_mask(r);
-  };
-  a.x = clean(a.x);
-  a.y = clean(a.y);
-  a.z = clean(a.z);
-  a.w = clean(a.w);
-  b.x = clean(b.x);
-  b.y = clean(b.y);
-  b.z = clean(b.z);
-  b.w = clean(b.w);
-  const uint32_t m = bf16x2_maxabs(bf16x2_maxabs(bf16x2_maxabs(a.x, a.y), bf16x2_maxabs(a.z, a.w)),
-                                   bf16x2_maxabs(bf16x2_maxabs(b.x, b.y), bf16x2_maxabs(b.z, b.w)));
-  const float amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
+  // Fast path, taken when no lane's tile holds a NaN or an infinity (the
+  // NaN-propagating |max| of the raw values is finite): the NoPE formula
+  // (e*1 - o*0, o*1 + e*0) then changes nothing but signs of zeros, and the
+  // clean-up below maps every zero to +0.0, so masking the zeros does both.
+  const uint32_t mr =
+      bf16x2_maxabs_nan(bf16x2_maxabs_nan(bf16x2_maxabs_nan(a.x, a.y), bf16x2_maxabs_nan(a.z, a.w)),
+                        bf16x2_maxabs_nan(bf16x2_maxabs_nan(b.x, b.y), bf16x2_maxabs_nan(b.z, b.w)));
+  const bool special = (mr & 0x7F80u) == 0x7F80u || (mr & 0x7F800000u) == 0x7F800000u;
+  float amax;
+  if (!__any_sync(0xFFFFFFFFu, special)) {
+    auto zero = [](uint32_t v) { return v & bf16x2_nonzero_number_mask(v); };
+    a = make_uint4(zero(a.x), zero(a.y), zero(a.z), zero(a.w));
+    b = make_uint4(zero(b.x), zero(b.y), zero(b.z), zero(b.w));
+    amax = fmaxf(fabsf(bf16_lo(mr)), fabsf(bf16_hi(mr)));
+  } else {
+    auto clean = [](uint32_t v) {
+      const uint32_t r = nope_pair(v);
+      return r & bf16x2_nonzero_number_mask(r);
+    };
+    a = make_uint4(clean(a.x), clean(a.y), clean(a.z), clean(a.w));
+    b = make_uint4(clean(b.x), clean(b.y), clean(b.z), clean(b.w));
+    const uint32_t m =
+        bf16x2_maxabs(bf16x2_maxabs(bf16x2_maxabs(a.x, a.y), bf16x2_maxabs(a.z, a.w)),
+                      bf16x2_maxabs(bf16x2_maxabs(b.x, b.y), bf16x2_maxabs(b.z, b.w)));
+    amax = fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
+  }
   ScaleEntry e;
   const uint32_t sbyte = nvfp4_scale(amax, table, e);
   const float2 q0 = nvfp4_code_value2(a.x, e), q1 = nvfp4_code_value2(a.y, e);
@@ -361,21 +373,8 @@ __device__ __forceinline__ void nvfp4_rotary_pair(uint32_t xr, float c, float sn
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
   ScaleEntry sc;
   const uint32_t sbyte = nvfp4_scale(amax, table, sc);
-  const float s = sc.s, y = sc.y;
-  const float2 r2 = make_float2(re, ro), y2 = make_float2(y, y);
-  const float2 q0 = mul2_rn(r2, y2);
-  const float qe0 = q0.x, qo0 = q0.y;
-  const bool ok = __fmul_rn(amax, y) < 0x1p61f && markstein_ok(re, qe0) && markstein_ok(ro, qo0);
-  float qe, qo;
-  if (__all_sync(0xFFFFFFFFu, ok)) {
-    // RN(r - q0 s) is exact; -s q0 == -(q0 s)
-    const float2 q1 = fma2_rn(fma2_rn(q0, make_float2(-s, -s), r2), y2, q0);
-    qe = q1.x;
-    qo = q1.y;
-  } else {
-    qe = nvfp4_quotient_ieee(re, s);
-    qo = nvfp4_quotient_ieee(ro, s);
-  }
+  const float2 q = nvfp4_rotary_code_value2(make_float2(re, ro), sc);
+  const float qe = q.x, qo = q.y;
   st_u8(codes + 224 + lane, cvt_e2m1x2(qe, qo));
   if ((lane & 7) == 0) st_u8(scales + 28 + (lane >> 3), sbyte);
 }
@@ -668,7 +667,7 @@ __global__ void __launch_bounds__(kRopeThreads, 5) nvfp4_insert_kernel(RopeParam
   __shared__ float4 scale_table[128];  // ScaleEntry of every E4M3 byte 0..127
   if (threadIdx.x < 128) {
     const ScaleEntry e = make_scale_entry(threadIdx.x);
-    scale_table[threadIdx.x] = make_float4(e.s, e.y, e.yh, e.yl);
+    scale_table[threadIdx.x] = make_float4(e.s, e.yh, e.yl, 0.0f);
   }
   __syncthreads();
   const int lane = threadIdx.x & 31;
@@ -765,8 +764,17 @@ inline uint32_t host_e4m3(float f) {
 // for the product modes. A power of two with a normal reciprocal takes the
 // product. Otherwise yh = RD(1/scale), yl = RN((1 - scale*yh) * yh) (the
 // residual is exact), and the two-term rule is used only if it gives the
-// division's E4M3 code for every bf16 pattern: an exhaustive check, run once
-// per distinct scale (the last answer is cached).
+// division's E4M3 code for every bf16 pattern: an exhaustive check (65,536
+// host iterations), run once per distinct scale. The answers for the last
+// kFp8Cached distinct scales are kept (one word each: (scale bits << 2) |
+// (mode + 1), replaced round robin), so that layers with different scales do
+// not repeat the check on every call. Concurrent callers at worst repeat a
+// check; every word they read is a complete answer.
+constexpr int kFp8Cached = 8;
+std::atomic<uint64_t> g_fp8_modes[kFp8Cached];
+std::atomic<uint32_t> g_fp8_next{0};
+std::atomic<int64_t> g_fp8_checks{0};
+
 inline int32_t fp8_quotient_mode(float scale, float& yh, float& yl) {
   int ex = 0;
   if (std::frexp(scale, &ex) == 0.5f && ex >= -124 && ex <= 127) {
@@ -779,9 +787,11 @@ inline int32_t fp8_quotient_mode(float scale, float& yh, float& yl) {
   yl = std::fmaf(-scale, yh, 1.0f) * yh;
   uint32_t bits = 0;
   std::memcpy(&bits, &scale, 4);
-  static std::atomic<uint64_t> last{0};  // (scale bits << 2) | (mode + 1)
-  const uint64_t seen = last.load(std::memory_order_relaxed);
-  if (seen != 0 && (seen >> 2) == bits) return (int32_t)(seen & 3u) - 1;
+  for (int k = 0; k < kFp8Cached; ++k) {
+    const uint64_t seen = g_fp8_modes[k].load(std::memory_order_relaxed);
+    if (seen != 0 && (seen >> 2) == bits) return (int32_t)(seen & 3u) - 1;
+  }
+  g_fp8_checks.fetch_add(1, std::memory_order_relaxed);
   int32_t mode = kTwoTerm;
   for (uint32_t b = 0; b < 65536u && mode == kTwoTerm; ++b) {
     const uint32_t w = b << 16;
@@ -791,7 +801,8 @@ inline int32_t fp8_quotient_mode(float scale, float& yh, float& yl) {
     volatile float t = x * yl;
     if (host_e4m3(q) != host_e4m3(std::fmaf(x, yh, t))) mode = kDivide;
   }
-  last.store(((uint64_t)bits << 2) | (uint64_t)(mode + 1), std::memory_order_relaxed);
+  const uint32_t k = g_fp8_next.fetch_add(1, std::memory_order_relaxed) % kFp8Cached;
+  g_fp8_modes[k].store(((uint64_t)bits << 2) | (uint64_t)(mode + 1), std::memory_order_relaxed);
   return mode;
 }
 
@@ -929,6 +940,10 @@ extern "C" int kvq_plain_fp8_quotient_mode(float fp8_scale) {
   if (!(fp8_scale > 0.0f && fp8_scale <= 3.0e38f)) return KVQ_EINVAL;
   float yh = 1.0f, yl = 0.0f;
   return fp8_quotient_mode(fp8_scale, yh, yl);
+}
+
+extern "C" int64_t kvq_plain_fp8_checks_run(void) {
+  return kvq::g_fp8_checks.load(std::memory_order_relaxed);
 }
 
 extern "C" int rope_plain_insert(const void* latent_bf16, int64_t num_tokens,

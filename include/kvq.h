@@ -286,9 +286,16 @@ int rope_plain_insert(const void* latent_bf16, int64_t num_tokens, int64_t row_s
  *      this scale; the binary32 rotary values by division;
  *   2  scale a power of two with a normal reciprocal: every value by
  *      RN(x * (1/scale)), the same rounding of the same exact quotient.
- * The check runs once per distinct scale (the last answer is cached).
- * KVQ_EINVAL unless 0 < fp8_scale <= 3e38. Host-only: launches nothing. */
+ * The check (65,536 host iterations on the calling thread) runs once per
+ * distinct scale: the answers for the last 8 distinct scales are kept, so
+ * up to 8 layers with different scales each pay it once. KVQ_EINVAL unless
+ * 0 < fp8_scale <= 3e38. Host-only: launches nothing. */
 int kvq_plain_fp8_quotient_mode(float fp8_scale);
+
+/* Number of those exhaustive host checks run so far in this process (by
+ * kvq_plain_fp8_quotient_mode or rope_plain_insert). A diagnostic of this
+ * library; the pages have no counterpart. */
+int64_t kvq_plain_fp8_checks_run(void);
 
 /*
  * save_ring_rows — store the compressor's fp32 [kv | score] rows of 1024
@@ -471,6 +478,7 @@ int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries, int64_t 
  */
 int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries, int64_t num_heads,
                                                   int64_t topk);
+
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,8 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(L):
     names = declared_functions()
     assert set(names) == {"kvq_strerror", "kvq_row_bytes", "kvq_pointer_kind",
-                          "kvq_plain_fp8_quotient_mode", "mxfp4_mla_store",
+                          "kvq_plain_fp8_quotient_mode", "kvq_plain_fp8_checks_run",
+                          "mxfp4_mla_store",
                           "mxfp4_mla_rmsnorm_store",
                           "rope_quant_insert_mxfp8", "rope_quant_insert_nvfp4",
                           "rope_quant_insert_v4", "rope_plain_insert", "save_ring_rows",
@@ -261,3 +262,27 @@ def test_pointer_kind_host_side(L):
     assert L.kvq_pointer_kind(None) == -1
     buf = ctypes.create_string_buffer(64)
     assert L.kvq_pointer_kind(ctypes.addressof(buf)) in (-2, 0)
+
+
+def test_fp8_quotient_check_runs_once_per_scale_for_up_to_eight_scales(L):
+    """Alternating fp8 scales (layers with different scales) pay the
+    exhaustive host check once each, not on every call; a ninth distinct
+    scale evicts the oldest answer."""
+    scales = [0.01371 + 0.00077 * k for k in range(9)]   # none a power of two, none used elsewhere
+    before = L.kvq_plain_fp8_checks_run()
+    modes = [L.kvq_plain_fp8_quotient_mode(s) for s in scales[:2]]
+    assert L.kvq_plain_fp8_checks_run() - before == 2
+    for _ in range(5):
+        assert [L.kvq_plain_fp8_quotient_mode(s) for s in scales[:2]] == modes
+    assert L.kvq_plain_fp8_checks_run() - before == 2
+    for s in scales[:8]:
+        L.kvq_plain_fp8_quotient_mode(s)
+    assert L.kvq_plain_fp8_checks_run() - before == 8
+    for _ in range(3):
+        for s in scales[:8]:
+            L.kvq_plain_fp8_quotient_mode(s)
+    assert L.kvq_plain_fp8_checks_run() - before == 8
+    L.kvq_plain_fp8_quotient_mode(scales[8])
+    assert L.kvq_plain_fp8_checks_run() - before == 9
+    assert L.kvq_plain_fp8_quotient_mode(0.25) == 2          # power of two: no check
+    assert L.kvq_plain_fp8_checks_run() - before == 9

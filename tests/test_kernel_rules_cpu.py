@@ -130,3 +130,91 @@ def test_plain_fp8_quotient_mode_rejects_bad_scales():
     import fp8_quantized_paged_store_gb300 as kvq
     for bad in (0.0, -1.0, float("nan"), float("inf")):
         assert kvq.lib().kvq_plain_fp8_quotient_mode(bad) == -1
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 codes of binary32 rotary values (rope_quant_insert_nvfp4, elements
+# 448..511): the kernel decides the E2M1 code of RN(r / s) from
+# q = RN(r*yh + RN(r*yl)) + 0.0 with the same two-term reciprocal, for any
+# binary32 r (no range check, no division).
+
+_MIDPOINTS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def _rotary_codes_kernel(r, yh, yl):
+    """The kernel's steps: t = RN(r*yl), q = RN(r*yh + t) (one rounding of the
+    exact sum), q + 0.0; then the GPU conversion, whose code for -0 is 8."""
+    with np.errstate(all="ignore"):
+        t = (r * yl).astype(np.float32)
+        q = (r.astype(LD) * LD(yh) + t.astype(LD)).astype(np.float32)
+        q = (q + np.float32(0)).astype(np.float32)
+    got = oracle.e2m1_code(q)
+    return np.where(np.signbit(q) & (got == 0), 8, got)
+
+
+def _rotary_codes_oracle(r, s):
+    with np.errstate(all="ignore"):
+        return oracle.e2m1_code((r / s).astype(np.float32))
+
+
+def _around(v, k=3):
+    """The binary32 values nearest the real v (given in long double), k on
+    each side of RN(v), both signs."""
+    f = np.float32(v)
+    vals = [f]
+    lo = hi = f
+    for _ in range(k):
+        lo = np.nextafter(lo, np.float32(-np.inf))
+        hi = np.nextafter(hi, np.float32(np.inf))
+        vals += [lo, hi]
+    a = np.array(vals, np.float32)
+    return np.concatenate([a, -a])
+
+
+@pytest.mark.skipif(np.finfo(LD).nmant < 63, reason="needs 64-bit long double mantissa")
+def test_nvfp4_rotary_two_term_decides_every_code_near_every_midpoint():
+    """For every positive E4M3 scale s and every E2M1 midpoint M, the binary32
+    r closest to M*s and to B*s for both binary32 rounding boundaries B next
+    to M (the only places where a one-unit difference between q and RN(r/s)
+    could change the code): codes equal. The r closest to B*s keep r/s more
+    than 2**-28 (relative) from B (the minimum over all cases is 2**-27.9),
+    while q's sum is within 2**-44 of r/s: no r anywhere can land between."""
+    min_margin = 1.0
+    for sb in range(1, 127):
+        s = np.float32(oracle.e4m3_decode(np.array([sb], np.uint8))[0])
+        yh, yl = _two_term(s)
+        for m in _MIDPOINTS:
+            mf = np.float32(m)
+            up = LD(np.nextafter(mf, np.float32(np.inf))) - LD(mf)
+            down = LD(mf) - LD(np.nextafter(mf, np.float32(0)))
+            for b in (LD(mf), LD(mf) + up / 2, LD(mf) - down / 2):
+                r = _around(b * LD(s))
+                want = _rotary_codes_oracle(r, s)
+                got = _rotary_codes_kernel(r, yh, yl)
+                bad = np.nonzero(got != want)[0]
+                assert bad.size == 0, (sb, m, r[bad[:3]], want[bad[:3]], got[bad[:3]])
+                if b != LD(mf):
+                    rel = np.abs(r.astype(LD) / LD(s) - b * np.sign(r.astype(LD))) / b
+                    min_margin = min(min_margin, float(rel.min()))
+    assert min_margin > 2.0 ** -28, min_margin
+
+
+@pytest.mark.skipif(np.finfo(LD).nmant < 63, reason="needs 64-bit long double mantissa")
+def test_nvfp4_rotary_two_term_random_and_special_values():
+    """Random binary32 values over the codes' whole range at every scale,
+    plus zeros of both signs, quotients that underflow to -0, subnormals,
+    huge values and (with s = 448, the only scale an infinite tile reaches)
+    infinities."""
+    rng = np.random.default_rng(11)
+    special = np.array([0.0, -0.0, 2.0 ** -149, -2.0 ** -149, -2.0 ** -140, 1e-38, -1e-38,
+                        3e38, -3e38, 2.0 ** 100, -2.0 ** 100], np.float32)
+    for sb in range(1, 127):
+        s = np.float32(oracle.e4m3_decode(np.array([sb], np.uint8))[0])
+        yh, yl = _two_term(s)
+        r = (rng.uniform(-8, 8, 20_000) * s).astype(np.float32)
+        wide = (rng.standard_normal(2_000) * np.exp2(rng.uniform(-140, 120, 2_000)))
+        r = np.concatenate([r, wide.astype(np.float32), special])
+        if s == np.float32(448):
+            r = np.concatenate([r, np.array([np.inf, -np.inf], np.float32)])
+        bad = np.nonzero(_rotary_codes_kernel(r, yh, yl) != _rotary_codes_oracle(r, s))[0]
+        assert bad.size == 0, (sb, r[bad[:3]])
