@@ -90,6 +90,10 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_mla_sparse_attention.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64, _i64,
                                                  _p, _i64, ctypes.c_float, _p, _i64, _i64, _p, _p,
                                                  _p, _i64, _p]
+        L.mxfp4_mla_sparse_attention_noalloc.restype = ctypes.c_int
+        L.mxfp4_mla_sparse_attention_noalloc.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64,
+                                                         _i64, _i64, _p, _i64, ctypes.c_float, _p,
+                                                         _i64, _i64, _p, _p, _p]
         L.mxfp4_mla_sparse_attention_workspace_size.restype = _i64
         L.mxfp4_mla_sparse_attention_workspace_size.argtypes = [_i64, _i64, _i64]
         _LIB = L

@@ -13,6 +13,9 @@ extern "C" const char* kvq_strerror(int status) {
       return "invalid argument (shape, range, null pointer or alignment); nothing was launched";
     case KVQ_ECUDA:
       return "CUDA kernel launch failed";
+    case KVQ_ESCRATCH:
+      return "the shapes need more scratch than the library's built-in array holds; nothing was "
+             "launched";
     default:
       return "unknown status";
   }

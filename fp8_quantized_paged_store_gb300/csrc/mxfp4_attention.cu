@@ -1037,3 +1037,66 @@ extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_querie
   }
   return launch_attention(p, stream);
 }
+
+// ------------------------------------------------- built-in scratch variant ---
+//
+// For callers that must not allocate device memory themselves: code embedded
+// in a host framework that owns every byte of device memory through its own
+// pool and hands a library no allocator (an allocation behind its back is
+// memory it neither counts nor limits), and latency-critical loops that
+// cannot afford cudaMalloc, which may synchronise the device. Such callers
+// can still pass their inputs and outputs; this entry point takes the split
+// schedule's scratch from an array in this library's own device memory
+// instead of from a workspace argument.
+//
+// The array is a file-scope __device__ object of kScratchBytes (40 MiB: the
+// split schedule of 128 heads over up to 159 SMs). Every GPU that loads this
+// library's attention code holds it until the process exits. Host code only
+// has a host-side stand-in for its name, so the device address is looked up
+// with cudaGetSymbolAddress once per device, with that device current, on
+// the first call made on it. Nothing in it needs to start at zero: each call
+// writes every piece it later reads. All calls share it and it keeps the last
+// call's contents, so two calls whose kernels overlap on the GPU (different
+// streams, or different host threads, on one device) race on it and must be
+// ordered by the caller.
+constexpr int64_t kScratchBytes = 40ll << 20;
+__device__ __align__(256) unsigned char g_attention_scratch[kScratchBytes];
+
+int scratch_address(void** out) {
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ECUDA;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attention_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return KVQ_ECUDA;
+    }
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return KVQ_OK;
+}
+
+extern "C" int mxfp4_mla_sparse_attention_noalloc(
+    const void* q_bf16, int64_t num_queries, int64_t num_heads, int64_t q_query_stride,
+    int64_t q_head_stride, const uint8_t* cache, int64_t num_blocks, int64_t block_size,
+    int64_t block_stride_rows, const int64_t* indices, int64_t topk, float sm_scale,
+    void* out_bf16, int64_t out_query_stride, int64_t out_head_stride, float* lse,
+    int32_t* status, cudaStream_t stream) {
+  using namespace kvq;
+  AttnParams p;
+  int rc = attention_params(q_bf16, num_queries, num_heads, q_query_stride, q_head_stride, cache,
+                            num_blocks, block_size, block_stride_rows, indices, topk, sm_scale,
+                            out_bf16, out_query_stride, out_head_stride, lse, status, p);
+  if (rc != KVQ_OK || num_queries == 0) return rc;
+  if (p.tiles > 0) {
+    const int64_t grid = split_grid(p.total);
+    if (split_bytes(grid, num_heads) > kScratchBytes) return KVQ_ESCRATCH;
+    void* scratch = nullptr;
+    rc = scratch_address(&scratch);
+    if (rc != KVQ_OK) return rc;
+    split_layout(p, grid, scratch);
+  }
+  return launch_attention(p, stream);
+}

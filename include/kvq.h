@@ -61,6 +61,7 @@ extern "C" {
 #define KVQ_OK 0
 #define KVQ_EINVAL (-1)
 #define KVQ_ECUDA (-2)
+#define KVQ_ESCRATCH (-3) /* the shapes need more scratch than the built-in array */
 
 /* Short English description of a status code (static storage). */
 const char* kvq_strerror(int status);
@@ -479,6 +480,39 @@ int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries, int64_t 
 int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries, int64_t num_heads,
                                                   int64_t topk);
 
+/*
+ * mxfp4_mla_sparse_attention_noalloc — mxfp4_mla_sparse_attention with the
+ * split schedule's scratch taken from an array inside this library, for
+ * callers that must not allocate device memory: code embedded in a host
+ * framework that owns all device memory through its own pool and passes no
+ * allocator down (memory allocated behind its back is neither counted nor
+ * limited by it), and latency-critical loops that cannot afford cudaMalloc,
+ * which may synchronise the device. The pages have no counterpart: this is a
+ * convenience of this library. The caller still passes every input and
+ * output; arguments, layouts, results and errors are those of
+ * mxfp4_mla_sparse_attention with a workspace, plus:
+ *   - The scratch is one 40 MiB (41,943,040-byte) __device__ array, enough
+ *     for 128 heads split over up to 159 SMs. Every GPU that loads the
+ *     library's attention code holds it until the process exits.
+ *   - Shapes whose split schedule needs more than that (see
+ *     mxfp4_mla_sparse_attention_workspace_size) return KVQ_ESCRATCH and
+ *     launch nothing.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *     that first call before any stream capture on the device.
+ *   - Nothing in the array needs to start at zero. Every call shares it and
+ *     it keeps the last call's contents: calls whose kernels may overlap on
+ *     the GPU (other streams, other host threads, one device) race on it,
+ *     and the caller must order them.
+ */
+int mxfp4_mla_sparse_attention_noalloc(const void* q_bf16, int64_t num_queries,
+                                       int64_t num_heads, int64_t q_query_stride,
+                                       int64_t q_head_stride, const uint8_t* cache,
+                                       int64_t num_blocks, int64_t block_size,
+                                       int64_t block_stride_rows, const int64_t* indices,
+                                       int64_t topk, float sm_scale, void* out_bf16,
+                                       int64_t out_query_stride, int64_t out_head_stride,
+                                       float* lse, int32_t* status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

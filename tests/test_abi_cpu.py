@@ -36,7 +36,8 @@ def test_every_declared_symbol_is_exported(L):
                           "rope_quant_insert_v4", "rope_plain_insert", "save_ring_rows",
                           "fused_save_compress_norm",
                           "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention",
-                          "mxfp4_mla_sparse_attention_workspace_size"}
+                          "mxfp4_mla_sparse_attention_workspace_size",
+                          "mxfp4_mla_sparse_attention_noalloc"}
     for n in names:
         assert hasattr(L, n), n
     # exported with C linkage from the shared object itself
