@@ -425,6 +425,31 @@ def live_copy_gbs(torch, src, stream, reps=5):
     return 2 * src.numel() * src.element_size() / (best * 1e-3) / 1e9
 
 
+def l2_fetch_granularity(torch, nbytes):
+    """Set the current context's cudaLimitMaxL2FetchGranularity (a hint of
+    the CUDA runtime, per process) to `nbytes` and return the previous value,
+    or None if the runtime cannot be reached (then nothing changes)."""
+    import ctypes
+    import glob
+    if nbytes is None:
+        return None
+    torch.cuda.synchronize()
+    libs = glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib",
+                                  "libcudart.so*")) + ["libcudart.so.13", "libcudart.so.12"]
+    for name in libs:
+        try:
+            rt = ctypes.CDLL(name)
+            old = ctypes.c_size_t(0)
+            if rt.cudaDeviceGetLimit(ctypes.byref(old), 0x05) != 0:
+                continue
+            if rt.cudaDeviceSetLimit(0x05, ctypes.c_size_t(nbytes)) != 0:
+                continue
+            return int(old.value)
+        except (OSError, AttributeError):
+            continue
+    return None
+
+
 def time_events(torch, fn, reps, stream, flush=None):
     """Mean and per-rep kernel times (ms) with CUDA events on `stream`."""
     times = []
@@ -521,15 +546,29 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
     call = lambda: kvq.mxfp4_mla_gather_dequant(cache, idx, out=outb)  # noqa: E731
     for _ in range(3):
         call()
+    ms_default, _ = time_events(torch, call, 20, stream, flush=flush)
+    # The rows are 272 bytes at random: with the context's default L2 fetch
+    # granularity a miss brings whole 128-byte lines (1.3x the rows' bytes
+    # from DRAM); with cudaLimitMaxL2FetchGranularity = 32 the L2 fetches the
+    # sectors asked for. A per-process context limit, restored afterwards.
+    limit_was = l2_fetch_granularity(torch, 32)
+    for _ in range(3):
+        call()
     ms, _ = time_events(torch, call, 20, stream, flush=flush)
+    l2_fetch_granularity(torch, limit_was)
     out["mxfp4_mla_gather_dequant"] = {
+        "l2_fetch_granularity_bytes": 32 if limit_was is not None else "unchanged (no runtime)",
+        "ms_default_l2_fetch": ms_default,
+        "frac_of_peak_default_l2_fetch": algo / (ms_default * 1e-3) / 1e9 / peak,
         "workload": "128 queries x 2048 indices (trailing pads) from 1,048,576 slots",
         "rows_per_s": idx.numel() / (ms * 1e-3), "ms": ms, "algorithmic_bytes": algo,
         "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
         "l2": "flushed before each rep (512 MB written, then 1 GiB read)"}
 
-    # sparse MLA decode attention on the same packed cache and indices: one
-    # CTA per (query, value half), then the split-K schedule (reported)
+    # sparse MLA decode attention on the same packed cache and indices, both
+    # schedules timed: one CTA per (query, value half), and the key tiles
+    # split over the SMs with a log-sum-exp merge; the line reports the one
+    # the binding picks by default for this shape
     call, _, _, status0 = attention_case(torch, kvq, dev, cache, idx, valid, split=False)
     for _ in range(3):
         call()
@@ -537,7 +576,9 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
     call, flops, hbm, status = attention_case(torch, kvq, dev, cache, idx, valid)
     for _ in range(3):
         call()
-    ms, _ = time_events(torch, call, 20, stream, flush=flush)
+    ms_split, _ = time_events(torch, call, 20, stream, flush=flush)
+    split = kvq.attention_prefers_split(128, 2048, dev)
+    ms = ms_split if split else ms_unsplit
     tpeak, tpeak_src = bf16_peak()
     out["mxfp4_mla_sparse_attention"] = {
         "workload": "128 queries x 128 heads x 2048 top-k (trailing pads), 1,048,576 slots",
@@ -545,9 +586,9 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
         "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tpeak, "bf16_peak_tflops": tpeak,
         "bf16_peak_source": tpeak_src, "hbm_bytes": hbm, "gbs": hbm / (ms * 1e-3) / 1e9,
         "wait_status": int(status.item()) | int(status0.item()),
-        "schedule": "split-K: key tiles split evenly over one CTA per SM, partials merged by "
-                    "log-sum-exp (both kernels timed)",
-        "unsplit_ms": ms_unsplit, "unsplit_tflops": flops / (ms_unsplit * 1e-3) / 1e12,
+        "schedule": ("split: key tiles over one CTA per SM, pieces merged by log-sum-exp"
+                     if split else "one CTA per (query, value half)") + " (the binding's default)",
+        "unsplit_ms": ms_unsplit, "split_ms": ms_split,
         "l2": "flushed before each rep (512 MB written, then 1 GiB read)"}
     return out
 

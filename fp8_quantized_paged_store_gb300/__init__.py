@@ -25,6 +25,7 @@ __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp
            "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
            "save_ring_rows", "fused_save_compress_norm",
            "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "attention_workspace_size",
+           "attention_prefers_split",
            "row_bytes",
            "cache_view", "KvqError", "lib", "KVQ_PTR_DEVICE", "KVQ_PTR_HOST_MAPPED",
            "LIBRARY_PATH"]
@@ -412,16 +413,18 @@ def mxfp4_mla_gather_dequant(cache: torch.Tensor, indices: torch.Tensor, out: to
 
 def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: torch.Tensor,
                                sm_scale: float, out: torch.Tensor = None, lse: torch.Tensor = None,
-                               status: torch.Tensor = None, workspace=True, stream=None):
+                               status: torch.Tensor = None, workspace="auto", stream=None):
     """q: bf16 [num_queries, num_heads <= 128, 512] (unit last stride, strides
     multiples of 8); cache: uint8 paged view (see cache_view) of 272-byte rows;
     indices: int64 [num_queries, topk] (contiguous; -1 pads). Returns (out bf16
     [num_queries, num_heads, 512], lse fp32 [num_queries, num_heads] or None).
 
-    ``workspace``: True (default) splits the key tiles evenly over the SMs
-    with a workspace allocated here, False runs one CTA per (query, value
-    half) with none, or a uint8 device tensor of at least
-    ``attention_workspace_size(...)`` bytes to use.
+    ``workspace``: "auto" (default) splits the key tiles evenly over the SMs
+    (with a workspace allocated here) when one CTA per (query, value half)
+    would leave the SMs idle for much of its last wave (see
+    ``attention_prefers_split``), True always splits, False never does, and
+    a uint8 device tensor of at least ``attention_workspace_size(...)``
+    bytes splits with that workspace.
     ``status``: an int32 device tensor of one element that the kernel sets
     nonzero if an internal wait timed out (the output is then undefined); the
     caller reads it. Without one, a status word is made here and read back
@@ -452,6 +455,10 @@ def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: to
         if own_status:
             status = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
         _need(status, torch.int32, "status")
+        if isinstance(workspace, str):
+            if workspace != "auto":
+                raise ValueError('workspace must be "auto", True, False or a uint8 tensor')
+            workspace = attention_prefers_split(nq, indices.shape[1], cuda_dev)
         if workspace is True:
             nbytes = attention_workspace_size(nq, nh, indices.shape[1])
             workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=cuda_dev) \
@@ -479,3 +486,19 @@ def attention_workspace_size(num_queries: int, num_heads: int, topk: int) -> int
     if n < 0:
         raise KvqError("mxfp4_mla_sparse_attention_workspace_size", n)
     return n
+
+
+def attention_prefers_split(num_queries: int, topk: int, device=None) -> bool:
+    """Whether splitting the key tiles over the SMs should beat one CTA per
+    (query, value half) on this device: it does when the unsplit grid of
+    2 x num_queries CTAs (one per SM at a time) would use less than 3/4 of
+    the SM-waves it occupies. The split costs a log-sum-exp merge and a
+    pipeline restart per segment, so a nearly full last wave is not worth
+    it."""
+    if topk <= 0 or num_queries <= 0:
+        return False
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    units = 2 * num_queries
+    waves = -(-units // sms)
+    return units / (waves * sms) < 0.75

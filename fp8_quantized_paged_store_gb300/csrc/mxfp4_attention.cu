@@ -127,6 +127,7 @@ struct AttnParams {
   // into `grid` contiguous ranges, CTA b taking [total*b/grid,
   // total*(b+1)/grid).
   int64_t tiles, units, total;
+  int64_t nq;  // queries
   int64_t grid;
   // Partial results of units split between CTAs (null when grid is one CTA
   // per unit, so that nothing is split): piece slot 2b (CTA b's first
@@ -255,6 +256,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -342,22 +356,34 @@ struct Packed {
   uint32_t s;
 };
 
-// Position in a CTA's run of tiles: unit (query << 1 | value half) and the
-// tile within the unit.
+// Position in a CTA's run of tiles: query n, value half v, and tile t within
+// the unit (n, v); next() says whether it entered a new unit. The split schedule orders units half-major (every query's half 0,
+// then every query's half 1), so that the two halves of a query run at the
+// same time on different CTAs and read the same packed rows through L2.
+// Unsplit (one CTA per unit), a CTA's tiles never leave its unit.
+template <bool kSplit>
 struct Cursor {
-  int64_t unit, t;
-  __device__ __forceinline__ void next(int64_t tiles) {
-    if (++t == tiles) {
+  int64_t n, t;
+  int32_t v;
+  __device__ __forceinline__ bool next(const AttnParams& p) {
+    ++t;
+    if (kSplit && t == p.tiles) {
       t = 0;
-      ++unit;
+      if (++n == p.nq) {
+        n = 0;
+        ++v;
+      }
+      return true;
     }
+    return false;
   }
 };
 
 // Slot index of key j of the cursor's tile, or -1 past the query's top-k.
-__device__ __forceinline__ int64_t key_index(const AttnParams& p, const Cursor& c, int j) {
+template <bool kSplit>
+__device__ __forceinline__ int64_t key_index(const AttnParams& p, const Cursor<kSplit>& c, int j) {
   const int64_t k = c.t * kTileKeys + j;
-  return k < p.topk ? ld_once_i64(p.indices + (c.unit >> 1) * p.topk + k) : -1;
+  return k < p.topk ? ld_once_i64(p.indices + c.n * p.topk + k) : -1;
 }
 
 __device__ __forceinline__ uint32_t ld_issue_u16(const void* p) {
@@ -489,22 +515,22 @@ __device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_
 }
 
 __device__ __noinline__ void load_q_tmem(const AttnParams& p, int64_t n, uint32_t tmem,
-                                            int tid) {
+                                         int tid) {
   const uint32_t lane_base = tmem + ((uint32_t)((tid >> 5) * 32) << 16);
   const uint8_t* qrow = p.q + n * p.q_qstride + (int64_t)tid * p.q_hstride;
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    uint32_t w[16];
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[32];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 8; ++k) {
       const uint4 x =
-          tid < p.num_heads ? ld_once_v4(qrow + 64 * c + 16 * k) : make_uint4(0, 0, 0, 0);
+          tid < p.num_heads ? ld_once_v4(qrow + 128 * c + 16 * k) : make_uint4(0, 0, 0, 0);
       w[4 * k] = x.x;
       w[4 * k + 1] = x.y;
       w[4 * k + 2] = x.z;
       w[4 * k + 3] = x.w;
     }
-    tmem_st16(lane_base + kColQ + 16 * c, w);
+    tmem_st32(lane_base + kColQ + 32 * c, w);
   }
 }
 
@@ -523,36 +549,38 @@ __device__ __forceinline__ bool drain_mmas(uint32_t bar) {
 // lanes of this warp): the bf16 output row half, or for a unit split between
 // CTAs the fp32 output normalised by this piece's softmax sum and that sum's
 // log-sum-exp (log2 units) in piece slot `slot`.
-__device__ __forceinline__ void write_segment(const AttnParams& p, int64_t unit, bool whole,
+// Reads O out 16 columns at a time, which keeps the softmax loop's live
+// state in registers around it.
+template <bool kSplit>
+__device__ __forceinline__ void write_segment(const AttnParams& p, int64_t n, int v, bool whole,
                                               int64_t slot, uint32_t lane_base, int h,
                                               float m_ref, float l) {
+  if (!kSplit) whole = true;
   const bool store = h < p.num_heads;
-  const int64_t n = unit >> 1;
-  const int v = (int)(unit & 1);
   const float inv = l > 0.0f ? 1.0f / l : 0.0f;
   uint8_t* orow = p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
   float* prow = whole ? nullptr : p.part_o + (slot * p.num_heads + h) * kHalf;
 #pragma unroll 1
-  for (int c = 0; c < kHalf / 32; ++c) {
-    uint32_t o[32];
-    tmem_ld32(lane_base + kColO + 32 * c, o);
+  for (int c = 0; c < kHalf / 16; ++c) {
+    uint32_t o[16];
+    tmem_ld16(lane_base + kColO + 16 * c, o);
     if (whole) {
-      uint32_t w[16];
+      uint32_t w[8];
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
+      for (int k = 0; k < 8; ++k)
         w[k] = l > 0.0f ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv,
                                       __uint_as_float(o[2 * k + 1]) * inv)
                         : 0u;
       if (store) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_v4(orow + 64 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
+        for (int u = 0; u < 2; ++u)
+          st_v4(orow + 32 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
                                                     w[4 * u + 3]));
       }
     } else if (store) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_v4(prow + 32 * c + 4 * u,
+      for (int u = 0; u < 4; ++u)
+        st_v4(prow + 16 * c + 4 * u,
               make_uint4(__float_as_uint(__uint_as_float(o[4 * u]) * inv),
                          __float_as_uint(__uint_as_float(o[4 * u + 1]) * inv),
                          __float_as_uint(__uint_as_float(o[4 * u + 2]) * inv),
@@ -574,6 +602,10 @@ __device__ __forceinline__ int64_t range_begin(const AttnParams& p, int64_t b) {
   return p.grid == p.units ? b * p.tiles : p.total * b / p.grid;
 }
 
+// kSplit: the split schedule (ranges of tiles over units, pieces, Q reloads
+// between segments); otherwise one CTA per unit, which compiles without any
+// of that.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -600,10 +632,13 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
   // this CTA's run of tiles [g0, g1) and where it starts
-  const int64_t g0 = range_begin(p, b), g1 = range_begin(p, b + 1);
-  const int64_t n_tiles = g1 - g0;  // >= 1: grid <= total
-  const int64_t u_first = g0 / p.tiles;
-  const Cursor start{u_first, g0 - u_first * p.tiles};
+  const int64_t g0 = kSplit ? range_begin(p, b) : b * p.tiles;
+  const int64_t n_tiles = kSplit ? range_begin(p, b + 1) - g0 : p.tiles;  // >= 1: grid <= total
+  const int64_t u_first = kSplit ? g0 / p.tiles : b;
+  Cursor<kSplit> start;
+  start.t = g0 - u_first * p.tiles;
+  start.n = kSplit ? u_first % p.nq : b >> 1;
+  start.v = (int32_t)(kSplit ? u_first / p.nq : b & 1);
 
   if (warp == kIssuerWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   if (tid == 0) {
@@ -619,12 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  load_q_smem(p, u_first >> 1, q_base, tid, kThreads);
+  load_q_smem(p, start.n, q_base, tid, kThreads);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) load_q_tmem(p, u_first >> 1, tmem, tid);
+  if (warp < 4) load_q_tmem(p, start.n, tmem, tid);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -635,12 +670,12 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     // i-th tile goes to stage i % kStages, free once the p.v of tile
     // i - kStages has completed; rows are loaded kDepth tiles ahead.
     const int e = warp - 4, j = lane;
-    Cursor cl = start;  // the tile whose rows are loaded next
+    Cursor<kSplit> cl = start;  // the tile whose rows are loaded next
     Packed buf[kDepth];
 #pragma unroll
     for (int u = 0; u < kDepth; ++u) {
       buf[u] = load_packed(p, u < n_tiles ? key_index(p, cl, j) : -1, e);
-      cl.next(p.tiles);
+      cl.next(p);
     }
     int64_t s_next = kDepth < n_tiles ? key_index(p, cl, j) : -1;
     bool live = true;
@@ -651,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
         if (i < n_tiles && live) {
           const Packed cur = buf[u];
           buf[u] = load_packed(p, s_next, e);  // tile i + kDepth
-          cl.next(p.tiles);
+          cl.next(p);
           s_next = i + kDepth + 1 < n_tiles ? key_index(p, cl, j) : -1;
           const uint32_t st = (uint32_t)(i % kStages);
           if (i >= kStages &&
@@ -678,13 +713,16 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       // waits for softmax to have read out the previous segment's output;
       // the first q.k of a new query waits for softmax to have loaded its Q.
       // Segment boundaries are observed one at a time, in order.
-      Cursor cq = start, cp = start;
+      Cursor<kSplit> cq = start, cp = start;
       int64_t qi = 0, pi = 0, seen = 0;
+      int32_t qseg = 0, pseg = 0;  // segments of the next q.k and p.v tiles
       uint32_t idle = 0;
       auto seg_ready = [&](int64_t k) -> bool {
-        while (seen < k) {
-          if (!mbar_test(bars + kBarSeg, (uint32_t)(seen & 1))) return false;
-          ++seen;
+        if constexpr (kSplit) {
+          while (seen < k) {
+            if (!mbar_test(bars + kBarSeg, (uint32_t)(seen & 1))) return false;
+            ++seen;
+          }
         }
         return true;
       };
@@ -692,29 +730,27 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
         bool progress = false;
         if (pi < qi && mbar_test(bars + kBarPFull + 8 * (uint32_t)(pi % kStages),
                                  (uint32_t)((pi / kStages) & 1))) {
-          const bool first = pi == 0 || cp.t == 0;
-          if (!first || pi == 0 || seg_ready(cp.unit - u_first)) {
+          const bool first = pi == 0 || (kSplit && cp.t == 0);
+          if (!first || pi == 0 || seg_ready(pseg)) {
             tc_fence_after();
-            issue_pv((uint32_t)(pi % kStages), (int)(cp.unit & 1), first, k_base, tmem);
+            issue_pv((uint32_t)(pi % kStages), cp.v, first, k_base, tmem);
             mma_commit(bars + kBarPvDone + 8 * (uint32_t)(pi % kStages));
             ++pi;
-            cp.next(p.tiles);
+            pseg += cp.next(p) ? 1 : 0;
             progress = true;
           }
         }
         if (!progress && qi < n_tiles) {
           const uint32_t st = (uint32_t)(qi % kStages);
-          Cursor c2 = cq;
-          c2.next(p.tiles);
-          const bool pair =
-              (st & 1u) == 0 && qi + 1 < n_tiles && (c2.unit >> 1) == (cq.unit >> 1);
-          const int64_t q_unit0 = cq.unit & ~(int64_t)1;  // first unit of the tile's query
-          const int64_t q_seg = (q_unit0 > u_first ? q_unit0 : u_first) - u_first;
+          Cursor<kSplit> c2 = cq;
+          const int32_t qseg2 = qseg + (c2.next(p) ? 1 : 0);
+          // pairs stay within a unit (its next tile is not a unit's first)
+          const bool pair = (st & 1u) == 0 && qi + 1 < n_tiles && (!kSplit || c2.t != 0);
           if (qi + (pair ? 1 : 0) - pi < kStages &&
               mbar_test(bars + kBarKFull + 8 * st, (uint32_t)((qi / kStages) & 1)) &&
               (!pair || mbar_test(bars + kBarKFull + 8 * (st + 1),
                                   (uint32_t)(((qi + 1) / kStages) & 1))) &&
-              seg_ready(q_seg)) {
+              seg_ready(qseg)) {
             tc_fence_after();
             if (pair) {
               issue_qk<true>(st, q_desc, k_base, tmem);
@@ -722,12 +758,13 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
               mma_commit(bars + kBarSFull + 8 * (st + 1));
               qi += 2;
               cq = c2;
-              cq.next(p.tiles);
+              qseg = qseg2 + (cq.next(p) ? 1 : 0);
             } else {
               issue_qk<false>(st, q_desc, k_base, tmem);
               mma_commit(bars + kBarSFull + 8 * st);
               qi += 1;
               cq = c2;
+              qseg = qseg2;
             }
             progress = true;
           }
@@ -751,18 +788,19 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     float m_ref = kNegInf;  // reference max of the segment (log2 units)
     float l = 0.0f;         // sum of p against m_ref
     bool live = true;
-    Cursor c = start;
+    Cursor<kSplit> c = start;
+    bool first_seg = true;  // in the CTA's first segment
     int64_t s_key = key_index(p, c, lane);
     for (int64_t i = 0; i < n_tiles && live; ++i) {
-      const bool seg_first = i == 0 || c.t == 0;
-      const bool seg_last = i == n_tiles - 1 || c.t == p.tiles - 1;
+      const bool seg_first = i == 0 || (kSplit && c.t == 0);
+      const bool seg_last = i == n_tiles - 1 || (kSplit && c.t == p.tiles - 1);
       if (seg_first) {
         m_ref = kNegInf;
         l = 0.0f;
       }
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, s_key >= 0 && s_key < p.num_slots);
-      Cursor cn = c;
-      cn.next(p.tiles);
+      Cursor<kSplit> cn = c;
+      const bool new_unit = cn.next(p);
       s_key = i + 1 < n_tiles ? key_index(p, cn, lane) : -1;
       const uint32_t st = (uint32_t)(i % kStages);
       if (!warp_wait(bars + kBarSFull + 8 * st, (uint32_t)((i / kStages) & 1), abort)) {
@@ -835,20 +873,22 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
         tc_fence_after();
         // whole: the segment runs from the unit's first tile to its last
         // (recomputed here rather than kept live through the loop)
-        const int64_t cta = blockIdx.x, r0 = range_begin(p, cta), uf = r0 / p.tiles;
-        const bool whole = c.t + 1 == p.tiles && (c.unit > uf || r0 == uf * p.tiles);
-        write_segment(p, c.unit, whole, 2 * cta + (c.unit == uf ? 0 : 1), lane_base, tid, m_ref,
-                      l);
-        if (i + 1 < n_tiles) {
-          if ((cn.unit >> 1) != (c.unit >> 1)) {
-            load_q_smem(p, cn.unit >> 1, q_base, tid, 128);
-            load_q_tmem(p, cn.unit >> 1, tmem, tid);
+        const int64_t cta = blockIdx.x;
+        const bool whole = c.t + 1 == p.tiles &&
+                           (!first_seg || (kSplit ? range_begin(p, cta) % p.tiles : 0) == 0);
+        write_segment<kSplit>(p, c.n, c.v, whole, 2 * cta + (first_seg ? 0 : 1), lane_base, tid,
+                              m_ref, l);
+        if (kSplit && i + 1 < n_tiles) {
+          if (cn.n != c.n) {
+            load_q_smem(p, cn.n, q_base, tid, 128);
+            load_q_tmem(p, cn.n, tmem, tid);
           }
           tc_fence_before();
           mbar_arrive(bars + kBarSeg);
         }
       }
       c = cn;
+      if (new_unit) first_seg = false;
     }
   }
   tc_fence_before();
@@ -860,52 +900,63 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   }
 }
 
-// Combines the pieces of every unit split between CTAs. Block j looks at the
-// boundary between CTAs j and j + 1; the unit it falls inside (if any) is
-// merged by the block of its first boundary, over the pieces of CTAs
-// b_first..b_last: out = sum_b 2**(lse_b - L) o_b / sum_b 2**(lse_b - L),
-// L = max_b lse_b, and the unit's log-sum-exp L + log2(sum) (in natural
-// log units, half 0 only). A unit without any valid key gets zeros and -inf.
-// Thread t: head t / 64 + 4k, columns 4 (t % 64) .. 4 (t % 64) + 3.
-__global__ void __launch_bounds__(256) mxfp4_attention_merge_kernel(AttnParams p) {
+// Combines the pieces of every unit split between CTAs. Block (j, g) looks at
+// the boundary between CTAs j and j + 1 and heads 8g..8g+7; the unit the
+// boundary falls inside (if any) is merged by the blocks of its first
+// boundary, over the pieces of CTAs b_first..b_last:
+// out = sum_b 2**(lse_b - L) o_b / sum_b 2**(lse_b - L), L = max_b lse_b, and
+// the unit's log-sum-exp L + log2(sum) (in natural log units, half 0 only).
+// A unit without any valid key gets zeros and -inf. The pieces' slots are
+// worked out once per block (threads in parallel, into shared memory); then
+// 64 threads take a head, four columns each.
+constexpr int kMergeMaxPieces = 1024;  // grid <= 1023
+constexpr int kMergeHeads = 8;         // heads per block (64 threads each)
+
+__global__ void __launch_bounds__(64 * kMergeHeads) mxfp4_attention_merge_kernel(AttnParams p) {
+  __shared__ int32_t piece_slot[kMergeMaxPieces];
   const int64_t j = blockIdx.x;
   const int64_t gb = p.total * (j + 1) / p.grid;
   const int64_t unit = gb / p.tiles;
   if (gb == unit * p.tiles) return;  // the boundary lies between units
   const int64_t g0 = p.total * j / p.grid;
-  if (g0 > unit * p.tiles) return;   // merged by the block of an earlier boundary
+  if (g0 > unit * p.tiles) return;   // merged by the blocks of an earlier boundary
   const int64_t b_last = ((unit + 1) * p.tiles * p.grid - 1) / p.total;
-  const int64_t n = unit >> 1;
-  const int v = (int)(unit & 1);
+  const int pieces = (int)(b_last - j + 1);
+  for (int k = threadIdx.x; k < pieces; k += blockDim.x) {
+    const int64_t bb = j + k;
+    piece_slot[k] = (int32_t)(2 * bb + ((p.total * bb / p.grid) / p.tiles == unit ? 0 : 1));
+  }
+  __syncthreads();
+  const int64_t H = p.num_heads;
+  const int64_t h = (int64_t)blockIdx.y * kMergeHeads + (threadIdx.x >> 6);
+  if (h >= H) return;
+  const int64_t n = unit % p.nq;  // half-major unit order
+  const int v = (int)(unit / p.nq);
   const int c4 = threadIdx.x & 63;
   const float kNegInf = -__int_as_float(0x7F800000);
-  for (int64_t h = threadIdx.x >> 6; h < p.num_heads; h += 4) {
-    float L = kNegInf;
-    for (int64_t bb = j; bb <= b_last; ++bb) {
-      const int64_t slot = 2 * bb + ((p.total * bb / p.grid) / p.tiles == unit ? 0 : 1);
-      L = fmaxf(L, p.part_lse[slot * p.num_heads + h]);
+  float L = kNegInf;
+#pragma unroll 4
+  for (int k = 0; k < pieces; ++k) L = fmaxf(L, p.part_lse[piece_slot[k] * H + h]);
+  float W = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (L != kNegInf) {
+#pragma unroll 4
+    for (int k = 0; k < pieces; ++k) {
+      const int64_t row = piece_slot[k] * H + h;
+      const float w = exp2f(p.part_lse[row] - L);
+      const float4 o = *reinterpret_cast<const float4*>(p.part_o + row * kHalf + 4 * c4);
+      W += w;
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
     }
-    float W = 0.0f;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (L != kNegInf) {
-      for (int64_t bb = j; bb <= b_last; ++bb) {
-        const int64_t slot = 2 * bb + ((p.total * bb / p.grid) / p.tiles == unit ? 0 : 1);
-        const float w = exp2f(p.part_lse[slot * p.num_heads + h] - L);
-        const float4 o = *reinterpret_cast<const float4*>(
-            p.part_o + (slot * p.num_heads + h) * kHalf + 4 * c4);
-        W += w;
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
-      }
-    }
-    const float inv = W > 0.0f ? 1.0f / W : 0.0f;
-    st_v2(p.out + n * p.o_qstride + h * p.o_hstride + (int64_t)(v * kHalf + 4 * c4) * 2,
-          pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    if (v == 0 && p.lse && c4 == 0)
-      p.lse[n * p.num_heads + h] = W > 0.0f ? (L + log2f(W)) * 0.69314718055994531f : kNegInf;
   }
+  const float inv = W > 0.0f ? 1.0f / W : 0.0f;
+  st_v2(p.out + n * p.o_qstride + h * p.o_hstride + (int64_t)(v * kHalf + 4 * c4) * 2,
+        pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (v == 0 && p.lse && c4 == 0)
+    p.lse[n * H + h] = W > 0.0f ? (L + log2f(W)) * 0.69314718055994531f : kNegInf;
 }
 
 }  // namespace
@@ -964,6 +1015,7 @@ int attention_params(const void* q_bf16, int64_t num_queries, int64_t num_heads,
   p.status = status;
   p.tiles = tiles;
   p.units = 2 * num_queries;
+  p.nq = num_queries;
   p.total = 2 * num_queries * tiles;
   p.grid = 2 * num_queries;  // one CTA per unit unless split
   p.part_o = nullptr;
@@ -989,15 +1041,23 @@ int launch_attention(const kvq::AttnParams& p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ECUDA;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(mxfp4_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mxfp4_attention_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(mxfp4_attention_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return KVQ_ECUDA;
     attr_done[dev] = 1;
   }
-  mxfp4_attention_kernel<<<(unsigned)p.grid, kThreads, kSmemBytes, stream>>>(p);
+  if (p.part_o)
+    mxfp4_attention_kernel<true><<<(unsigned)p.grid, kThreads, kSmemBytes, stream>>>(p);
+  else
+    mxfp4_attention_kernel<false><<<(unsigned)p.grid, kThreads, kSmemBytes, stream>>>(p);
   int rc = launch_status();
   if (rc != KVQ_OK || !p.part_o || p.grid < 2) return rc;
-  mxfp4_attention_merge_kernel<<<(unsigned)(p.grid - 1), 256, 0, stream>>>(p);
+  const dim3 mgrid((unsigned)(p.grid - 1), (unsigned)((p.num_heads + kMergeHeads - 1) / kMergeHeads));
+  mxfp4_attention_merge_kernel<<<mgrid, 64 * kMergeHeads, 0, stream>>>(p);
   return launch_status();
 }
 
