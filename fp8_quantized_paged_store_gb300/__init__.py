@@ -25,7 +25,7 @@ __all__ = ["mxfp4_mla_store", "mxfp4_mla_rmsnorm_store", "rope_quant_insert_mxfp
            "rope_quant_insert_nvfp4", "rope_quant_insert_v4", "rope_plain_insert",
            "save_ring_rows", "fused_save_compress_norm",
            "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention", "attention_workspace_size",
-           "attention_prefers_split",
+           "attention_prefers_split", "mxfp4_mla_sparse_attention_ragged",
            "row_bytes",
            "cache_view", "KvqError", "lib", "KVQ_PTR_DEVICE", "KVQ_PTR_HOST_MAPPED",
            "LIBRARY_PATH"]
@@ -95,6 +95,10 @@ def lib() -> ctypes.CDLL:
         L.mxfp4_mla_sparse_attention_noalloc.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64,
                                                          _i64, _i64, _p, _i64, ctypes.c_float, _p,
                                                          _i64, _i64, _p, _p, _p]
+        L.mxfp4_mla_sparse_attention_ragged.restype = ctypes.c_int
+        L.mxfp4_mla_sparse_attention_ragged.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64,
+                                                        _i64, _p, _i64, _p, ctypes.c_float, _p,
+                                                        _i64, _i64, _p, _p, _p]
         L.mxfp4_mla_sparse_attention_workspace_size.restype = _i64
         L.mxfp4_mla_sparse_attention_workspace_size.argtypes = [_i64, _i64, _i64]
         _LIB = L
@@ -476,6 +480,56 @@ def mxfp4_mla_sparse_attention(q: torch.Tensor, cache: torch.Tensor, indices: to
                 workspace.numel() if workspace is not None else 0, s))
     if own_status and int(status.item()) != 0:
         raise KvqError("mxfp4_mla_sparse_attention", KVQ_ETIMEOUT)
+    return out, lse
+
+
+def mxfp4_mla_sparse_attention_ragged(q: torch.Tensor, cache: torch.Tensor,
+                                      indices: torch.Tensor, key_offsets: torch.Tensor,
+                                      sm_scale: float, out: torch.Tensor = None,
+                                      lse: torch.Tensor = None, status: torch.Tensor = None,
+                                      stream=None):
+    """Sparse attention over ragged index runs (sparse prefill): query n uses
+    indices[key_offsets[n]:key_offsets[n + 1]] of a flat int64 tensor.
+    q: bf16 [num_queries, num_heads <= 128, 512] as for
+    mxfp4_mla_sparse_attention; key_offsets: int64 [num_queries + 1],
+    contiguous, on the device. Returns (out, lse); ``status`` as there."""
+    _need(q, torch.bfloat16, "q")
+    _need(indices, torch.int64, "indices")
+    _need(key_offsets, torch.int64, "key_offsets")
+    if q.dim() != 3 or q.shape[2] != 512 or q.stride(2) != 1:
+        raise ValueError("q must be [num_queries, num_heads, 512] with unit last stride")
+    nq, nh, _ = q.shape
+    if indices.dim() != 1 or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous 1-D tensor")
+    if tuple(key_offsets.shape) != (nq + 1,) or not key_offsets.is_contiguous():
+        raise ValueError("key_offsets must be a contiguous [num_queries + 1] tensor")
+    nb, bs, bsr = cache_view(cache, row_bytes(512, 32))
+    dev = _device("mxfp4_mla_sparse_attention_ragged",
+                  (q, cache, indices, key_offsets, out, lse, status), stream)
+    cuda_dev = torch.device("cuda", dev if dev is not None else torch.cuda.current_device())
+    if out is None:
+        out = torch.empty((nq, nh, 512), dtype=torch.bfloat16, device=q.device,
+                          pin_memory=not q.is_cuda)
+    _need(out, torch.bfloat16, "out")
+    if out.dim() != 3 or tuple(out.shape) != (nq, nh, 512) or out.stride(2) != 1:
+        raise ValueError("out must be [num_queries, num_heads, 512] with unit last stride")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+        if tuple(lse.shape) != (nq, nh) or not lse.is_contiguous():
+            raise ValueError("lse must be a contiguous [num_queries, num_heads] tensor")
+    own_status = status is None
+    if own_status:
+        with torch.cuda.device(cuda_dev):
+            status = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    _need(status, torch.int32, "status")
+    _launch("mxfp4_mla_sparse_attention_ragged", (q, cache, indices, key_offsets, out, lse, status),
+            stream, lambda s: lib().mxfp4_mla_sparse_attention_ragged(
+                q.data_ptr(), nq, nh, q.stride(0), q.stride(1), cache.data_ptr(), nb, bs, bsr,
+                indices.data_ptr() if indices.numel() else None, indices.numel(),
+                key_offsets.data_ptr(), float(sm_scale), out.data_ptr(), out.stride(0),
+                out.stride(1), lse.data_ptr() if lse is not None else None, status.data_ptr(), s))
+    if own_status and int(status.item()) != 0:
+        raise KvqError("mxfp4_mla_sparse_attention_ragged", KVQ_ETIMEOUT)
     return out, lse
 
 

@@ -136,6 +136,11 @@ struct AttnParams {
   // sum's log-sum-exp in log2 units (-inf for a piece without valid keys).
   float* part_o;
   float* part_lse;
+  // Ragged index runs (one CTA per unit only): query n's indices are
+  // indices[key_offsets[n] .. key_offsets[n + 1]), each bound clamped to
+  // [0, num_indices]; null for the fixed [num_queries, topk] layout.
+  const int64_t* key_offsets;
+  int64_t num_indices;
 };
 
 // ------------------------------------------------------------------ PTX ---
@@ -379,11 +384,16 @@ struct Cursor {
   }
 };
 
-// Slot index of key j of the cursor's tile, or -1 past the query's top-k.
+// Slot index of key j of the cursor's tile, or -1 past the query's indices.
+// Split: query c.n's row of the [num_queries, topk] indices. One CTA per
+// unit: the CTA's own run [key_off, key_off + key_len) (a row of the fixed
+// layout, or a ragged run).
 template <bool kSplit>
-__device__ __forceinline__ int64_t key_index(const AttnParams& p, const Cursor<kSplit>& c, int j) {
+__device__ __forceinline__ int64_t key_index(const AttnParams& p, const Cursor<kSplit>& c, int j,
+                                             int64_t key_off, int64_t key_len) {
   const int64_t k = c.t * kTileKeys + j;
-  return k < p.topk ? ld_once_i64(p.indices + c.n * p.topk + k) : -1;
+  if (kSplit) return k < p.topk ? ld_once_i64(p.indices + c.n * p.topk + k) : -1;
+  return k < key_len ? ld_once_i64(p.indices + key_off + k) : -1;
 }
 
 __device__ __forceinline__ uint32_t ld_issue_u16(const void* p) {
@@ -610,7 +620,23 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t b = blockIdx.x;
-  if (p.tiles == 0) {
+  // One CTA per unit: this CTA's run of indices (a row of the fixed layout,
+  // or its query's ragged run) and its number of tiles.
+  int64_t key_off = 0, key_len = p.topk;
+  if (!kSplit) {
+    const int64_t n0 = b >> 1;
+    if (p.key_offsets) {
+      int64_t lo = ld_once_i64(p.key_offsets + n0), hi = ld_once_i64(p.key_offsets + n0 + 1);
+      lo = lo < 0 ? 0 : (lo > p.num_indices ? p.num_indices : lo);
+      hi = hi < lo ? lo : (hi > p.num_indices ? p.num_indices : hi);
+      key_off = lo;
+      key_len = hi - lo;
+    } else {
+      key_off = n0 * p.topk;
+    }
+  }
+  const int64_t unit_tiles = kSplit ? p.tiles : (key_len + kTileKeys - 1) / kTileKeys;
+  if (unit_tiles == 0) {
     // no keys at all: every output row is zero and every log-sum-exp -inf
     // (one CTA per unit)
     const int64_t n = b >> 1;
@@ -632,11 +658,11 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
   // this CTA's run of tiles [g0, g1) and where it starts
-  const int64_t g0 = kSplit ? range_begin(p, b) : b * p.tiles;
-  const int64_t n_tiles = kSplit ? range_begin(p, b + 1) - g0 : p.tiles;  // >= 1: grid <= total
+  const int64_t g0 = kSplit ? range_begin(p, b) : 0;
+  const int64_t n_tiles = kSplit ? range_begin(p, b + 1) - g0 : unit_tiles;  // >= 1
   const int64_t u_first = kSplit ? g0 / p.tiles : b;
   Cursor<kSplit> start;
-  start.t = g0 - u_first * p.tiles;
+  start.t = kSplit ? g0 - u_first * p.tiles : 0;
   start.n = kSplit ? u_first % p.nq : b >> 1;
   start.v = (int32_t)(kSplit ? u_first / p.nq : b & 1);
 
@@ -674,10 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     Packed buf[kDepth];
 #pragma unroll
     for (int u = 0; u < kDepth; ++u) {
-      buf[u] = load_packed(p, u < n_tiles ? key_index(p, cl, j) : -1, e);
+      buf[u] = load_packed(p, u < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1, e);
       cl.next(p);
     }
-    int64_t s_next = kDepth < n_tiles ? key_index(p, cl, j) : -1;
+    int64_t s_next = kDepth < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1;
     bool live = true;
     for (int64_t i0 = 0; i0 < n_tiles && live; i0 += kDepth) {
 #pragma unroll
@@ -687,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
           const Packed cur = buf[u];
           buf[u] = load_packed(p, s_next, e);  // tile i + kDepth
           cl.next(p);
-          s_next = i + kDepth + 1 < n_tiles ? key_index(p, cl, j) : -1;
+          s_next = i + kDepth + 1 < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1;
           const uint32_t st = (uint32_t)(i % kStages);
           if (i >= kStages &&
               !mbar_wait(bars + kBarPvDone + 8 * st, (uint32_t)(((i / kStages) - 1) & 1), abort)) {
@@ -790,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     bool live = true;
     Cursor<kSplit> c = start;
     bool first_seg = true;  // in the CTA's first segment
-    int64_t s_key = key_index(p, c, lane);
+    int64_t s_key = key_index(p, c, lane, key_off, key_len);
     for (int64_t i = 0; i < n_tiles && live; ++i) {
       const bool seg_first = i == 0 || (kSplit && c.t == 0);
       const bool seg_last = i == n_tiles - 1 || (kSplit && c.t == p.tiles - 1);
@@ -801,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, s_key >= 0 && s_key < p.num_slots);
       Cursor<kSplit> cn = c;
       const bool new_unit = cn.next(p);
-      s_key = i + 1 < n_tiles ? key_index(p, cn, lane) : -1;
+      s_key = i + 1 < n_tiles ? key_index(p, cn, lane, key_off, key_len) : -1;
       const uint32_t st = (uint32_t)(i % kStages);
       if (!warp_wait(bars + kBarSFull + 8 * st, (uint32_t)((i / kStages) & 1), abort)) {
         live = false;
@@ -1020,6 +1046,8 @@ int attention_params(const void* q_bf16, int64_t num_queries, int64_t num_heads,
   p.grid = 2 * num_queries;  // one CTA per unit unless split
   p.part_o = nullptr;
   p.part_lse = nullptr;
+  p.key_offsets = nullptr;
+  p.num_indices = 0;
   return KVQ_OK;
 }
 
@@ -1062,6 +1090,27 @@ int launch_attention(const kvq::AttnParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+extern "C" int mxfp4_mla_sparse_attention_ragged(
+    const void* q_bf16, int64_t num_queries, int64_t num_heads, int64_t q_query_stride,
+    int64_t q_head_stride, const uint8_t* cache, int64_t num_blocks, int64_t block_size,
+    int64_t block_stride_rows, const int64_t* indices, int64_t num_indices,
+    const int64_t* key_offsets, float sm_scale, void* out_bf16, int64_t out_query_stride,
+    int64_t out_head_stride, float* lse, int32_t* status, cudaStream_t stream) {
+  using namespace kvq;
+  if (num_indices < 0) return KVQ_EINVAL;
+  AttnParams p;
+  int rc = attention_params(q_bf16, num_queries, num_heads, q_query_stride, q_head_stride, cache,
+                            num_blocks, block_size, block_stride_rows, indices, 0, sm_scale,
+                            out_bf16, out_query_stride, out_head_stride, lse, status, p);
+  if (rc != KVQ_OK || num_queries == 0) return rc;
+  if (!key_offsets || !aligned(key_offsets, 8) || (num_indices > 0 && !indices)) return KVQ_EINVAL;
+  p.key_offsets = key_offsets;
+  p.num_indices = num_indices;
+  p.tiles = 1;  // per CTA from its run; one CTA per (query, value half)
+  p.total = p.units;
+  return launch_attention(p, stream);
+}
 
 extern "C" int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries,
                                                              int64_t num_heads, int64_t topk) {

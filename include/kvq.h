@@ -470,6 +470,34 @@ int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries, int64_t 
                                cudaStream_t stream);
 
 /*
+ * mxfp4_mla_sparse_attention_ragged — the same attention for ragged index
+ * runs, as sparse prefill produces them: [pr] Details, read path (one
+ * sparse-attention kernel serves sparse prefill and decode). Query n attends
+ * over indices[key_offsets[n] .. key_offsets[n + 1]) of one flat int64
+ * array instead of a padded [num_queries, topk] row; the runs may have any
+ * lengths, including 0 (out = 0, lse = -inf).
+ *
+ * indices      int64 [num_indices], 8-byte aligned (-1 entries and indices
+ *              outside the cache are dropped, as above)
+ * key_offsets  int64 [num_queries + 1] in device memory, 8-byte aligned:
+ *              query n's run starts at key_offsets[n] and ends at
+ *              key_offsets[n + 1]; each bound is clamped to [0, num_indices]
+ *              and an end below its start gives an empty run, so no offset
+ *              makes the kernel read outside `indices`
+ * Other arguments, results, arithmetic and errors as
+ * mxfp4_mla_sparse_attention without a workspace: one CTA per (query, value
+ * half); the number of key tiles of each CTA comes from its run.
+ */
+int mxfp4_mla_sparse_attention_ragged(const void* q_bf16, int64_t num_queries, int64_t num_heads,
+                                      int64_t q_query_stride, int64_t q_head_stride,
+                                      const uint8_t* cache, int64_t num_blocks,
+                                      int64_t block_size, int64_t block_stride_rows,
+                                      const int64_t* indices, int64_t num_indices,
+                                      const int64_t* key_offsets, float sm_scale, void* out_bf16,
+                                      int64_t out_query_stride, int64_t out_head_stride,
+                                      float* lse, int32_t* status, cudaStream_t stream);
+
+/*
  * mxfp4_mla_sparse_attention_workspace_size — bytes of workspace that
  * mxfp4_mla_sparse_attention needs to split these shapes over the current
  * device's SMs: 2 x CTAs x num_heads x (256 x 4 + 4) (CTAs = min(SMs,

@@ -37,7 +37,8 @@ def test_every_declared_symbol_is_exported(L):
                           "fused_save_compress_norm",
                           "mxfp4_mla_gather_dequant", "mxfp4_mla_sparse_attention",
                           "mxfp4_mla_sparse_attention_workspace_size",
-                          "mxfp4_mla_sparse_attention_noalloc"}
+                          "mxfp4_mla_sparse_attention_noalloc",
+                          "mxfp4_mla_sparse_attention_ragged"}
     for n in names:
         assert hasattr(L, n), n
     # exported with C linkage from the shared object itself
@@ -200,6 +201,21 @@ def test_attention_validation_on_host(L):
     a = list(ok); a[17] = A16 + 16; a[18] = need
     assert f(*a) == -1
     a = list(ok); a[17] = A16; a[18] = need - 1
+    assert f(*a) == -1
+
+
+def test_ragged_attention_validation_on_host(L):
+    f = L.mxfp4_mla_sparse_attention_ragged
+    ok = [A16, 2, 128, 128 * 512, 512, A16, 1, 8, 8, A8, 40, A8 + 0x100, 0.05, A16, 128 * 512, 512,
+          None, None, None]
+    empty = list(ok); empty[1] = 0; empty[0] = None
+    assert f(*empty) == 0
+    bad = {1: -1, 2: 0, 2.1: 129, 10: -1, 11: None, 11.1: A8 + 4, 12: float("nan"), 9: A8 + 4,
+           0: A16 + 2, 4: 500, 6: 0}
+    for k, v in bad.items():
+        a = list(ok); a[int(k)] = v
+        assert f(*a) == -1, (k, v)
+    a = list(ok); a[9] = None                      # indices null with indices to read
     assert f(*a) == -1
 
 

@@ -204,3 +204,82 @@ def test_rejects_bad_arguments_on_gpu():
         kvq.mxfp4_mla_sparse_attention(q, cache, idx, 0.1)    # 129 heads
     with pytest.raises(kvq.KvqError):
         kvq.mxfp4_mla_sparse_attention(q[:, :4], cache, idx, float("nan"))
+
+
+def _check_ragged(q, cache, runs, sm_scale, num_slots, first_offset=0, extra_tail=0):
+    """Ragged runs against the oracle on the same runs padded with -1 into
+    [num_queries, longest run]: pads are dropped, so the two are the same
+    attention."""
+    dev = torch.device("cuda", 0)
+    nq = len(runs)
+    lens = [len(r) for r in runs]
+    flat = np.concatenate([np.full(first_offset, 7, np.int64)] + [np.asarray(r, np.int64)
+                                                                    for r in runs]
+                          + [np.full(extra_tail, 7, np.int64)])
+    offsets = first_offset + np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    width = max(1, max(lens))
+    padded = np.full((nq, width), -1, np.int64)
+    for n, r in enumerate(runs):
+        padded[n, :len(r)] = r
+    want, want_lse, mass = attn_oracle(q, cache, 1, num_slots, num_slots, padded, sm_scale)
+    qd = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).to(dev).view(torch.bfloat16)
+    cd = torch.from_numpy(cache).to(dev)
+    lse = torch.empty((nq, q.shape[1]), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, _ = kvq.mxfp4_mla_sparse_attention_ragged(qd, cd, torch.from_numpy(flat).to(dev),
+                                                   torch.from_numpy(offsets).to(dev), sm_scale,
+                                                   lse=lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "a kernel wait timed out"
+    got = out.float().cpu().numpy().astype(np.float64)
+    bound = 2.0 ** -7 * (mass + np.abs(want)) + 2.0 ** -100
+    bad = np.argwhere(np.abs(got - want) > bound)
+    assert bad.size == 0, bad[:5]
+    l = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(l), fin) and np.all(np.isneginf(l[~fin]))
+    np.testing.assert_allclose(l[fin], want_lse[fin], rtol=0, atol=2e-3)
+    return got
+
+
+@pytest.mark.parametrize("heads", [128, 48])
+def test_ragged_runs_of_every_length(heads):
+    """Sparse prefill: one flat index array cut into runs of 0, 1, 31, 32,
+    33, 300, 700 and 2048 indices (with pads and out-of-range entries); an
+    empty run gives out = 0 and lse = -inf."""
+    cache = _fill_cache(8192, seed=40)
+    rng = np.random.default_rng(41)
+    lens = [0, 1, 31, 32, 33, 300, 700, 2048, 5]
+    runs = []
+    for L in lens:
+        r = rng.integers(-1, 8192, L)
+        if L:
+            r[0] = rng.integers(0, 8192)
+        if L > 10:
+            r[3] = 9000                          # outside the cache: dropped
+        runs.append(r)
+    q = _queries(42 + heads, len(runs), heads)
+    got = _check_ragged(q, cache, runs, 1 / np.sqrt(512), 8192)
+    assert np.all(got[0] == 0)
+
+
+def test_ragged_offsets_are_clamped_to_the_index_array():
+    """A run may start past index 0; a last offset past the array's end is
+    clamped to it, and an end below its start is an empty run."""
+    cache = _fill_cache(4096, seed=43)
+    rng = np.random.default_rng(44)
+    runs = [rng.integers(0, 4096, 64), rng.integers(0, 4096, 40)]
+    q = _queries(45, 2, 128)
+    _check_ragged(q, cache, runs, 0.05, 4096, first_offset=5, extra_tail=3)
+    dev = torch.device("cuda", 0)
+    qd = torch.from_numpy(q.view(np.int16)).to(dev).view(torch.bfloat16)
+    cd = torch.from_numpy(cache).to(dev)
+    flat = torch.from_numpy(np.concatenate(runs).astype(np.int64)).to(dev)
+    off = torch.tensor([0, 64, 10_000], dtype=torch.int64, device=dev)  # run 1 clamped to 40
+    a, _ = kvq.mxfp4_mla_sparse_attention_ragged(qd, cd, flat, off, 0.05)
+    b, _ = kvq.mxfp4_mla_sparse_attention_ragged(
+        qd, cd, flat, torch.tensor([0, 64, 104], dtype=torch.int64, device=dev), 0.05)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    c, _ = kvq.mxfp4_mla_sparse_attention_ragged(
+        qd, cd, flat, torch.tensor([50, 20, 104], dtype=torch.int64, device=dev), 0.05)
+    assert torch.all(c[0].float() == 0)          # end below start: empty
