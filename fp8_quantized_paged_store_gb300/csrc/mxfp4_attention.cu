@@ -160,10 +160,13 @@ __device__ __forceinline__ void cp_async_16a(uint32_t dst, const void* src) {
 }
 
 // Global loads issued where they stand (asm volatile): a producer's prefetch
-// of packed rows must not be moved down to its first use a tile later.
+// of packed rows must not be moved down to its first use a tile later. They
+// allocate in L1: a lane's two 16-byte loads fall in one 32-byte sector, and
+// the eight producer warps all read each row's scale sector (without L1 the
+// CTA sent ~2.9x the rows' sectors to L2 and ran 10% slower).
 __device__ __forceinline__ uint4 ld_issue_v4(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
@@ -398,7 +401,7 @@ __device__ __forceinline__ int64_t key_index(const AttnParams& p, const Cursor<k
 
 __device__ __forceinline__ uint32_t ld_issue_u16(const void* p) {
   uint16_t r;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
   return r;
 }
 
