@@ -683,7 +683,24 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  load_q_smem(p, start.n, q_base, tid, kThreads);
+  // The producers issue their first kDepth tiles of row loads at once, while
+  // the softmax and issuer warps (160 threads) load Q: the two start-up
+  // latencies overlap.
+  const bool producer = warp >= 4 && warp < kIssuerWarp;
+  const int e = warp - 4, j = lane;
+  Cursor<kSplit> cl = start;  // a producer's next tile to load
+  Packed buf[kDepth];
+  int64_t s_next = -1;
+  if (producer) {
+#pragma unroll
+    for (int u = 0; u < kDepth; ++u) {
+      buf[u] = load_packed(p, u < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1, e);
+      cl.next(p);
+    }
+    s_next = kDepth < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1;
+  } else {
+    load_q_smem(p, start.n, q_base, tid < 128 ? tid : tid - 256, 160);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -693,20 +710,11 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   __syncthreads();
   tc_fence_after();
 
-  if (warp >= 4 && warp < kIssuerWarp) {
+  if (producer) {
     // ------------------------------------------------------------ producers
     // Lane = key of the tile, warp 4 + e = dims [64e, 64e + 64). The CTA's
     // i-th tile goes to stage i % kStages, free once the p.v of tile
     // i - kStages has completed; rows are loaded kDepth tiles ahead.
-    const int e = warp - 4, j = lane;
-    Cursor<kSplit> cl = start;  // the tile whose rows are loaded next
-    Packed buf[kDepth];
-#pragma unroll
-    for (int u = 0; u < kDepth; ++u) {
-      buf[u] = load_packed(p, u < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1, e);
-      cl.next(p);
-    }
-    int64_t s_next = kDepth < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1;
     bool live = true;
     for (int64_t i0 = 0; i0 < n_tiles && live; i0 += kDepth) {
 #pragma unroll
@@ -936,13 +944,19 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
 // out = sum_b 2**(lse_b - L) o_b / sum_b 2**(lse_b - L), L = max_b lse_b, and
 // the unit's log-sum-exp L + log2(sum) (in natural log units, half 0 only).
 // A unit without any valid key gets zeros and -inf. The pieces' slots are
-// worked out once per block (threads in parallel, into shared memory); then
-// 64 threads take a head, four columns each.
+// worked out in parallel into shared memory; 64 threads take a head, four
+// columns each. A unit of up to kMergeFew pieces is summed by each thread
+// on its own; beyond that (the launch then gives the block dynamic shared
+// memory for kMergeHeads x pieces weights), every (head, piece) weight is
+// first worked out in parallel, and the sums keep several loads in flight.
 constexpr int kMergeMaxPieces = 1024;  // grid <= 1023
 constexpr int kMergeHeads = 8;         // heads per block (64 threads each)
+constexpr int kMergeFew = 4;
 
-__global__ void __launch_bounds__(64 * kMergeHeads) mxfp4_attention_merge_kernel(AttnParams p) {
+__global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_kernel(AttnParams p) {
   __shared__ int32_t piece_slot[kMergeMaxPieces];
+  __shared__ float head_l[kMergeHeads][2], head_w[kMergeHeads][2];
+  extern __shared__ float merge_dyn[];  // [kMergeHeads][pieces]: log-sum-exp, then weight
   const int64_t j = blockIdx.x;
   const int64_t gb = p.total * (j + 1) / p.grid;
   const int64_t unit = gb / p.tiles;
@@ -957,24 +971,76 @@ __global__ void __launch_bounds__(64 * kMergeHeads) mxfp4_attention_merge_kernel
   }
   __syncthreads();
   const int64_t H = p.num_heads;
-  const int64_t h = (int64_t)blockIdx.y * kMergeHeads + (threadIdx.x >> 6);
-  if (h >= H) return;
+  const float kNegInf = -__int_as_float(0x7F800000);
   const int64_t n = unit % p.nq;  // half-major unit order
   const int v = (int)(unit / p.nq);
-  const int c4 = threadIdx.x & 63;
-  const float kNegInf = -__int_as_float(0x7F800000);
+  uint32_t dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  if (pieces <= kMergeFew || dyn_bytes < (uint32_t)(kMergeHeads * pieces) * 4u) {
+    const int64_t h = (int64_t)blockIdx.y * kMergeHeads + (threadIdx.x >> 6);
+    if (h >= H) return;
+    const int c4 = threadIdx.x & 63;
+    float L = kNegInf;
+#pragma unroll 4
+    for (int k = 0; k < pieces; ++k) L = fmaxf(L, p.part_lse[piece_slot[k] * H + h]);
+    float W = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (L != kNegInf) {
+#pragma unroll 4
+      for (int k = 0; k < pieces; ++k) {
+        const int64_t row = piece_slot[k] * H + h;
+        const float w = exp2f(p.part_lse[row] - L);
+        const float4 o = *reinterpret_cast<const float4*>(p.part_o + row * kHalf + 4 * c4);
+        W += w;
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+    }
+    const float inv = W > 0.0f ? 1.0f / W : 0.0f;
+    st_v2(p.out + n * p.o_qstride + h * p.o_hstride + (int64_t)(v * kHalf + 4 * c4) * 2,
+          pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (v == 0 && p.lse && c4 == 0)
+      p.lse[n * H + h] = W > 0.0f ? (L + log2f(W)) * 0.69314718055994531f : kNegInf;
+    return;
+  }
+  for (int t = threadIdx.x; t < kMergeHeads * pieces; t += blockDim.x) {
+    const int hh = t / pieces, k = t - hh * pieces;
+    const int64_t h = (int64_t)blockIdx.y * kMergeHeads + hh;
+    merge_dyn[hh * pieces + k] = h < H ? p.part_lse[piece_slot[k] * H + h] : kNegInf;
+  }
+  __syncthreads();
+  const int hh = threadIdx.x >> 6, c4 = threadIdx.x & 63, half = c4 >> 5;
+  // L: the head's largest log-sum-exp (64 threads, two warps)
   float L = kNegInf;
-#pragma unroll 4
-  for (int k = 0; k < pieces; ++k) L = fmaxf(L, p.part_lse[piece_slot[k] * H + h]);
+  for (int k = c4; k < pieces; k += 64) L = fmaxf(L, merge_dyn[hh * pieces + k]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xFFFFFFFFu, L, o));
+  if ((c4 & 31) == 0) head_l[hh][half] = L;
+  __syncthreads();
+  L = fmaxf(head_l[hh][0], head_l[hh][1]);
+  // weights 2**(lse_b - L) (0 for a piece without valid keys) and their sum
   float W = 0.0f;
+  for (int k = c4; k < pieces; k += 64) {
+    const float w = L != kNegInf ? exp2f(merge_dyn[hh * pieces + k] - L) : 0.0f;
+    merge_dyn[hh * pieces + k] = w;
+    W += w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xFFFFFFFFu, W, o);
+  if ((c4 & 31) == 0) head_w[hh][half] = W;
+  __syncthreads();
+  W = head_w[hh][0] + head_w[hh][1];
+  const int64_t h = (int64_t)blockIdx.y * kMergeHeads + hh;
+  if (h >= H) return;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (L != kNegInf) {
-#pragma unroll 4
+  if (W > 0.0f) {
+#pragma unroll 8
     for (int k = 0; k < pieces; ++k) {
-      const int64_t row = piece_slot[k] * H + h;
-      const float w = exp2f(p.part_lse[row] - L);
-      const float4 o = *reinterpret_cast<const float4*>(p.part_o + row * kHalf + 4 * c4);
-      W += w;
+      const float w = merge_dyn[hh * pieces + k];
+      const float4 o =
+          *reinterpret_cast<const float4*>(p.part_o + (piece_slot[k] * H + h) * kHalf + 4 * c4);
       acc.x += w * o.x;
       acc.y += w * o.y;
       acc.z += w * o.z;
@@ -994,11 +1060,14 @@ __global__ void __launch_bounds__(64 * kMergeHeads) mxfp4_attention_merge_kernel
 namespace {
 
 // CTAs of the split schedule: one per SM (each holds all of tensor memory),
-// at most one per tile.
+// with at least kMinSplitTiles tiles each (a CTA's start-up and its piece's
+// write and merge cost a few tiles' time).
+constexpr int64_t kMinSplitTiles = 4;
 int64_t split_grid(int64_t total) {
   int64_t sms = kvq::sm_count();
   if (sms > 1023) sms = 1023;
-  return total < sms ? total : sms;
+  const int64_t want = total / kMinSplitTiles > 1 ? total / kMinSplitTiles : 1;
+  return want < sms ? want : sms;
 }
 
 // Checks shared by the entry points; fills `p` (without workspace).
@@ -1088,7 +1157,13 @@ int launch_attention(const kvq::AttnParams& p, cudaStream_t stream) {
   int rc = launch_status();
   if (rc != KVQ_OK || !p.part_o || p.grid < 2) return rc;
   const dim3 mgrid((unsigned)(p.grid - 1), (unsigned)((p.num_heads + kMergeHeads - 1) / kMergeHeads));
-  mxfp4_attention_merge_kernel<<<mgrid, 64 * kMergeHeads, 0, stream>>>(p);
+  // the most pieces a unit can have: every CTA takes at least total / grid tiles
+  const int64_t per_cta = p.total / p.grid;
+  const int64_t most = p.tiles / (per_cta > 0 ? per_cta : 1) + 2;
+  const size_t dyn = most > kMergeFew
+                         ? (size_t)kMergeHeads * (size_t)(most < kMergeMaxPieces ? most : kMergeMaxPieces) * 4
+                         : 0;
+  mxfp4_attention_merge_kernel<<<mgrid, 64 * kMergeHeads, dyn, stream>>>(p);
   return launch_status();
 }
 

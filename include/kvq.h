@@ -447,7 +447,8 @@ int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks, int64_t b
  *                  mxfp4_mla_sparse_attention_workspace_size(num_queries,
  *                  num_heads, topk) bytes, 256-byte aligned, or NULL.
  *                  With a workspace the queries' key tiles are split evenly
- *                  over one CTA per SM (the split-K of the read path [pr]:
+ *                  over up to one CTA per SM, each taking at least four
+ *                  32-key tiles (the split-K of the read path [pr]:
  *                  a ragged sparse-attention kernel plus a split-K partial
  *                  kernel): pieces of a (query, value half) cut between two
  *                  CTAs are written there as fp32 partial outputs with their
@@ -501,7 +502,8 @@ int mxfp4_mla_sparse_attention_ragged(const void* q_bf16, int64_t num_queries, i
  * mxfp4_mla_sparse_attention_workspace_size — bytes of workspace that
  * mxfp4_mla_sparse_attention needs to split these shapes over the current
  * device's SMs: 2 x CTAs x num_heads x (256 x 4 + 4) (CTAs = min(SMs,
- * 2 x num_queries x ceil(topk / 32))), 0 when there is nothing to split
+ * max(1, floor(2 x num_queries x ceil(topk / 32) / 4))): every CTA takes at
+ * least four 32-key tiles), 0 when there is nothing to split
  * (num_queries or topk 0), KVQ_EINVAL for shapes the attention rejects.
  * No page counterpart: a host query of this library.
  */

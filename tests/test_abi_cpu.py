@@ -221,8 +221,8 @@ def test_ragged_attention_validation_on_host(L):
 
 def test_attention_workspace_size(L):
     """2 x CTAs x heads x (256 fp32 + one log-sum-exp), CTAs = min(SMs,
-    2 x queries x tiles of 32 keys); 0 when nothing can be split; -1 for
-    shapes the attention rejects."""
+    max(1, (2 x queries x tiles of 32 keys) // 4)); 0 when nothing can be
+    split; -1 for shapes the attention rejects."""
     g = L.mxfp4_mla_sparse_attention_workspace_size
     assert g(0, 128, 2048) == 0 and g(3, 128, 0) == 0
     assert g(-1, 128, 16) == -1 and g(2, 0, 16) == -1 and g(2, 129, 16) == -1
@@ -230,8 +230,10 @@ def test_attention_workspace_size(L):
     per_cta = 2 * 128 * (256 * 4 + 4)
     big = g(128, 128, 2048)
     assert big % per_cta == 0 and 1 <= big // per_cta <= 2 * 128 * 64
-    # one query, one tile per unit: two CTAs at most
-    assert g(1, 128, 32) == 2 * per_cta and g(1, 64, 1) == 2 * 2 * 64 * (256 * 4 + 4)
+    # one query, one tile per unit: one CTA (at least four tiles each)
+    assert g(1, 128, 32) == per_cta and g(1, 64, 1) == 2 * 64 * (256 * 4 + 4)
+    # one query of 2048 keys: 128 tiles, 32 CTAs of four
+    assert g(1, 128, 2048) == 32 * per_cta
 
 
 def test_tensors_on_two_devices_are_refused_before_any_launch():
