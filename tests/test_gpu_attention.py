@@ -172,9 +172,11 @@ def test_full_workload_128_queries_2048_keys(split):
                                            (3, 333, 128), (77, 64, 16), (200, 96, 128)])
 def test_split_schedules(nq, topk, heads):
     """Shapes whose units are cut into many pieces (one query: each value
-    half spread over ~76 CTAs, up to ~77 pieces merged), into a few, or not
-    at all (more units than SMs, tiles per unit small), with ragged top-k
-    and pads; both schedules against the oracle."""
+    half spread over 32 or 64 CTAs of at least four tiles, up to ~65 pieces
+    merged through the merge's parallel-weight path; five queries: ~15
+    pieces each), into a few (three queries of 333 keys: the per-thread
+    path), or not at all (more units than SMs, tiles per unit small), with
+    ragged top-k and pads; both schedules against the oracle."""
     cache = _fill_cache(8192, seed=20 + nq)
     q = _queries(21 + topk, nq, heads)
     rng = np.random.default_rng(22 + heads)
