@@ -104,26 +104,28 @@ def bf16_peak():
         return 1900.0, "fallback (1.9 PFLOP/s)"
 
 
-def attention_case(torch, kvq, dev, cache, idx, valid, split=True):
+def attention_case(torch, kvq, dev, cache, idx, split=True, nq=128):
     """(call, flops, hbm bytes, status tensor) of sparse attention over the
-    gather workload's cache and indices: 128 queries x 128 heads. ``split``:
-    the key tiles split evenly over the SMs with a preallocated workspace
-    (the attention kernel and the merge of split units, both timed), else one
-    CTA per (query, value half)."""
+    gather workload's cache and the first `nq` of its 128 index rows, 128
+    heads. ``split``: the key tiles cut into chunks over the SMs with a
+    preallocated workspace (the attention kernel and the merge of the
+    chunks, both timed) where the library splits the shape, else one CTA per
+    (query, value half)."""
     q = torch.from_numpy(workloads.attention_queries(0, 128, 128).view(np.int16)).to(dev)
-    q = q.view(torch.bfloat16)
-    idx2 = idx.view(128, -1)
-    outa = torch.empty((128, 128, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((128, 128), dtype=torch.float32, device=dev)
+    q = q.view(torch.bfloat16)[:nq]
+    idx2 = idx.view(128, -1)[:nq]
+    valid = int((idx2 >= 0).sum())
+    outa = torch.empty((nq, 128, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((nq, 128), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = False
     if split:
-        ws = torch.empty(max(1, kvq.attention_workspace_size(128, 128, idx2.shape[1])),
+        ws = torch.empty(max(1, kvq.attention_workspace_size(nq, 128, idx2.shape[1])),
                          dtype=torch.uint8, device=dev)
     call = lambda: kvq.mxfp4_mla_sparse_attention(  # noqa: E731
         q, cache, idx2, 1.0 / 512 ** 0.5, out=outa, lse=lse, status=status, workspace=ws)
     flops = 4.0 * 128 * valid * 512            # q.k and p.v over the valid keys, 128 heads
-    hbm = ROW * valid + 8 * idx.numel() + 2 * 128 * 128 * 1024 + 4 * 128 * 128
+    hbm = ROW * valid + 8 * idx2.numel() + 2 * nq * 128 * 1024 + 4 * nq * 128
     return call, flops, hbm, status
 
 
@@ -596,30 +598,34 @@ def secondary_paths(torch, kvq, dev, peak, store_inputs):
         "gbs": algo / (ms * 1e-3) / 1e9, "frac_of_peak": algo / (ms * 1e-3) / 1e9 / peak,
         "l2": "flushed before each rep (512 MB written, then 1 GiB read)"}
 
-    # sparse MLA decode attention on the same packed cache and indices, both
-    # schedules timed: one CTA per (query, value half), and the key tiles
-    # split over the SMs with a log-sum-exp merge; the line reports the one
-    # the binding picks by default for this shape
-    call, _, _, status0 = attention_case(torch, kvq, dev, cache, idx, valid, split=False)
-    for _ in range(3):
-        call()
-    ms_unsplit, _ = time_events(torch, call, 20, stream, flush=flush)
-    call, flops, hbm, status = attention_case(torch, kvq, dev, cache, idx, valid)
-    for _ in range(3):
-        call()
-    ms_split, _ = time_events(torch, call, 20, stream, flush=flush)
-    split = kvq.attention_prefers_split(128, 2048, dev)
-    ms = ms_split if split else ms_unsplit
+    # sparse MLA decode attention on the same packed cache and indices: 128
+    # queries (the line reports the schedule the binding picks, one CTA per
+    # (query, value half): 256 units fill the SMs), and a decode batch of 4
+    # queries with both schedules timed (the binding splits it: each unit's
+    # key tiles cut into chunks over the SMs, merged by log-sum-exp)
     tpeak, tpeak_src = bf16_peak()
+    timed = {}
+    for nq, split in ((128, False), (4, False), (4, True)):
+        call, flops, hbm, status = attention_case(torch, kvq, dev, cache, idx, split, nq)
+        for _ in range(3):
+            call()
+        ms, _ = time_events(torch, call, 20, stream, flush=flush)
+        timed[(nq, split)] = (ms, flops, hbm, int(status.item()))
+    ms, flops, hbm, st = timed[(128, False)]
+    ms4u, flops4, _, st4u = timed[(4, False)]
+    ms4s, _, _, st4s = timed[(4, True)]
+    split4 = kvq.attention_prefers_split(4, 2048, dev)
     out["mxfp4_mla_sparse_attention"] = {
         "workload": "128 queries x 128 heads x 2048 top-k (trailing pads), 1,048,576 slots",
         "ms": ms, "algorithmic_flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
         "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tpeak, "bf16_peak_tflops": tpeak,
         "bf16_peak_source": tpeak_src, "hbm_bytes": hbm, "gbs": hbm / (ms * 1e-3) / 1e9,
-        "wait_status": int(status.item()) | int(status0.item()),
-        "schedule": ("split: key tiles over one CTA per SM, pieces merged by log-sum-exp"
-                     if split else "one CTA per (query, value half)") + " (the binding's default)",
-        "unsplit_ms": ms_unsplit, "split_ms": ms_split,
+        "wait_status": st | st4u | st4s,
+        "schedule": "one CTA per (query, value half) (the binding's default for 128 queries)",
+        "decode_batch_4": {
+            "workload": "the first 4 of the 128 queries", "unsplit_ms": ms4u, "split_ms": ms4s,
+            "tflops": flops4 / ((ms4s if split4 else ms4u) * 1e-3) / 1e12,
+            "binding_splits": split4},
         "l2": "flushed before each rep (512 MB written, then 1 GiB read)"}
     return out
 
@@ -850,7 +856,7 @@ def run_profile(args):
             algo = 8 * idx.numel() + ROW * valid + 1024 * idx.numel()
             l2_fetch_granularity(torch, 32)  # as the benchmark line measures it
         else:  # the schedule the binding picks for this shape, as the benchmark line
-            call, _, algo, _ = attention_case(torch, kvq, dev, cache, idx, valid,
+            call, _, algo, _ = attention_case(torch, kvq, dev, cache, idx,
                                               split=kvq.attention_prefers_split(128, 2048, dev))
     for _ in range(args.warmup):
         call()

@@ -543,15 +543,14 @@ def attention_workspace_size(num_queries: int, num_heads: int, topk: int) -> int
 
 
 def attention_prefers_split(num_queries: int, topk: int, device=None) -> bool:
-    """Whether splitting the key tiles over the SMs should beat one CTA per
-    (query, value half) on this device: it does when the unsplit grid of
-    2 x num_queries CTAs (one per SM at a time) would fill at most a third
-    of the SMs. Measured on a GB300 (128 heads, 2048 keys): the split is 2.7x
-    faster for one query, 2.3x for four, 1.3x for sixteen, equal at 32 and
-    slower from 64 on, where its segment restarts and log-sum-exp merge cost
-    more than the idle SMs of a partial wave."""
+    """Whether to split the key tiles over the SMs on this device: whenever
+    the library would (its workspace size is nonzero: the 2 x num_queries
+    (query, value half) units fill at most half of the SMs and each has at
+    least eight 32-key tiles). Measured on a GB300 (128 heads, 2048 keys) the
+    split is 3.0x faster than one CTA per unit for one query, 3.0x for four,
+    2.0x for sixteen and 1.4x for 32."""
     if topk <= 0 or num_queries <= 0:
         return False
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    return 3 * 2 * num_queries <= sms
+    with torch.cuda.device(dev):
+        return lib().mxfp4_mla_sparse_attention_workspace_size(num_queries, 1, topk) > 0

@@ -10,18 +10,15 @@
 // Work decomposition. A unit of work is (query, half of the 512 value
 // columns): the two units of a query both form the full scores q.k
 // (512-deep) and each accumulates 256 output columns. A unit is a run of
-// 32-key tiles; the units' tiles laid end to end (query-major, half 0 before
-// half 1) are cut into one contiguous range per CTA of a grid of one CTA per
-// SM, so that every SM gets the same number of tiles whatever the number of
-// units (the split-K of the read path). A CTA walks its range as segments,
-// one per unit it touches: a segment that covers its whole unit writes the
-// output; one that covers part of a unit writes an fp32 partial (the output
-// normalised by the piece's own softmax sum, and that sum's log-sum-exp)
-// into a caller-provided workspace, and a second, small kernel combines the
-// pieces of each split unit by their log-sum-exps. Between segments the CTA
-// reads the output accumulator out and, when the query changes, reloads Q;
-// the producers keep streaming the next segment's keys meanwhile. Without a
-// workspace the grid has one CTA per unit and nothing is split.
+// 32-key tiles. Without a workspace each unit is one CTA (query n's halves
+// on CTAs 2n and 2n + 1), which writes its output. With one (the split-K of
+// the read path, for few queries), every unit is cut into `chunks` runs of
+// at most `chunk_tiles` tiles, one CTA each (unit u's chunks on CTAs
+// u * chunks ..): the CTA writes an fp32 partial, the output of its chunk
+// normalised by the chunk's own softmax sum and that sum's log-sum-exp,
+// into the caller's workspace, and a second, small kernel combines each
+// unit's partials by their log-sum-exps. A CTA's work is one contiguous run
+// of one unit either way.
 //
 // Each CTA: tensor memory (512 columns x 128 lanes,
 // lane = head) holds the output accumulator (256 columns), four 32-key score
@@ -96,11 +93,10 @@ constexpr uint32_t kSmemUsed = kOffAbort + 16;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
 
 // mbarriers, one of each per stage (the CTA's i-th tile uses stage i % kStages),
-// then one that softmax completes at every segment boundary (the output
-// accumulator has been read out and, for a new query, Q reloaded), and one
-// the issuer commits its last MMAs to before tensor memory is released
+// then one the issuer commits its last MMAs to before tensor memory is
+// released
 constexpr uint32_t kBarKFull = 0, kBarSFull = 32, kBarPFull = 64, kBarPvDone = 96;
-constexpr uint32_t kBarSeg = 128, kBarDrain = 136;
+constexpr uint32_t kBarDrain = 128;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
@@ -122,21 +118,21 @@ struct AttnParams {
   int64_t o_qstride, o_hstride;
   float* lse;              // [num_queries, num_heads] or null
   int32_t* status;         // or null
-  // Schedule: unit k = (query k / 2, value half k % 2) is `tiles` tiles of
-  // 32 keys; the units' tiles laid end to end (`total` of them) are split
-  // into `grid` contiguous ranges, CTA b taking [total*b/grid,
-  // total*(b+1)/grid).
-  int64_t tiles, units, total;
+  // Schedule: unit u = (query u / 2, value half u % 2) is `tiles` tiles of
+  // 32 keys, cut into `chunks` runs of `chunk_tiles` tiles (the last may be
+  // shorter), CTA b taking chunk b % chunks of unit b / chunks.
+  int64_t tiles, units;
   int64_t nq;  // queries
-  int64_t grid;
-  // Partial results of units split between CTAs (null when grid is one CTA
-  // per unit, so that nothing is split): piece slot 2b (CTA b's first
-  // segment) or 2b + 1 (its last), [2 * grid][num_heads][256] fp32 outputs
-  // normalised by the piece's softmax sum, and [2 * grid][num_heads] that
-  // sum's log-sum-exp in log2 units (-inf for a piece without valid keys).
+  int64_t chunks, chunk_tiles;
+  int64_t grid;  // units * chunks
+  // Partial results (null when every unit is one chunk): CTA b's
+  // [num_heads][256] fp32 output of its chunk normalised by the chunk's
+  // softmax sum at part_o + b * num_heads * 256, and that sum's log-sum-exp
+  // in log2 units (-inf for a chunk without valid keys) at
+  // part_lse + b * num_heads.
   float* part_o;
   float* part_lse;
-  // Ragged index runs (one CTA per unit only): query n's indices are
+  // Ragged index runs (one chunk per unit only): query n's indices are
   // indices[key_offsets[n] .. key_offsets[n + 1]), each bound clamped to
   // [0, num_indices]; null for the fixed [num_queries, topk] layout.
   const int64_t* key_offsets;
@@ -364,38 +360,12 @@ struct Packed {
   uint32_t s;
 };
 
-// Position in a CTA's run of tiles: query n, value half v, and tile t within
-// the unit (n, v); next() says whether it entered a new unit. The split schedule orders units half-major (every query's half 0,
-// then every query's half 1), so that the two halves of a query run at the
-// same time on different CTAs and read the same packed rows through L2.
-// Unsplit (one CTA per unit), a CTA's tiles never leave its unit.
-template <bool kSplit>
-struct Cursor {
-  int64_t n, t;
-  int32_t v;
-  __device__ __forceinline__ bool next(const AttnParams& p) {
-    ++t;
-    if (kSplit && t == p.tiles) {
-      t = 0;
-      if (++n == p.nq) {
-        n = 0;
-        ++v;
-      }
-      return true;
-    }
-    return false;
-  }
-};
-
-// Slot index of key j of the cursor's tile, or -1 past the query's indices.
-// Split: query c.n's row of the [num_queries, topk] indices. One CTA per
-// unit: the CTA's own run [key_off, key_off + key_len) (a row of the fixed
-// layout, or a ragged run).
-template <bool kSplit>
-__device__ __forceinline__ int64_t key_index(const AttnParams& p, const Cursor<kSplit>& c, int j,
+// Slot index of key j of tile t of the CTA's run of indices
+// [key_off, key_off + key_len) (its chunk of a row of the fixed layout, or a
+// ragged run), or -1 past the run.
+__device__ __forceinline__ int64_t key_index(const AttnParams& p, int64_t t, int j,
                                              int64_t key_off, int64_t key_len) {
-  const int64_t k = c.t * kTileKeys + j;
-  if (kSplit) return k < p.topk ? ld_once_i64(p.indices + c.n * p.topk + k) : -1;
+  const int64_t k = t * kTileKeys + j;
   return k < key_len ? ld_once_i64(p.indices + key_off + k) : -1;
 }
 
@@ -489,7 +459,7 @@ __device__ __forceinline__ void issue_qk(uint32_t st, uint64_t q_desc, uint32_t 
 // over the stage's score columns) is the TMEM A operand, 8 columns per step
 // of 16 keys; V is the stage's key rows read MN-major from column block 4v
 // (LBO: the stage's next K-block, SBO: next 8 keys). `first` starts a new
-// accumulation (the first tile of a segment).
+// accumulation (the CTA's first tile).
 __device__ __forceinline__ void issue_pv(uint32_t st, int v, bool first, uint32_t k_base,
                                          uint32_t tmem) {
   const uint64_t v_desc = smem_desc(k_base + ((uint32_t)v * 4 * kStages + st) * kKBlock,
@@ -503,13 +473,13 @@ __device__ __forceinline__ void issue_pv(uint32_t st, int v, bool first, uint32_
 
 // ---------------------------------------------------------------- kernel ---
 
-// Q of query n into the operand buffers (not inlined: they run once per query
-// change, and inlined into the softmax loop they made its live state spill):
-// dims 256..511 of head r into the
-// swizzled K-major shared-memory layout (zero rows past num_heads), 16 bytes
-// per cp.async by threads [0, nthreads); then, by the 128 softmax threads
-// only (warps 0-3, head = thread), dims 0..255 into TMEM lane `head`,
-// columns kColQ.. as bf16 pairs (the A operand of the first 16 q.k steps).
+// Q of query n into the operand buffers, once per CTA (not inlined: they run
+// once, and kept out of line they leave the roles' loops their registers):
+// dims 256..511 of head r into the swizzled K-major shared-memory layout
+// (zero rows past num_heads), 16 bytes per cp.async by threads
+// [0, nthreads); then, by the 128 softmax threads only (warps 0-3,
+// head = thread), dims 0..255 into TMEM lane `head`, columns kColQ.. as bf16
+// pairs (the A operand of the first 16 q.k steps).
 __device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_t q_base,
                                             int tid, int nthreads) {
   const uint8_t* qn = p.q + n * p.q_qstride;
@@ -558,26 +528,23 @@ __device__ __forceinline__ bool drain_mmas(uint32_t bar) {
   return false;
 }
 
-// One head's result for the segment just finished (thread = head, O in TMEM
-// lanes of this warp): the bf16 output row half, or for a unit split between
-// CTAs the fp32 output normalised by this piece's softmax sum and that sum's
-// log-sum-exp (log2 units) in piece slot `slot`.
-// Reads O out 16 columns at a time, which keeps the softmax loop's live
-// state in registers around it.
-template <bool kSplit>
-__device__ __forceinline__ void write_segment(const AttnParams& p, int64_t n, int v, bool whole,
-                                              int64_t slot, uint32_t lane_base, int h,
-                                              float m_ref, float l) {
-  if (!kSplit) whole = true;
+// One head's result (thread = head, O in TMEM lanes of this warp): the bf16
+// output row half or, for a chunk of a split unit (kPiece), the fp32 output
+// normalised by the chunk's softmax sum and that sum's log-sum-exp (log2
+// units) in CTA b's partial slot. Reads O out 16 columns at a time, which
+// keeps the softmax loop's live state in registers around it.
+template <bool kPiece>
+__device__ __forceinline__ void write_result(const AttnParams& p, int64_t n, int v, int64_t b,
+                                             uint32_t lane_base, int h, float m_ref, float l) {
   const bool store = h < p.num_heads;
   const float inv = l > 0.0f ? 1.0f / l : 0.0f;
   uint8_t* orow = p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
-  float* prow = whole ? nullptr : p.part_o + (slot * p.num_heads + h) * kHalf;
+  float* prow = kPiece ? p.part_o + (b * p.num_heads + h) * kHalf : nullptr;
 #pragma unroll 1
   for (int c = 0; c < kHalf / 16; ++c) {
     uint32_t o[16];
     tmem_ld16(lane_base + kColO + 16 * c, o);
-    if (whole) {
+    if (!kPiece) {
       uint32_t w[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -602,56 +569,64 @@ __device__ __forceinline__ void write_segment(const AttnParams& p, int64_t n, in
   }
   if (!store) return;
   const float lse2 = l > 0.0f ? m_ref + log2f(l) : -__int_as_float(0x7F800000);
-  if (!whole)
-    p.part_lse[slot * p.num_heads + h] = lse2;
+  if (kPiece)
+    p.part_lse[b * p.num_heads + h] = lse2;
   else if (v == 0 && p.lse)
     p.lse[n * p.num_heads + h] =
         l > 0.0f ? lse2 * 0.69314718055994531f : -__int_as_float(0x7F800000);
 }
 
-// First tile of CTA b's range. One CTA per unit: the unit's tiles; split
-// (at most 1023 CTAs, total * 1024 in range): total * b / grid.
-__device__ __forceinline__ int64_t range_begin(const AttnParams& p, int64_t b) {
-  return p.grid == p.units ? b * p.tiles : p.total * b / p.grid;
-}
-
-// kSplit: the split schedule (ranges of tiles over units, pieces, Q reloads
-// between segments); otherwise one CTA per unit, which compiles without any
-// of that.
-template <bool kSplit>
+// kPiece: a chunk of a split unit, written as an fp32 partial; otherwise a
+// whole unit, written as the bf16 output (the same kernel otherwise).
+template <bool kPiece>
 __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t b = blockIdx.x;
-  // One CTA per unit: this CTA's run of indices (a row of the fixed layout,
-  // or its query's ragged run) and its number of tiles.
-  int64_t key_off = 0, key_len = p.topk;
-  if (!kSplit) {
-    const int64_t n0 = b >> 1;
-    if (p.key_offsets) {
-      int64_t lo = ld_once_i64(p.key_offsets + n0), hi = ld_once_i64(p.key_offsets + n0 + 1);
-      lo = lo < 0 ? 0 : (lo > p.num_indices ? p.num_indices : lo);
-      hi = hi < lo ? lo : (hi > p.num_indices ? p.num_indices : hi);
-      key_off = lo;
-      key_len = hi - lo;
-    } else {
-      key_off = n0 * p.topk;
-    }
+  // this CTA's unit (query n, value half v) and run of indices: chunk
+  // b % chunks of a row of the fixed layout, or the query's ragged run. The
+  // grid and the chunk count fit 32 bits (a 64-bit division here, a runtime
+  // call, cost the whole kernel 10% in registers and time).
+  const uint32_t chunks32 = (uint32_t)p.chunks;
+  const uint32_t unit32 = (uint32_t)blockIdx.x / chunks32;
+  const int64_t chunk = (int64_t)((uint32_t)blockIdx.x - unit32 * chunks32);
+  const int64_t n = unit32 >> 1;
+  const int v = (int)(unit32 & 1u);
+  int64_t key_off, key_len;
+  if (p.key_offsets) {
+    int64_t lo = ld_once_i64(p.key_offsets + n), hi = ld_once_i64(p.key_offsets + n + 1);
+    lo = lo < 0 ? 0 : (lo > p.num_indices ? p.num_indices : lo);
+    hi = hi < lo ? lo : (hi > p.num_indices ? p.num_indices : hi);
+    key_off = lo;
+    key_len = hi - lo;
+  } else {
+    const int64_t first = chunk * p.chunk_tiles * kTileKeys;
+    const int64_t rest = p.topk - first;
+    const int64_t span = p.chunk_tiles * kTileKeys;
+    key_off = n * p.topk + first;
+    key_len = rest < 0 ? 0 : (rest < span ? rest : span);
   }
-  const int64_t unit_tiles = kSplit ? p.tiles : (key_len + kTileKeys - 1) / kTileKeys;
-  if (unit_tiles == 0) {
+  const int64_t n_tiles = (key_len + kTileKeys - 1) / kTileKeys;
+  if (n_tiles == 0) {
     // no keys at all: every output row is zero and every log-sum-exp -inf
-    // (one CTA per unit)
-    const int64_t n = b >> 1;
-    const int v = (int)(b & 1);
-    for (int id = tid; id < p.num_heads * 32; id += kThreads)
-      st_v4(p.out + n * p.o_qstride + (int64_t)(id >> 5) * p.o_hstride + v * kHalf * 2 +
-                (id & 31) * 16,
-            make_uint4(0, 0, 0, 0));
-    if (v == 0 && p.lse)
+    // (an empty partial for a chunk)
+    if constexpr (kPiece) {
+      for (int id = tid; id < p.num_heads * (kHalf / 4); id += kThreads)
+        reinterpret_cast<float4*>(p.part_o + b * p.num_heads * kHalf)[id] =
+            make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       for (int h = tid; h < p.num_heads; h += kThreads)
-        p.lse[n * p.num_heads + h] = -__int_as_float(0x7F800000);
-    return;
+        p.part_lse[b * p.num_heads + h] = -__int_as_float(0x7F800000);
+      return;
+    } else {
+      for (int id = tid; id < p.num_heads * 32; id += kThreads)
+        st_v4(p.out + n * p.o_qstride + (int64_t)(id >> 5) * p.o_hstride + v * kHalf * 2 +
+                  (id & 31) * 16,
+              make_uint4(0, 0, 0, 0));
+      if (v == 0 && p.lse)
+        for (int h = tid; h < p.num_heads; h += kThreads)
+          p.lse[n * p.num_heads + h] = -__int_as_float(0x7F800000);
+      return;
+    }
   }
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -660,14 +635,6 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   const uint32_t bars = base + kOffBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kOffAbort);
-  // this CTA's run of tiles [g0, g1) and where it starts
-  const int64_t g0 = kSplit ? range_begin(p, b) : 0;
-  const int64_t n_tiles = kSplit ? range_begin(p, b + 1) - g0 : unit_tiles;  // >= 1
-  const int64_t u_first = kSplit ? g0 / p.tiles : b;
-  Cursor<kSplit> start;
-  start.t = kSplit ? g0 - u_first * p.tiles : 0;
-  start.n = kSplit ? u_first % p.nq : b >> 1;
-  start.v = (int32_t)(kSplit ? u_first / p.nq : b & 1);
 
   if (warp == kIssuerWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   if (tid == 0) {
@@ -678,7 +645,6 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       mbar_init(bars + kBarPFull + 8 * s, 128);
       mbar_init(bars + kBarPvDone + 8 * s, 1);
     }
-    mbar_init(bars + kBarSeg, 128);
     mbar_init(bars + kBarDrain, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -688,24 +654,21 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   // latencies overlap.
   const bool producer = warp >= 4 && warp < kIssuerWarp;
   const int e = warp - 4, j = lane;
-  Cursor<kSplit> cl = start;  // a producer's next tile to load
   Packed buf[kDepth];
   int64_t s_next = -1;
   if (producer) {
 #pragma unroll
-    for (int u = 0; u < kDepth; ++u) {
-      buf[u] = load_packed(p, u < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1, e);
-      cl.next(p);
-    }
-    s_next = kDepth < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1;
+    for (int u = 0; u < kDepth; ++u)
+      buf[u] = load_packed(p, u < n_tiles ? key_index(p, u, j, key_off, key_len) : -1, e);
+    s_next = kDepth < n_tiles ? key_index(p, kDepth, j, key_off, key_len) : -1;
   } else {
-    load_q_smem(p, start.n, q_base, tid < 128 ? tid : tid - 256, 160);
+    load_q_smem(p, n, q_base, tid < 128 ? tid : tid - 256, 160);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) load_q_tmem(p, start.n, tmem, tid);
+  if (warp < 4) load_q_tmem(p, n, tmem, tid);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -723,8 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
         if (i < n_tiles && live) {
           const Packed cur = buf[u];
           buf[u] = load_packed(p, s_next, e);  // tile i + kDepth
-          cl.next(p);
-          s_next = i + kDepth + 1 < n_tiles ? key_index(p, cl, j, key_off, key_len) : -1;
+          s_next = i + kDepth + 1 < n_tiles ? key_index(p, i + kDepth + 1, j, key_off, key_len)
+                                            : -1;
           const uint32_t st = (uint32_t)(i % kStages);
           if (i >= kStages &&
               !mbar_wait(bars + kBarPvDone + 8 * st, (uint32_t)(((i / kStages) - 1) & 1), abort)) {
@@ -743,65 +706,38 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       const uint64_t q_desc = smem_desc(q_base, 16, 1024, 2);
       // Event-driven over the CTA's tiles: O += P(pi) V(pi) as soon as
       // softmax has written P(pi) (it frees a key stage, so it goes first);
-      // else q.k of tile qi (with tile qi + 1 when qi's stage is even and
-      // both tiles belong to the same query) once its keys are written and
-      // the p.v that last read its tensor-memory columns has been issued
-      // (MMAs from this thread run in order). The first p.v of a segment
-      // waits for softmax to have read out the previous segment's output;
-      // the first q.k of a new query waits for softmax to have loaded its Q.
-      // Segment boundaries are observed one at a time, in order.
-      Cursor<kSplit> cq = start, cp = start;
-      int64_t qi = 0, pi = 0, seen = 0;
-      int32_t qseg = 0, pseg = 0;  // segments of the next q.k and p.v tiles
+      // else q.k of tile qi (with tile qi + 1 when qi's stage is even) once
+      // its keys are written and the p.v that last read its tensor-memory
+      // columns has been issued (MMAs from this thread run in order).
+      int64_t qi = 0, pi = 0;
       uint32_t idle = 0;
-      auto seg_ready = [&](int64_t k) -> bool {
-        if constexpr (kSplit) {
-          while (seen < k) {
-            if (!mbar_test(bars + kBarSeg, (uint32_t)(seen & 1))) return false;
-            ++seen;
-          }
-        }
-        return true;
-      };
       while (pi < n_tiles) {
         bool progress = false;
         if (pi < qi && mbar_test(bars + kBarPFull + 8 * (uint32_t)(pi % kStages),
                                  (uint32_t)((pi / kStages) & 1))) {
-          const bool first = pi == 0 || (kSplit && cp.t == 0);
-          if (!first || pi == 0 || seg_ready(pseg)) {
-            tc_fence_after();
-            issue_pv((uint32_t)(pi % kStages), cp.v, first, k_base, tmem);
-            mma_commit(bars + kBarPvDone + 8 * (uint32_t)(pi % kStages));
-            ++pi;
-            pseg += cp.next(p) ? 1 : 0;
-            progress = true;
-          }
+          tc_fence_after();
+          issue_pv((uint32_t)(pi % kStages), v, pi == 0, k_base, tmem);
+          mma_commit(bars + kBarPvDone + 8 * (uint32_t)(pi % kStages));
+          ++pi;
+          progress = true;
         }
         if (!progress && qi < n_tiles) {
           const uint32_t st = (uint32_t)(qi % kStages);
-          Cursor<kSplit> c2 = cq;
-          const int32_t qseg2 = qseg + (c2.next(p) ? 1 : 0);
-          // pairs stay within a unit (its next tile is not a unit's first)
-          const bool pair = (st & 1u) == 0 && qi + 1 < n_tiles && (!kSplit || c2.t != 0);
+          const bool pair = (st & 1u) == 0 && qi + 1 < n_tiles;
           if (qi + (pair ? 1 : 0) - pi < kStages &&
               mbar_test(bars + kBarKFull + 8 * st, (uint32_t)((qi / kStages) & 1)) &&
               (!pair || mbar_test(bars + kBarKFull + 8 * (st + 1),
-                                  (uint32_t)(((qi + 1) / kStages) & 1))) &&
-              seg_ready(qseg)) {
+                                  (uint32_t)(((qi + 1) / kStages) & 1)))) {
             tc_fence_after();
             if (pair) {
               issue_qk<true>(st, q_desc, k_base, tmem);
               mma_commit(bars + kBarSFull + 8 * st);
               mma_commit(bars + kBarSFull + 8 * (st + 1));
               qi += 2;
-              cq = c2;
-              qseg = qseg2 + (cq.next(p) ? 1 : 0);
             } else {
               issue_qk<false>(st, q_desc, k_base, tmem);
               mma_commit(bars + kBarSFull + 8 * st);
               qi += 1;
-              cq = c2;
-              qseg = qseg2;
             }
             progress = true;
           }
@@ -822,28 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     // -------------------------------------------------------------- softmax
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const float kNegInf = -__int_as_float(0x7F800000);
-    float m_ref = kNegInf;  // reference max of the segment (log2 units)
+    float m_ref = kNegInf;  // reference max (log2 units)
     float l = 0.0f;         // sum of p against m_ref
-    bool live = true;
-    Cursor<kSplit> c = start;
-    bool first_seg = true;  // in the CTA's first segment
-    int64_t s_key = key_index(p, c, lane, key_off, key_len);
-    for (int64_t i = 0; i < n_tiles && live; ++i) {
-      const bool seg_first = i == 0 || (kSplit && c.t == 0);
-      const bool seg_last = i == n_tiles - 1 || (kSplit && c.t == p.tiles - 1);
-      if (seg_first) {
-        m_ref = kNegInf;
-        l = 0.0f;
-      }
+    int64_t s_key = key_index(p, 0, lane, key_off, key_len);
+    for (int64_t i = 0; i < n_tiles; ++i) {
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, s_key >= 0 && s_key < p.num_slots);
-      Cursor<kSplit> cn = c;
-      const bool new_unit = cn.next(p);
-      s_key = i + 1 < n_tiles ? key_index(p, cn, lane, key_off, key_len) : -1;
+      s_key = i + 1 < n_tiles ? key_index(p, i + 1, lane, key_off, key_len) : -1;
       const uint32_t st = (uint32_t)(i % kStages);
-      if (!warp_wait(bars + kBarSFull + 8 * st, (uint32_t)((i / kStages) & 1), abort)) {
-        live = false;
-        break;
-      }
+      if (!warp_wait(bars + kBarSFull + 8 * st, (uint32_t)((i / kStages) & 1), abort)) break;
       tc_fence_after();
       const uint32_t scol = lane_base + kColS + st * kTileKeys;
       uint32_t sr[32];
@@ -858,14 +780,12 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       const bool need = mt > m_ref + 8.0f;
       if (__any_sync(0xFFFFFFFFu, need)) {
         const float f = need ? ex2(m_ref - mt) : 1.0f;  // ex2(-inf) = 0
-        if (!seg_first) {
+        if (i > 0) {
           // O may be touched only once the p.v of tile i - 1 has completed
           const int64_t w = i - 1;
           if (!warp_wait(bars + kBarPvDone + 8 * (uint32_t)(w % kStages),
-                         (uint32_t)((w / kStages) & 1), abort)) {
-            live = false;
+                         (uint32_t)((w / kStages) & 1), abort))
             break;
-          }
           tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < kHalf / 32; ++cc) {
@@ -900,32 +820,12 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       l += lsum0 + lsum1;
       tc_fence_before();
       mbar_arrive(bars + kBarPFull + 8 * st);
-      if (seg_last) {
-        // the segment's output: wait for its last p.v, read O out, then (if
-        // another segment follows) load Q of a new query and release O
-        if (!warp_wait(bars + kBarPvDone + 8 * st, (uint32_t)((i / kStages) & 1), abort)) {
-          live = false;
-          break;
-        }
+      if (i == n_tiles - 1) {
+        // the result: wait for the last p.v, then read O out
+        if (!warp_wait(bars + kBarPvDone + 8 * st, (uint32_t)((i / kStages) & 1), abort)) break;
         tc_fence_after();
-        // whole: the segment runs from the unit's first tile to its last
-        // (recomputed here rather than kept live through the loop)
-        const int64_t cta = blockIdx.x;
-        const bool whole = c.t + 1 == p.tiles &&
-                           (!first_seg || (kSplit ? range_begin(p, cta) % p.tiles : 0) == 0);
-        write_segment<kSplit>(p, c.n, c.v, whole, 2 * cta + (first_seg ? 0 : 1), lane_base, tid,
-                              m_ref, l);
-        if (kSplit && i + 1 < n_tiles) {
-          if (cn.n != c.n) {
-            load_q_smem(p, cn.n, q_base, tid, 128);
-            load_q_tmem(p, cn.n, tmem, tid);
-          }
-          tc_fence_before();
-          mbar_arrive(bars + kBarSeg);
-        }
+        write_result<kPiece>(p, n, v, b, lane_base, tid, m_ref, l);
       }
-      c = cn;
-      if (new_unit) first_seg = false;
     }
   }
   tc_fence_before();
@@ -937,43 +837,29 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   }
 }
 
-// Combines the pieces of every unit split between CTAs. Block (j, g) looks at
-// the boundary between CTAs j and j + 1 and heads 8g..8g+7; the unit the
-// boundary falls inside (if any) is merged by the blocks of its first
-// boundary, over the pieces of CTAs b_first..b_last:
-// out = sum_b 2**(lse_b - L) o_b / sum_b 2**(lse_b - L), L = max_b lse_b, and
-// the unit's log-sum-exp L + log2(sum) (in natural log units, half 0 only).
-// A unit without any valid key gets zeros and -inf. The pieces' slots are
-// worked out in parallel into shared memory; 64 threads take a head, four
-// columns each. A unit of up to kMergeFew pieces is summed by each thread
-// on its own; beyond that (the launch then gives the block dynamic shared
-// memory for kMergeHeads x pieces weights), every (head, piece) weight is
-// first worked out in parallel, and the sums keep several loads in flight.
-constexpr int kMergeMaxPieces = 1024;  // grid <= 1023
-constexpr int kMergeHeads = 8;         // heads per block (64 threads each)
+// Combines the partials of every split unit. Block (u, g) takes unit u and
+// heads 8g..8g+7, over the partials of CTAs u * chunks .. u * chunks +
+// chunks - 1: out = sum_b 2**(lse_b - L) o_b / sum_b 2**(lse_b - L),
+// L = max_b lse_b, and the unit's log-sum-exp L + log2(sum) (in natural log
+// units, half 0 only). A unit without any valid key gets zeros and -inf.
+// 64 threads take a head, four columns each. Up to kMergeFew partials are
+// summed by each thread on its own; beyond that (the launch then gives the
+// block dynamic shared memory for kMergeHeads x chunks weights), every
+// (head, partial) weight is first worked out in parallel, and the sums keep
+// several loads in flight.
+constexpr int kMergeHeads = 8;  // heads per block (64 threads each)
 constexpr int kMergeFew = 4;
 
 __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_kernel(AttnParams p) {
-  __shared__ int32_t piece_slot[kMergeMaxPieces];
   __shared__ float head_l[kMergeHeads][2], head_w[kMergeHeads][2];
-  extern __shared__ float merge_dyn[];  // [kMergeHeads][pieces]: log-sum-exp, then weight
-  const int64_t j = blockIdx.x;
-  const int64_t gb = p.total * (j + 1) / p.grid;
-  const int64_t unit = gb / p.tiles;
-  if (gb == unit * p.tiles) return;  // the boundary lies between units
-  const int64_t g0 = p.total * j / p.grid;
-  if (g0 > unit * p.tiles) return;   // merged by the blocks of an earlier boundary
-  const int64_t b_last = ((unit + 1) * p.tiles * p.grid - 1) / p.total;
-  const int pieces = (int)(b_last - j + 1);
-  for (int k = threadIdx.x; k < pieces; k += blockDim.x) {
-    const int64_t bb = j + k;
-    piece_slot[k] = (int32_t)(2 * bb + ((p.total * bb / p.grid) / p.tiles == unit ? 0 : 1));
-  }
-  __syncthreads();
+  extern __shared__ float merge_dyn[];  // [kMergeHeads][chunks]: log-sum-exp, then weight
+  const int64_t unit = blockIdx.x;
+  const int pieces = (int)p.chunks;
+  const int64_t b0 = unit * p.chunks;  // the unit's first CTA
   const int64_t H = p.num_heads;
   const float kNegInf = -__int_as_float(0x7F800000);
-  const int64_t n = unit % p.nq;  // half-major unit order
-  const int v = (int)(unit / p.nq);
+  const int64_t n = unit >> 1;
+  const int v = (int)(unit & 1);
   uint32_t dyn_bytes;
   asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
   if (pieces <= kMergeFew || dyn_bytes < (uint32_t)(kMergeHeads * pieces) * 4u) {
@@ -982,13 +868,13 @@ __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_ker
     const int c4 = threadIdx.x & 63;
     float L = kNegInf;
 #pragma unroll 4
-    for (int k = 0; k < pieces; ++k) L = fmaxf(L, p.part_lse[piece_slot[k] * H + h]);
+    for (int k = 0; k < pieces; ++k) L = fmaxf(L, p.part_lse[(b0 + k) * H + h]);
     float W = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (L != kNegInf) {
 #pragma unroll 4
       for (int k = 0; k < pieces; ++k) {
-        const int64_t row = piece_slot[k] * H + h;
+        const int64_t row = (b0 + k) * H + h;
         const float w = exp2f(p.part_lse[row] - L);
         const float4 o = *reinterpret_cast<const float4*>(p.part_o + row * kHalf + 4 * c4);
         W += w;
@@ -1008,7 +894,7 @@ __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_ker
   for (int t = threadIdx.x; t < kMergeHeads * pieces; t += blockDim.x) {
     const int hh = t / pieces, k = t - hh * pieces;
     const int64_t h = (int64_t)blockIdx.y * kMergeHeads + hh;
-    merge_dyn[hh * pieces + k] = h < H ? p.part_lse[piece_slot[k] * H + h] : kNegInf;
+    merge_dyn[hh * pieces + k] = h < H ? p.part_lse[(b0 + k) * H + h] : kNegInf;
   }
   __syncthreads();
   const int hh = threadIdx.x >> 6, c4 = threadIdx.x & 63, half = c4 >> 5;
@@ -1020,7 +906,7 @@ __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_ker
   if ((c4 & 31) == 0) head_l[hh][half] = L;
   __syncthreads();
   L = fmaxf(head_l[hh][0], head_l[hh][1]);
-  // weights 2**(lse_b - L) (0 for a piece without valid keys) and their sum
+  // weights 2**(lse_b - L) (0 for a partial without valid keys) and their sum
   float W = 0.0f;
   for (int k = c4; k < pieces; k += 64) {
     const float w = L != kNegInf ? exp2f(merge_dyn[hh * pieces + k] - L) : 0.0f;
@@ -1040,7 +926,7 @@ __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_ker
     for (int k = 0; k < pieces; ++k) {
       const float w = merge_dyn[hh * pieces + k];
       const float4 o =
-          *reinterpret_cast<const float4*>(p.part_o + (piece_slot[k] * H + h) * kHalf + 4 * c4);
+          *reinterpret_cast<const float4*>(p.part_o + ((b0 + k) * H + h) * kHalf + 4 * c4);
       acc.x += w * o.x;
       acc.y += w * o.y;
       acc.z += w * o.z;
@@ -1059,15 +945,18 @@ __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_ker
 
 namespace {
 
-// CTAs of the split schedule: one per SM (each holds all of tensor memory),
-// with at least kMinSplitTiles tiles each (a CTA's start-up and its piece's
-// write and merge cost a few tiles' time).
+// Chunks per unit of the split schedule: as many as fill the SMs with one
+// CTA each (every CTA holds all of tensor memory), of at least
+// kMinSplitTiles tiles (a CTA's start-up, its partial's write and the merge
+// cost a few tiles' time), and none empty; 1 means no split.
 constexpr int64_t kMinSplitTiles = 4;
-int64_t split_grid(int64_t total) {
-  int64_t sms = kvq::sm_count();
-  if (sms > 1023) sms = 1023;
-  const int64_t want = total / kMinSplitTiles > 1 ? total / kMinSplitTiles : 1;
-  return want < sms ? want : sms;
+int64_t split_chunks(int64_t units, int64_t tiles) {
+  if (units <= 0 || tiles <= 0) return 1;
+  int64_t c = kvq::sm_count() / units;
+  if (c > tiles / kMinSplitTiles) c = tiles / kMinSplitTiles;
+  if (c < 2) return 1;
+  const int64_t per = (tiles + c - 1) / c;
+  return (tiles + per - 1) / per;
 }
 
 // Checks shared by the entry points; fills `p` (without workspace).
@@ -1114,8 +1003,9 @@ int attention_params(const void* q_bf16, int64_t num_queries, int64_t num_heads,
   p.tiles = tiles;
   p.units = 2 * num_queries;
   p.nq = num_queries;
-  p.total = 2 * num_queries * tiles;
-  p.grid = 2 * num_queries;  // one CTA per unit unless split
+  p.chunks = 1;  // one CTA per unit unless split
+  p.chunk_tiles = tiles;
+  p.grid = p.units;
   p.part_o = nullptr;
   p.part_lse = nullptr;
   p.key_offsets = nullptr;
@@ -1123,16 +1013,19 @@ int attention_params(const void* q_bf16, int64_t num_queries, int64_t num_heads,
   return KVQ_OK;
 }
 
-// Bytes of the split schedule's partial results (0 without keys).
+// Bytes of the split schedule's partial results: one per CTA.
 int64_t split_bytes(int64_t grid, int64_t num_heads) {
-  return 2 * grid * num_heads * (int64_t)(kvq::kHalf * 4 + 4);
+  return grid * num_heads * (int64_t)(kvq::kHalf * 4 + 4);
 }
 
-// Lays the partial results out in `ws` (256-byte aligned) for `grid` CTAs.
-void split_layout(kvq::AttnParams& p, int64_t grid, void* ws) {
-  p.grid = grid;
+// Cuts every unit into `chunks` runs and lays the partial results out in
+// `ws` (256-byte aligned).
+void split_layout(kvq::AttnParams& p, int64_t chunks, void* ws) {
+  p.chunks = chunks;
+  p.chunk_tiles = (p.tiles + chunks - 1) / chunks;
+  p.grid = p.units * chunks;
   p.part_o = static_cast<float*>(ws);
-  p.part_lse = p.part_o + 2 * grid * p.num_heads * kvq::kHalf;
+  p.part_lse = p.part_o + p.grid * p.num_heads * kvq::kHalf;
 }
 
 int launch_attention(const kvq::AttnParams& p, cudaStream_t stream) {
@@ -1155,14 +1048,9 @@ int launch_attention(const kvq::AttnParams& p, cudaStream_t stream) {
   else
     mxfp4_attention_kernel<false><<<(unsigned)p.grid, kThreads, kSmemBytes, stream>>>(p);
   int rc = launch_status();
-  if (rc != KVQ_OK || !p.part_o || p.grid < 2) return rc;
-  const dim3 mgrid((unsigned)(p.grid - 1), (unsigned)((p.num_heads + kMergeHeads - 1) / kMergeHeads));
-  // the most pieces a unit can have: every CTA takes at least total / grid tiles
-  const int64_t per_cta = p.total / p.grid;
-  const int64_t most = p.tiles / (per_cta > 0 ? per_cta : 1) + 2;
-  const size_t dyn = most > kMergeFew
-                         ? (size_t)kMergeHeads * (size_t)(most < kMergeMaxPieces ? most : kMergeMaxPieces) * 4
-                         : 0;
+  if (rc != KVQ_OK || !p.part_o) return rc;
+  const dim3 mgrid((unsigned)p.units, (unsigned)((p.num_heads + kMergeHeads - 1) / kMergeHeads));
+  const size_t dyn = p.chunks > kMergeFew ? (size_t)kMergeHeads * (size_t)p.chunks * 4 : 0;
   mxfp4_attention_merge_kernel<<<mgrid, 64 * kMergeHeads, dyn, stream>>>(p);
   return launch_status();
 }
@@ -1185,9 +1073,7 @@ extern "C" int mxfp4_mla_sparse_attention_ragged(
   if (!key_offsets || !aligned(key_offsets, 8) || (num_indices > 0 && !indices)) return KVQ_EINVAL;
   p.key_offsets = key_offsets;
   p.num_indices = num_indices;
-  p.tiles = 1;  // per CTA from its run; one CTA per (query, value half)
-  p.total = p.units;
-  return launch_attention(p, stream);
+  return launch_attention(p, stream);  // one CTA per (query, value half), tiles from its run
 }
 
 extern "C" int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries,
@@ -1198,7 +1084,8 @@ extern "C" int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries
   const int64_t tiles = (topk + kvq::kTileKeys - 1) / kvq::kTileKeys;
   if (tiles > 0 && 2 * num_queries > INT64_MAX / 1024 / tiles) return KVQ_EINVAL;
   if (tiles == 0 || num_queries == 0) return 0;
-  return split_bytes(split_grid(2 * num_queries * tiles), num_heads);
+  const int64_t chunks = split_chunks(2 * num_queries, tiles);
+  return chunks > 1 ? split_bytes(2 * num_queries * chunks, num_heads) : 0;
 }
 
 extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_queries,
@@ -1216,11 +1103,11 @@ extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_querie
                             num_blocks, block_size, block_stride_rows, indices, topk, sm_scale,
                             out_bf16, out_query_stride, out_head_stride, lse, status, p);
   if (rc != KVQ_OK || num_queries == 0) return rc;
-  if (workspace && p.tiles > 0) {
-    const int64_t grid = split_grid(p.total);
-    if (workspace_bytes < split_bytes(grid, num_heads) || !aligned(workspace, 256))
-      return KVQ_EINVAL;
-    split_layout(p, grid, workspace);
+  if (workspace) {
+    const int64_t chunks = split_chunks(p.units, p.tiles);
+    const int64_t need = chunks > 1 ? split_bytes(p.units * chunks, num_heads) : 0;
+    if (workspace_bytes < need || !aligned(workspace, 256)) return KVQ_EINVAL;
+    if (chunks > 1) split_layout(p, chunks, workspace);
   }
   return launch_attention(p, stream);
 }
@@ -1237,7 +1124,7 @@ extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_querie
 // instead of from a workspace argument.
 //
 // The array is a file-scope __device__ object of kScratchBytes (40 MiB: the
-// split schedule of 128 heads over up to 159 SMs). Every GPU that loads this
+// split schedule of 128 heads over up to 318 SMs). Every GPU that loads this
 // library's attention code holds it until the process exits. Host code only
 // has a host-side stand-in for its name, so the device address is looked up
 // with cudaGetSymbolAddress once per device, with that device current, on
@@ -1277,13 +1164,13 @@ extern "C" int mxfp4_mla_sparse_attention_noalloc(
                             num_blocks, block_size, block_stride_rows, indices, topk, sm_scale,
                             out_bf16, out_query_stride, out_head_stride, lse, status, p);
   if (rc != KVQ_OK || num_queries == 0) return rc;
-  if (p.tiles > 0) {
-    const int64_t grid = split_grid(p.total);
-    if (split_bytes(grid, num_heads) > kScratchBytes) return KVQ_ESCRATCH;
+  const int64_t chunks = split_chunks(p.units, p.tiles);
+  if (chunks > 1) {
+    if (split_bytes(p.units * chunks, num_heads) > kScratchBytes) return KVQ_ESCRATCH;
     void* scratch = nullptr;
     rc = scratch_address(&scratch);
     if (rc != KVQ_OK) return rc;
-    split_layout(p, grid, scratch);
+    split_layout(p, chunks, scratch);
   }
   return launch_attention(p, stream);
 }

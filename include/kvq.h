@@ -446,17 +446,18 @@ int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks, int64_t b
  * workspace        device memory of at least workspace_bytes >=
  *                  mxfp4_mla_sparse_attention_workspace_size(num_queries,
  *                  num_heads, topk) bytes, 256-byte aligned, or NULL.
- *                  With a workspace the queries' key tiles are split evenly
- *                  over up to one CTA per SM, each taking at least four
- *                  32-key tiles (the split-K of the read path [pr]:
- *                  a ragged sparse-attention kernel plus a split-K partial
- *                  kernel): pieces of a (query, value half) cut between two
- *                  CTAs are written there as fp32 partial outputs with their
- *                  log-sum-exps and merged by a second kernel launched on
- *                  the same stream. Its contents need no initialisation and
- *                  are garbage afterwards; two calls in flight at once must
- *                  not share it. Without one, one CTA takes each (query,
- *                  value half) whole (no second kernel). Both give results
+ *                  With a workspace, when there are too few (query, value
+ *                  half) units to fill the SMs, every unit's key tiles are
+ *                  cut into equal chunks of at least four 32-key tiles, one
+ *                  CTA each, so that the grid fills the SMs (the split-K of
+ *                  the read path [pr]: a ragged sparse-attention kernel plus
+ *                  a split-K partial kernel): each chunk's fp32 partial
+ *                  output and log-sum-exp are written there and merged by a
+ *                  second kernel launched on the same stream. Its contents
+ *                  need no initialisation and are garbage afterwards; two
+ *                  calls in flight at once must not share it. Without one,
+ *                  or when the units already fill the SMs, one CTA takes
+ *                  each unit whole (no second kernel). Both give results
  *                  within the bound above; they may differ in the last bits.
  *                  KVQ_EINVAL if the workspace is too small or misaligned.
  * The library allocates nothing and keeps no pointer after the call.
@@ -501,10 +502,11 @@ int mxfp4_mla_sparse_attention_ragged(const void* q_bf16, int64_t num_queries, i
 /*
  * mxfp4_mla_sparse_attention_workspace_size — bytes of workspace that
  * mxfp4_mla_sparse_attention needs to split these shapes over the current
- * device's SMs: 2 x CTAs x num_heads x (256 x 4 + 4) (CTAs = min(SMs,
- * max(1, floor(2 x num_queries x ceil(topk / 32) / 4))): every CTA takes at
- * least four 32-key tiles), 0 when there is nothing to split
- * (num_queries or topk 0), KVQ_EINVAL for shapes the attention rejects.
+ * device's SMs: CTAs x num_heads x (256 x 4 + 4), CTAs = units x chunks with
+ * units = 2 x num_queries, chunks = min(floor(SMs / units),
+ * floor(ceil(topk / 32) / 4)) reduced so that no chunk is empty; 0 when
+ * nothing is split (chunks below 2: the units fill the SMs, or topk is
+ * short), KVQ_EINVAL for shapes the attention rejects.
  * No page counterpart: a host query of this library.
  */
 int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries, int64_t num_heads,
@@ -522,7 +524,7 @@ int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries, int64_t n
  * output; arguments, layouts, results and errors are those of
  * mxfp4_mla_sparse_attention with a workspace, plus:
  *   - The scratch is one 40 MiB (41,943,040-byte) __device__ array, enough
- *     for 128 heads split over up to 159 SMs. Every GPU that loads the
+ *     for 128 heads split over up to 318 SMs. Every GPU that loads the
  *     library's attention code holds it until the process exits.
  *   - Shapes whose split schedule needs more than that (see
  *     mxfp4_mla_sparse_attention_workspace_size) return KVQ_ESCRATCH and

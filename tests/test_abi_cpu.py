@@ -195,12 +195,13 @@ def test_attention_validation_on_host(L):
     # cache rows whose byte offsets leave int64: rejected like the store's
     a = list(ok); a[6] = 1 << 40; a[8] = 1 << 30
     assert f(*a) == -1
-    # a workspace that is misaligned or smaller than the query says
-    need = L.mxfp4_mla_sparse_attention_workspace_size(2, 128, 16)
+    # a workspace that is misaligned or smaller than the query says (2048
+    # keys: the two queries' units are cut into chunks)
+    need = L.mxfp4_mla_sparse_attention_workspace_size(2, 128, 2048)
     assert need > 0
-    a = list(ok); a[17] = A16 + 16; a[18] = need
+    a = list(ok); a[10] = 2048; a[17] = A16 + 16; a[18] = need
     assert f(*a) == -1
-    a = list(ok); a[17] = A16; a[18] = need - 1
+    a = list(ok); a[10] = 2048; a[17] = A16; a[18] = need - 1
     assert f(*a) == -1
 
 
@@ -219,21 +220,41 @@ def test_ragged_attention_validation_on_host(L):
     assert f(*a) == -1
 
 
+def _sms():
+    """The SM count the library sees (148 when no GPU is present)."""
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count \
+        if torch.cuda.is_available() else 148
+
+
+def _chunks(units, tiles, sms):
+    """Chunks per unit: min(SMs // units, tiles // 4), none empty; 1 below 2."""
+    c = min(sms // units, tiles // 4)
+    if c < 2:
+        return 1
+    per = -(-tiles // c)
+    return -(-tiles // per)
+
+
 def test_attention_workspace_size(L):
-    """2 x CTAs x heads x (256 fp32 + one log-sum-exp), CTAs = min(SMs,
-    max(1, (2 x queries x tiles of 32 keys) // 4)); 0 when nothing can be
-    split; -1 for shapes the attention rejects."""
+    """CTAs x heads x (256 fp32 + one log-sum-exp), CTAs = 2 x queries x
+    chunks; 0 when nothing is split (the units fill the SMs, or too few
+    tiles); -1 for shapes the attention rejects."""
     g = L.mxfp4_mla_sparse_attention_workspace_size
     assert g(0, 128, 2048) == 0 and g(3, 128, 0) == 0
     assert g(-1, 128, 16) == -1 and g(2, 0, 16) == -1 and g(2, 129, 16) == -1
     assert g(2, 128, -1) == -1
-    per_cta = 2 * 128 * (256 * 4 + 4)
-    big = g(128, 128, 2048)
-    assert big % per_cta == 0 and 1 <= big // per_cta <= 2 * 128 * 64
-    # one query, one tile per unit: one CTA (at least four tiles each)
-    assert g(1, 128, 32) == per_cta and g(1, 64, 1) == 2 * 64 * (256 * 4 + 4)
-    # one query of 2048 keys: 128 tiles, 32 CTAs of four
-    assert g(1, 128, 2048) == 32 * per_cta
+    sms = _sms()
+    piece = 128 * (256 * 4 + 4)
+    assert g(128, 128, 2048) == 0                      # 256 units fill the SMs
+    assert g(1, 128, 32) == 0 and g(1, 64, 1) == 0     # one tile per unit
+    # one query of 2048 keys: 64 tiles per half, 16 chunks of four
+    assert g(1, 128, 2048) == 2 * 16 * piece
+    for nq, nh, topk in ((3, 64, 4096), (5, 128, 700), (20, 128, 2048)):
+        tiles = -(-topk // 32)
+        c = _chunks(2 * nq, tiles, sms)
+        want = 2 * nq * c * nh * (256 * 4 + 4) if c > 1 else 0
+        assert g(nq, nh, topk) == want, (nq, nh, topk)
 
 
 def test_tensors_on_two_devices_are_refused_before_any_launch():

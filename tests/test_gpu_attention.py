@@ -171,12 +171,12 @@ def test_full_workload_128_queries_2048_keys(split):
 @pytest.mark.parametrize("nq,topk,heads", [(1, 4096, 128), (1, 8192, 64), (5, 2048, 128),
                                            (3, 333, 128), (77, 64, 16), (200, 96, 128)])
 def test_split_schedules(nq, topk, heads):
-    """Shapes whose units are cut into many pieces (one query: each value
-    half spread over 32 or 64 CTAs of at least four tiles, up to ~65 pieces
-    merged through the merge's parallel-weight path; five queries: ~15
-    pieces each), into a few (three queries of 333 keys: the per-thread
-    path), or not at all (more units than SMs, tiles per unit small), with
-    ragged top-k and pads; both schedules against the oracle."""
+    """Shapes whose units are cut into many chunks (one query: each value
+    half cut into 32 or 64 chunks, merged through the merge's parallel-weight
+    path; five queries: ~15 chunks each), into a few (three queries of 333
+    keys: two chunks, the per-thread path), or not at all (more units than
+    SMs, or few tiles per unit), with ragged top-k and pads; both schedules
+    against the oracle."""
     cache = _fill_cache(8192, seed=20 + nq)
     q = _queries(21 + topk, nq, heads)
     rng = np.random.default_rng(22 + heads)
@@ -190,8 +190,9 @@ def test_split_workspace_too_small_is_refused():
     dev = torch.device("cuda", 0)
     q = torch.zeros((2, 128, 512), dtype=torch.bfloat16, device=dev)
     cache = torch.zeros(64 * 272, dtype=torch.uint8, device=dev)
-    idx = torch.zeros((2, 64), dtype=torch.int64, device=dev)
-    need = kvq.attention_workspace_size(2, 128, 64)
+    idx = torch.zeros((2, 2048), dtype=torch.int64, device=dev)
+    need = kvq.attention_workspace_size(2, 128, 2048)
+    assert need > 0
     ws = torch.empty(need - 256, dtype=torch.uint8, device=dev)
     with pytest.raises(kvq.KvqError):
         kvq.mxfp4_mla_sparse_attention(q, cache, idx, 0.1, workspace=ws)

@@ -93,7 +93,7 @@ def test_noalloc_refuses_shapes_beyond_its_scratch_and_bad_arguments():
     schedule of 128 heads on this GPU, so a valid shape never exceeds it
     here, and the size query says so."""
     L = kvq.lib()
-    need = L.mxfp4_mla_sparse_attention_workspace_size(4096, 128, 2048)
+    need = L.mxfp4_mla_sparse_attention_workspace_size(1, 128, 8192)
     assert 0 < need <= 40 << 20
     dev = torch.device("cuda", 0)
     q = torch.zeros((2, 129, 512), dtype=torch.bfloat16, device=dev)
