@@ -38,6 +38,7 @@ struct GatherParams {
   int64_t num_indices;
   uint8_t* out;        // row k starts at out + k * out_pitch
   int64_t out_pitch;   // bytes
+  int64_t per_warp, extra;  // warp w's rows: per_warp, plus one for w < extra
 };
 
 constexpr int kGatherPrefetch = 7;  // rows per warp in flight
@@ -82,9 +83,8 @@ __global__ void __launch_bounds__(kGatherThreads) mxfp4_gather_kernel(GatherPara
   uint8_t* ring = reinterpret_cast<uint8_t*>(smem) + kLutBytes +
                   warp_in_block * (kGatherStages * kStagePitch);
   const int64_t warp = (int64_t)blockIdx.x * kGatherWarps + warp_in_block;
-  const int64_t num_warps = (int64_t)gridDim.x * kGatherWarps;
-  const int64_t k_begin = p.num_indices * warp / num_warps;
-  const int64_t k_end = p.num_indices * (warp + 1) / num_warps;
+  const int64_t k_begin = warp * p.per_warp + (warp < p.extra ? warp : p.extra);
+  const int64_t k_end = k_begin + p.per_warp + (warp < p.extra ? 1 : 0);
   const int n = (int)(k_end - k_begin);  // < 2**31, checked at launch
   if (n <= 0) return;
   const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -176,6 +176,8 @@ extern "C" int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks
       work_blocks, resident_blocks_per_sm(k, kGatherThreads, kGatherSmem, g_gather_occupancy[flat]));
   // each warp's row count must fit the kernel's 32-bit loop counter
   if (num_indices / ((int64_t)grid * kGatherWarps) >= (int64_t)0x7FFFFFFF) return KVQ_EINVAL;
+  p.per_warp = num_indices / ((int64_t)grid * kGatherWarps);
+  p.extra = num_indices - p.per_warp * ((int64_t)grid * kGatherWarps);
   k<<<grid, kGatherThreads, kGatherSmem, stream>>>(p);
   return launch_status();
 }

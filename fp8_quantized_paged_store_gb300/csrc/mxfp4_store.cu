@@ -52,6 +52,10 @@ struct StoreParams {
   int64_t block_stride_rows;
   const uint8_t* weight;  // RMSNorm weight, bf16 [512] (fused variant only)
   float eps;
+  // warp w's tokens: per_warp, plus one for w < extra (set at launch, so
+  // that no warp divides 64-bit numbers: a runtime call that costs the
+  // kernel ~1.5% through its registers)
+  int64_t per_warp, extra;
 };
 
 // Eight bf16 (one 16-byte load) of a group with scale 2**e -> eight E2M1
@@ -283,9 +287,8 @@ __global__ void __launch_bounds__(kStoreThreads) mxfp4_store_kernel(StoreParams 
   constexpr bool kRuns = !kNorm;
   uint4* ring = smem + warp_in_block * (kStages * kStageVecs) + (kRuns ? 2 * lane : lane);
   const int64_t warp = (int64_t)blockIdx.x * kStoreWarps + warp_in_block;
-  const int64_t num_warps = (int64_t)gridDim.x * kStoreWarps;
-  const int64_t t_begin = p.num_tokens * warp / num_warps;
-  const int64_t t_end = p.num_tokens * (warp + 1) / num_warps;
+  const int64_t t_begin = warp * p.per_warp + (warp < p.extra ? warp : p.extra);
+  const int64_t t_end = t_begin + p.per_warp + (warp < p.extra ? 1 : 0);
   const int n = (int)(t_end - t_begin);  // < 2**31, checked at launch
   if (n <= 0) return;
   const uint8_t* src = p.latent + t_begin * p.row_pitch + (kRuns ? 32 : 16) * lane;
@@ -394,6 +397,8 @@ int store_entry(const void* latent_bf16, int64_t num_tokens, int64_t latent_dim,
                                                    g_store_occupancy[2 * norm + flat]));
   // each warp's token count must fit the kernel's 32-bit loop counter
   if (num_tokens / ((int64_t)grid * kStoreWarps) >= (int64_t)0x7FFFFFFF) return KVQ_EINVAL;
+  p.per_warp = num_tokens / ((int64_t)grid * kStoreWarps);
+  p.extra = num_tokens - p.per_warp * ((int64_t)grid * kStoreWarps);
   k<<<grid, kStoreThreads, kStoreSmem, stream>>>(p);
   return launch_status();
 }
