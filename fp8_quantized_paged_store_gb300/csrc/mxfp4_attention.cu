@@ -85,6 +85,8 @@ constexpr uint32_t kKBlock = kTileKeys * 128;            // bytes of one K-block
 // (s even) is one 64-row block and q.k runs at N = 64 over a pair of stages.
 constexpr uint32_t kKBlockStride = kStages * kKBlock;
 constexpr uint32_t kOffQ = 0;
+// dims 0..255 of Q are staged in the ring before the first tile arrives
+static_assert(kHeads * 256 * 2 <= kStages * kKBytes, "Q staging exceeds the key ring");
 constexpr uint32_t kOffK = kOffQ + kQhiBytes;            // kStages buffers
 constexpr uint32_t kOffBar = kOffK + kStages * kKBytes;  // eighteen mbarriers
 constexpr uint32_t kOffTmemSlot = kOffBar + 160;
@@ -143,6 +145,15 @@ struct AttnParams {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint4 lds_v4_at(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void sts_v4(uint32_t a, uint4 v) {
@@ -474,21 +485,32 @@ __device__ __forceinline__ void issue_pv(uint32_t st, int v, bool first, uint32_
 // ---------------------------------------------------------------- kernel ---
 
 // Q of query n into the operand buffers, once per CTA (not inlined: they run
-// once, and kept out of line they leave the roles' loops their registers):
-// dims 256..511 of head r into the swizzled K-major shared-memory layout
-// (zero rows past num_heads), 16 bytes per cp.async by threads
-// [0, nthreads); then, by the 128 softmax threads only (warps 0-3,
-// head = thread), dims 0..255 into TMEM lane `head`, columns kColQ.. as bf16
-// pairs (the A operand of the first 16 q.k steps).
+// once, and kept out of line they leave the roles' loops their registers).
+// load_q_smem, by threads [0, nthreads), 16 bytes per cp.async, all in
+// flight at once: dims 256..511 of head r into the swizzled K-major
+// shared-memory layout of the A operand, and dims 0..255 into a staging
+// area (head r's 32 chunks at stage + 512 r, chunk c at position
+// (c & ~7) | ((c ^ r) & 7), so that the eight lanes of a 16-byte load phase
+// below hit eight bank groups); zero rows past num_heads. load_q_tmem, by
+// the 128 softmax threads (warps 0-3, head = thread): the staged dims 0..255
+// into TMEM lane `head`, columns kColQ.. as bf16 pairs (the A operand of the
+// first 16 q.k steps).
+__device__ __forceinline__ uint32_t q_stage_pos(int r, int c) {
+  return (uint32_t)((c & ~7) | ((c ^ r) & 7)) << 4;
+}
+
 __device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_t q_base,
-                                            int tid, int nthreads) {
+                                         uint32_t stage, int tid, int nthreads) {
   const uint8_t* qn = p.q + n * p.q_qstride;
-  for (int id = tid; id < kHeads * 32; id += nthreads) {
-    const int r = id >> 5, c32 = id & 31;
-    const uint32_t dst = q_base + (uint32_t)(c32 >> 3) * (kHeads * 128) + (uint32_t)r * 128 +
-                         ((((uint32_t)c32 & 7) ^ ((uint32_t)r & 7)) << 4);
+  for (int id = tid; id < kHeads * 64; id += nthreads) {
+    const int r = (id >> 5) & (kHeads - 1), c32 = id & 31;
+    const bool hi = id >= kHeads * 32;
+    const uint32_t dst =
+        hi ? q_base + (uint32_t)(c32 >> 3) * (kHeads * 128) + (uint32_t)r * 128 +
+                 ((((uint32_t)c32 & 7) ^ ((uint32_t)r & 7)) << 4)
+           : stage + (uint32_t)r * 512 + q_stage_pos(r, c32);
     if (r < p.num_heads)
-      cp_async_16a(dst, qn + r * p.q_hstride + 512 + c32 * 16);
+      cp_async_16a(dst, qn + r * p.q_hstride + (hi ? 512 : 0) + c32 * 16);
     else
       sts_v4(dst, make_uint4(0, 0, 0, 0));
   }
@@ -497,17 +519,15 @@ __device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_
   fence_proxy_async();
 }
 
-__device__ __noinline__ void load_q_tmem(const AttnParams& p, int64_t n, uint32_t tmem,
-                                         int tid) {
+__device__ __noinline__ void load_q_tmem(uint32_t stage, uint32_t tmem, int tid) {
   const uint32_t lane_base = tmem + ((uint32_t)((tid >> 5) * 32) << 16);
-  const uint8_t* qrow = p.q + n * p.q_qstride + (int64_t)tid * p.q_hstride;
+  const uint32_t row = stage + (uint32_t)tid * 512;
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t w[32];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint4 x =
-          tid < p.num_heads ? ld_once_v4(qrow + 128 * c + 16 * k) : make_uint4(0, 0, 0, 0);
+      const uint4 x = lds_v4_at(row + q_stage_pos(tid, 8 * c + k));
       w[4 * k] = x.x;
       w[4 * k + 1] = x.y;
       w[4 * k + 2] = x.z;
@@ -662,13 +682,15 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       buf[u] = load_packed(p, u < n_tiles ? key_index(p, u, j, key_off, key_len) : -1, e);
     s_next = kDepth < n_tiles ? key_index(p, kDepth, j, key_off, key_len) : -1;
   } else {
-    load_q_smem(p, n, q_base, tid < 128 ? tid : tid - 256, 160);
+    // dims 0..255 staged in the key ring, which the producers fill only
+    // after the second barrier below
+    load_q_smem(p, n, q_base, k_base, tid < 128 ? tid : tid - 256, 160);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) load_q_tmem(p, n, tmem, tid);
+  if (warp < 4) load_q_tmem(k_base, tmem, tid);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
