@@ -413,18 +413,27 @@ __device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, in
 // kb*kKBlockStride + j*128 + ((c ^ (j & 7)) << 4) + 2*(d & 7), kb = d / 64,
 // c = (d % 64) / 8. With lane = key, each 8-lane phase of a 16-byte store
 // covers eight keys and all eight bank groups.
+// The range check of the two scale bytes is made once, so that the common
+// case is one branch-free run of sixteen independent permute chains.
 __device__ __forceinline__ void dequant_share(const Packed& x, uint32_t kbuf, int j, int e) {
   const uint32_t row = kbuf + (uint32_t)e * kKBlockStride + (uint32_t)j * 128;
   const uint32_t swz = (uint32_t)(j & 7);
+  const uint32_t sb0 = x.s & 0xFFu, sb1 = (x.s >> 8) & 0xFFu;
+  if (sb0 - 2u <= 250u && sb1 - 2u <= 250u) {
+    const ByteTables t0 = make_tables(sb0), t1 = make_tables(sb1);
+    const uint32_t words[8] = {x.c[0].x, x.c[0].y, x.c[0].z, x.c[0].w,
+                               x.c[1].x, x.c[1].y, x.c[1].z, x.c[1].w};
 #pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const uint32_t sb = (x.s >> (8 * g)) & 0xFFu;
-    const ByteTables tb = make_tables(sb);
-    const uint32_t words[4] = {x.c[g].x, x.c[g].y, x.c[g].z, x.c[g].w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t c = (uint32_t)(4 * g + u);  // chunk of 8 dims within the K-block
-      sts_v4(row + ((c ^ swz) << 4), decode8_direct(words[u], sb, tb));
+    for (int c = 0; c < 8; ++c)  // chunk of 8 dims within the K-block
+      sts_v4(row + (((uint32_t)c ^ swz) << 4), decode8_fast(words[c], c < 4 ? t0 : t1));
+  } else {
+    const uint32_t words[8] = {x.c[0].x, x.c[0].y, x.c[0].z, x.c[0].w,
+                               x.c[1].x, x.c[1].y, x.c[1].z, x.c[1].w};
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t sb = c < 4 ? sb0 : sb1;
+      sts_v4(row + (((uint32_t)c ^ swz) << 4),
+             sb - 2u <= 250u ? decode8_fast(words[c], make_tables(sb)) : decode8_slow(words[c], sb));
     }
   }
 }

@@ -105,10 +105,10 @@ __device__ __forceinline__ uint4 decode8(uint32_t c, uint32_t scale_byte, const 
   return r;
 }
 
-// As decode8, with the byte tables built in registers (no table in memory).
-__device__ __forceinline__ uint4 decode8_direct(uint32_t c, uint32_t scale_byte,
-                                                const ByteTables& t) {
-  if (scale_byte - 2u > 250u) return decode8_slow(c, scale_byte);
+// Eight codes of one group -> 16 bytes of bf16, by byte tables built in
+// registers (no table in memory); for a scale byte in [2, 252] only, which
+// the caller checks once per group.
+__device__ __forceinline__ uint4 decode8_fast(uint32_t c, const ByteTables& t) {
   const uint32_t c4 = c << 4;
   uint4 r;
   decode4<0>(c, c4, t, r.x, r.y);

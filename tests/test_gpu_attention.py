@@ -156,6 +156,46 @@ def test_growing_scores_exercise_the_output_rescale():
     _check(q, cache, idx, 2.0, 1, 1024, 1024, split=False)
 
 
+def test_scale_bytes_outside_the_permute_range():
+    """Scale bytes 0, 1, 253 and 254 (results subnormal, or within a factor 4
+    of the bf16 maximum) take the arithmetic decode instead of the byte
+    permutes. About a third of the rows get byte 0 or 1 in half their groups.
+    Rows 7, 135, 263 and 391 get byte 253 or 254 in four groups each (disjoint
+    between them), with codes limited to magnitudes up to 1.5 so that every
+    decoded value stays finite; each query's top-k holds one of them, and the
+    query (near 2**-112, which keeps q.k in range) has the signs of that
+    row's large values in its dims. Its logit then exceeds every other key's
+    by far more than 8 (log2 units), so it sets the running max when it
+    arrives and the unnormalised p.v sums stay below the fp32 maximum: the
+    output in its dims is its decoded values."""
+    rng = np.random.default_rng(20)
+    cache = _fill_cache(512, seed=21).reshape(512, 272)
+    for r in range(0, 512, 3):
+        groups = rng.choice(16, 8, replace=False)
+        cache[r, 256 + groups] = rng.integers(0, 2, 8)
+    huge = [7, 135, 263, 391]
+    for i, r in enumerate(huge):
+        for g in range(4 * i, 4 * i + 4):
+            cache[r, 256 + g] = 253 + (g & 1)
+            cache[r, 16 * g:16 * g + 16] &= 0xBB   # nibble magnitude index <= 3
+    cache = cache.reshape(-1)
+    z = np.abs(rng.standard_normal((4, 128, 512)))
+    z = np.maximum(z, 2.0 ** -10) * 2.0 ** -112 * rng.choice([-1.0, 1.0], (4, 128, 512))
+    for i, r in enumerate(huge):
+        codes = cache[r * 272 + 64 * i:r * 272 + 64 * i + 64]
+        nib = np.stack([codes & 15, codes >> 4], 1).reshape(-1)
+        z[i, :, 128 * i:128 * i + 128] = np.abs(z[i, :, 128 * i:128 * i + 128]) * np.where(
+            nib & 8, -1.0, 1.0)
+    q = workloads.f32_to_bf16_bits(z.astype(np.float32))
+    rest = np.setdiff1d(np.arange(512), huge)
+    idx = np.stack([rng.permutation(rest)[:150] for _ in range(4)]).astype(np.int64)
+    idx[0, 40], idx[1, 100], idx[2, 149], idx[3, 3] = huge
+    idx[1, ::37] = -1
+    for split in (True, False):
+        out, want = _check(q, cache, idx, 4e-5, 1, 512, 512, split=split)
+        assert np.all(np.isfinite(out)) and np.abs(want).max() > 2.0 ** 100
+
+
 @pytest.mark.parametrize("split", [True, False])
 def test_full_workload_128_queries_2048_keys(split):
     """The benchmark workload: 1,048,576-slot cache, 128 queries x 128 heads x
