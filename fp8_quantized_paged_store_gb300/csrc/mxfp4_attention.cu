@@ -57,6 +57,8 @@
 // exact bf16 inputs (the dequantized rows are exact); the probabilities are
 // rounded to bf16 for the p.v product while the normaliser sums them
 // unrounded; the output is rounded to bf16 once at the end.
+#include <cuda.h>
+
 #include <cstdint>
 
 #include "kvq.h"
@@ -99,6 +101,8 @@ constexpr size_t kSmemBytes = kSmemUsed + 1024;  // room to align the base to 10
 // released
 constexpr uint32_t kBarKFull = 0, kBarSFull = 32, kBarPFull = 64, kBarPvDone = 96;
 constexpr uint32_t kBarDrain = 128;
+constexpr uint32_t kBarQ = 136;  // Q's eight tensor-map boxes landed
+static_assert(kBarQ + 8 <= kOffTmemSlot - kOffBar, "mbarriers overlap the TMEM slot");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
@@ -108,6 +112,12 @@ constexpr uint32_t kColQ = 384;   // Q dims 0..255 as 128 columns of bf16 pairs
 constexpr uint32_t kWaitPolls = 1u << 22;
 
 struct AttnParams {
+  // Q as a [queries][num_heads][512] bf16 tensor map (boxes of 64 dims x 128
+  // heads, 128-byte swizzle, heads past num_heads read as zeros), valid when
+  // q_tma is set: Q in device memory and the map encoded. Otherwise Q is
+  // copied in 16-byte pieces.
+  CUtensorMap qmap;
+  int q_tma;
   const uint8_t* q;      // head h of query n at q + n * q_qstride + h * q_hstride (bytes)
   int64_t q_qstride, q_hstride;
   int64_t num_heads;
@@ -198,6 +208,22 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
+}
+
+// arrive once and expect `bytes` from asynchronous copies in this phase
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// one box of a 3-D tensor map into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -493,19 +519,24 @@ __device__ __forceinline__ void issue_pv(uint32_t st, int v, bool first, uint32_
 
 // ---------------------------------------------------------------- kernel ---
 
-// Q of query n into the operand buffers, once per CTA (not inlined: they run
-// once, and kept out of line they leave the roles' loops their registers).
-// load_q_smem, by threads [0, nthreads), 16 bytes per cp.async, all in
-// flight at once: dims 256..511 of head r into the swizzled K-major
-// shared-memory layout of the A operand, and dims 0..255 into a staging
-// area (head r's 32 chunks at stage + 512 r, chunk c at position
-// (c & ~7) | ((c ^ r) & 7), so that the eight lanes of a 16-byte load phase
-// below hit eight bank groups); zero rows past num_heads. load_q_tmem, by
-// the 128 softmax threads (warps 0-3, head = thread): the staged dims 0..255
-// into TMEM lane `head`, columns kColQ.. as bf16 pairs (the A operand of the
-// first 16 q.k steps).
-__device__ __forceinline__ uint32_t q_stage_pos(int r, int c) {
-  return (uint32_t)((c & ~7) | ((c ^ r) & 7)) << 4;
+// Q of query n into the operand buffers, once per CTA. Both halves take
+// the layout of the A operand of q.k, 128-byte-swizzled K-major: 64-dim
+// K-block kb of head r at base + kb * 16384 + r * 128, 16-byte chunk c of
+// that row at ((c ^ (r & 7)) << 4); dims 256..511 at q_base (read by the
+// MMAs), dims 0..255 staged at `stage` in the still empty key ring and
+// moved to tensor memory by the softmax threads (below). Eight tensor-map
+// boxes issued by one thread when Q is in device memory (they do not queue
+// behind the SM's outstanding-miss limit, as 8,192 separate 16-byte copies
+// do); otherwise load_q_smem: the same bytes by threads [0, nthreads), 16
+// bytes per cp.async, zero rows past num_heads. Neither is inlined: they run
+// once, and kept out of line they leave the roles' loops their registers.
+__device__ __noinline__ void load_q_boxes(const AttnParams& p, int64_t n, uint32_t q_base,
+                                          uint32_t stage, uint32_t bar) {
+  mbar_expect_tx(bar, 8 * kHeads * 128);
+#pragma unroll 1
+  for (int kb = 0; kb < 8; ++kb)
+    tma_load_3d((kb < 4 ? stage : q_base) + (uint32_t)(kb & 3) * (kHeads * 128), &p.qmap, 64 * kb,
+                0, (int)n, bar);
 }
 
 __device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_t q_base,
@@ -514,10 +545,8 @@ __device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_
   for (int id = tid; id < kHeads * 64; id += nthreads) {
     const int r = (id >> 5) & (kHeads - 1), c32 = id & 31;
     const bool hi = id >= kHeads * 32;
-    const uint32_t dst =
-        hi ? q_base + (uint32_t)(c32 >> 3) * (kHeads * 128) + (uint32_t)r * 128 +
-                 ((((uint32_t)c32 & 7) ^ ((uint32_t)r & 7)) << 4)
-           : stage + (uint32_t)r * 512 + q_stage_pos(r, c32);
+    const uint32_t dst = (hi ? q_base : stage) + (uint32_t)(c32 >> 3) * (kHeads * 128) +
+                         (uint32_t)r * 128 + ((((uint32_t)c32 & 7) ^ ((uint32_t)r & 7)) << 4);
     if (r < p.num_heads)
       cp_async_16a(dst, qn + r * p.q_hstride + (hi ? 512 : 0) + c32 * 16);
     else
@@ -528,15 +557,19 @@ __device__ __noinline__ void load_q_smem(const AttnParams& p, int64_t n, uint32_
   fence_proxy_async();
 }
 
+// By the 128 softmax threads (warps 0-3, head = thread): the staged dims
+// 0..255 into TMEM lane `head`, columns kColQ.. as bf16 pairs (the A operand
+// of the first 16 q.k steps). The eight lanes of a 16-byte load phase read
+// eight rows at eight different chunk positions: no bank conflicts.
 __device__ __noinline__ void load_q_tmem(uint32_t stage, uint32_t tmem, int tid) {
   const uint32_t lane_base = tmem + ((uint32_t)((tid >> 5) * 32) << 16);
-  const uint32_t row = stage + (uint32_t)tid * 512;
+  const uint32_t row = stage + (uint32_t)tid * 128, swz = (uint32_t)(tid & 7);
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t w[32];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint4 x = lds_v4_at(row + q_stage_pos(tid, 8 * c + k));
+      const uint4 x = lds_v4_at(row + (uint32_t)c * (kHeads * 128) + (((uint32_t)k ^ swz) << 4));
       w[4 * k] = x.x;
       w[4 * k + 1] = x.y;
       w[4 * k + 2] = x.z;
@@ -608,7 +641,8 @@ __device__ __forceinline__ void write_result(const AttnParams& p, int64_t n, int
 // kPiece: a chunk of a split unit, written as an fp32 partial; otherwise a
 // whole unit, written as the bf16 output (the same kernel otherwise).
 template <bool kPiece>
-__global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    mxfp4_attention_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t b = blockIdx.x;
@@ -675,8 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
       mbar_init(bars + kBarPvDone + 8 * s, 1);
     }
     mbar_init(bars + kBarDrain, 1);
+    mbar_init(bars + kBarQ, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (p.q_tma) load_q_boxes(p, n, q_base, k_base, bars + kBarQ);
   }
   // The producers issue their first kDepth tiles of row loads at once, while
   // the softmax and issuer warps (160 threads) load Q: the two start-up
@@ -690,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     for (int u = 0; u < kDepth; ++u)
       buf[u] = load_packed(p, u < n_tiles ? key_index(p, u, j, key_off, key_len) : -1, e);
     s_next = kDepth < n_tiles ? key_index(p, kDepth, j, key_off, key_len) : -1;
-  } else {
+  } else if (!p.q_tma) {
     // dims 0..255 staged in the key ring, which the producers fill only
     // after the second barrier below
     load_q_smem(p, n, q_base, k_base, tid < 128 ? tid : tid - 256, 160);
@@ -699,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) load_q_tmem(k_base, tmem, tid);
+  if (warp < 4 && (!p.q_tma || warp_wait(bars + kBarQ, 0, abort))) load_q_tmem(k_base, tmem, tid);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -733,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
     }
   } else if (warp == kIssuerWarp) {
     // --------------------------------------------------------------- issuer
-    if (lane == 0) {
+    if (lane == 0 && (!p.q_tma || mbar_wait(bars + kBarQ, 0, abort))) {
       const uint64_t q_desc = smem_desc(q_base, 16, 1024, 2);
       // Event-driven over the CTA's tiles: O += P(pi) V(pi) as soon as
       // softmax has written P(pi) (it frees a key stage, so it goes first);
@@ -861,6 +897,12 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp4_attention_kernel(AttnParams
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && p.q_tma) {
+    // the Q boxes have landed unless a wait for them timed out: then wait
+    // (bounded) for them before the CTA's shared memory is released
+    for (uint32_t i = 0; i < kWaitPolls && !mbar_test(bars + kBarQ, 0); ++i) {
+    }
+  }
   if (tid == 0 && *abort && p.status) atomicExch(p.status, 1);
   if (warp == kIssuerWarp) {
     tc_fence_after();
@@ -1059,8 +1101,55 @@ void split_layout(kvq::AttnParams& p, int64_t chunks, void* ws) {
   p.part_lse = p.part_o + p.grid * p.num_heads * kvq::kHalf;
 }
 
-int launch_attention(const kvq::AttnParams& p, cudaStream_t stream) {
+// cuTensorMapEncodeTiled through the runtime (no link to the driver
+// library), looked up once; null when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult found;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &found) != cudaSuccess ||
+        found != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// Q's tensor map: [queries][num_heads][512] bf16 with the caller's strides,
+// boxes of 64 dims x 128 heads x 1 query, 128-byte swizzle, out-of-range
+// heads read as zeros. Only for Q in device memory (a host-mapped Q keeps
+// the 16-byte copies); false when the map cannot be made.
+bool encode_q_map(kvq::AttnParams& p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p.q) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const EncodeTiledFn fn = encode_tiled();
+  if (a.type != cudaMemoryTypeDevice || !fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kvq::kDim, (cuuint64_t)p.num_heads, (cuuint64_t)p.nq};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.q_hstride, (cuuint64_t)p.q_qstride};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kvq::kHeads, 1};
+  const cuuint32_t unit[3] = {1, 1, 1};
+  return fn(&p.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(static_cast<const void*>(p.q)), dims, strides, box, unit,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch_attention(const kvq::AttnParams& params, cudaStream_t stream) {
   using namespace kvq;
+  AttnParams p = params;
+  p.q_tma = encode_q_map(p) ? 1 : 0;
   static int attr_done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ECUDA;
