@@ -593,20 +593,27 @@ __device__ __forceinline__ bool drain_mmas(uint32_t bar) {
 // One head's result (thread = head, O in TMEM lanes of this warp): the bf16
 // output row half or, for a chunk of a split unit (kPiece), the fp32 output
 // normalised by the chunk's softmax sum and that sum's log-sum-exp (log2
-// units) in CTA b's partial slot. Reads O out 16 columns at a time, which
-// keeps the softmax loop's live state in registers around it.
+// units) in CTA b's partial slot. O is read out 16 columns at a time, which
+// keeps the softmax loop's live state in registers around it. The bf16 row
+// (32 bytes per read) goes straight to memory. The fp32 row (64 bytes per
+// read, 1 KB per head) goes first into this warp's 32 rows of a staging
+// area in the idle key ring (16-byte chunk j of row r at ((j ^ (r & 7)) <<
+// 4): the eight lanes of a store phase hit eight bank groups); then the warp
+// writes each row with 16 bytes per lane, 512 contiguous bytes per store
+// instead of 32 separate rows (measured: faster for the fp32 partials,
+// slower for the bf16 rows).
 template <bool kPiece>
 __device__ __forceinline__ void write_result(const AttnParams& p, int64_t n, int v, int64_t b,
-                                             uint32_t lane_base, int h, float m_ref, float l) {
-  const bool store = h < p.num_heads;
+                                             uint32_t lane_base, uint32_t stage, int h, float m_ref,
+                                             float l) {
   const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-  uint8_t* orow = p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
-  float* prow = kPiece ? p.part_o + (b * p.num_heads + h) * kHalf : nullptr;
+  if constexpr (!kPiece) {
+    const bool store = h < p.num_heads;
+    uint8_t* orow = p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
 #pragma unroll 1
-  for (int c = 0; c < kHalf / 16; ++c) {
-    uint32_t o[16];
-    tmem_ld16(lane_base + kColO + 16 * c, o);
-    if (!kPiece) {
+    for (int c = 0; c < kHalf / 16; ++c) {
+      uint32_t o[16];
+      tmem_ld16(lane_base + kColO + 16 * c, o);
       uint32_t w[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -619,23 +626,42 @@ __device__ __forceinline__ void write_result(const AttnParams& p, int64_t n, int
           st_v4(orow + 32 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
                                                     w[4 * u + 3]));
       }
-    } else if (store) {
+    }
+    if (store && v == 0 && p.lse)
+      p.lse[n * p.num_heads + h] =
+          l > 0.0f ? (m_ref + log2f(l)) * 0.69314718055994531f : -__int_as_float(0x7F800000);
+  } else {
+    constexpr uint32_t kRowBytes = kHalf * 4;
+    const int lane = h & 31;
+    const uint32_t wrow = stage + (uint32_t)(h >> 5) * 32 * kRowBytes;  // this warp's rows
+    const uint32_t mine = wrow + (uint32_t)lane * kRowBytes, swz = (uint32_t)(lane & 7);
+#pragma unroll 1
+    for (int c = 0; c < kHalf / 16; ++c) {
+      uint32_t o[16];
+      tmem_ld16(lane_base + kColO + 16 * c, o);
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        st_v4(prow + 16 * c + 4 * u,
-              make_uint4(__float_as_uint(__uint_as_float(o[4 * u]) * inv),
-                         __float_as_uint(__uint_as_float(o[4 * u + 1]) * inv),
-                         __float_as_uint(__uint_as_float(o[4 * u + 2]) * inv),
-                         __float_as_uint(__uint_as_float(o[4 * u + 3]) * inv)));
+        sts_v4(mine + ((((uint32_t)(4 * c + u)) ^ swz) << 4),
+               make_uint4(__float_as_uint(__uint_as_float(o[4 * u]) * inv),
+                          __float_as_uint(__uint_as_float(o[4 * u + 1]) * inv),
+                          __float_as_uint(__uint_as_float(o[4 * u + 2]) * inv),
+                          __float_as_uint(__uint_as_float(o[4 * u + 3]) * inv)));
     }
+    __syncwarp();
+    const int64_t h0 = h - lane;  // this warp's first head
+#pragma unroll 1
+    for (int r = 0; r < 32 && h0 + r < p.num_heads; ++r) {
+      const uint32_t src = wrow + (uint32_t)r * kRowBytes, rs = (uint32_t)(r & 7);
+      float* prow = p.part_o + (b * p.num_heads + h0 + r) * kHalf;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t j = (uint32_t)(lane + 32 * u);
+        st_v4(prow + 4 * j, lds_v4_at(src + ((j ^ rs) << 4)));
+      }
+    }
+    if (h < p.num_heads)
+      p.part_lse[b * p.num_heads + h] = l > 0.0f ? m_ref + log2f(l) : -__int_as_float(0x7F800000);
   }
-  if (!store) return;
-  const float lse2 = l > 0.0f ? m_ref + log2f(l) : -__int_as_float(0x7F800000);
-  if (kPiece)
-    p.part_lse[b * p.num_heads + h] = lse2;
-  else if (v == 0 && p.lse)
-    p.lse[n * p.num_heads + h] =
-        l > 0.0f ? lse2 * 0.69314718055994531f : -__int_as_float(0x7F800000);
 }
 
 // kPiece: a chunk of a split unit, written as an fp32 partial; otherwise a
@@ -646,6 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t b = blockIdx.x;
+  // the merge (launched as this grid's programmatic dependent) may be
+  // scheduled once every CTA of this grid has started; it waits for the
+  // whole grid before it reads a partial
+  if constexpr (kPiece) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // this CTA's unit (query n, value half v) and run of indices: chunk
   // b % chunks of a row of the fixed layout, or the query's ragged run. The
   // grid and the chunk count fit 32 bits (a 64-bit division here, a runtime
@@ -891,7 +921,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the result: wait for the last p.v, then read O out
         if (!warp_wait(bars + kBarPvDone + 8 * st, (uint32_t)((i / kStages) & 1), abort)) break;
         tc_fence_after();
-        write_result<kPiece>(p, n, v, b, lane_base, tid, m_ref, l);
+        // the key ring is idle: every p.v has completed
+        write_result<kPiece>(p, n, v, b, lane_base, k_base, tid, m_ref, l);
       }
     }
   }
@@ -926,6 +957,10 @@ constexpr int kMergeFew = 4;
 __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_kernel(AttnParams p) {
   __shared__ float head_l[kMergeHeads][2], head_w[kMergeHeads][2];
   extern __shared__ float merge_dyn[];  // [kMergeHeads][chunks]: log-sum-exp, then weight
+  // launched as the split grid's programmatic dependent: the block may be
+  // resident while that grid still runs, and waits here for all of it (and
+  // its memory) to complete; a no-op for an ordinary launch
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t unit = blockIdx.x;
   const int pieces = (int)p.chunks;
   const int64_t b0 = unit * p.chunks;  // the unit's first CTA
@@ -1171,7 +1206,23 @@ int launch_attention(const kvq::AttnParams& params, cudaStream_t stream) {
   if (rc != KVQ_OK || !p.part_o) return rc;
   const dim3 mgrid((unsigned)p.units, (unsigned)((p.num_heads + kMergeHeads - 1) / kMergeHeads));
   const size_t dyn = p.chunks > kMergeFew ? (size_t)kMergeHeads * (size_t)p.chunks * 4 : 0;
-  mxfp4_attention_merge_kernel<<<mgrid, 64 * kMergeHeads, dyn, stream>>>(p);
+  // a programmatic dependent launch: the merge's launch latency overlaps the
+  // attention grid's tail (every attention CTA is resident from the start: a
+  // split grid has at most one CTA per SM)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = mgrid;
+  cfg.blockDim = dim3(64 * kMergeHeads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mxfp4_attention_merge_kernel, p) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ECUDA;
+  }
   return launch_status();
 }
 
