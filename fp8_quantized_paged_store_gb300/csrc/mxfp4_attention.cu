@@ -17,8 +17,14 @@
 // u * chunks ..): the CTA writes an fp32 partial, the output of its chunk
 // normalised by the chunk's own softmax sum and that sum's log-sum-exp,
 // into the caller's workspace, and a second, small kernel combines each
-// unit's partials by their log-sum-exps. A CTA's work is one contiguous run
-// of one unit either way.
+// unit's partials by their log-sum-exps (launched as a programmatic
+// dependent of the first, so its launch overlaps the first grid's tail). A
+// CTA's work is one contiguous run of one unit either way.
+//
+// Start-up: one thread loads Q with eight tensor-map boxes (TMA) into the
+// two swizzled operand layouts, while the producers issue their first row
+// loads; the first half of Q is staged in the still empty key ring and
+// moved to tensor memory by the softmax warps.
 //
 // Each CTA: tensor memory (512 columns x 128 lanes,
 // lane = head) holds the output accumulator (256 columns), four 32-key score
@@ -29,8 +35,9 @@
 // The other 256 dims of Q stay in shared memory next to four 32 KB key tiles
 // of 32 keys (a ring of four stages). Three groups of warps run as a
 // pipeline through mbarriers:
-//   - producers (warps 4-11, lane = key, warp 4+e = dims [64e, 64e + 64)):
-//     load the packed rows three tiles ahead into registers (pads and
+//   - producers (warps 4-11; a lane takes one key of the tile and one
+//     64-dim K-block, a warp 8 keys x 4 K-blocks):
+//     load the packed rows two tiles ahead into registers (pads and
 //     out-of-range indices load nothing and decode to zero rows),
 //     dequantize them with byte permutes into a 128-byte-swizzled K-major
 //     bf16 key tile, and arrive on its "full" barrier; a stage is reused once
@@ -46,7 +53,9 @@
 //   - softmax (warps 0-3, one head per thread): read S(t), run the online
 //     softmax in fp32 (exp2, running max with a rescale of the output only
 //     when the max grows by more than 2**8), and store P (bf16 pairs) into
-//     tensor memory.
+//     tensor memory; after the last tile, read O out of tensor memory and
+//     write the result (an fp32 partial through a staging area in the idle
+//     key ring, so that the stores are whole 512-byte runs).
 // Every wait is bounded; a timeout sets a CTA-wide abort flag that ends the
 // other roles' waits, and the CTA reports through an optional status word.
 // Before tensor memory is released, the issuing thread waits (bounded, abort
@@ -77,7 +86,7 @@ constexpr int kHalf = 256;      // output columns per CTA
 constexpr int kThreads = 416;   // softmax warps 0-3, producers 4-11, issuer 12
 constexpr int kIssuerWarp = 12;
 constexpr int kRow = 272;       // packed row bytes
-constexpr int kDepth = 3;       // tiles a producer has in flight
+constexpr int kDepth = 2;       // tiles a producer has in flight (three: 1.3% slower)
 
 constexpr uint32_t kQhiBytes = kHeads * 256 * 2;         // dims 256..511: 4 K-blocks x 128 rows
 constexpr uint32_t kKBytes = kTileKeys * kDim * 2;       // 8 K-blocks x 32 rows x 128 B
@@ -437,8 +446,8 @@ __device__ __forceinline__ Packed load_packed(const AttnParams& p, int64_t s, in
 // Dims [64e, 64e + 64) (K-block e) of key j into the stage whose K-block 0
 // is at `kbuf`, 128-byte-swizzled K-major: element (key j, dim d) at
 // kb*kKBlockStride + j*128 + ((c ^ (j & 7)) << 4) + 2*(d & 7), kb = d / 64,
-// c = (d % 64) / 8. With lane = key, each 8-lane phase of a 16-byte store
-// covers eight keys and all eight bank groups.
+// c = (d % 64) / 8. The eight lanes of a 16-byte store phase hold eight
+// consecutive keys of one K-block, so they cover all eight bank groups.
 // The range check of the two scale bytes is made once, so that the common
 // case is one branch-free run of sixteen independent permute chains.
 __device__ __forceinline__ void dequant_share(const Packed& x, uint32_t kbuf, int j, int e) {
@@ -748,7 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the softmax and issuer warps (160 threads) load Q: the two start-up
   // latencies overlap.
   const bool producer = warp >= 4 && warp < kIssuerWarp;
-  const int e = warp - 4, j = lane;
+  // producer lane: key j of the tile, dims [64e, 64e + 64); warp 4 + w takes
+  // keys 8 (w % 4) .. + 7 and K-blocks 4 (w / 4) .. + 3, so that a 16-byte
+  // load instruction touches 8 rows (not 32) and a store phase 8 keys
+  const int e = 4 * ((warp - 4) >> 2) + (lane >> 3), j = 8 * ((warp - 4) & 3) + (lane & 7);
   Packed buf[kDepth];
   int64_t s_next = -1;
   if (producer) {
@@ -772,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (producer) {
     // ------------------------------------------------------------ producers
-    // Lane = key of the tile, warp 4 + e = dims [64e, 64e + 64). The CTA's
+    // Lane = key j of the tile, dims [64e, 64e + 64). The CTA's
     // i-th tile goes to stage i % kStages, free once the p.v of tile
     // i - kStages has completed; rows are loaded kDepth tiles ahead.
     bool live = true;
