@@ -425,7 +425,13 @@ int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks, int64_t b
  * Arithmetic: bf16 inputs, fp32 accumulation on the tensor cores, fp32
  * softmax with exp2, probabilities rounded to bf16 for the p.v product, the
  * output rounded to bf16 once: |out - exact| is within about 2**-8 of
- * sum_j softmax(s)_j |k_j[d]| plus the final bf16 rounding.
+ * sum_j softmax(s)_j |k_j[d]| plus the final bf16 rounding. Range: the
+ * softmax rescales its output accumulator only when a head's running max
+ * grows by more than 32 (log2 units), so the unnormalised fp32 sums reach
+ * (number of valid keys) x 2**32 x max|k|: the result is exact in the sense
+ * above while that stays below 2**128: for 2048 keys, |k| < 2**85, which
+ * every row whose scale bytes are at most 209 meets (a dequantized value is
+ * at most 6 x 2**(scale byte - 127)).
  *
  * q_bf16           bf16; head h of query n at element
  *                  n*q_query_stride + h*q_head_stride (both multiples of 8,

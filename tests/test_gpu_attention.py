@@ -144,7 +144,9 @@ def test_queries_without_valid_keys_and_empty_topk():
 
 def test_growing_scores_exercise_the_output_rescale():
     """Keys ordered by increasing score with a large scale: the running max
-    grows by more than 2**8 (log2 units) from tile to tile several times."""
+    grows by more than the kernel's rescale threshold (32 log2 units) from
+    tile to tile: at least once for 99 of the 128 heads, three times for
+    head 0."""
     cache = _fill_cache(1024, seed=10)
     q = _queries(11, 1, 128)
     rows = oracle.mxfp4_mla_gather_dequant(cache, 1, 1024, 1024, np.arange(1024, dtype=np.int64))
@@ -165,9 +167,10 @@ def test_scale_bytes_outside_the_permute_range():
     decoded value stays finite; each query's top-k holds one of them, and the
     query (near 2**-112, which keeps q.k in range) has the signs of that
     row's large values in its dims. Its logit then exceeds every other key's
-    by far more than 8 (log2 units), so it sets the running max when it
-    arrives and the unnormalised p.v sums stay below the fp32 maximum: the
-    output in its dims is its decoded values."""
+    by at least 61 (log2 units), more than the kernel's rescale threshold of
+    32, so it sets the running max when it arrives and the unnormalised p.v
+    sums stay below the fp32 maximum: the output in its dims is its decoded
+    values."""
     rng = np.random.default_rng(20)
     cache = _fill_cache(512, seed=21).reshape(512, 272)
     for r in range(0, 512, 3):
