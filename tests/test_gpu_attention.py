@@ -252,6 +252,61 @@ def test_rejects_bad_arguments_on_gpu():
         kvq.mxfp4_mla_sparse_attention(q[:, :4], cache, idx, float("nan"))
 
 
+def test_split_and_unsplit_replay_in_a_cuda_graph():
+    """Both schedules captured in a CUDA graph (the split one is two
+    launches, the merge a programmatic dependent of the attention grid; Q is
+    read through a tensor map passed by value) replay to the eager bits, and
+    follow the query buffer when it is overwritten in place."""
+    dev = torch.device("cuda", 0)
+    cache = torch.from_numpy(_fill_cache(4096, seed=30)).to(dev)
+    rng = np.random.default_rng(31)
+    idx = torch.from_numpy(np.stack([rng.permutation(4096)[:2048] for _ in range(4)])).to(dev)
+    q = torch.from_numpy(_queries(32, 4, 128).view(np.int16)).to(dev).view(torch.bfloat16)
+    q2 = torch.from_numpy(_queries(33, 4, 128).view(np.int16)).to(dev).view(torch.bfloat16)
+    ws = torch.empty(kvq.attention_workspace_size(4, 128, 2048), dtype=torch.uint8, device=dev)
+    assert ws.numel() > 0  # 4 queries x 2048 keys split
+    for w in (ws, False):
+        out = torch.empty((4, 128, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((4, 128), dtype=torch.float32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def call():
+            kvq.mxfp4_mla_sparse_attention(q, cache, idx, 0.05, out=out, lse=lse, status=status,
+                                           workspace=w)
+
+        call()
+        torch.cuda.synchronize()
+        want_o, want_l = out.clone(), lse.clone()
+        q_saved = q.clone()
+        q.copy_(q2)
+        call()
+        torch.cuda.synchronize()
+        want_o2, want_l2 = out.clone(), lse.clone()
+        q.copy_(q_saved)
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            call()  # warm-up on the capture stream
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        out.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), want_o.view(torch.int16))
+        assert torch.equal(lse, want_l)
+        q.copy_(q2)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), want_o2.view(torch.int16))
+        assert torch.equal(lse, want_l2)
+        assert int(status.item()) == 0
+        q.copy_(q_saved)
+
+
 def _check_ragged(q, cache, runs, sm_scale, num_slots, first_offset=0, extra_tail=0):
     """Ragged runs against the oracle on the same runs padded with -1 into
     [num_queries, longest run]: pads are dropped, so the two are the same
