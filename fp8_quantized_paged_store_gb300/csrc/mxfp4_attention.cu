@@ -766,9 +766,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (p.q_tma) load_q_boxes(p, n, q_base, k_base, bars + kBarQ);
   }
-  // The producers issue their first kDepth tiles of row loads at once, while
-  // the softmax and issuer warps (160 threads) load Q: the two start-up
-  // latencies overlap.
+  // The producers issue their first kDepth tiles of row loads at once while
+  // Q is on its way (the tensor-map boxes issued above, or, for a
+  // host-mapped Q, the copies of the softmax and issuer warps' 160 threads):
+  // the two start-up latencies overlap.
   const bool producer = warp >= 4 && warp < kIssuerWarp;
   // producer lane: key j of the tile, dims [64e, 64e + 64); warp 4 + w takes
   // keys 8 (w % 4) .. + 7 and K-blocks 4 (w / 4) .. + 3, so that a 16-byte
