@@ -252,6 +252,35 @@ def test_rejects_bad_arguments_on_gpu():
         kvq.mxfp4_mla_sparse_attention(q[:, :4], cache, idx, float("nan"))
 
 
+def test_one_query_broadcast_with_query_stride_zero():
+    """Every query the same row of memory (query stride 0: a view made by
+    expand): the tensor map of Q then has a zero stride, or, if it cannot be
+    made, Q is copied in 16-byte pieces; each query's output must match the
+    oracle on its own indices, and equal ones for equal index rows."""
+    dev = torch.device("cuda", 0)
+    cache_np = _fill_cache(2048, seed=40)
+    cache = torch.from_numpy(cache_np).to(dev)
+    rng = np.random.default_rng(41)
+    idx_np = np.stack([rng.permutation(2048)[:300] for _ in range(3)]).astype(np.int64)
+    idx_np = np.concatenate([idx_np, idx_np[:1]])  # query 3 repeats query 0's indices
+    q1 = _queries(42, 1, 96)
+    qd = torch.from_numpy(q1.view(np.int16)).to(dev).view(torch.bfloat16).expand(4, 96, 512)
+    assert qd.stride(0) == 0
+    for split in (True, False):
+        lse = torch.empty((4, 96), dtype=torch.float32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        out, _ = kvq.mxfp4_mla_sparse_attention(qd, cache, torch.from_numpy(idx_np).to(dev), 0.05,
+                                                lse=lse, status=status, workspace=split)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        o = out.float().cpu().numpy().astype(np.float64)
+        want, want_lse, mass = attn_oracle(np.repeat(q1, 4, axis=0), cache_np, 1, 2048, 2048,
+                                           idx_np, 0.05)
+        assert np.all(np.abs(o - want) <= 2.0 ** -7 * (mass + np.abs(want)) + 2.0 ** -100)
+        np.testing.assert_allclose(lse.cpu().numpy(), want_lse, rtol=0, atol=2e-3)
+        assert torch.equal(out[3].view(torch.int16), out[0].view(torch.int16))
+
+
 def test_split_and_unsplit_replay_in_a_cuda_graph():
     """Both schedules captured in a CUDA graph (the split one is two
     launches, the merge a programmatic dependent of the attention grid; Q is

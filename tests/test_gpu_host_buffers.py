@@ -132,22 +132,26 @@ def test_ring_rows_into_host_state():
     assert np.array_equal(state_h.numpy().view(np.uint32), want.view(np.uint32))
 
 
-def test_attention_query_and_output_on_host():
+@pytest.mark.parametrize("heads", [128, 48])
+def test_attention_query_and_output_on_host(heads):
     """Sparse attention with the queries read from and the output and lse
     written to pinned host memory (packed cache and indices on the device):
-    the same bits as with every buffer on the device."""
-    w = workloads.sparse_attention(seed=3, num_queries=8, num_heads=128, topk=256,
+    the same bits as with every buffer on the device. A host-mapped query
+    is copied in 16-byte pieces that zero the rows past num_heads
+    themselves; a device one arrives by tensor-map boxes whose out-of-range
+    rows read as zeros: 48 heads compare the two."""
+    w = workloads.sparse_attention(seed=3, num_queries=8, num_heads=heads, topk=256,
                                    num_slots=16_384)
     cache = torch.zeros(16_384 * ROW, dtype=torch.uint8, device=G.DEV)
     kvq.mxfp4_mla_store(G.bf16_dev(w["fill_latent"]), G.to_dev(w["fill_slots"]), cache)
     idx = G.to_dev(w["indices"])
-    q_np = w["q"].reshape(8, 128, 512)
+    q_np = w["q"].reshape(8, heads, 512)
     status = torch.zeros(1, dtype=torch.int32, device=G.DEV)
-    lse_d = torch.empty((8, 128), dtype=torch.float32, device=G.DEV)
+    lse_d = torch.empty((8, heads), dtype=torch.float32, device=G.DEV)
     out_d, _ = kvq.mxfp4_mla_sparse_attention(G.bf16_dev(q_np), cache, idx, w["sm_scale"],
                                               lse=lse_d, status=status)
     q_h = _pinned(q_np.view(np.int16)).view(torch.bfloat16)
-    lse_h = torch.empty((8, 128), dtype=torch.float32).pin_memory()
+    lse_h = torch.empty((8, heads), dtype=torch.float32).pin_memory()
     out_h, _ = kvq.mxfp4_mla_sparse_attention(q_h, cache, idx, w["sm_scale"], lse=lse_h,
                                               status=status)
     torch.cuda.synchronize()
