@@ -33,8 +33,8 @@
 // first 256 dims of Q as bf16 pairs (128): the q.k products over those dims
 // take Q from tensor memory and read only the key tile from shared memory.
 // The other 256 dims of Q stay in shared memory next to four 32 KB key tiles
-// of 32 keys (a ring of four stages). Three groups of warps run as a
-// pipeline through mbarriers:
+// of 32 keys (a ring of four stages). Four roles run as a pipeline through
+// mbarriers:
 //   - producers (warps 4-11; a lane takes one key of the tile and one
 //     64-dim K-block, a warp 8 keys x 4 K-blocks):
 //     load the packed rows two tiles ahead into registers (pads and
@@ -42,14 +42,17 @@
 //     dequantize them with byte permutes into a 128-byte-swizzled K-major
 //     bf16 key tile, and arrive on its "full" barrier; a stage is reused once
 //     the p.v that last read it has completed;
-//   - the issuer (warp 12, one thread), event-driven: O += P(u) V(u)
-//     (M 128, N 256, K 32; V is the key tile read MN-major) as soon as
-//     softmax has written P(u), else S = Q K^T over two tiles at once
+//   - the q.k issuer (warp 12, one thread): S = Q K^T over two tiles at once
 //     (M 128, N 64, K 512: the ring is laid out K-block-major, so the same
 //     K-block of two neighbouring stages is one 64-row operand) once both
-//     are written and the p.v that last read their tensor-memory columns has
-//     been issued (MMAs from one thread run in order); tcgen05.commit on
-//     mbarriers tracks completion;
+//     are written; a stage's keys are rewritten only after the p.v of the
+//     tile four back has completed, so the score columns it overwrites are
+//     free;
+//   - the p.v issuer (warp 13, one thread): O += P(u) V(u) (M 128, N 256,
+//     K 32; V is the key tile read MN-major) as soon as softmax has written
+//     P(u). Two issuers, so that a p.v never waits behind the 32 MMAs of a
+//     q.k pair (one thread issuing both took ~1K cycles to react to P);
+//     tcgen05.commit on mbarriers tracks completion;
 //   - softmax (warps 0-3, one head per thread): read S(t), run the online
 //     softmax in fp32 (exp2, running max with a rescale of the output only
 //     when the max grows by more than 2**32), and store P (bf16 pairs) into
@@ -58,7 +61,7 @@
 //     key ring, so that the stores are whole 512-byte runs).
 // Every wait is bounded; a timeout sets a CTA-wide abort flag that ends the
 // other roles' waits, and the CTA reports through an optional status word.
-// Before tensor memory is released, the issuing thread waits (bounded, abort
+// Before tensor memory is released, each issuing thread waits (bounded, abort
 // or not) for every MMA it issued, so that none writes released tensor
 // memory or arrives on a released barrier.
 //
@@ -83,8 +86,9 @@ constexpr int kDim = 512;       // latent width (score depth)
 constexpr int kTileKeys = 32;   // MMA N of q.k, K of p.v
 constexpr int kStages = 4;      // key tiles (and score / probability buffers) in the ring
 constexpr int kHalf = 256;      // output columns per CTA
-constexpr int kThreads = 416;   // softmax warps 0-3, producers 4-11, issuer 12
+constexpr int kThreads = 448;   // softmax 0-3, producers 4-11, q.k issuer 12, p.v issuer 13
 constexpr int kIssuerWarp = 12;
+constexpr int kPvWarp = 13;
 constexpr int kRow = 272;       // packed row bytes
 constexpr int kDepth = 2;       // tiles a producer has in flight (three: 1.3% slower)
 
@@ -106,12 +110,13 @@ constexpr uint32_t kSmemUsed = kOffAbort + 16;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
 
 // mbarriers, one of each per stage (the CTA's i-th tile uses stage i % kStages),
-// then one the issuer commits its last MMAs to before tensor memory is
-// released
+// then one per issuer that it commits its last MMAs to before tensor memory
+// is released, and Q's
 constexpr uint32_t kBarKFull = 0, kBarSFull = 32, kBarPFull = 64, kBarPvDone = 96;
-constexpr uint32_t kBarDrain = 128;
-constexpr uint32_t kBarQ = 136;  // Q's eight tensor-map boxes landed
-static_assert(kBarQ + 8 <= kOffTmemSlot - kOffBar, "mbarriers overlap the TMEM slot");
+constexpr uint32_t kBarDrain = 128;   // the q.k issuer's drain
+constexpr uint32_t kBarQ = 136;       // Q's eight tensor-map boxes landed
+constexpr uint32_t kBarDrain2 = 144;  // the p.v issuer's drain
+static_assert(kBarDrain2 + 8 <= kOffTmemSlot - kOffBar, "mbarriers overlap the TMEM slot");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
@@ -762,6 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bars + kBarDrain, 1);
     mbar_init(bars + kBarQ, 1);
+    mbar_init(bars + kBarDrain2, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (p.q_tma) load_q_boxes(p, n, q_base, k_base, bars + kBarQ);
@@ -824,57 +830,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kIssuerWarp) {
-    // --------------------------------------------------------------- issuer
+    // ------------------------------------------------------- q.k issuer
+    // S = Q K^T of tile qi (with tile qi + 1 when qi's stage is even) once
+    // its keys are written. A stage's keys are rewritten only after the p.v
+    // of the tile four back has completed, so its score columns are free.
     if (lane == 0 && (!p.q_tma || mbar_wait(bars + kBarQ, 0, abort))) {
       const uint64_t q_desc = smem_desc(q_base, 16, 1024, 2);
-      // Event-driven over the CTA's tiles: O += P(pi) V(pi) as soon as
-      // softmax has written P(pi) (it frees a key stage, so it goes first);
-      // else q.k of tile qi (with tile qi + 1 when qi's stage is even) once
-      // its keys are written and the p.v that last read its tensor-memory
-      // columns has been issued (MMAs from this thread run in order).
-      int64_t qi = 0, pi = 0;
-      uint32_t idle = 0;
-      while (pi < n_tiles) {
-        bool progress = false;
-        if (pi < qi && mbar_test(bars + kBarPFull + 8 * (uint32_t)(pi % kStages),
-                                 (uint32_t)((pi / kStages) & 1))) {
-          tc_fence_after();
-          issue_pv((uint32_t)(pi % kStages), v, pi == 0, k_base, tmem);
-          mma_commit(bars + kBarPvDone + 8 * (uint32_t)(pi % kStages));
-          ++pi;
-          progress = true;
-        }
-        if (!progress && qi < n_tiles) {
-          const uint32_t st = (uint32_t)(qi % kStages);
-          const bool pair = (st & 1u) == 0 && qi + 1 < n_tiles;
-          if (qi + (pair ? 1 : 0) - pi < kStages &&
-              mbar_test(bars + kBarKFull + 8 * st, (uint32_t)((qi / kStages) & 1)) &&
-              (!pair || mbar_test(bars + kBarKFull + 8 * (st + 1),
-                                  (uint32_t)(((qi + 1) / kStages) & 1)))) {
-            tc_fence_after();
-            if (pair) {
-              issue_qk<true>(st, q_desc, k_base, tmem);
-              mma_commit(bars + kBarSFull + 8 * st);
-              mma_commit(bars + kBarSFull + 8 * (st + 1));
-              qi += 2;
-            } else {
-              issue_qk<false>(st, q_desc, k_base, tmem);
-              mma_commit(bars + kBarSFull + 8 * st);
-              qi += 1;
-            }
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle = 0;
-        } else if (++idle >= kWaitPolls) {
-          *abort = 1;
+      for (int64_t qi = 0; qi < n_tiles;) {
+        const uint32_t st = (uint32_t)(qi % kStages);
+        const bool pair = (st & 1u) == 0 && qi + 1 < n_tiles;
+        if (!mbar_wait(bars + kBarKFull + 8 * st, (uint32_t)((qi / kStages) & 1), abort)) break;
+        if (pair && !mbar_wait(bars + kBarKFull + 8 * (st + 1),
+                               (uint32_t)(((qi + 1) / kStages) & 1), abort))
           break;
-        } else if ((idle & 31u) == 31u && *abort) {
-          break;
+        tc_fence_after();
+        if (pair) {
+          issue_qk<true>(st, q_desc, k_base, tmem);
+          mma_commit(bars + kBarSFull + 8 * st);
+          mma_commit(bars + kBarSFull + 8 * (st + 1));
+          qi += 2;
+        } else {
+          issue_qk<false>(st, q_desc, k_base, tmem);
+          mma_commit(bars + kBarSFull + 8 * st);
+          qi += 1;
         }
       }
       if (!drain_mmas(bars + kBarDrain)) *abort = 1;
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------- p.v issuer
+    // O += P(pi) V(pi) as soon as softmax has written P(pi).
+    if (lane == 0) {
+      for (int64_t pi = 0; pi < n_tiles; ++pi) {
+        const uint32_t st = (uint32_t)(pi % kStages);
+        if (!mbar_wait(bars + kBarPFull + 8 * st, (uint32_t)((pi / kStages) & 1), abort)) break;
+        tc_fence_after();
+        issue_pv(st, v, pi == 0, k_base, tmem);
+        mma_commit(bars + kBarPvDone + 8 * st);
+      }
+      if (!drain_mmas(bars + kBarDrain2)) *abort = 1;
     }
     __syncwarp();
   } else {
