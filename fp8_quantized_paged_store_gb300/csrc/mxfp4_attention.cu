@@ -35,20 +35,22 @@
 // The other 256 dims of Q stay in shared memory next to four 32 KB key tiles
 // of 32 keys (a ring of four stages). Four roles run as a pipeline through
 // mbarriers:
-//   - producers (warps 4-11; a lane takes one key of the tile and one
-//     64-dim K-block, a warp 8 keys x 4 K-blocks):
-//     load the packed rows two tiles ahead into registers (pads and
+//   - producers (warps 4-19, two groups of 8: warps 4-11 take the even
+//     tiles, 12-19 the odd ones, so that each warp has two tile periods
+//     for a tile's work; a lane takes one key of the tile and one 64-dim
+//     K-block, a warp 8 keys x 4 K-blocks):
+//     load the packed rows two of its tiles ahead into registers (pads and
 //     out-of-range indices load nothing and decode to zero rows),
 //     dequantize them with byte permutes into a 128-byte-swizzled K-major
 //     bf16 key tile, and arrive on its "full" barrier; a stage is reused once
 //     the p.v that last read it has completed;
-//   - the q.k issuer (warp 12, one thread): S = Q K^T over two tiles at once
+//   - the q.k issuer (warp 20, one thread): S = Q K^T over two tiles at once
 //     (M 128, N 64, K 512: the ring is laid out K-block-major, so the same
 //     K-block of two neighbouring stages is one 64-row operand) once both
 //     are written; a stage's keys are rewritten only after the p.v of the
 //     tile four back has completed, so the score columns it overwrites are
 //     free;
-//   - the p.v issuer (warp 13, one thread): O += P(u) V(u) (M 128, N 256,
+//   - the p.v issuer (warp 21, one thread): O += P(u) V(u) (M 128, N 256,
 //     K 32; V is the key tile read MN-major) as soon as softmax has written
 //     P(u). Two issuers, so that a p.v never waits behind the 32 MMAs of a
 //     q.k pair (one thread issuing both took ~1K cycles to react to P);
@@ -86,9 +88,9 @@ constexpr int kDim = 512;       // latent width (score depth)
 constexpr int kTileKeys = 32;   // MMA N of q.k, K of p.v
 constexpr int kStages = 4;      // key tiles (and score / probability buffers) in the ring
 constexpr int kHalf = 256;      // output columns per CTA
-constexpr int kThreads = 448;   // softmax 0-3, producers 4-11, q.k issuer 12, p.v issuer 13
-constexpr int kIssuerWarp = 12;
-constexpr int kPvWarp = 13;
+constexpr int kThreads = 704;   // softmax 0-3, producers 4-19 (two groups), q.k issuer 20, p.v issuer 21
+constexpr int kIssuerWarp = 20;
+constexpr int kPvWarp = 21;
 constexpr int kRow = 272;       // packed row bytes
 constexpr int kDepth = 2;       // tiles a producer has in flight (three: 1.3% slower)
 
@@ -774,24 +776,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // The producers issue their first kDepth tiles of row loads at once while
   // Q is on its way (the tensor-map boxes issued above, or, for a
-  // host-mapped Q, the copies of the softmax and issuer warps' 160 threads):
+  // host-mapped Q, the copies of the softmax and q.k issuer warps' 160
+  // threads):
   // the two start-up latencies overlap.
   const bool producer = warp >= 4 && warp < kIssuerWarp;
-  // producer lane: key j of the tile, dims [64e, 64e + 64); warp 4 + w takes
-  // keys 8 (w % 4) .. + 7 and K-blocks 4 (w / 4) .. + 3, so that a 16-byte
-  // load instruction touches 8 rows (not 32) and a store phase 8 keys
-  const int e = 4 * ((warp - 4) >> 2) + (lane >> 3), j = 8 * ((warp - 4) & 3) + (lane & 7);
+  // producer lane: key j of the tile, dims [64e, 64e + 64); warp 4 + 8 g + w
+  // (group g: tiles of parity g) takes keys 8 (w % 4) .. + 7 and K-blocks
+  // 4 (w / 4) .. + 3, so that a 16-byte load instruction touches 8 rows
+  // (not 32) and a store phase 8 keys
+  const int grp = ((warp - 4) >> 3) & 1, pw = (warp - 4) & 7;
+  const int e = 4 * (pw >> 2) + (lane >> 3), j = 8 * (pw & 3) + (lane & 7);
   Packed buf[kDepth];
   int64_t s_next = -1;
   if (producer) {
 #pragma unroll
     for (int u = 0; u < kDepth; ++u)
-      buf[u] = load_packed(p, u < n_tiles ? key_index(p, u, j, key_off, key_len) : -1, e);
-    s_next = kDepth < n_tiles ? key_index(p, kDepth, j, key_off, key_len) : -1;
+      buf[u] = load_packed(p, grp + 2 * u < n_tiles ? key_index(p, grp + 2 * u, j, key_off, key_len) : -1, e);
+    s_next = grp + 2 * kDepth < n_tiles ? key_index(p, grp + 2 * kDepth, j, key_off, key_len) : -1;
   } else if (!p.q_tma) {
     // dims 0..255 staged in the key ring, which the producers fill only
     // after the second barrier below
-    load_q_smem(p, n, q_base, k_base, tid < 128 ? tid : tid - 256, 160);
+    load_q_smem(p, n, q_base, k_base, tid < 128 ? tid : tid - 512, 160);
   }
   tc_fence_before();
   __syncthreads();
@@ -804,18 +809,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (producer) {
     // ------------------------------------------------------------ producers
-    // Lane = key j of the tile, dims [64e, 64e + 64). The CTA's
-    // i-th tile goes to stage i % kStages, free once the p.v of tile
-    // i - kStages has completed; rows are loaded kDepth tiles ahead.
+    // Lane = key j of the tile, dims [64e, 64e + 64); group grp takes
+    // tiles grp, grp + 2, ... The CTA's i-th tile goes to stage
+    // i % kStages, free once the p.v of tile i - kStages has completed; rows
+    // are loaded kDepth of the group's tiles ahead.
     bool live = true;
-    for (int64_t i0 = 0; i0 < n_tiles && live; i0 += kDepth) {
+    for (int64_t i0 = grp; i0 < n_tiles && live; i0 += 2 * kDepth) {
 #pragma unroll
       for (int u = 0; u < kDepth; ++u) {
-        const int64_t i = i0 + u;
+        const int64_t i = i0 + 2 * u;
         if (i < n_tiles && live) {
           const Packed cur = buf[u];
-          buf[u] = load_packed(p, s_next, e);  // tile i + kDepth
-          s_next = i + kDepth + 1 < n_tiles ? key_index(p, i + kDepth + 1, j, key_off, key_len)
+          buf[u] = load_packed(p, s_next, e);  // tile i + 2 kDepth
+          s_next = i + 2 * kDepth + 2 < n_tiles ? key_index(p, i + 2 * kDepth + 2, j, key_off, key_len)
                                             : -1;
           const uint32_t st = (uint32_t)(i % kStages);
           if (i >= kStages &&
