@@ -88,7 +88,8 @@ constexpr int kDim = 512;       // latent width (score depth)
 constexpr int kTileKeys = 32;   // MMA N of q.k, K of p.v
 constexpr int kStages = 4;      // key tiles (and score / probability buffers) in the ring
 constexpr int kHalf = 256;      // output columns per CTA
-constexpr int kThreads = 704;   // softmax 0-3, producers 4-19 (two groups), q.k issuer 20, p.v issuer 21
+// softmax warps 0-3, producers 4-19 (two groups), q.k issuer 20, p.v issuer 21
+constexpr int kThreads = 704;
 constexpr int kIssuerWarp = 20;
 constexpr int kPvWarp = 21;
 constexpr int kRow = 272;       // packed row bytes
@@ -488,7 +489,8 @@ __device__ __forceinline__ void dequant_share(const Packed& x, uint32_t kbuf, in
     for (int c = 0; c < 8; ++c) {
       const uint32_t sb = c < 4 ? sb0 : sb1;
       sts_v4(row + (((uint32_t)c ^ swz) << 4),
-             sb - 2u <= 250u ? decode8_fast(words[c], make_tables(sb)) : decode8_slow(words[c], sb));
+             sb - 2u <= 250u ? decode8_fast(words[c], make_tables(sb))
+                             : decode8_slow(words[c], sb));
     }
   }
 }
@@ -790,9 +792,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t s_next = -1;
   if (producer) {
 #pragma unroll
-    for (int u = 0; u < kDepth; ++u)
-      buf[u] = load_packed(p, grp + 2 * u < n_tiles ? key_index(p, grp + 2 * u, j, key_off, key_len) : -1, e);
-    s_next = grp + 2 * kDepth < n_tiles ? key_index(p, grp + 2 * kDepth, j, key_off, key_len) : -1;
+    for (int u = 0; u < kDepth; ++u) {
+      const int64_t t = grp + 2 * u;  // the group's u-th tile
+      buf[u] = load_packed(p, t < n_tiles ? key_index(p, t, j, key_off, key_len) : -1, e);
+    }
+    const int64_t t = grp + 2 * kDepth;
+    s_next = t < n_tiles ? key_index(p, t, j, key_off, key_len) : -1;
   } else if (!p.q_tma) {
     // dims 0..255 staged in the key ring, which the producers fill only
     // after the second barrier below
@@ -821,8 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < n_tiles && live) {
           const Packed cur = buf[u];
           buf[u] = load_packed(p, s_next, e);  // tile i + 2 kDepth
-          s_next = i + 2 * kDepth + 2 < n_tiles ? key_index(p, i + 2 * kDepth + 2, j, key_off, key_len)
-                                            : -1;
+          const int64_t t = i + 2 * kDepth + 2;
+          s_next = t < n_tiles ? key_index(p, t, j, key_off, key_len) : -1;
           const uint32_t st = (uint32_t)(i % kStages);
           if (i >= kStages &&
               !mbar_wait(bars + kBarPvDone + 8 * st, (uint32_t)(((i / kStages) - 1) & 1), abort)) {
