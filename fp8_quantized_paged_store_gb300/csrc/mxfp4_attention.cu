@@ -14,7 +14,7 @@
 // on CTAs 2n and 2n + 1), which writes its output. With one (the split-K of
 // the read path, for few queries), every unit is cut into `chunks` runs of
 // at most `chunk_tiles` tiles, one CTA each (unit u's chunks on CTAs
-// u * chunks ..): the CTA writes an fp32 partial, the output of its chunk
+// u * chunks ..): the CTA writes a bf16 partial, the output of its chunk
 // normalised by the chunk's own softmax sum and that sum's log-sum-exp,
 // into the caller's workspace, and a second, small kernel combines each
 // unit's partials by their log-sum-exps (launched as a programmatic
@@ -59,8 +59,7 @@
 //     softmax in fp32 (exp2, running max with a rescale of the output only
 //     when the max grows by more than 2**32), and store P (bf16 pairs) into
 //     tensor memory; after the last tile, read O out of tensor memory and
-//     write the result (an fp32 partial through a staging area in the idle
-//     key ring, so that the stores are whole 512-byte runs).
+//     write the result (the bf16 output, or a chunk's bf16 partial).
 // Every wait is bounded; a timeout sets a CTA-wide abort flag that ends the
 // other roles' waits, and the CTA reports through an optional status word.
 // Before tensor memory is released, each issuing thread waits (bounded, abort
@@ -168,11 +167,11 @@ struct AttnParams {
   int64_t chunks, chunk_tiles;
   int64_t grid;  // units * chunks
   // Partial results (null when every unit is one chunk): CTA b's
-  // [num_heads][256] fp32 output of its chunk normalised by the chunk's
-  // softmax sum at part_o + b * num_heads * 256, and that sum's log-sum-exp
-  // in log2 units (-inf for a chunk without valid keys) at
+  // [num_heads][256] bf16 output of its chunk normalised by the chunk's
+  // softmax sum at part_o + b * num_heads * 512 bytes, and that sum's
+  // log-sum-exp in log2 units (-inf for a chunk without valid keys) at
   // part_lse + b * num_heads.
-  float* part_o;
+  uint8_t* part_o;
   float* part_lse;
   // Ragged index runs (one chunk per unit only): query n's indices are
   // indices[key_offsets[n] .. key_offsets[n + 1]), each bound clamped to
@@ -622,80 +621,45 @@ __device__ __forceinline__ bool drain_mmas(uint32_t bar) {
 }
 
 // One head's result (thread = head, O in TMEM lanes of this warp): the bf16
-// output row half or, for a chunk of a split unit (kPiece), the fp32 output
-// normalised by the chunk's softmax sum and that sum's log-sum-exp (log2
-// units) in CTA b's partial slot. O is read out 16 columns at a time, which
-// keeps the softmax loop's live state in registers around it. The bf16 row
-// (32 bytes per read) goes straight to memory. The fp32 row (64 bytes per
-// read, 1 KB per head) goes first into this warp's 32 rows of a staging
-// area in the idle key ring (16-byte chunk j of row r at ((j ^ (r & 7)) <<
-// 4): the eight lanes of a store phase hit eight bank groups); then the warp
-// writes each row with 16 bytes per lane, 512 contiguous bytes per store
-// instead of 32 separate rows (measured: faster for the fp32 partials,
-// slower for the bf16 rows).
+// output row half or, for a chunk of a split unit (kPiece), the bf16 output
+// normalised by the chunk's softmax sum (a partial) and that sum's
+// log-sum-exp (log2 units) in CTA b's partial slot. O is read out 16
+// columns at a time, which keeps the softmax loop's live state in registers
+// around it, and goes straight to memory (32 bytes per read).
 template <bool kPiece>
 __device__ __forceinline__ void write_result(const AttnParams& p, int64_t n, int v, int64_t b,
-                                             uint32_t lane_base, uint32_t stage, int h, float m_ref,
-                                             float l) {
+                                             uint32_t lane_base, int h, float m_ref, float l) {
   const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-  if constexpr (!kPiece) {
-    const bool store = h < p.num_heads;
-    uint8_t* orow = p.out + n * p.o_qstride + (int64_t)h * p.o_hstride + (int64_t)v * kHalf * 2;
+  const bool store = h < p.num_heads;
+  uint8_t* orow = kPiece ? p.part_o + (b * p.num_heads + h) * (kHalf * 2)
+                         : p.out + n * p.o_qstride + (int64_t)h * p.o_hstride +
+                               (int64_t)v * kHalf * 2;
 #pragma unroll 1
-    for (int c = 0; c < kHalf / 16; ++c) {
-      uint32_t o[16];
-      tmem_ld16(lane_base + kColO + 16 * c, o);
-      uint32_t w[8];
+  for (int c = 0; c < kHalf / 16; ++c) {
+    uint32_t o[16];
+    tmem_ld16(lane_base + kColO + 16 * c, o);
+    uint32_t w[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        w[k] = l > 0.0f ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv,
-                                      __uint_as_float(o[2 * k + 1]) * inv)
-                        : 0u;
-      if (store) {
+    for (int k = 0; k < 8; ++k)
+      w[k] = l > 0.0f ? pack_bf16x2(__uint_as_float(o[2 * k]) * inv,
+                                    __uint_as_float(o[2 * k + 1]) * inv)
+                      : 0u;
+    if (store) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
-          st_v4(orow + 32 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                                    w[4 * u + 3]));
-      }
+      for (int u = 0; u < 2; ++u)
+        st_v4(orow + 32 * c + 16 * u, make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                  w[4 * u + 3]));
     }
-    if (store && v == 0 && p.lse)
-      p.lse[n * p.num_heads + h] =
-          l > 0.0f ? (m_ref + log2f(l)) * 0.69314718055994531f : -__int_as_float(0x7F800000);
-  } else {
-    constexpr uint32_t kRowBytes = kHalf * 4;
-    const int lane = h & 31;
-    const uint32_t wrow = stage + (uint32_t)(h >> 5) * 32 * kRowBytes;  // this warp's rows
-    const uint32_t mine = wrow + (uint32_t)lane * kRowBytes, swz = (uint32_t)(lane & 7);
-#pragma unroll 1
-    for (int c = 0; c < kHalf / 16; ++c) {
-      uint32_t o[16];
-      tmem_ld16(lane_base + kColO + 16 * c, o);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        sts_v4(mine + ((((uint32_t)(4 * c + u)) ^ swz) << 4),
-               make_uint4(__float_as_uint(__uint_as_float(o[4 * u]) * inv),
-                          __float_as_uint(__uint_as_float(o[4 * u + 1]) * inv),
-                          __float_as_uint(__uint_as_float(o[4 * u + 2]) * inv),
-                          __float_as_uint(__uint_as_float(o[4 * u + 3]) * inv)));
-    }
-    __syncwarp();
-    const int64_t h0 = h - lane;  // this warp's first head
-#pragma unroll 1
-    for (int r = 0; r < 32 && h0 + r < p.num_heads; ++r) {
-      const uint32_t src = wrow + (uint32_t)r * kRowBytes, rs = (uint32_t)(r & 7);
-      float* prow = p.part_o + (b * p.num_heads + h0 + r) * kHalf;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t j = (uint32_t)(lane + 32 * u);
-        st_v4(prow + 4 * j, lds_v4_at(src + ((j ^ rs) << 4)));
-      }
-    }
-    if (h < p.num_heads)
-      p.part_lse[b * p.num_heads + h] = l > 0.0f ? m_ref + log2f(l) : -__int_as_float(0x7F800000);
   }
+  if (!store) return;
+  const float lse2 = l > 0.0f ? m_ref + log2f(l) : -__int_as_float(0x7F800000);
+  if (kPiece)
+    p.part_lse[b * p.num_heads + h] = lse2;
+  else if (v == 0 && p.lse)
+    p.lse[n * p.num_heads + h] = l > 0.0f ? lse2 * 0.69314718055994531f : lse2;
 }
 
-// kPiece: a chunk of a split unit, written as an fp32 partial; otherwise a
+// kPiece: a chunk of a split unit, written as a bf16 partial; otherwise a
 // whole unit, written as the bf16 output (the same kernel otherwise).
 template <bool kPiece>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -735,9 +699,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // no keys at all: every output row is zero and every log-sum-exp -inf
     // (an empty partial for a chunk)
     if constexpr (kPiece) {
-      for (int id = tid; id < p.num_heads * (kHalf / 4); id += kThreads)
-        reinterpret_cast<float4*>(p.part_o + b * p.num_heads * kHalf)[id] =
-            make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int id = tid; id < p.num_heads * 32; id += kThreads)
+        st_v4(p.part_o + (b * p.num_heads + (id >> 5)) * (kHalf * 2) + (id & 31) * 16,
+              make_uint4(0, 0, 0, 0));
       for (int h = tid; h < p.num_heads; h += kThreads)
         p.part_lse[b * p.num_heads + h] = -__int_as_float(0x7F800000);
       return;
@@ -953,8 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the result: wait for the last p.v, then read O out
         if (!warp_wait(bars + kBarPvDone + 8 * st, (uint32_t)((i / kStages) & 1), abort)) break;
         tc_fence_after();
-        // the key ring is idle: every p.v has completed
-        write_result<kPiece>(p, n, v, b, lane_base, k_base, tid, m_ref, l);
+        write_result<kPiece>(p, n, v, b, lane_base, tid, m_ref, l);
       }
     }
   }
@@ -984,6 +947,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (head, partial) weight is first worked out in parallel, and the sums keep
 // several loads in flight.
 constexpr int kMergeHeads = 8;  // heads per block (64 threads each)
+
+// Four consecutive bf16 columns of a partial as fp32.
+__device__ __forceinline__ float4 partial4(const uint8_t* at) {
+  const uint2 x = *reinterpret_cast<const uint2*>(at);
+  return make_float4(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xFFFF0000u),
+                     __uint_as_float(x.y << 16), __uint_as_float(x.y & 0xFFFF0000u));
+}
 constexpr int kMergeFew = 4;
 
 __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_kernel(AttnParams p) {
@@ -1016,7 +986,7 @@ __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_ker
       for (int k = 0; k < pieces; ++k) {
         const int64_t row = (b0 + k) * H + h;
         const float w = exp2f(p.part_lse[row] - L);
-        const float4 o = *reinterpret_cast<const float4*>(p.part_o + row * kHalf + 4 * c4);
+        const float4 o = partial4(p.part_o + row * (kHalf * 2) + 8 * c4);
         W += w;
         acc.x += w * o.x;
         acc.y += w * o.y;
@@ -1065,8 +1035,7 @@ __global__ void __launch_bounds__(64 * kMergeHeads, 4) mxfp4_attention_merge_ker
 #pragma unroll 8
     for (int k = 0; k < pieces; ++k) {
       const float w = merge_dyn[hh * pieces + k];
-      const float4 o =
-          *reinterpret_cast<const float4*>(p.part_o + ((b0 + k) * H + h) * kHalf + 4 * c4);
+      const float4 o = partial4(p.part_o + ((b0 + k) * H + h) * (kHalf * 2) + 8 * c4);
       acc.x += w * o.x;
       acc.y += w * o.y;
       acc.z += w * o.z;
@@ -1155,7 +1124,7 @@ int attention_params(const void* q_bf16, int64_t num_queries, int64_t num_heads,
 
 // Bytes of the split schedule's partial results: one per CTA.
 int64_t split_bytes(int64_t grid, int64_t num_heads) {
-  return grid * num_heads * (int64_t)(kvq::kHalf * 4 + 4);
+  return grid * num_heads * (int64_t)(kvq::kHalf * 2 + 4);
 }
 
 // Cuts every unit into `chunks` runs and lays the partial results out in
@@ -1164,8 +1133,8 @@ void split_layout(kvq::AttnParams& p, int64_t chunks, void* ws) {
   p.chunks = chunks;
   p.chunk_tiles = (p.tiles + chunks - 1) / chunks;
   p.grid = p.units * chunks;
-  p.part_o = static_cast<float*>(ws);
-  p.part_lse = p.part_o + p.grid * p.num_heads * kvq::kHalf;
+  p.part_o = static_cast<uint8_t*>(ws);
+  p.part_lse = reinterpret_cast<float*>(p.part_o + p.grid * p.num_heads * kvq::kHalf * 2);
 }
 
 // cuTensorMapEncodeTiled through the runtime (no link to the driver
@@ -1327,7 +1296,7 @@ extern "C" int mxfp4_mla_sparse_attention(const void* q_bf16, int64_t num_querie
 // instead of from a workspace argument.
 //
 // The array is a file-scope __device__ object of kScratchBytes (40 MiB: the
-// split schedule of 128 heads over up to 318 SMs). Every GPU that loads this
+// split schedule of 128 heads over up to 635 SMs). Every GPU that loads this
 // library's attention code holds it until the process exits. Host code only
 // has a host-side stand-in for its name, so the device address is looked up
 // with cudaGetSymbolAddress once per device, with that device current, on

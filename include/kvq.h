@@ -457,9 +457,14 @@ int mxfp4_mla_gather_dequant(const uint8_t* cache, int64_t num_blocks, int64_t b
  *                  cut into equal chunks of at least four 32-key tiles, one
  *                  CTA each, so that the grid fills the SMs (the split-K of
  *                  the read path [pr]: a ragged sparse-attention kernel plus
- *                  a split-K partial kernel): each chunk's fp32 partial
- *                  output and log-sum-exp are written there and merged by a
- *                  second kernel launched on the same stream. Its contents
+ *                  a split-K partial kernel): each chunk's output
+ *                  normalised by its own softmax sum (bf16, a partial) and
+ *                  that sum's log-sum-exp are written there and merged by a
+ *                  second kernel launched on the same stream (a
+ *                  programmatic dependent launch: it overlaps the first
+ *                  grid's tail and waits for all of it). A partial's
+ *                  rounding adds at most 2**-9 of the softmax-weighted
+ *                  magnitudes to the bound above. Its contents
  *                  need no initialisation and are garbage afterwards; two
  *                  calls in flight at once must not share it. Without one,
  *                  or when the units already fill the SMs, one CTA takes
@@ -508,7 +513,7 @@ int mxfp4_mla_sparse_attention_ragged(const void* q_bf16, int64_t num_queries, i
 /*
  * mxfp4_mla_sparse_attention_workspace_size — bytes of workspace that
  * mxfp4_mla_sparse_attention needs to split these shapes over the current
- * device's SMs: CTAs x num_heads x (256 x 4 + 4), CTAs = units x chunks with
+ * device's SMs: CTAs x num_heads x (256 x 2 + 4), CTAs = units x chunks with
  * units = 2 x num_queries, chunks = min(floor(SMs / units),
  * floor(ceil(topk / 32) / 4)) reduced so that no chunk is empty; 0 when
  * nothing is split (chunks below 2: the units fill the SMs, or topk is
@@ -530,7 +535,7 @@ int64_t mxfp4_mla_sparse_attention_workspace_size(int64_t num_queries, int64_t n
  * output; arguments, layouts, results and errors are those of
  * mxfp4_mla_sparse_attention with a workspace, plus:
  *   - The scratch is one 40 MiB (41,943,040-byte) __device__ array, enough
- *     for 128 heads split over up to 318 SMs. Every GPU that loads the
+ *     for 128 heads split over up to 635 SMs. Every GPU that loads the
  *     library's attention code holds it until the process exits.
  *   - Shapes whose split schedule needs more than that (see
  *     mxfp4_mla_sparse_attention_workspace_size) return KVQ_ESCRATCH and

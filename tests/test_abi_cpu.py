@@ -237,7 +237,7 @@ def _chunks(units, tiles, sms):
 
 
 def test_attention_workspace_size(L):
-    """CTAs x heads x (256 fp32 + one log-sum-exp), CTAs = 2 x queries x
+    """CTAs x heads x (256 bf16 + one fp32 log-sum-exp), CTAs = 2 x queries x
     chunks; 0 when nothing is split (the units fill the SMs, or too few
     tiles); -1 for shapes the attention rejects."""
     g = L.mxfp4_mla_sparse_attention_workspace_size
@@ -245,7 +245,7 @@ def test_attention_workspace_size(L):
     assert g(-1, 128, 16) == -1 and g(2, 0, 16) == -1 and g(2, 129, 16) == -1
     assert g(2, 128, -1) == -1
     sms = _sms()
-    piece = 128 * (256 * 4 + 4)
+    piece = 128 * (256 * 2 + 4)
     assert g(128, 128, 2048) == 0                      # 256 units fill the SMs
     assert g(1, 128, 32) == 0 and g(1, 64, 1) == 0     # one tile per unit
     # one query of 2048 keys: 64 tiles per half, 16 chunks of four
@@ -253,7 +253,7 @@ def test_attention_workspace_size(L):
     for nq, nh, topk in ((3, 64, 4096), (5, 128, 700), (20, 128, 2048)):
         tiles = -(-topk // 32)
         c = _chunks(2 * nq, tiles, sms)
-        want = 2 * nq * c * nh * (256 * 4 + 4) if c > 1 else 0
+        want = 2 * nq * c * nh * (256 * 2 + 4) if c > 1 else 0
         assert g(nq, nh, topk) == want, (nq, nh, topk)
 
 

@@ -14,7 +14,8 @@ lse: |lse - exact| <= 2e-3.
 Both schedules are checked: key tiles split evenly over the SMs (pieces of a
 (query, value half) cut between CTAs merged by log-sum-exp; the default), and
 one CTA per (query, value half). The bound holds for both: a split piece's
-output is kept in fp32 and the merge rounds to bf16 once.
+output (normalised by its own softmax sum) is rounded to bf16, which adds
+at most 2**-9 of the first term, and the merge rounds to bf16 once more.
 The packed cache is written by the oracle's store, never by the CUDA path.
 """
 import numpy as np
