@@ -376,11 +376,13 @@ def _check_ragged(q, cache, runs, sm_scale, num_slots, first_offset=0, extra_tai
 @pytest.mark.parametrize("heads", [128, 48])
 def test_ragged_runs_of_every_length(heads):
     """Sparse prefill: one flat index array cut into runs of 0, 1, 31, 32,
-    33, 300, 700 and 2048 indices (with pads and out-of-range entries); an
-    empty run gives out = 0 and lse = -inf."""
+    33, 65, 150, 220, 300, 700 and 2048 indices (with pads and out-of-range
+    entries): 0 to 64 tiles, odd counts above one among them (3, 5, 7: the
+    last tile's q.k unpaired, the producer groups' shares unequal); an empty
+    run gives out = 0 and lse = -inf."""
     cache = _fill_cache(8192, seed=40)
     rng = np.random.default_rng(41)
-    lens = [0, 1, 31, 32, 33, 300, 700, 2048, 5]
+    lens = [0, 1, 31, 32, 33, 65, 150, 220, 300, 700, 2048, 5]
     runs = []
     for L in lens:
         r = rng.integers(-1, 8192, L)
