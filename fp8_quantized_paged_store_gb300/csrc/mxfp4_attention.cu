@@ -39,7 +39,7 @@
 //     tiles, 12-19 the odd ones, so that each warp has two tile periods
 //     for a tile's work; a lane takes one key of the tile and one 64-dim
 //     K-block, a warp 8 keys x 4 K-blocks):
-//     load the packed rows two of its tiles ahead into registers (pads and
+//     load the packed rows one of its tiles ahead into registers (pads and
 //     out-of-range indices load nothing and decode to zero rows),
 //     dequantize them with byte permutes into a 128-byte-swizzled K-major
 //     bf16 key tile, and arrive on its "full" barrier; a stage is reused once
@@ -92,7 +92,9 @@ constexpr int kThreads = 704;
 constexpr int kIssuerWarp = 20;
 constexpr int kPvWarp = 21;
 constexpr int kRow = 272;       // packed row bytes
-constexpr int kDepth = 2;       // tiles a producer has in flight (three: 1.3% slower)
+// row loads a producer keeps in flight, in tiles of its group (every other
+// tile): one covers two tile periods (two: 1.5% slower, three: spills)
+constexpr int kDepth = 1;
 
 constexpr uint32_t kQhiBytes = kHeads * 256 * 2;         // dims 256..511: 4 K-blocks x 128 rows
 constexpr uint32_t kKBytes = kTileKeys * kDim * 2;       // 8 K-blocks x 32 rows x 128 B
